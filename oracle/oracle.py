@@ -1,0 +1,287 @@
+"""fp64 CPU oracle for the paged K/V attention path.
+
+TEST INFRASTRUCTURE ONLY.  Nothing in the product path may import, call or
+execute this module: only ``tests/``, ``__graft_entry__.smoke()`` and the
+CPU-baseline / reference arm of ``bench.py`` use it.  It shares no code with
+the CUDA library (``paged_kv_cache_189_gb300/csrc``) and imports nothing from
+it; both sides are fed from the seeded input generators alone.
+
+It is deliberately plain and slow: literal loops for the byte-exact steps,
+numpy float64 for the arithmetic, one matmul per (sequence, K/V head) as the
+only library primitive.  Each function cites the passage it follows, using the
+titles of the two pull-request pages the method comes from:
+
+* [VG]  "Paged causal K/V cache and cached attention for VisualGen"
+        (TensorRT-LLM pull request 19938);
+* [SP]  "Support shared-prefix attention for n-sample requests in FMHA"
+        (TensorRT-LLM pull request 20841).
+
+Conventions (the readings taken where the pages are silent are marked READING):
+
+* bf16 values are the top 16 bits of an IEEE float32; pools and queries are
+  handled as raw uint16 bit patterns and widened exactly to float64.
+* K and V pools are ``[num_pages, page_size, Hkv, D]``; slot ``s`` is page
+  ``s // page_size``, offset ``s % page_size`` ([VG] Description, Cache: slot
+  ids are view_page * tokens_per_page + slot).  READING: token-major page layout.
+* Query row ``i < q_real`` of a sequence with ``kv_len`` keys sits at absolute
+  position ``kv_len - q_real + i``: each block's new tokens are the last keys
+  of its row ([VG] Description, Cache, "Exact window" bullet).
+* LSE is the natural log of the sum of exponentials of the scaled scores.
+  READING: [SP] mentions both a natural-log and a base-2 LSE; natural log is
+  the one its FlashAttention-4 path keeps.
+* Padding rows (``i >= q_real``) and rows with no visible key: O = 0,
+  LSE = -inf ([VG] Description, Attention, seq_len bullet: padding rows come
+  back zero; [SP] commit log: an empty run has LSE -inf).
+* Softmax scale defaults to 1/sqrt(D).
+
+Parity pins: every function here is checked in ``tests/test_oracle_pins.py``
+against something other than itself (library routines on a different
+formulation, closed forms, hand-derived visible-key sets, invariants).
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+MASK_NONE = "none"
+MASK_CAUSAL = "causal"
+MASK_BLOCK_CAUSAL = "block_causal"
+
+
+# ----------------------------------------------------------------------------
+# bf16 decoding
+# ----------------------------------------------------------------------------
+
+def bf16_bits(x) -> np.ndarray:
+    """Raw uint16 bit patterns of a bf16 torch tensor or a uint16 array."""
+    if isinstance(x, np.ndarray):
+        assert x.dtype == np.uint16
+        return x
+    import torch
+    assert x.dtype == torch.bfloat16, x.dtype
+    return x.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def bf16_to_f64(bits: np.ndarray) -> np.ndarray:
+    """Exact widening: a bf16 is the upper half of a float32."""
+    return (bits.astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)
+
+
+# ----------------------------------------------------------------------------
+# (1) scatter of new K/V rows into pool slots
+# ----------------------------------------------------------------------------
+
+def kv_scatter_slots(k_src, v_src, slots, k_pool, v_pool, slots2=None, src_idx=None,
+                     num_slots=None):
+    """Copy token rows into pool slots, bit for bit.
+
+    [VG] Description, Cache, "Chunk K/V write" bullet and the per-file notes on
+    scatterKvSlots: every token is written to one or two pool slots, reading the
+    source rows once with any token/head stride; optional source indices.
+
+    ``k_src``/``v_src``: ``[T_src, Hkv, D]`` bit arrays (any dtype, copied as
+    is).  ``slots``/``slots2``: ``[T]`` int64.  ``src_idx``: ``[T]`` or None
+    (READING: destination token ``t`` reads source row ``src_idx[t]``).  A
+    negative slot is skipped (READING: the sentinel the pages' slot copy uses).
+    If ``num_slots`` is given, a slot >= num_slots or a source index out of
+    range is skipped and reported (READING: the library's checked mode).
+
+    Returns ``(k_pool_out, v_pool_out, n_rejected)`` as new arrays.
+    """
+    k_out = np.array(k_pool, copy=True)
+    v_out = np.array(v_pool, copy=True)
+    num_pages, page_size = k_out.shape[0], k_out.shape[1]
+    T = len(slots)
+    n_src = k_src.shape[0]
+    rejected = 0
+    for t in range(T):
+        src = t if src_idx is None else int(src_idx[t])
+        if num_slots is not None and not (0 <= src < n_src):
+            rejected += 1
+            continue
+        for dest in (slots, slots2):
+            if dest is None:
+                continue
+            s = int(dest[t])
+            if s < 0:
+                continue
+            if num_slots is not None and s >= num_slots:
+                rejected += 1
+                continue
+            page, off = s // page_size, s % page_size
+            k_out[page, off] = k_src[src]
+            v_out[page, off] = v_src[src]
+    return k_out, v_out, rejected
+
+
+# ----------------------------------------------------------------------------
+# (4) in-place row rotation of a rolling buffer
+# ----------------------------------------------------------------------------
+
+def rotate_rows(x: np.ndarray, shift: int) -> np.ndarray:
+    """Rotate every row left by ``shift`` elements: ``out[r, c] = x[r, (c + shift) mod cols]``.
+
+    [VG] Description, Cache: eviction is an in-place rotation (new op
+    rotate_rows_), and the per-file notes: supported element sizes, shifts and
+    strided rows; no-op cases.  READING: left rotation (``torch.roll`` by
+    ``-shift``), shift taken modulo cols, negative shifts allowed.
+
+    ``x``: ``[rows, cols, elem_bytes]`` uint8 (an element is an opaque group of
+    bytes).  Returns a new array.
+    """
+    out = np.array(x, copy=True)
+    rows, cols = x.shape[0], x.shape[1]
+    if rows == 0 or cols <= 1:
+        return out
+    source_col = (np.arange(cols) + shift) % cols
+    for r in range(rows):
+        out[r] = x[r][source_col]
+    return out
+
+
+# ----------------------------------------------------------------------------
+# (2) attention through the paged pool
+# ----------------------------------------------------------------------------
+
+def visible_keys(i: int, q_real: int, kv_len: int, mask: str, causal_block: int) -> int:
+    """Number of leading keys (logical positions ``0 .. n-1``) query row ``i`` sees.
+
+    * none: every key of the row.
+    * causal: keys up to and including the row's own position
+      ``kv_len - q_real + i``.
+    * block_causal: [VG] Description, Cache, frame-causal bullet and the
+      causal_block_size docstring: the real tokens are cut into consecutive
+      blocks of ``causal_block``; full attention within a block, causal across
+      blocks.  Row ``i`` is in block ``i // causal_block`` and sees all keys
+      before this step's tokens plus every new token up to the end of its
+      block.  READING: a last, shorter block when q_real is not a multiple.
+    * padding rows (``i >= q_real``) see nothing ([VG] seq_len bullet).
+    """
+    if i >= q_real:
+        return 0
+    first_new = kv_len - q_real
+    if mask == MASK_NONE:
+        return kv_len
+    if mask == MASK_CAUSAL:
+        return first_new + i + 1
+    if mask == MASK_BLOCK_CAUSAL:
+        assert causal_block > 0
+        block_end = (i // causal_block + 1) * causal_block
+        return first_new + min(q_real, block_end)
+    raise ValueError(mask)
+
+
+def gather_sequence(pool_bits: np.ndarray, table_row, kv_len: int) -> np.ndarray:
+    """Materialise one sequence's contiguous ``[kv_len, Hkv, D]`` float64 keys
+    (or values): logical key ``j`` lives at page ``table_row[j // P]``, offset
+    ``j % P`` ([VG] Description, Attention: paged attention over per-block
+    rows through the page table)."""
+    P = pool_bits.shape[1]
+    j = np.arange(kv_len)
+    pages = np.asarray(table_row)[j // P].astype(np.int64)
+    return bf16_to_f64(pool_bits[pages, j % P])
+
+
+def paged_attention(q, k_pool, v_pool, block_table, kv_lens, q_indptr, q_real=None,
+                    mask=MASK_CAUSAL, causal_block=0, scale=None, rows=None):
+    """Attention of every query row over its sequence's keys read through the
+    block table: ``O = softmax(scale * q K^T + mask) V`` and
+    ``LSE = ln sum_j exp(scale * q . k_j)`` over the visible keys.
+
+    [VG] Description, Attention (paged attention over per-block rows; seq_len
+    is the real query count and padding rows come back zero) and [SP] (the
+    prefix / tail calls return output and LSE).
+
+    ``q``: ``[rows, Hq, D]`` bf16 bits; pools ``[pages, P, Hkv, D]`` bf16 bits;
+    ``block_table`` ``[B, max_pages]``; ``kv_lens`` ``[B]``; ``q_indptr``
+    ``[B + 1]``; ``q_real`` ``[B]`` or None (all rows real).  Query head ``h``
+    reads K/V head ``h // (Hq / Hkv)`` (grouped-query heads).
+    ``rows``: optional iterable of query-row indices to compute (others are
+    left NaN) for spot checks of large cases.
+
+    Returns ``(O [rows, Hq, D] float64, LSE [rows, Hq] float64)``.
+    """
+    q_bits = bf16_bits(q)
+    kb = bf16_bits(k_pool)
+    vb = bf16_bits(v_pool)
+    block_table = np.asarray(block_table)
+    kv_lens = np.asarray(kv_lens)
+    q_indptr = np.asarray(q_indptr)
+    total_rows, Hq, D = q_bits.shape
+    Hkv = kb.shape[2]
+    assert Hq % Hkv == 0
+    G = Hq // Hkv
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    B = len(kv_lens)
+    want = None if rows is None else set(int(r) for r in rows)
+    O = np.full((total_rows, Hq, D), np.nan)
+    LSE = np.full((total_rows, Hq), np.nan)
+    for b in range(B):
+        r0, r1 = int(q_indptr[b]), int(q_indptr[b + 1])
+        seq_rows = [r for r in range(r0, r1) if want is None or r in want]
+        if not seq_rows:
+            continue
+        kv_len = int(kv_lens[b])
+        qr = (r1 - r0) if q_real is None else int(np.asarray(q_real)[b])
+        K = gather_sequence(kb, block_table[b], kv_len)   # [kv_len, Hkv, D]
+        V = gather_sequence(vb, block_table[b], kv_len)
+        Qb = bf16_to_f64(q_bits[seq_rows])                  # [n, Hq, D]
+        nvis = np.array([visible_keys(r - r0, qr, kv_len, mask, causal_block)
+                         for r in seq_rows])
+        visible = np.arange(kv_len)[None, :] < nvis[:, None]   # [n, kv_len]
+        for h in range(Hq):
+            kvh = h // G
+            s = scale * (Qb[:, h, :] @ K[:, kvh, :].T)          # [n, kv_len]
+            s = np.where(visible, s, -np.inf)
+            has_keys = nvis > 0
+            m = np.where(has_keys, s.max(axis=1, initial=-np.inf), 0.0)
+            w = np.exp(s - m[:, None])                          # exactly 0 on masked keys
+            tot = w.sum(axis=1)
+            safe_tot = np.where(has_keys, tot, 1.0)
+            o = (w @ V[:, kvh, :]) / safe_tot[:, None]
+            O[seq_rows, h] = np.where(has_keys[:, None], o, 0.0)
+            LSE[seq_rows, h] = np.where(has_keys, m + np.log(safe_tot), -np.inf)
+    return O, LSE
+
+
+# ----------------------------------------------------------------------------
+# (3) exact merge of two attention states
+# ----------------------------------------------------------------------------
+
+def merge_attn_states(o_a, lse_a, o_b, lse_b):
+    """Join two partial attention states over disjoint key sets.
+
+    [SP] Dev/commit notes: the prefix attention and the private-tail attention
+    each return an output and its LSE, and one merge kernel joins them; an
+    empty run has LSE -inf.  With ``m = max(La, Lb)``, ``wa = e^(La - m)``,
+    ``wb = e^(Lb - m)``: ``O = (wa Oa + wb Ob) / (wa + wb)`` and
+    ``L = m + ln(wa + wb)``.  READING: two empty states give O = 0, L = -inf.
+
+    ``o_*``: ``[..., D]`` float; ``lse_*``: ``[...]``.  Returns float64 arrays.
+    """
+    o_a = np.asarray(o_a, dtype=np.float64)
+    o_b = np.asarray(o_b, dtype=np.float64)
+    la = np.asarray(lse_a, dtype=np.float64)
+    lb = np.asarray(lse_b, dtype=np.float64)
+    o = np.zeros(np.broadcast_shapes(o_a.shape, o_b.shape))
+    lse = np.full(np.broadcast_shapes(la.shape, lb.shape), -np.inf)
+    for idx in np.ndindex(*lse.shape):
+        a, b = la[idx], lb[idx]
+        if a == -np.inf and b == -np.inf:
+            continue
+        m = max(a, b)
+        wa = math.exp(a - m) if a != -np.inf else 0.0
+        wb = math.exp(b - m) if b != -np.inf else 0.0
+        o[idx] = (wa * o_a[idx] + wb * o_b[idx]) / (wa + wb)
+        lse[idx] = m + math.log(wa + wb)
+    return o, lse
+
+
+def merge_many(os_, lses):
+    """n-way merge of partial states, folded left with the two-way merge."""
+    o, lse = os_[0], lses[0]
+    for o_i, l_i in zip(os_[1:], lses[1:]):
+        o, lse = merge_attn_states(o, lse, o_i, l_i)
+    return np.asarray(o, dtype=np.float64), np.asarray(lse, dtype=np.float64)
