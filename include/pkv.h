@@ -1,0 +1,212 @@
+/*
+ * pkv.h -- C ABI of the paged K/V attention library for GB300 (sm_103a).
+ *
+ * The library covers the data-parallel hot path of attention read through a
+ * paged K/V cache, as described by two TensorRT-LLM pull-request pages:
+ *
+ *   [VG] "Paged causal K/V cache and cached attention for VisualGen"
+ *        (pull request 19938), and
+ *   [SP] "Support shared-prefix attention for n-sample requests in FMHA"
+ *        (pull request 20841).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Every data pointer is a DEVICE pointer owned by the caller.  The library
+ *    never allocates, frees, synchronises or reads device memory back on the
+ *    host: each call validates its arguments on the host, enqueues its kernels
+ *    on `stream` (a cudaStream_t; NULL = the legacy default stream) and returns.
+ *    This is the CUDA-graph rule of [VG] Description, Cache ("CUDA-graph safe"
+ *    bullet): every kernel input lives in caller-owned device memory, so a
+ *    captured call replays with whatever those buffers hold.
+ *  - Validation failures return a status before anything is enqueued; the
+ *    reason is available from pkv_last_error() (thread-local).  Empty inputs
+ *    (zero tokens, rows or heads) return PKV_OK without a launch ([VG] per-file
+ *    notes on rotateRows: no-op cases).
+ *  - Strides are in ELEMENTS, not bytes.
+ *  - Paged pool layout: K and V are separate pools of `num_pages` pages; page
+ *    p starts at element p * page_stride and holds `page_size` slots of
+ *    [num_kv_heads][head_dim] contiguous elements (token-major).  Slot id
+ *    s = page * page_size + offset ([VG] Description, Cache: slot ids are
+ *    view_page * tokens_per_page + slot).  page_stride >= page_size *
+ *    num_kv_heads * head_dim, so one allocation may hold K and V interleaved
+ *    per page.
+ *  - Device-side indices (slots, block-table entries, source indices) are the
+ *    caller's responsibility, as in [VG] (per-file notes on scatterKvSlots:
+ *    device slot indices are not range-checked).  With PKV_FLAG_CHECKED the
+ *    kernels range-check them, skip the offending access and OR an error bit
+ *    into *err (a device int32 the caller zeroes); nothing faults.
+ *  - Duplicate destination slots in one scatter race: the value left in the
+ *    slot is unspecified ([VG] per-file notes on scatterKvSlots).
+ *  - Calls are not internally synchronised with each other; calls on
+ *    different streams that touch the same memory race.
+ */
+#ifndef PKV_H_
+#define PKV_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    PKV_OK = 0,
+    PKV_ERR_INVALID_ARG = 1, /* a pointer, size or stride is not valid     */
+    PKV_ERR_UNSUPPORTED = 2, /* valid, but not a combination built here    */
+    PKV_ERR_WORKSPACE = 3,   /* workspace missing, misaligned or too small */
+    PKV_ERR_CUDA = 4         /* a CUDA runtime/driver call failed          */
+} pkv_status;
+
+typedef enum { PKV_BF16 = 0, PKV_F16 = 1, PKV_F32 = 2 } pkv_dtype;
+
+typedef enum {
+    PKV_MASK_NONE = 0,         /* every key of the sequence is visible       */
+    PKV_MASK_CAUSAL = 1,       /* row i sees keys 0 .. kv_len - q_real + i   */
+    PKV_MASK_BLOCK_CAUSAL = 2  /* full within a causal block, causal across  */
+} pkv_mask;
+
+/* flags */
+#define PKV_FLAG_CHECKED 0x1u     /* range-check device indices, report in *err */
+#define PKV_FLAG_SIMT_ONLY 0x2u   /* paged_attention: use the generic SIMT kernel
+                                     (a slow cross-check of the fast kernels)   */
+
+/* bits OR-ed into *err in checked mode */
+#define PKV_ERRBIT_SLOT 0x1       /* scatter slot >= num_pages * page_size      */
+#define PKV_ERRBIT_SRC 0x2        /* scatter source index out of range          */
+#define PKV_ERRBIT_PAGE 0x4       /* block-table entry outside [0, num_pages)   */
+#define PKV_ERRBIT_LEN 0x8        /* kv_len / q rows beyond the host bounds      */
+
+/* Human-readable name of a status, and the last validation message of this thread. */
+const char* pkv_status_string(pkv_status status);
+const char* pkv_last_error(void);
+
+/*
+ * kv_scatter_slots -- write new K/V token rows into pool slots.
+ *
+ * [VG] Description, Cache ("Chunk K/V write" bullet) and the per-file notes on
+ * scatterKvSlots: one kernel reads each source row once, with any token/head
+ * stride (so K/V sliced from a fused QKV tensor need no copy), and writes it to
+ * one or two pool slots; optional source indices.
+ *
+ * For t in [0, num_tokens):  src = src_idx ? src_idx[t] : t;
+ *   if slots[t] >= 0:            K/V pool slot slots[t]  <- k_src/v_src row src
+ *   if slots2 && slots2[t] >= 0: K/V pool slot slots2[t] <- the same row
+ * A row is [num_kv_heads][head_dim] elements; source element (t, h, d) is at
+ * t * src_token_stride + h * src_head_stride + d (K and V share the strides).
+ * Negative slots are skipped (padding rows).  Values are copied bit for bit.
+ *
+ *  k_src, v_src   device, num_src_rows rows (dtype elements)
+ *  slots          device int64 [num_tokens]; slots2 and src_idx: device int64
+ *                 [num_tokens] or NULL
+ *  k_pool, v_pool device pools (layout above)
+ *  dtype          element type (only its size matters: 2 or 4 bytes)
+ *  err            device int32, required with PKV_FLAG_CHECKED, else ignored
+ */
+pkv_status kv_scatter_slots(const void* k_src, const void* v_src, int64_t num_tokens,
+                            int64_t num_src_rows, int num_kv_heads, int head_dim,
+                            int64_t src_token_stride, int64_t src_head_stride,
+                            const int64_t* slots, const int64_t* slots2,
+                            const int64_t* src_idx, void* k_pool, void* v_pool,
+                            int64_t num_pages, int page_size, int64_t page_stride,
+                            pkv_dtype dtype, unsigned flags, int32_t* err, void* stream);
+
+/*
+ * paged_attention -- attention of packed query rows over K/V read page by page
+ * through per-sequence block tables.
+ *
+ * [VG] Description, Attention: paged attention over per-block rows, 32-token
+ * pages, a real-token seq_len separate from the growing key count, padding rows
+ * neither attended nor attending and returned as zeros; frame-causal blocks
+ * (Cache, frame-causal bullet).  [SP]: the shared-prefix and private-tail
+ * calls each return the output and its LSE for an exact merge.
+ *
+ * Sequence b owns query rows q_indptr[b] .. q_indptr[b+1]-1 and kv_lens[b]
+ * keys; logical key j is slot block_table[b * block_table_stride + j / page_size]
+ * * page_size + j % page_size.  The first q_real[b] rows are real (q_real NULL:
+ * all rows), row i at absolute position kv_lens[b] - q_real[b] + i (the new
+ * tokens are the last keys of their row, [VG] Cache, "Exact window" bullet).
+ * Query head h reads K/V head h / (num_q_heads / num_kv_heads).
+ * Visible keys of real row i: mask NONE: all kv_len; CAUSAL: the first
+ * kv_len - q_real + i + 1; BLOCK_CAUSAL (block size causal_block > 0): the
+ * first kv_len - q_real + min(q_real, (i / causal_block + 1) * causal_block).
+ *
+ *   out[r, h, :] = sum_j softmax_j(scale * q[r,h] . k_j) v_j   (visible j)
+ *   lse[r, h]    = ln sum_j exp(scale * q[r,h] . k_j)          (natural log)
+ * Padding rows and rows with no visible key: out = 0, lse = -inf.
+ *
+ *  q            device bf16; element (row, h, d) at row*q_token_stride +
+ *               h*q_head_stride + d (d contiguous, 16-byte aligned rows)
+ *  k_pool/v_pool device bf16 pools; page_size must be 32
+ *  block_table  device int32 [batch][block_table_stride]; entries past a
+ *               row's last page are never read
+ *  kv_lens      device int32 [batch]; q_indptr device int32 [batch + 1];
+ *  q_real       device int32 [batch] or NULL
+ *  batch, max_q_rows, max_kv_len: HOST upper bounds of batch size, rows per
+ *               sequence and keys per sequence; they size the grid, so a call
+ *               captured in a CUDA graph stays valid while the device values
+ *               stay within them (keys beyond max_kv_len are not attended)
+ *  head_dim     64 or 128; num_q_heads % num_kv_heads == 0
+ *  scale        softmax scale; <= 0 selects 1/sqrt(head_dim)
+ *  out          device [total_rows][num_q_heads][head_dim], bf16 or f32 (dense)
+ *  lse          device f32 [total_rows][num_q_heads] or NULL
+ *  workspace    device scratch of paged_attention_workspace_size(...) bytes
+ *               (256-byte aligned); may be NULL when that size is 0
+ *  num_splits   key splits per sequence (split-KV); 0 = chosen from the bounds
+ */
+size_t paged_attention_workspace_size(int batch, int max_q_rows, int num_q_heads,
+                                      int num_kv_heads, int head_dim, int max_kv_len,
+                                      int num_splits, unsigned flags);
+
+pkv_status paged_attention(const void* q, int64_t q_token_stride, int64_t q_head_stride,
+                           const void* k_pool, const void* v_pool, int64_t num_pages,
+                           int page_size, int64_t page_stride, const int32_t* block_table,
+                           int64_t block_table_stride, const int32_t* kv_lens,
+                           const int32_t* q_indptr, const int32_t* q_real, int batch,
+                           int max_q_rows, int max_kv_len, int num_q_heads, int num_kv_heads,
+                           int head_dim, pkv_mask mask, int causal_block, float scale,
+                           void* out, pkv_dtype out_dtype, float* lse, void* workspace,
+                           size_t workspace_bytes, int num_splits, unsigned flags,
+                           int32_t* err, void* stream);
+
+/*
+ * merge_attn_states -- exact merge of two attention states over disjoint key
+ * sets (shared-prefix state with private-tail state).
+ *
+ * [SP] commit notes: the prefix and the tail attention each return an output
+ * and its LSE and one merge joins them; an empty run has LSE -inf.  Per (row,
+ * head):  m = max(La, Lb), wa = e^(La-m), wb = e^(Lb-m),
+ *         out = (wa*Oa + wb*Ob) / (wa + wb),  lse_out = m + ln(wa + wb);
+ * both empty (-inf): out = 0, lse_out = -inf.
+ *
+ *  o_a, o_b     device [rows][num_heads][head_dim] of in_dtype (bf16 or f32)
+ *  lse_a, lse_b device f32 [rows][num_heads] (natural log)
+ *  o_out        device [rows][num_heads][head_dim] of out_dtype; may alias o_a
+ *  lse_out      device f32 or NULL; may alias lse_a
+ *  head_dim     a multiple of 4, at most 512
+ */
+pkv_status merge_attn_states(const void* o_a, const float* lse_a, const void* o_b,
+                             const float* lse_b, pkv_dtype in_dtype, int64_t rows,
+                             int num_heads, int head_dim, void* o_out, pkv_dtype out_dtype,
+                             float* lse_out, void* stream);
+
+/*
+ * rotate_rows -- rotate every row of a 2-D buffer left in place.
+ *
+ * [VG] Description, Cache: eviction is an in-place rotation on the device (op
+ * rotate_rows_), and the per-file notes on rotateRows: supported element sizes,
+ * shifts, strided rows, no-op cases.  For every row r:
+ *     x[r][c] <- x[r][(c + shift) mod cols]      (c in [0, cols))
+ * i.e. torch.roll(row, -shift).  Any shift (negative, or beyond cols) is taken
+ * modulo cols.  Elements are opaque groups of elem_size bytes, elem_size in
+ * {1, 2, 4, 8, 16}; row r starts at byte r * row_stride * elem_size.  rows == 0
+ * or cols <= 1: no launch.  Rows must not overlap.
+ */
+pkv_status rotate_rows(void* x, int64_t rows, int64_t cols, int64_t row_stride,
+                       int elem_size, int64_t shift, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PKV_H_ */

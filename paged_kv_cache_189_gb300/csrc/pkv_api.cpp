@@ -1,0 +1,347 @@
+// pkv_api.cpp -- the C ABI: argument validation, kernel choice, split-KV
+// planning, TMA tensor maps, status strings.  Nothing here touches device
+// memory; every check runs on the host before anything is enqueued.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <algorithm>
+#include <mutex>
+#include <string>
+
+#include "pkv.h"
+#include "pkv_internal.h"
+
+namespace {
+
+thread_local std::string g_last_error;
+
+pkv_status fail(pkv_status st, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
+pkv_status fail(pkv_status st, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof(buf), fmt, ap);
+    va_end(ap);
+    g_last_error = buf;
+    return st;
+}
+
+pkv_status ok() {
+    g_last_error.clear();
+    return PKV_OK;
+}
+
+pkv_status from_cuda(cudaError_t e, const char* what) {
+    if (e == cudaSuccess) return ok();
+    return fail(PKV_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+bool aligned(const void* p, size_t n) { return (reinterpret_cast<uintptr_t>(p) % n) == 0; }
+
+int elem_size(pkv_dtype d) {
+    switch (d) {
+        case PKV_BF16: return 2;
+        case PKV_F16: return 2;
+        case PKV_F32: return 4;
+    }
+    return 0;
+}
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point, so the
+// library needs no link-time dependency on libcuda.
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// One K (or V) pool as a 4-D tensor {D, Hkv, page slots, pages}; a box is
+// 64 columns x 1 head x 32 slots x 1 page (4 KiB), 128-byte swizzled.
+pkv_status make_pool_map(CUtensorMap* m, const void* base, int D, int Hkv, int page_size,
+                         int64_t num_pages, int64_t page_stride) {
+    auto fn = encode_fn();
+    if (!fn) return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
+    cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(Hkv),
+                          static_cast<cuuint64_t>(page_size), static_cast<cuuint64_t>(num_pages)};
+    cuuint64_t strides[3] = {static_cast<cuuint64_t>(D) * 2,
+                             static_cast<cuuint64_t>(Hkv) * D * 2,
+                             static_cast<cuuint64_t>(page_stride) * 2};
+    cuuint32_t box[4] = {64, 1, static_cast<cuuint32_t>(page_size), 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides,
+                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled(pool) failed: %d", (int)r);
+    return PKV_OK;
+}
+
+enum class Kernel { kNone, kDecode, kSimt };
+
+struct Plan {
+    Kernel kernel = Kernel::kNone;
+    int splits = 1;
+    int split_keys = 0;
+    size_t ws_bytes = 0;
+};
+
+constexpr int kDecodeSplitKeys = 512;  // 16 pages: the pages' minimum split of 512 tokens
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+Plan plan_attention(int batch, int max_q_rows, int Hq, int Hkv, int D, int max_kv_len,
+                    int num_splits, unsigned flags) {
+    Plan pl;
+    const int G = Hkv > 0 ? Hq / Hkv : 0;
+    if ((flags & PKV_FLAG_SIMT_ONLY) || max_q_rows != 1 || !pkv::decode_supported(D, G)) {
+        pl.kernel = Kernel::kSimt;
+        return pl;
+    }
+    pl.kernel = Kernel::kDecode;
+    int keys = kDecodeSplitKeys;
+    if (num_splits > 0) {
+        const int per = (max_kv_len + num_splits - 1) / num_splits;
+        keys = std::max(32, (per + 31) / 32 * 32);
+    }
+    pl.split_keys = keys;
+    pl.splits = std::max(1, (max_kv_len + keys - 1) / keys);
+    if (pl.splits > 1) {
+        const size_t states = static_cast<size_t>(batch) * max_q_rows * Hq * pl.splits;
+        pl.ws_bytes = round_up(states * D * sizeof(float), 256) + round_up(states * sizeof(float), 256);
+    }
+    return pl;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* pkv_status_string(pkv_status s) {
+    switch (s) {
+        case PKV_OK: return "PKV_OK";
+        case PKV_ERR_INVALID_ARG: return "PKV_ERR_INVALID_ARG";
+        case PKV_ERR_UNSUPPORTED: return "PKV_ERR_UNSUPPORTED";
+        case PKV_ERR_WORKSPACE: return "PKV_ERR_WORKSPACE";
+        case PKV_ERR_CUDA: return "PKV_ERR_CUDA";
+    }
+    return "PKV_UNKNOWN_STATUS";
+}
+
+const char* pkv_last_error(void) { return g_last_error.c_str(); }
+
+pkv_status kv_scatter_slots(const void* k_src, const void* v_src, int64_t num_tokens,
+                            int64_t num_src_rows, int num_kv_heads, int head_dim,
+                            int64_t src_token_stride, int64_t src_head_stride,
+                            const int64_t* slots, const int64_t* slots2, const int64_t* src_idx,
+                            void* k_pool, void* v_pool, int64_t num_pages, int page_size,
+                            int64_t page_stride, pkv_dtype dtype, unsigned flags, int32_t* err,
+                            void* stream) {
+    const int esz = elem_size(dtype);
+    if (esz == 0) return fail(PKV_ERR_INVALID_ARG, "scatter: unknown dtype %d", (int)dtype);
+    if (num_tokens < 0 || num_src_rows < 0 || num_kv_heads < 0 || head_dim < 0 || num_pages < 0)
+        return fail(PKV_ERR_INVALID_ARG, "scatter: negative size");
+    if (num_tokens == 0 || num_kv_heads == 0 || head_dim == 0) return ok();
+    if (!k_src || !v_src || !slots || !k_pool || !v_pool)
+        return fail(PKV_ERR_INVALID_ARG, "scatter: null pointer");
+    if (page_size <= 0) return fail(PKV_ERR_INVALID_ARG, "scatter: page_size must be positive");
+    if (page_stride < static_cast<int64_t>(page_size) * num_kv_heads * head_dim)
+        return fail(PKV_ERR_INVALID_ARG, "scatter: page_stride %lld smaller than a page",
+                    (long long)page_stride);
+    if (src_token_stride < 0 || src_head_stride < 0)
+        return fail(PKV_ERR_INVALID_ARG, "scatter: negative source stride");
+    if (!src_idx && num_src_rows < num_tokens)
+        return fail(PKV_ERR_INVALID_ARG, "scatter: %lld source rows for %lld tokens",
+                    (long long)num_src_rows, (long long)num_tokens);
+    if (!aligned(k_src, esz) || !aligned(v_src, esz) || !aligned(k_pool, esz) || !aligned(v_pool, esz))
+        return fail(PKV_ERR_INVALID_ARG, "scatter: pointers not aligned to the element size");
+    if ((flags & PKV_FLAG_CHECKED) && !err)
+        return fail(PKV_ERR_INVALID_ARG, "scatter: checked mode needs an error flag");
+    pkv::ScatterArgs a{k_src, v_src, num_tokens, num_src_rows, num_kv_heads, head_dim, esz,
+                       src_token_stride, src_head_stride, slots, slots2, src_idx, k_pool, v_pool,
+                       num_pages, page_size, page_stride, (flags & PKV_FLAG_CHECKED) != 0, err};
+    return from_cuda(pkv::launch_scatter(a, static_cast<cudaStream_t>(stream)), "scatter launch");
+}
+
+size_t paged_attention_workspace_size(int batch, int max_q_rows, int num_q_heads,
+                                      int num_kv_heads, int head_dim, int max_kv_len,
+                                      int num_splits, unsigned flags) {
+    if (batch <= 0 || max_q_rows <= 0 || num_q_heads <= 0 || num_kv_heads <= 0 || max_kv_len < 0)
+        return 0;
+    return plan_attention(batch, max_q_rows, num_q_heads, num_kv_heads, head_dim, max_kv_len,
+                          num_splits, flags)
+        .ws_bytes;
+}
+
+pkv_status paged_attention(const void* q, int64_t q_token_stride, int64_t q_head_stride,
+                           const void* k_pool, const void* v_pool, int64_t num_pages,
+                           int page_size, int64_t page_stride, const int32_t* block_table,
+                           int64_t block_table_stride, const int32_t* kv_lens,
+                           const int32_t* q_indptr, const int32_t* q_real, int batch,
+                           int max_q_rows, int max_kv_len, int num_q_heads, int num_kv_heads,
+                           int head_dim, pkv_mask mask, int causal_block, float scale, void* out,
+                           pkv_dtype out_dtype, float* lse, void* workspace,
+                           size_t workspace_bytes, int num_splits, unsigned flags, int32_t* err,
+                           void* stream) {
+    if (batch < 0 || max_q_rows < 0 || max_kv_len < 0 || num_q_heads < 0 || num_kv_heads < 0 ||
+        num_pages < 0 || num_splits < 0)
+        return fail(PKV_ERR_INVALID_ARG, "attention: negative size");
+    if (batch == 0 || max_q_rows == 0 || num_q_heads == 0) return ok();
+    if (num_kv_heads == 0 || num_q_heads % num_kv_heads != 0)
+        return fail(PKV_ERR_INVALID_ARG, "attention: %d query heads is not a multiple of %d K/V heads",
+                    num_q_heads, num_kv_heads);
+    if (!q || !k_pool || !v_pool || !block_table || !kv_lens || !q_indptr || !out)
+        return fail(PKV_ERR_INVALID_ARG, "attention: null pointer");
+    if (page_size != 32)
+        return fail(PKV_ERR_UNSUPPORTED, "attention: page_size %d (only 32-token pages)", page_size);
+    if (head_dim != 64 && head_dim != 128)
+        return fail(PKV_ERR_UNSUPPORTED, "attention: head_dim %d (64 or 128)", head_dim);
+    if (mask != PKV_MASK_NONE && mask != PKV_MASK_CAUSAL && mask != PKV_MASK_BLOCK_CAUSAL)
+        return fail(PKV_ERR_INVALID_ARG, "attention: unknown mask %d", (int)mask);
+    if (mask == PKV_MASK_BLOCK_CAUSAL && causal_block <= 0)
+        return fail(PKV_ERR_INVALID_ARG, "attention: block-causal mask needs causal_block > 0");
+    if (out_dtype != PKV_BF16 && out_dtype != PKV_F32)
+        return fail(PKV_ERR_UNSUPPORTED, "attention: output dtype must be bf16 or f32");
+    if (batch > 65535 || num_kv_heads > 65535)
+        return fail(PKV_ERR_UNSUPPORTED, "attention: batch or K/V heads above 65535");
+    if (page_stride < static_cast<int64_t>(page_size) * num_kv_heads * head_dim || page_stride % 8)
+        return fail(PKV_ERR_INVALID_ARG,
+                    "attention: page_stride %lld must cover a page and be a multiple of 8",
+                    (long long)page_stride);
+    if (!aligned(q, 16) || !aligned(k_pool, 16) || !aligned(v_pool, 16) || q_token_stride % 8 ||
+        q_head_stride % 8 || q_token_stride < 0 || q_head_stride < 0)
+        return fail(PKV_ERR_INVALID_ARG,
+                    "attention: q / pools must be 16-byte aligned with strides multiple of 8");
+    if (!aligned(out, out_dtype == PKV_F32 ? 16 : 8) || (lse && !aligned(lse, 4)))
+        return fail(PKV_ERR_INVALID_ARG, "attention: output misaligned");
+    const int64_t pages_needed = (static_cast<int64_t>(max_kv_len) + page_size - 1) / page_size;
+    if (block_table_stride < pages_needed)
+        return fail(PKV_ERR_INVALID_ARG, "attention: block_table_stride %lld < %lld pages for max_kv_len",
+                    (long long)block_table_stride, (long long)pages_needed);
+    if ((flags & PKV_FLAG_CHECKED) && !err)
+        return fail(PKV_ERR_INVALID_ARG, "attention: checked mode needs an error flag");
+
+    const Plan pl = plan_attention(batch, max_q_rows, num_q_heads, num_kv_heads, head_dim,
+                                   max_kv_len, num_splits, flags);
+    if (pl.ws_bytes > 0) {
+        if (!workspace || workspace_bytes < pl.ws_bytes || !aligned(workspace, 256))
+            return fail(PKV_ERR_WORKSPACE, "attention: workspace needs %zu bytes, 256-byte aligned",
+                        pl.ws_bytes);
+    }
+
+    pkv::AttnParams p{};
+    p.q = q;
+    p.q_token_stride = q_token_stride;
+    p.q_head_stride = q_head_stride;
+    p.k_pool = k_pool;
+    p.v_pool = v_pool;
+    p.num_pages = num_pages;
+    p.page_stride = page_stride;
+    p.block_table = block_table;
+    p.block_table_stride = block_table_stride;
+    p.kv_lens = kv_lens;
+    p.q_indptr = q_indptr;
+    p.q_real = q_real;
+    p.batch = batch;
+    p.max_q_rows = max_q_rows;
+    p.max_kv_len = max_kv_len;
+    p.num_q_heads = num_q_heads;
+    p.num_kv_heads = num_kv_heads;
+    p.head_dim = head_dim;
+    p.mask = static_cast<int>(mask);
+    p.causal_block = causal_block;
+    const float sc = scale > 0.f ? scale : 1.0f / std::sqrt(static_cast<float>(head_dim));
+    p.scale_log2 = sc * 1.4426950408889634f;
+    p.out = out;
+    p.out_f32 = out_dtype == PKV_F32;
+    p.lse = lse;
+    p.num_splits = pl.splits;
+    p.split_keys = pl.split_keys;
+    p.checked = (flags & PKV_FLAG_CHECKED) != 0;
+    p.err = err;
+    if (pl.splits > 1) {
+        const size_t states = static_cast<size_t>(batch) * max_q_rows * num_q_heads * pl.splits;
+        p.ws_o = static_cast<float*>(workspace);
+        p.ws_lse = reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                            round_up(states * head_dim * sizeof(float), 256));
+    }
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+    if (pl.kernel == Kernel::kSimt) return from_cuda(pkv::launch_attn_simt(p, s), "attention (simt)");
+
+    CUtensorMap tk, tv;
+    pkv_status st = make_pool_map(&tk, k_pool, head_dim, num_kv_heads, page_size, num_pages, page_stride);
+    if (st != PKV_OK) return st;
+    st = make_pool_map(&tv, v_pool, head_dim, num_kv_heads, page_size, num_pages, page_stride);
+    if (st != PKV_OK) return st;
+    cudaError_t e = pkv::launch_decode(p, &tk, &tv, s);
+    if (e != cudaSuccess) return from_cuda(e, "attention (decode)");
+    if (pl.splits > 1) return from_cuda(pkv::launch_split_reduce(p, s), "attention (split reduce)");
+    return ok();
+}
+
+pkv_status merge_attn_states(const void* o_a, const float* lse_a, const void* o_b,
+                             const float* lse_b, pkv_dtype in_dtype, int64_t rows, int num_heads,
+                             int head_dim, void* o_out, pkv_dtype out_dtype, float* lse_out,
+                             void* stream) {
+    if (rows < 0 || num_heads < 0 || head_dim < 0)
+        return fail(PKV_ERR_INVALID_ARG, "merge: negative size");
+    if (rows == 0 || num_heads == 0 || head_dim == 0) return ok();
+    if (!o_a || !lse_a || !o_b || !lse_b || !o_out)
+        return fail(PKV_ERR_INVALID_ARG, "merge: null pointer");
+    if ((in_dtype != PKV_BF16 && in_dtype != PKV_F32) || (out_dtype != PKV_BF16 && out_dtype != PKV_F32))
+        return fail(PKV_ERR_UNSUPPORTED, "merge: dtypes must be bf16 or f32");
+    if (head_dim % 4 || head_dim > 512)
+        return fail(PKV_ERR_UNSUPPORTED, "merge: head_dim %d (a multiple of 4, at most 512)", head_dim);
+    const size_t ia = in_dtype == PKV_F32 ? 16 : 8, oa = out_dtype == PKV_F32 ? 16 : 8;
+    if (!aligned(o_a, ia) || !aligned(o_b, ia) || !aligned(o_out, oa) || !aligned(lse_a, 4) ||
+        !aligned(lse_b, 4) || (lse_out && !aligned(lse_out, 4)))
+        return fail(PKV_ERR_INVALID_ARG, "merge: misaligned pointer");
+    return from_cuda(pkv::launch_merge(o_a, lse_a, o_b, lse_b, in_dtype == PKV_F32, rows, num_heads,
+                                       head_dim, o_out, out_dtype == PKV_F32, lse_out,
+                                       static_cast<cudaStream_t>(stream)),
+                     "merge launch");
+}
+
+pkv_status rotate_rows(void* x, int64_t rows, int64_t cols, int64_t row_stride, int elem_size_b,
+                       int64_t shift, void* stream) {
+    if (rows < 0 || cols < 0) return fail(PKV_ERR_INVALID_ARG, "rotate: negative size");
+    if (elem_size_b != 1 && elem_size_b != 2 && elem_size_b != 4 && elem_size_b != 8 &&
+        elem_size_b != 16)
+        return fail(PKV_ERR_UNSUPPORTED, "rotate: element size %d (1, 2, 4, 8 or 16)", elem_size_b);
+    if (rows == 0 || cols <= 1) return ok();
+    if (!x) return fail(PKV_ERR_INVALID_ARG, "rotate: null pointer");
+    if (rows > 1 && row_stride < cols)
+        return fail(PKV_ERR_INVALID_ARG, "rotate: row_stride %lld < cols %lld (rows overlap)",
+                    (long long)row_stride, (long long)cols);
+    if (!aligned(x, elem_size_b)) return fail(PKV_ERR_INVALID_ARG, "rotate: misaligned buffer");
+    int64_t sh = shift % cols;
+    if (sh < 0) sh += cols;
+    if (sh == 0) return ok();
+    // widest unit (up to 16 bytes) that divides every byte quantity involved
+    const int64_t es = elem_size_b;
+    int unit = 16;
+    for (; unit > 1; unit >>= 1) {
+        const bool fits = (cols * es) % unit == 0 && (sh * es) % unit == 0 &&
+                          (rows == 1 || (row_stride * es) % unit == 0) && aligned(x, unit);
+        if (fits) break;
+    }
+    const int64_t ucols = cols * es / unit, ushift = sh * es / unit;
+    const int64_t ustride = rows == 1 ? ucols : row_stride * es / unit;
+    return from_cuda(pkv::launch_rotate(x, rows, ucols, ustride, unit, ushift,
+                                        static_cast<cudaStream_t>(stream)),
+                     "rotate launch");
+}
+
+}  // extern "C"

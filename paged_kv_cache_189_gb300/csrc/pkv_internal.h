@@ -1,0 +1,92 @@
+// pkv_internal.h -- host-side launcher interfaces between the C-ABI layer
+// (pkv_api.cpp: validation, dispatch, tensor maps) and the kernel files.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "pkv.h"
+
+namespace pkv {
+
+// ---------------------------- scatter --------------------------------------
+struct ScatterArgs {
+    const void* k_src;
+    const void* v_src;
+    int64_t num_tokens, num_src_rows;
+    int num_kv_heads, head_dim, elem_size;
+    int64_t src_token_stride, src_head_stride;  // elements
+    const int64_t* slots;
+    const int64_t* slots2;
+    const int64_t* src_idx;
+    void* k_pool;
+    void* v_pool;
+    int64_t num_pages;
+    int page_size;
+    int64_t page_stride;  // elements
+    bool checked;
+    int32_t* err;
+};
+cudaError_t launch_scatter(const ScatterArgs& a, cudaStream_t s);
+
+// ---------------------------- rotate ---------------------------------------
+// Rotation in units of `unit` bytes (1, 2, 4, 8 or 16); cols, shift and
+// row_stride are already expressed in units, 0 < shift < cols.
+cudaError_t launch_rotate(void* x, int64_t rows, int64_t cols, int64_t row_stride, int unit,
+                          int64_t shift, cudaStream_t s);
+
+// ---------------------------- merge ----------------------------------------
+cudaError_t launch_merge(const void* o_a, const float* lse_a, const void* o_b,
+                         const float* lse_b, bool in_f32, int64_t rows, int num_heads,
+                         int head_dim, void* o_out, bool out_f32, float* lse_out,
+                         cudaStream_t s);
+
+// ---------------------------- attention ------------------------------------
+// Everything the attention kernels need, resolved on the host.
+struct AttnParams {
+    const void* q;
+    int64_t q_token_stride, q_head_stride;
+    const void* k_pool;
+    const void* v_pool;
+    int64_t num_pages;
+    int64_t page_stride;
+    const int32_t* block_table;
+    int64_t block_table_stride;
+    const int32_t* kv_lens;
+    const int32_t* q_indptr;
+    const int32_t* q_real;
+    int batch, max_q_rows, max_kv_len;
+    int num_q_heads, num_kv_heads, head_dim;
+    int mask, causal_block;
+    float scale_log2;  // softmax scale * log2(e)
+    void* out;
+    bool out_f32;
+    float* lse;
+    int num_splits;
+    int split_keys;    // keys per split (multiple of the key tile)
+    float* ws_o;       // [rows_bound][Hq][splits][D] partial outputs (splits > 1)
+    float* ws_lse;     // [rows_bound][Hq][splits]
+    bool checked;
+    int32_t* err;
+};
+
+// Decode kernel (one query row per sequence), split-KV, SIMT; K/V pages
+// arrive by TMA.  tmap_k / tmap_v are CUtensorMap (128 bytes each).
+cudaError_t launch_decode(const AttnParams& p, const void* tmap_k, const void* tmap_v,
+                          cudaStream_t s);
+bool decode_supported(int head_dim, int group);
+
+// Generic SIMT kernel: any rows, masks, group sizes; no splits.  A slow
+// cross-check of the fast kernels and the path for shapes they do not cover.
+cudaError_t launch_attn_simt(const AttnParams& p, cudaStream_t s);
+
+// Tensor-core tile kernel (tcgen05 / TMEM, TMA-fed) for many query rows.
+cudaError_t launch_attn_tc(const AttnParams& p, const void* tmap_q, const void* tmap_k,
+                           const void* tmap_v, cudaStream_t s);
+bool attn_tc_supported(int head_dim, int group);
+int attn_tc_rows_per_tile(int group);  // query tokens per 128-row tile
+
+// n-way merge of split partials into out / lse.
+cudaError_t launch_split_reduce(const AttnParams& p, cudaStream_t s);
+
+}  // namespace pkv

@@ -1,0 +1,178 @@
+"""Python binding of the C ABI in ``include/pkv.h`` (ctypes).
+
+Argument marshalling only: every function here turns torch tensors into the
+pointers, sizes and strides the C entry point takes and raises on a non-OK
+status.  All arithmetic runs in the CUDA kernels of ``libpkv.so``; if the
+library has not been built this module raises instead of falling back to
+anything else.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from .build import LIB_PATH
+
+PKV_OK, PKV_ERR_INVALID_ARG, PKV_ERR_UNSUPPORTED, PKV_ERR_WORKSPACE, PKV_ERR_CUDA = range(5)
+PKV_BF16, PKV_F16, PKV_F32 = range(3)
+MASKS = {"none": 0, "causal": 1, "block_causal": 2}
+PKV_FLAG_CHECKED = 0x1
+PKV_FLAG_SIMT_ONLY = 0x2
+PKV_ERRBIT_SLOT, PKV_ERRBIT_SRC, PKV_ERRBIT_PAGE, PKV_ERRBIT_LEN, PKV_ERRBIT_TIMEOUT = (
+    0x1, 0x2, 0x4, 0x8, 0x10)
+
+# every symbol include/pkv.h declares
+EXPORTED = ("pkv_status_string", "pkv_last_error", "kv_scatter_slots",
+            "paged_attention_workspace_size", "paged_attention", "merge_attn_states",
+            "rotate_rows")
+
+_vp, _i64, _i32, _u32, _f32, _sz = (ctypes.c_void_p, ctypes.c_int64, ctypes.c_int,
+                                    ctypes.c_uint, ctypes.c_float, ctypes.c_size_t)
+_SIGNATURES = {
+    "pkv_status_string": (ctypes.c_char_p, [_i32]),
+    "pkv_last_error": (ctypes.c_char_p, []),
+    "kv_scatter_slots": (_i32, [_vp, _vp, _i64, _i64, _i32, _i32, _i64, _i64, _vp, _vp, _vp,
+                                _vp, _vp, _i64, _i32, _i64, _i32, _u32, _vp, _vp]),
+    "paged_attention_workspace_size": (_sz, [_i32, _i32, _i32, _i32, _i32, _i32, _i32, _u32]),
+    "paged_attention": (_i32, [_vp, _i64, _i64, _vp, _vp, _i64, _i32, _i64, _vp, _i64, _vp, _vp,
+                               _vp, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _f32, _vp,
+                               _i32, _vp, _vp, _sz, _i32, _u32, _vp, _vp]),
+    "merge_attn_states": (_i32, [_vp, _vp, _vp, _vp, _i32, _i64, _i32, _i32, _vp, _i32, _vp,
+                                 _vp]),
+    "rotate_rows": (_i32, [_vp, _i64, _i64, _i64, _i32, _i64, _vp]),
+}
+
+_lib = None
+
+
+class PkvError(RuntimeError):
+    def __init__(self, func, status, message):
+        self.status = status
+        super().__init__(f"{func}: {status_string(status)}: {message}")
+
+
+def lib(path: str | None = None) -> ctypes.CDLL:
+    """The loaded library with its C signatures declared."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or LIB_PATH
+    if not os.path.exists(p):
+        raise RuntimeError(f"libpkv.so is not built ({p}); call __graft_entry__.build() or "
+                           "paged_kv_cache_189_gb300.build.build() first")
+    L = ctypes.CDLL(p)
+    for name, (res, args) in _SIGNATURES.items():
+        fn = getattr(L, name)
+        fn.restype = res
+        fn.argtypes = args
+    if path is None:
+        _lib = L
+    return L
+
+
+def status_string(status: int) -> str:
+    return lib().pkv_status_string(status).decode()
+
+
+def last_error() -> str:
+    return lib().pkv_last_error().decode()
+
+
+def _check(func, status):
+    if status != PKV_OK:
+        raise PkvError(func, status, last_error())
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, torch.cuda.Stream):
+        return ctypes.c_void_p(stream.cuda_stream)
+    return ctypes.c_void_p(stream)
+
+
+def _dtype(t):
+    return {torch.bfloat16: PKV_BF16, torch.float16: PKV_F16, torch.float32: PKV_F32}[t.dtype]
+
+
+def _pool_geometry(pool):
+    """[num_pages, page_size, Hkv, D] with dense slots; page stride may be larger."""
+    assert pool.dim() == 4, "pool must be [num_pages, page_size, num_kv_heads, head_dim]"
+    n, P, H, D = pool.shape
+    if pool.stride(3) != 1 or pool.stride(2) != D or pool.stride(1) != H * D:
+        raise ValueError("pool slots must be dense [num_kv_heads, head_dim] rows")
+    return n, P, H, D, pool.stride(0)
+
+
+# ----------------------------------------------------------------------------
+def kv_scatter_slots(k_src, v_src, slots, k_pool, v_pool, slots2=None, src_idx=None,
+                     checked=False, err=None, stream=None):
+    """Write rows of ``k_src``/``v_src`` ``[T, Hkv, D]`` (any token/head stride,
+    unit dim stride) into pool slots ``slots`` (and ``slots2``) in place."""
+    assert k_src.stride() == v_src.stride() and k_src.shape == v_src.shape
+    assert k_src.stride(2) == 1
+    n, P, H, D, page_stride = _pool_geometry(k_pool)
+    assert v_pool.shape == k_pool.shape and v_pool.stride() == k_pool.stride()
+    T = slots.numel()
+    st = lib().kv_scatter_slots(
+        _ptr(k_src), _ptr(v_src), T, k_src.shape[0], H, D, k_src.stride(0), k_src.stride(1),
+        _ptr(slots), _ptr(slots2), _ptr(src_idx), _ptr(k_pool), _ptr(v_pool), n, P, page_stride,
+        _dtype(k_pool), PKV_FLAG_CHECKED if checked else 0, _ptr(err), _stream(stream))
+    _check("kv_scatter_slots", st)
+
+
+def paged_attention_workspace_size(batch, max_q_rows, num_q_heads, num_kv_heads, head_dim,
+                                   max_kv_len, num_splits=0, flags=0) -> int:
+    return int(lib().paged_attention_workspace_size(batch, max_q_rows, num_q_heads, num_kv_heads,
+                                                    head_dim, max_kv_len, num_splits, flags))
+
+
+def paged_attention(q, k_pool, v_pool, block_table, kv_lens, q_indptr, out, *, q_real=None,
+                    lse=None, batch=None, max_q_rows, max_kv_len, mask="causal",
+                    causal_block=0, scale=0.0, workspace=None, num_splits=0, flags=0, err=None,
+                    stream=None):
+    """Paged attention of packed query rows ``q [rows, Hq, D]`` (bf16) into
+    ``out [rows, Hq, D]`` (bf16 or f32) and ``lse [rows, Hq]`` (f32)."""
+    n, P, H, D, page_stride = _pool_geometry(k_pool)
+    assert v_pool.shape == k_pool.shape and v_pool.stride() == k_pool.stride()
+    assert q.stride(2) == 1 and out.is_contiguous()
+    if batch is None:
+        batch = kv_lens.numel()
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = lib().paged_attention(
+        _ptr(q), q.stride(0), q.stride(1), _ptr(k_pool), _ptr(v_pool), n, P, page_stride,
+        _ptr(block_table), block_table.stride(0), _ptr(kv_lens), _ptr(q_indptr), _ptr(q_real),
+        batch, max_q_rows, max_kv_len, q.shape[1], H, D, MASKS[mask], causal_block,
+        float(scale), _ptr(out), _dtype(out), _ptr(lse), _ptr(workspace), ws_bytes, num_splits,
+        flags, _ptr(err), _stream(stream))
+    _check("paged_attention", st)
+
+
+def merge_attn_states(o_a, lse_a, o_b, lse_b, o_out, lse_out=None, stream=None):
+    """Exact LSE merge of two states ``[rows, heads, D]`` into ``o_out``."""
+    rows, heads, D = o_a.shape
+    assert o_b.shape == o_a.shape and o_out.shape == o_a.shape and o_a.dtype == o_b.dtype
+    st = lib().merge_attn_states(_ptr(o_a), _ptr(lse_a), _ptr(o_b), _ptr(lse_b), _dtype(o_a),
+                                 rows, heads, D, _ptr(o_out), _dtype(o_out), _ptr(lse_out),
+                                 _stream(stream))
+    _check("merge_attn_states", st)
+
+
+def rotate_rows(x, shift, rows=None, cols=None, row_stride=None, elem_size=None, stream=None):
+    """Rotate every row of ``x`` left by ``shift`` elements in place.  By
+    default ``x`` is viewed as ``[rows, cols]`` of its own element type."""
+    if rows is None:
+        if x.dim() == 1:
+            rows, cols, row_stride = 1, x.shape[0], x.shape[0]
+        else:
+            assert x.dim() == 2 and x.stride(1) == 1
+            rows, cols, row_stride = x.shape[0], x.shape[1], x.stride(0)
+        elem_size = x.element_size()
+    st = lib().rotate_rows(_ptr(x), rows, cols, row_stride, elem_size, shift, _stream(stream))
+    _check("rotate_rows", st)

@@ -1,0 +1,116 @@
+"""CPU-only checks of the C ABI: the library builds for sm_103a, loads without
+a GPU, exports every function include/pkv.h declares, and rejects bad
+arguments on the host before touching CUDA (no compute calls here)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from paged_kv_cache_189_gb300 import build as pkv_build
+from paged_kv_cache_189_gb300 import pkv
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+FAKE = ctypes.c_void_p(0x1000)  # never dereferenced: validation fails first
+
+
+@pytest.fixture(scope="module")
+def L():
+    pkv_build.build()
+    return pkv.lib()
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "pkv.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"\b([a-z_][a-z0-9_]*)\s*\(", text)
+    keywords = {"if", "sizeof", "defined", "extern"}
+    return sorted({n for n in names if n not in keywords})
+
+
+def test_exports_every_declared_function(L):
+    decl = declared_functions()
+    assert set(decl) == set(pkv.EXPORTED), decl
+    for name in decl:
+        assert hasattr(L, name), name
+
+
+def test_status_strings(L):
+    assert pkv.status_string(0) == "PKV_OK"
+    assert pkv.status_string(pkv.PKV_ERR_UNSUPPORTED) == "PKV_ERR_UNSUPPORTED"
+
+
+def _attn(L, **kw):
+    a = dict(q=FAKE, qts=32 * 128, qhs=128, k=FAKE, v=FAKE, pages=10, ps=32, pstride=32 * 8 * 128,
+             bt=FAKE, bts=4, kl=FAKE, qi=FAKE, qr=None, batch=2, mq=1, mk=100, hq=32, hkv=8,
+             d=128, mask=1, cb=0, scale=0.0, out=FAKE, odt=0, lse=None, ws=None, wsb=0,
+             splits=0, flags=0, err=None)
+    a.update(kw)
+    return L.paged_attention(a["q"], a["qts"], a["qhs"], a["k"], a["v"], a["pages"], a["ps"],
+                             a["pstride"], a["bt"], a["bts"], a["kl"], a["qi"], a["qr"], a["batch"],
+                             a["mq"], a["mk"], a["hq"], a["hkv"], a["d"], a["mask"], a["cb"],
+                             a["scale"], a["out"], a["odt"], a["lse"], a["ws"], a["wsb"],
+                             a["splits"], a["flags"], a["err"], None)
+
+
+def test_attention_host_validation(L):
+    assert _attn(L, ps=16) == pkv.PKV_ERR_UNSUPPORTED
+    assert "page" in pkv.last_error()
+    assert _attn(L, d=96) == pkv.PKV_ERR_UNSUPPORTED
+    assert _attn(L, hq=30) == pkv.PKV_ERR_INVALID_ARG
+    assert _attn(L, mask=2, cb=0) == pkv.PKV_ERR_INVALID_ARG
+    assert _attn(L, mask=7) == pkv.PKV_ERR_INVALID_ARG
+    assert _attn(L, bts=2, mk=100) == pkv.PKV_ERR_INVALID_ARG      # 100 keys need 4 pages
+    assert _attn(L, pstride=100) == pkv.PKV_ERR_INVALID_ARG
+    assert _attn(L, q=ctypes.c_void_p(0x1002)) == pkv.PKV_ERR_INVALID_ARG  # misaligned
+    assert _attn(L, q=None) == pkv.PKV_ERR_INVALID_ARG
+    assert _attn(L, flags=pkv.PKV_FLAG_CHECKED, err=None) == pkv.PKV_ERR_INVALID_ARG
+    assert _attn(L, odt=pkv.PKV_F16) == pkv.PKV_ERR_UNSUPPORTED
+    # split-KV needs a workspace: 3000 keys -> 6 splits of 512
+    assert _attn(L, mk=3000, bts=94) == pkv.PKV_ERR_WORKSPACE
+    # empty problems return OK without touching the device
+    assert _attn(L, batch=0) == pkv.PKV_OK
+    assert _attn(L, mq=0) == pkv.PKV_OK
+
+
+def test_workspace_size(L):
+    # one split when everything fits in 512 keys: no workspace
+    assert pkv.paged_attention_workspace_size(64, 1, 32, 8, 128, 512) == 0
+    ws = pkv.paged_attention_workspace_size(64, 1, 32, 8, 128, 8193)
+    splits = 17
+    states = 64 * 32 * splits
+    assert ws >= states * 128 * 4 + states * 4
+    assert pkv.paged_attention_workspace_size(0, 1, 32, 8, 128, 8193) == 0
+
+
+def test_scatter_host_validation(L):
+    def sc(**kw):
+        a = dict(ks=FAKE, vs=FAKE, T=4, nsrc=4, h=2, d=64, ts=128, hs=64, sl=FAKE, sl2=None,
+                 idx=None, kp=FAKE, vp=FAKE, pages=2, ps=32, pstride=32 * 128, dt=0, flags=0,
+                 err=None)
+        a.update(kw)
+        return L.kv_scatter_slots(a["ks"], a["vs"], a["T"], a["nsrc"], a["h"], a["d"], a["ts"],
+                                  a["hs"], a["sl"], a["sl2"], a["idx"], a["kp"], a["vp"],
+                                  a["pages"], a["ps"], a["pstride"], a["dt"], a["flags"], a["err"],
+                                  None)
+    assert sc(T=0) == pkv.PKV_OK
+    assert sc(sl=None) == pkv.PKV_ERR_INVALID_ARG
+    assert sc(pstride=100) == pkv.PKV_ERR_INVALID_ARG
+    assert sc(nsrc=2) == pkv.PKV_ERR_INVALID_ARG
+    assert sc(dt=9) == pkv.PKV_ERR_INVALID_ARG
+    assert sc(flags=pkv.PKV_FLAG_CHECKED) == pkv.PKV_ERR_INVALID_ARG
+    assert sc(ks=ctypes.c_void_p(0x1001)) == pkv.PKV_ERR_INVALID_ARG
+
+
+def test_rotate_and_merge_host_validation(L):
+    assert L.rotate_rows(FAKE, 3, 10, 10, 3, 1, None) == pkv.PKV_ERR_UNSUPPORTED
+    assert L.rotate_rows(FAKE, 0, 10, 10, 4, 1, None) == pkv.PKV_OK      # no rows: no launch
+    assert L.rotate_rows(FAKE, 3, 1, 1, 4, 1, None) == pkv.PKV_OK        # one column: no launch
+    assert L.rotate_rows(FAKE, 3, 10, 10, 4, 20, None) == pkv.PKV_OK     # shift = 0 mod cols
+    assert L.rotate_rows(FAKE, 3, 10, 5, 4, 1, None) == pkv.PKV_ERR_INVALID_ARG
+    assert L.rotate_rows(None, 3, 10, 10, 4, 1, None) == pkv.PKV_ERR_INVALID_ARG
+    assert L.merge_attn_states(FAKE, FAKE, FAKE, FAKE, 0, 0, 4, 64, FAKE, 0, None, None) == pkv.PKV_OK
+    assert L.merge_attn_states(FAKE, FAKE, FAKE, FAKE, 0, 3, 4, 66, FAKE, 0, None, None) == \
+        pkv.PKV_ERR_UNSUPPORTED
+    assert L.merge_attn_states(FAKE, None, FAKE, FAKE, 0, 3, 4, 64, FAKE, 0, None, None) == \
+        pkv.PKV_ERR_INVALID_ARG

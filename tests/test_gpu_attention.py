@@ -1,0 +1,165 @@
+"""GPU parity of paged_attention (through the C-ABI) against the fp64 oracle.
+
+Tolerances (bf16 output vs fp64): max-abs 1e-2, mean-abs 1e-3, LSE 1e-3.
+Covers the decode kernel (split-KV and single split), the generic SIMT
+kernel, padding rows, empty sequences, page-permutation invariance (bit
+identical GPU outputs), checked mode, and the full-size decode workload."""
+import numpy as np
+import pytest
+import torch
+
+from oracle import oracle as orc
+from paged_kv_cache_189_gb300 import pkv, workloads as wl
+from pkv_testutil import assert_attention_close, gpu_step, oracle_step
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def test_tiny_decode_workload():
+    c = wl.tiny_decode()
+    out, lse, kg, vg, err = gpu_step(c)
+    O, L, kb, vb = oracle_step(c)
+    assert err == 0
+    assert_attention_close(out, lse, O, L, c)
+    np.testing.assert_array_equal(orc.bf16_bits(kg.cpu()), kb)
+    np.testing.assert_array_equal(orc.bf16_bits(vg.cpu()), vb)
+
+
+def test_tiny_decode_scatter_into_free_slots():
+    """The tiny workload's standalone scatter of two new rows into random free
+    slots: bit exact, and attention over the untouched sequences unchanged."""
+    c = wl.tiny_decode()
+    free = c.extra["free_slots"]
+    kg, vg = c.k_pool.to(DEV), c.v_pool.to(DEV)
+    pkv.kv_scatter_slots(c.new_k.to(DEV), c.new_v.to(DEV), free.to(DEV), kg, vg)
+    ko, vo, _ = orc.kv_scatter_slots(orc.bf16_bits(c.new_k), orc.bf16_bits(c.new_v), free.numpy(),
+                                     orc.bf16_bits(c.k_pool), orc.bf16_bits(c.v_pool))
+    np.testing.assert_array_equal(orc.bf16_bits(kg.cpu()), ko)
+    np.testing.assert_array_equal(orc.bf16_bits(vg.cpu()), vo)
+
+
+@pytest.mark.parametrize("Hq,Hkv,D", [(32, 8, 128), (8, 4, 128), (8, 8, 128), (4, 2, 64),
+                                      (16, 4, 64), (6, 6, 64)])
+@pytest.mark.parametrize("num_splits", [0, 1, 3])
+def test_decode_random(Hq, Hkv, D, num_splits):
+    c = wl.random_case(100 + Hq + D + num_splits, batch=7, Hq=Hq, Hkv=Hkv, D=D,
+                       kv_range=(1, 1500))
+    out, lse, *_ , err = gpu_step(c, num_splits=num_splits)
+    O, L, *_ = oracle_step(c)
+    assert err == 0
+    assert_attention_close(out, lse, O, L, c)
+
+
+def test_decode_f32_output_and_padding_rows():
+    """One-row sequences whose row is padding (q_real = 0) come back zero."""
+    c = wl.random_case(7, batch=6, Hq=32, Hkv=8, D=128, kv_range=(30, 700))
+    c.q_real[1] = 0
+    c.q_real[4] = 0
+    c.slots[1] = -1
+    c.slots[4] = -1
+    out, lse, *_ , err = gpu_step(c, out_dtype=torch.float32)
+    O, L, *_ = oracle_step(c)
+    assert_attention_close(out, lse, O, L, c)
+    assert (out[1] == 0).all() and (out[4] == 0).all()
+
+
+def test_decode_peaked_queries():
+    """Scaled-up queries concentrate the softmax, so a wrong visible set or a
+    wrong page shows up beyond the tolerance even at long lengths."""
+    c = wl.random_case(11, batch=5, Hq=32, Hkv=8, D=128, kv_range=(1000, 5000), q_scale=8.0)
+    out, lse, *_ = gpu_step(c)
+    O, L, *_ = oracle_step(c)
+    assert_attention_close(out, lse, O, L, c)
+
+
+def test_decode_page_permutation_bit_identical():
+    c = wl.random_case(12, batch=4, Hq=32, Hkv=8, D=128, kv_range=(100, 3000))
+    out1, lse1, *_ = gpu_step(c)
+    rng = np.random.default_rng(3)
+    perm = torch.from_numpy(rng.permutation(c.num_pages))
+    k2 = torch.empty_like(c.k_pool); k2[perm] = c.k_pool
+    v2 = torch.empty_like(c.v_pool); v2[perm] = c.v_pool
+    t = c.block_table.clone()
+    t[t >= 0] = perm[t[t >= 0].long()].to(torch.int32)
+    s = c.slots.clone()
+    s[s >= 0] = perm[s[s >= 0] // 32] * 32 + s[s >= 0] % 32
+    c.k_pool, c.v_pool, c.block_table, c.slots = k2, v2, t, s
+    out2, lse2, *_ = gpu_step(c)
+    assert torch.equal(out1, out2)
+    assert torch.equal(lse1, lse2)
+
+
+def test_decode_zero_length_and_empty_sequences():
+    c = wl.random_case(13, batch=4, Hq=8, Hkv=2, D=128, kv_range=(5, 60))
+    # sequence 2 has no keys at all (its only row is padding)
+    c.kv_lens[2] = 0
+    c.q_real[2] = 0
+    c.slots[2] = -1
+    out, lse, *_ = gpu_step(c)
+    O, L, *_ = oracle_step(c)
+    assert_attention_close(out, lse, O, L, c)
+
+
+def test_decode_checked_mode_bad_page_flags_error():
+    c = wl.random_case(14, batch=3, Hq=8, Hkv=2, D=128, kv_range=(40, 90))
+    c.block_table[1, 0] = c.num_pages + 5
+    *_, err = gpu_step(c, scatter=False, checked=True)
+    assert err & pkv.PKV_ERRBIT_PAGE
+
+
+def test_decode_graph_capture_replay():
+    """The call is capturable: a graph replays with new device contents."""
+    c = wl.random_case(15, batch=8, Hq=32, Hkv=8, D=128, kv_range=(600, 2000))
+    k_pool, v_pool = c.k_pool.to(DEV), c.v_pool.to(DEV)
+    q = c.q.to(DEV)
+    bt, kl, qi, qr = (c.block_table.to(DEV), c.kv_lens.to(DEV), c.q_indptr.to(DEV),
+                      c.q_real.to(DEV))
+    rows, Hq, D = q.shape
+    out = torch.empty(rows, Hq, D, dtype=torch.bfloat16, device=DEV)
+    lse = torch.empty(rows, Hq, device=DEV)
+    ws = torch.empty(pkv.paged_attention_workspace_size(c.batch, 1, Hq, 8, D, 2000), dtype=torch.uint8,
+                     device=DEV)
+    s = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        pkv.paged_attention(q, k_pool, v_pool, bt, kl, qi, out, q_real=qr, lse=lse, max_q_rows=1,
+                            max_kv_len=2000, workspace=ws)  # warm-up outside capture
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g, stream=s):
+            pkv.paged_attention(q, k_pool, v_pool, bt, kl, qi, out, q_real=qr, lse=lse,
+                                max_q_rows=1, max_kv_len=2000, workspace=ws)
+    q2 = wl.randn_bf16(tuple(q.shape), torch.Generator().manual_seed(99))
+    q.copy_(q2.to(DEV))
+    g.replay()
+    torch.cuda.synchronize()
+    c.q = q2
+    O, L, *_ = oracle_step(c, scatter=False)
+    assert_attention_close(out, lse, O, L, c)
+
+
+@pytest.mark.parametrize("mask,cb", [("causal", 0), ("block_causal", 5), ("none", 0)])
+def test_simt_kernel_multi_row(mask, cb):
+    c = wl.random_case(20, batch=4, Hq=8, Hkv=2, D=128, kv_range=(20, 400), q_range=(1, 40),
+                       pad_range=(0, 5), mask=mask, causal_block=cb)
+    out, lse, *_ = gpu_step(c, flags=pkv.PKV_FLAG_SIMT_ONLY)
+    O, L, *_ = oracle_step(c)
+    assert_attention_close(out, lse, O, L, c)
+
+
+def test_simt_kernel_matches_decode_kernel():
+    c = wl.random_case(21, batch=6, Hq=32, Hkv=8, D=128, kv_range=(50, 2500))
+    o1, l1, *_ = gpu_step(c)
+    o2, l2, *_ = gpu_step(c, flags=pkv.PKV_FLAG_SIMT_ONLY)
+    assert (o1.float() - o2.float()).abs().max().item() <= 1e-2
+    assert (l1 - l2).abs().max().item() <= 1e-3
+
+
+def test_gqa_decode_full_size():
+    """The GQA decode workload at its full size (64 sequences of up to 8193
+    keys, 32/8 heads): every output row against the oracle."""
+    c = wl.gqa_decode()
+    out, lse, kg, vg, err = gpu_step(c)
+    O, L, *_ = oracle_step(c)
+    assert err == 0
+    assert_attention_close(out, lse, O, L, c)
