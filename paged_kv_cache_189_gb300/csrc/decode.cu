@@ -3,31 +3,37 @@
 // "Paged causal K/V cache and cached attention for VisualGen", Description,
 // Attention (paged attention over 32-token pages through the block table,
 // real-token seq_len, zeroed padding rows) and "Support shared-prefix attention
-// for n-sample requests in FMHA", split-KV commit notes (when a batch cannot
-// fill the GPU, cut every row's keys into chunks of at least 512 tokens,
-// attend each chunk, then merge the chunk states by LSE).
+// for n-sample requests in FMHA", split-KV commit notes (cut every row's keys
+// into chunks of at least 512 tokens, attend each chunk, merge the chunk
+// states by LSE; a merge that walks every split per (token, heads)).
 //
-// Decode is bound by HBM: every K/V byte is read once and used for Hq/Hkv
-// query heads.  The GB300 design:
-//  * grid (split, K/V head, sequence); a split is 512 keys = 16 pages; CTAs
-//    whose split lies past the sequence's length exit at once, so the grid is
-//    sized from the host bound max_kv_len and stays graph-capturable.
-//  * one producer warp streams whole pages of one K/V head (32 x D of K and
-//    of V, two TMA boxes per 128 columns with 128-byte swizzling) into a
-//    4-stage shared-memory ring, completion on mbarriers.
+// Decode is bound by HBM: every K/V byte is read once and used for the
+// G = Hq/Hkv query heads that share it.  The GB300 design:
+//  * work unit = (split of 512 keys = 16 pages, K/V head, sequence).  Units are
+//    numbered split-major and handed out by an atomic ticket, so the kernel is
+//    persistent (a few CTAs per SM) and balances ragged lengths dynamically;
+//    the grid never depends on device lengths, so a call is graph-capturable.
+//  * one producer lane per CTA fetches tickets, skips units past a sequence's
+//    length, copies the unit's G query rows into shared memory with bulk
+//    copies, and streams the unit's pages of one K/V head (32 x D of K and of
+//    V, 64-column TMA boxes, 128-byte swizzle) into a 4-stage ring.  It runs
+//    ahead across unit boundaries, so the ring stays full while the consumers
+//    finish a unit.
 //  * four consumer warps each own 8 of a page's 32 keys (rows 8w..8w+7) and
-//    keep their own online-softmax state over their keys, so no cross-warp
-//    synchronisation is needed per page; the four states are merged once at
-//    the end.
-//  * QK: lane = (key k of 4, segment s of 8); a segment is 16 (D=128) or 8
-//    (D=64) dims whose query values live in registers for the whole call; the
-//    segment-to-chunk assignment makes every 8-lane phase of a 16-byte shared
-//    load hit 8 distinct bank groups under the swizzle.  Partial dots are
-//    summed across the 8 segments with shuffles.
+//    keep their own online softmax over those keys; their states are merged in
+//    shared memory once per unit.
+//  * QK: lane = (key of 4, segment of 8 x 16 dims); query values live in
+//    registers for the whole unit; the segment-to-chunk assignment makes every
+//    8-lane phase of a 16-byte shared load hit 8 distinct bank groups under
+//    the swizzle; packed fp32x2 FMAs; partial dots summed with shuffles.
 //  * PV: lane owns D/32 consecutive output dims for all G heads; the
-//    probabilities are broadcast through a small shared buffer.
+//    probabilities are broadcast as duplicated pairs through shared memory so
+//    the packed FMAs need no register moves.
+//  * split merge fused in: each split writes its (O, LSE) partial, and the
+//    last split of a (sequence, K/V head) to finish (an atomic count) merges
+//    all of them into the output.  No second kernel.
 //  * fp32 accumulation, base-2 online softmax with the scale folded into q,
-//    the running output rescaled only when the running maximum moves.
+//    output rescaled only when a warp's running maximum moves.
 #include <cuda.h>
 
 #include "pkv_common.cuh"
@@ -36,10 +42,22 @@
 namespace pkv {
 namespace {
 
+#ifndef PKV_DECODE_STAGES
+#define PKV_DECODE_STAGES 4
+#endif
+#ifndef PKV_DECODE_MIN_BLOCKS
+#define PKV_DECODE_MIN_BLOCKS 3
+#endif
+
 constexpr int kPage = 32;
-constexpr int kWarps = 4;       // consumer warps
-constexpr int kStages = 4;      // pages in flight per CTA
+constexpr int kWarps = 4;                      // consumer warps
+constexpr int kStages = PKV_DECODE_STAGES;     // pages in flight per CTA
+constexpr int kMinBlocks = PKV_DECODE_MIN_BLOCKS;  // CTAs per SM the sizes are chosen for
 constexpr int kThreads = (kWarps + 1) * 32;
+
+struct UnitDesc {
+    int b, kvh, split, key_begin, key_end, r0, nsplit, pad;
+};
 
 template <int D, int G>
 struct DecodeSmem {
@@ -47,329 +65,507 @@ struct DecodeSmem {
     static constexpr int kTileBytes = kPage * D * 2;          // one page-head of K (or V)
     static constexpr int kStageBytes = 2 * kTileBytes;
     static constexpr int kRingBytes = kStages * kStageBytes;
-    static constexpr int kPbufOff = kRingBytes;                // [warps][8 keys][G] f32
-    static constexpr int kPbufBytes = kWarps * 8 * G * 4;
-    static constexpr int kRedOff = kPbufOff + kPbufBytes;      // m, l: [warps][G] f32 each
-    static constexpr int kRedBytes = 2 * kWarps * G * 4;
-    static constexpr int kBarOff = (kRedOff + kRedBytes + 7) & ~7;
-    static constexpr int kBytes = kBarOff + 2 * kStages * 8;
-    static constexpr int kAlloc = kBytes + 1024;               // slack for 1024-byte alignment
-    static_assert(kWarps * G * D * 4 <= kRingBytes, "output reduction reuses the ring");
+    static constexpr int kRedHeads = G < 2 ? G : 2;            // heads per output-merge round
+    static constexpr int kQbufOff = kRingBytes;                // [2 slots][G][D] bf16
+    static constexpr int kQbufBytes = 2 * G * D * 2;
+    static constexpr int kRedOOff = kQbufOff + kQbufBytes;     // [warps][kRedHeads][D] f32
+    static constexpr int kRedOBytes = kWarps * kRedHeads * D * 4;
+    static constexpr int kPbufOff = kRedOOff + kRedOBytes;     // per warp: [8 keys][G] float2 + [G] alpha
+    static constexpr int kPbufWarp = 8 * G * 8 + G * 4;
+    static constexpr int kPbufBytes = kWarps * ((kPbufWarp + 15) & ~15);
+    static constexpr int kRedMLOff = kPbufOff + kPbufBytes;    // m, l: [warps][G] f32
+    static constexpr int kRedMLBytes = 2 * kWarps * G * 4;
+    static constexpr int kDescOff = kRedMLOff + kRedMLBytes;   // 2 UnitDesc + flags
+    static constexpr int kDescBytes = 2 * sizeof(UnitDesc) + 16;
+    static constexpr int kBarOff = (kDescOff + kDescBytes + 7) & ~7;
+    static constexpr int kBytes = kBarOff + (2 * kStages + 4) * 8;
+    // 228 KiB of shared memory per SM, 1 KiB of it reserved per CTA
+    static_assert(kBytes <= (228 / kMinBlocks - 1) * 1024, "CTAs per SM must fit in shared memory");
 };
 
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        ::"r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ void consumer_sync() {
+    asm volatile("bar.sync 1, %0;" ::"r"(kWarps * 32) : "memory");
+}
+
+// Sum each of the G per-lane partial dots over the 8 lanes of a key group
+// (lanes differing in bits 0..2) and leave one head's total per lane:
+// a transpose-style butterfly (G=4: 4 shuffles instead of 12).  The head a
+// lane ends with is head_of_lane<G>(seg).
+template <int G>
+__device__ __forceinline__ float reduce_heads(const float (&v)[G], int seg) {
+    if constexpr (G == 4) {
+        const bool hi = seg & 4;
+        float k0 = hi ? v[2] : v[0], k1 = hi ? v[3] : v[1];
+        const float s0 = hi ? v[0] : v[2], s1 = hi ? v[1] : v[3];
+        k0 += __shfl_xor_sync(0xffffffffu, s0, 4);
+        k1 += __shfl_xor_sync(0xffffffffu, s1, 4);
+        const bool hi2 = seg & 2;
+        float k = hi2 ? k1 : k0;
+        const float sn = hi2 ? k0 : k1;
+        k += __shfl_xor_sync(0xffffffffu, sn, 2);
+        k += __shfl_xor_sync(0xffffffffu, k, 1);
+        return k;
+    } else if constexpr (G == 2) {
+        const bool hi = seg & 4;
+        float k = hi ? v[1] : v[0];
+        const float sn = hi ? v[0] : v[1];
+        k += __shfl_xor_sync(0xffffffffu, sn, 4);
+        k += __shfl_xor_sync(0xffffffffu, k, 2);
+        k += __shfl_xor_sync(0xffffffffu, k, 1);
+        return k;
+    } else {
+        float k = v[0];
+        k += __shfl_xor_sync(0xffffffffu, k, 4);
+        k += __shfl_xor_sync(0xffffffffu, k, 2);
+        k += __shfl_xor_sync(0xffffffffu, k, 1);
+        return k;
+    }
+}
+template <int G>
+__device__ __forceinline__ int head_of_lane(int seg) {
+    return G == 4 ? (seg >> 1) : (G == 2 ? (seg >> 2) : 0);
+}
+
+// Per-warp running state: the lane's own head (max, sum over this warp's
+// keys) and the lane's output dims for every head.
+template <int G, int DPL>
+struct WarpState {
+    float m, l;
+    float2 o2[G][DPL / 2];
+};
+
+// One page for one consumer warp.  FULL: all 32 keys of the page are valid.
+template <int D, int G, bool FULL>
+__device__ __forceinline__ void decode_page(WarpState<G, D / 32>& ws, const float2 (&q2)[G][D / 16],
+                                            const uint8_t* K, const uint8_t* V, float2* pb,
+                                            float* alpha_buf, int warp, int kk, int seg, int lane,
+                                            int nvalid_rows) {
+    constexpr int kDPL = D / 32;
+    const int half = (D == 128) ? (seg >> 2) : 0;
+    const int c0 = (D == 128) ? ((seg & 3) + 4 * (seg >> 2)) : seg;
+    const int hg = head_of_lane<G>(seg);
+    const bool rep = (seg & (8 / G - 1)) == 0;  // one lane per (key, head) publishes
+
+    float s[2];
+#pragma unroll
+    for (int pass = 0; pass < 2; ++pass) {
+        const int row = warp * 8 + pass * 4 + kk;
+        float2 acc[G];
+#pragma unroll
+        for (int g = 0; g < G; ++g) acc[g] = make_float2(0.f, 0.f);
+        {
+            const uint4 a = *reinterpret_cast<const uint4*>(K + half * 4096 + sw128_offset(row, c0));
+            const uint32_t w[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const float2 kv = make_float2(bf16lo(w[j]), bf16hi(w[j]));
+#pragma unroll
+                for (int g = 0; g < G; ++g) acc[g] = __ffma2_rn(q2[g][j], kv, acc[g]);
+            }
+        }
+        if constexpr (D == 128) {
+            const uint4 a = *reinterpret_cast<const uint4*>(K + half * 4096 + sw128_offset(row, c0 ^ 4));
+            const uint32_t w[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const float2 kv = make_float2(bf16lo(w[j]), bf16hi(w[j]));
+#pragma unroll
+                for (int g = 0; g < G; ++g) acc[g] = __ffma2_rn(q2[g][4 + j], kv, acc[g]);
+            }
+        }
+        float part[G];
+#pragma unroll
+        for (int g = 0; g < G; ++g) part[g] = acc[g].x + acc[g].y;
+        const float t = reduce_heads<G>(part, seg);
+        s[pass] = (FULL || (pass * 4 + kk) < nvalid_rows) ? t : -INFINITY;
+    }
+
+    // online softmax of the lane's head over this warp's 8 keys
+    float mx = fmaxf(s[0], s[1]);
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+    const float m_new = fmaxf(ws.m, mx);
+    float p0 = 0.f, p1 = 0.f, alpha = 1.f;
+    if (m_new != -INFINITY) {
+        alpha = fast_exp2(ws.m - m_new);  // 0 on the first keys, 1 if unchanged
+        p0 = fast_exp2(s[0] - m_new);
+        p1 = fast_exp2(s[1] - m_new);
+        ws.m = m_new;
+    }
+    ws.l = ws.l * alpha + (rep ? p0 + p1 : 0.f);
+    if (rep) {
+        pb[kk * G + hg] = make_float2(p0, p0);
+        pb[(4 + kk) * G + hg] = make_float2(p1, p1);
+        if (kk == 0) alpha_buf[hg] = alpha;
+    }
+    __syncwarp();
+
+    // rescale the output of any head whose maximum moved (warp-uniform test)
+    float al[G];
+#pragma unroll
+    for (int g = 0; g < G; ++g) al[g] = alpha_buf[g];
+    bool moved = false;
+#pragma unroll
+    for (int g = 0; g < G; ++g) moved |= al[g] != 1.f;
+    if (moved) {
+#pragma unroll
+        for (int g = 0; g < G; ++g)
+#pragma unroll
+            for (int j = 0; j < kDPL / 2; ++j)
+                ws.o2[g][j] = make_float2(ws.o2[g][j].x * al[g], ws.o2[g][j].y * al[g]);
+    }
+
+    // PV over the warp's keys of this page
+    const int pv_half = (D == 128) ? (lane >> 4) : 0;
+    const int pv_chunk = (D == 128) ? ((lane & 15) >> 1) : (lane >> 2);
+    const int pv_byte = (D == 128) ? ((lane & 1) * 8) : ((lane & 3) * 4);
+#pragma unroll
+    for (int k8 = 0; k8 < 8; ++k8) {
+        if (FULL || k8 < nvalid_rows) {
+            const int row = warp * 8 + k8;
+            const uint8_t* vp = V + pv_half * 4096 + sw128_offset(row, pv_chunk) + pv_byte;
+            if constexpr (kDPL == 4) {
+                const uint2 w = *reinterpret_cast<const uint2*>(vp);
+                const float2 va = make_float2(bf16lo(w.x), bf16hi(w.x));
+                const float2 vb = make_float2(bf16lo(w.y), bf16hi(w.y));
+#pragma unroll
+                for (int g = 0; g < G; ++g) {
+                    const float2 pp = pb[k8 * G + g];
+                    ws.o2[g][0] = __ffma2_rn(pp, va, ws.o2[g][0]);
+                    ws.o2[g][1] = __ffma2_rn(pp, vb, ws.o2[g][1]);
+                }
+            } else {
+                const uint32_t w = *reinterpret_cast<const uint32_t*>(vp);
+                const float2 va = make_float2(bf16lo(w), bf16hi(w));
+#pragma unroll
+                for (int g = 0; g < G; ++g) ws.o2[g][0] = __ffma2_rn(pb[k8 * G + g], va, ws.o2[g][0]);
+            }
+        }
+    }
+    __syncwarp();
+}
+
 template <int D, int G>
-__global__ void __launch_bounds__(kThreads, 3)
+__global__ void __launch_bounds__(kThreads, kMinBlocks)
     decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                   const AttnParams p) {
     using S = DecodeSmem<D, G>;
-    constexpr int kSegDims = D / 8;   // query dims held per QK lane
     constexpr int kDPL = D / 32;      // output dims per PV lane
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                               ~static_cast<uintptr_t>(1023));
+    // The dynamic shared window of a CTA starts 1024-byte aligned (no static
+    // shared memory here), which the 128-byte TMA swizzle pattern relies on.
+    extern __shared__ __align__(1024) uint8_t smem[];
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + S::kBarOff);
     uint64_t* empty = full + kStages;
-    float* pbuf = reinterpret_cast<float*>(smem + S::kPbufOff);
-    float* red_m = reinterpret_cast<float*>(smem + S::kRedOff);
+    uint64_t* dfull = empty + kStages;   // [2] unit descriptor + its query rows landed
+    uint64_t* dempty = dfull + 2;        // [2] consumers done with the descriptor slot
+    UnitDesc* desc = reinterpret_cast<UnitDesc*>(smem + S::kDescOff);
+    int* flags = reinterpret_cast<int*>(smem + S::kDescOff + 2 * sizeof(UnitDesc));
+    float* red_o = reinterpret_cast<float*>(smem + S::kRedOOff);
+    float* red_m = reinterpret_cast<float*>(smem + S::kRedMLOff);
     float* red_l = red_m + kWarps * G;
-    float* red_o = reinterpret_cast<float*>(smem);  // reuses the ring after the main loop
 
-    const int split = blockIdx.x;
-    const int kvh = blockIdx.y;
-    const int b = blockIdx.z;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-
-    const int r0 = p.q_indptr[b];
-    const int nrows = p.q_indptr[b + 1] - r0;
-    if (nrows <= 0) return;
-    const int qreal = p.q_real ? p.q_real[b] : nrows;
-    int kv_len = p.kv_lens[b];
-    if (p.checked && threadIdx.x == 0 && split == 0 && kvh == 0 &&
-        (kv_len > p.max_kv_len || kv_len < 0 || nrows > 1))
-        set_err(p.err, PKV_ERRBIT_LEN);
-    kv_len = min(max(kv_len, 0), p.max_kv_len);
-    if (qreal <= 0) kv_len = 0;  // a padding row attends nothing
-    const int key_begin = split * p.split_keys;
-    const int key_end = min(kv_len, key_begin + p.split_keys);
     const int Hq = p.num_q_heads;
+    const int Hkv = p.num_kv_heads;
+    const int SK = p.split_keys;
+    const int S_ = p.num_splits;
+    const int64_t rows_bound = static_cast<int64_t>(p.batch) * p.max_q_rows;
 
-    if (key_end <= key_begin) {
-        // no keys here: with a single split this CTA owns the final output row
-        if (p.num_splits == 1 && split == 0) {
-            for (int e = threadIdx.x; e < G * D; e += blockDim.x) {
-                const int h = kvh * G + e / D;
-                const int64_t o = (static_cast<int64_t>(r0) * Hq + h) * D + (e % D);
-                if (p.out_f32) static_cast<float*>(p.out)[o] = 0.f;
-                else static_cast<__nv_bfloat16*>(p.out)[o] = __float2bfloat16_rn(0.f);
-                if (p.lse && (e % D) == 0) p.lse[static_cast<int64_t>(r0) * Hq + h] = -INFINITY;
-            }
-        }
+    if ((smem_u32(smem) & 1023u) != 0) {  // never expected; refuse rather than misread tiles
+        if (threadIdx.x == 0) set_err(p.err, PKV_ERRBIT_TIMEOUT);
         return;
     }
-    const int npages = (key_end - key_begin + kPage - 1) / kPage;
-    const int page0 = key_begin / kPage;
-
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], kWarps);
         }
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&dfull[s], 1);
+            mbar_init(&dempty[s], kWarps);
+        }
+        flags[0] = 0;  // "this CTA merges the splits of its unit"
+        flags[1] = 0;  // set when a consumer wait gives up
         fence_mbar_init();
     }
     __syncthreads();
 
     if (warp == kWarps) {
-        // ---------------- producer: one lane issues the page loads ----------
-        if (lane == 0) {
-            prefetch_tmap(&tm_k);
-            prefetch_tmap(&tm_v);
-            const int32_t* bt = p.block_table + static_cast<int64_t>(b) * p.block_table_stride + page0;
-            int issued = 0;
-            for (int i = 0; i < npages; ++i) {
+        // ====================== producer ======================================
+        if (lane != 0) return;
+        prefetch_tmap(&tm_k);
+        prefetch_tmap(&tm_v);
+        int* ticket = p.ws_counters;
+        const int BH = p.batch * Hkv;
+        const int units = BH * S_;
+        int i = 0;  // pages issued so far (ring position)
+        bool alive = true;
+        for (int k = 0; alive; ++k) {
+            UnitDesc d;
+            d.b = -1;
+            for (;;) {
+                const int u = atomicAdd(ticket, 1);
+                if (u >= units) break;
+                const int split = u / BH;
+                const int bh = u - split * BH;
+                const int b = bh / Hkv;
+                const int r0 = p.q_indptr[b];
+                const int nrows = p.q_indptr[b + 1] - r0;
+                if (nrows <= 0) continue;
+                const int qreal = p.q_real ? p.q_real[b] : nrows;
+                int kv_len = p.kv_lens[b];
+                if (p.checked && (kv_len > p.max_kv_len || kv_len < 0 || nrows > 1))
+                    set_err(p.err, PKV_ERRBIT_LEN);
+                kv_len = min(max(kv_len, 0), p.max_kv_len);
+                if (qreal <= 0) kv_len = 0;  // a padding row attends nothing
+                const int kb = split * SK;
+                const int ke = min(kv_len, kb + SK);
+                // a unit with keys, or split 0 of a row without keys (writes zeros)
+                if (ke > kb || split == 0) {
+                    d.b = b;
+                    d.kvh = bh - b * Hkv;
+                    d.split = split;
+                    d.key_begin = kb;
+                    d.key_end = max(ke, kb);
+                    d.r0 = r0;
+                    d.nsplit = (kv_len + SK - 1) / SK;
+                    break;
+                }
+            }
+            const int slot = k & 1;
+            if (k >= 2 && !mbar_wait(&dempty[slot], ((k >> 1) - 1) & 1)) {
+                set_err(p.err, PKV_ERRBIT_TIMEOUT);
+                d.b = -1;  // tell the consumers to stop (they may time out too)
+            }
+            desc[slot] = d;
+            if (d.b >= 0 && d.key_end > d.key_begin) {
+                mbar_arrive_expect_tx(&dfull[slot], G * D * 2);
+                const __nv_bfloat16* qrow = static_cast<const __nv_bfloat16*>(p.q) +
+                                            static_cast<int64_t>(d.r0) * p.q_token_stride;
+#pragma unroll
+                for (int g = 0; g < G; ++g)
+                    bulk_load(smem + S::kQbufOff + (slot * G + g) * D * 2,
+                              qrow + static_cast<int64_t>(d.kvh * G + g) * p.q_head_stride,
+                              D * 2, &dfull[slot]);
+            } else {
+                mbar_arrive(&dfull[slot]);
+            }
+            if (d.b < 0) break;
+            const int npages = (d.key_end - d.key_begin + kPage - 1) / kPage;
+            const int32_t* bt =
+                p.block_table + static_cast<int64_t>(d.b) * p.block_table_stride + d.key_begin / kPage;
+            for (int pi = 0; pi < npages; ++pi, ++i) {
                 const int st = i % kStages;
                 if (i >= kStages && !mbar_wait(&empty[st], ((i / kStages) - 1) & 1)) {
                     set_err(p.err, PKV_ERRBIT_TIMEOUT);
+                    alive = false;
                     break;
                 }
-                int phys = bt[i];
+                int phys = bt[pi];
                 if (p.checked && (phys < 0 || phys >= p.num_pages)) {
                     set_err(p.err, PKV_ERRBIT_PAGE);
-                    phys = static_cast<int>(p.num_pages);  // out of the tensor: TMA fills zeros
+                    phys = static_cast<int>(p.num_pages);  // outside the tensor: TMA fills zeros
                 }
                 uint8_t* kd = smem + st * S::kStageBytes;
                 uint8_t* vd = kd + S::kTileBytes;
                 mbar_arrive_expect_tx(&full[st], S::kStageBytes);
 #pragma unroll
                 for (int h = 0; h < S::kHalves; ++h) {
-                    tma_load_4d(kd + h * 4096, &tm_k, &full[st], h * 64, kvh, 0, phys);
-                    tma_load_4d(vd + h * 4096, &tm_v, &full[st], h * 64, kvh, 0, phys);
+                    tma_load_4d(kd + h * 4096, &tm_k, &full[st], h * 64, d.kvh, 0, phys);
+                    tma_load_4d(vd + h * 4096, &tm_v, &full[st], h * 64, d.kvh, 0, phys);
                 }
-                issued = i + 1;
             }
-            // do not leave while copies into this CTA's shared memory are in flight
-            for (int i = max(0, issued - kStages); i < issued; ++i)
-                mbar_wait(&full[i % kStages], (i / kStages) & 1);
         }
+        // do not leave while copies into this CTA's shared memory are in flight
+        for (int j = max(0, i - kStages); j < i; ++j) mbar_wait(&full[j % kStages], (j / kStages) & 1);
         return;
     }
 
-    // ---------------- consumers ---------------------------------------------
+    // ====================== consumers =========================================
     const int kk = lane >> 3;   // key within a pass of 4
     const int seg = lane & 7;   // QK segment
-    // chunks (16 bytes = 8 dims) of a 128-column half that this segment reads
     const int half = (D == 128) ? (seg >> 2) : 0;
     const int c0 = (D == 128) ? ((seg & 3) + 4 * (seg >> 2)) : seg;
-    const int c1 = c0 ^ 4;
+    const int hg = head_of_lane<G>(seg);
+    const bool rep = (seg & (8 / G - 1)) == 0;
+    float2* pb = reinterpret_cast<float2*>(smem + S::kPbufOff + warp * ((S::kPbufWarp + 15) & ~15));
+    float* alpha_buf = reinterpret_cast<float*>(pb + 8 * G);
 
-    float q[G][kSegDims];
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
-        const __nv_bfloat16* qh = static_cast<const __nv_bfloat16*>(p.q) +
-                                  static_cast<int64_t>(r0) * p.q_token_stride +
-                                  static_cast<int64_t>(kvh * G + g) * p.q_head_stride +
-                                  half * 64;
-        const uint4 a = *reinterpret_cast<const uint4*>(qh + c0 * 8);
-        const uint32_t wa[4] = {a.x, a.y, a.z, a.w};
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            q[g][2 * j] = bf16lo(wa[j]) * p.scale_log2;
-            q[g][2 * j + 1] = bf16hi(wa[j]) * p.scale_log2;
-        }
-        if constexpr (D == 128) {
-            const uint4 c = *reinterpret_cast<const uint4*>(qh + c1 * 8);
-            const uint32_t wc[4] = {c.x, c.y, c.z, c.w};
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                q[g][8 + 2 * j] = bf16lo(wc[j]) * p.scale_log2;
-                q[g][8 + 2 * j + 1] = bf16hi(wc[j]) * p.scale_log2;
-            }
-        }
-    }
-
-    float m[G], l[G], o[G][kDPL];
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
-        m[g] = -INFINITY;
-        l[g] = 0.f;
-#pragma unroll
-        for (int j = 0; j < kDPL; ++j) o[g][j] = 0.f;
-    }
-    float* pb = pbuf + warp * 8 * G;
-    // PV addressing of this lane's output dims [lane*kDPL, lane*kDPL + kDPL)
-    const int pv_half = (D == 128) ? (lane >> 4) : 0;
-    const int pv_chunk = (D == 128) ? ((lane & 15) >> 1) : (lane >> 2);
-    const int pv_byte = (D == 128) ? ((lane & 1) * 8) : ((lane & 3) * 4);
-
-    bool ok = true;
-    for (int i = 0; i < npages; ++i) {
-        const int st = i % kStages;
-        if (!mbar_wait(&full[st], (i / kStages) & 1)) {
+    int i = 0;  // pages consumed so far (ring position)
+    for (int k = 0;; ++k) {
+        const int slot = k & 1;
+        if (!mbar_wait(&dfull[slot], (k >> 1) & 1)) {
             if (lane == 0) set_err(p.err, PKV_ERRBIT_TIMEOUT);
-            ok = false;
             break;
         }
-        const uint8_t* K = smem + st * S::kStageBytes;
-        const uint8_t* V = K + S::kTileBytes;
-        const int key0 = key_begin + i * kPage;
+        const UnitDesc d = desc[slot];
+        if (d.b < 0) break;
 
-        float s[2][G];
-#pragma unroll
-        for (int pass = 0; pass < 2; ++pass) {
-            const int row = warp * 8 + pass * 4 + kk;
-            float acc[G];
-#pragma unroll
-            for (int g = 0; g < G; ++g) acc[g] = 0.f;
-            {
-                const uint4 a = *reinterpret_cast<const uint4*>(K + half * 4096 + sw128_offset(row, c0));
-                const uint32_t w[4] = {a.x, a.y, a.z, a.w};
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const float k0 = bf16lo(w[j]), k1 = bf16hi(w[j]);
-#pragma unroll
-                    for (int g = 0; g < G; ++g) acc[g] = fmaf(q[g][2 * j + 1], k1, fmaf(q[g][2 * j], k0, acc[g]));
-                }
-            }
-            if constexpr (D == 128) {
-                const uint4 a = *reinterpret_cast<const uint4*>(K + half * 4096 + sw128_offset(row, c1));
-                const uint32_t w[4] = {a.x, a.y, a.z, a.w};
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const float k0 = bf16lo(w[j]), k1 = bf16hi(w[j]);
-#pragma unroll
-                    for (int g = 0; g < G; ++g)
-                        acc[g] = fmaf(q[g][8 + 2 * j + 1], k1, fmaf(q[g][8 + 2 * j], k0, acc[g]));
-                }
-            }
+        // query rows of the unit, pre-scaled into the base-2 domain
+        float2 q2[G][D / 16];
+        if (d.key_end > d.key_begin) {
 #pragma unroll
             for (int g = 0; g < G; ++g) {
-                acc[g] += __shfl_xor_sync(0xffffffffu, acc[g], 1);
-                acc[g] += __shfl_xor_sync(0xffffffffu, acc[g], 2);
-                acc[g] += __shfl_xor_sync(0xffffffffu, acc[g], 4);
-            }
-            const bool valid = key0 + row < key_end;
+                const __nv_bfloat16* qh =
+                    reinterpret_cast<const __nv_bfloat16*>(smem + S::kQbufOff) + (slot * G + g) * D + half * 64;
+                const uint4 a = *reinterpret_cast<const uint4*>(qh + c0 * 8);
+                const uint32_t wa[4] = {a.x, a.y, a.z, a.w};
 #pragma unroll
-            for (int g = 0; g < G; ++g) s[pass][g] = valid ? acc[g] : -INFINITY;
-        }
-
-        // online softmax over this warp's 8 keys of the page
+                for (int j = 0; j < 4; ++j)
+                    q2[g][j] = make_float2(bf16lo(wa[j]) * p.scale_log2, bf16hi(wa[j]) * p.scale_log2);
+                if constexpr (D == 128) {
+                    const uint4 c = *reinterpret_cast<const uint4*>(qh + (c0 ^ 4) * 8);
+                    const uint32_t wc[4] = {c.x, c.y, c.z, c.w};
 #pragma unroll
-        for (int g = 0; g < G; ++g) {
-            float mx = fmaxf(s[0][g], s[1][g]);
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-            const float m_new = fmaxf(m[g], mx);
-            float p0 = 0.f, p1 = 0.f;
-            if (m_new != -INFINITY) {
-                if (m_new != m[g]) {  // warp-uniform
-                    const float alpha = fast_exp2(m[g] - m_new);
-                    l[g] *= alpha;
-#pragma unroll
-                    for (int j = 0; j < kDPL; ++j) o[g][j] *= alpha;
-                    m[g] = m_new;
+                    for (int j = 0; j < 4; ++j)
+                        q2[g][4 + j] =
+                            make_float2(bf16lo(wc[j]) * p.scale_log2, bf16hi(wc[j]) * p.scale_log2);
                 }
-                p0 = fast_exp2(s[0][g] - m_new);
-                p1 = fast_exp2(s[1][g] - m_new);
-            }
-            if (seg == 0) {
-                l[g] += p0 + p1;
-                pb[kk * G + g] = p0;
-                pb[(4 + kk) * G + g] = p1;
             }
         }
         __syncwarp();
+        if (lane == 0) mbar_arrive(&dempty[slot]);
 
-        // PV over the warp's valid keys of this page
-        const int nvalid = min(8, key_end - (key0 + warp * 8));
+        WarpState<G, kDPL> ws;
+        ws.m = -INFINITY;
+        ws.l = 0.f;
 #pragma unroll
-        for (int k8 = 0; k8 < 8; ++k8) {
-            if (k8 < nvalid) {
-                const int row = warp * 8 + k8;
-                float pg[G];
+        for (int g = 0; g < G; ++g)
 #pragma unroll
-                for (int g = 0; g < G; ++g) pg[g] = pb[k8 * G + g];
-                const uint8_t* vp = V + pv_half * 4096 + sw128_offset(row, pv_chunk) + pv_byte;
-                float v[kDPL];
-                if constexpr (kDPL == 4) {
-                    const uint2 w = *reinterpret_cast<const uint2*>(vp);
-                    v[0] = bf16lo(w.x); v[1] = bf16hi(w.x);
-                    v[2] = bf16lo(w.y); v[3] = bf16hi(w.y);
-                } else {
-                    const uint32_t w = *reinterpret_cast<const uint32_t*>(vp);
-                    v[0] = bf16lo(w); v[1] = bf16hi(w);
+            for (int j = 0; j < kDPL / 2; ++j) ws.o2[g][j] = make_float2(0.f, 0.f);
+
+        const int npages = (d.key_end - d.key_begin + kPage - 1) / kPage;
+        bool failed = false;
+        for (int pi = 0; pi < npages; ++pi, ++i) {
+            const int st = i % kStages;
+            if (!mbar_wait(&full[st], (i / kStages) & 1)) {
+                // give up on this unit but still take part in the barriers below,
+                // so that every consumer warp leaves together
+                if (lane == 0) set_err(p.err, PKV_ERRBIT_TIMEOUT);
+                failed = true;
+                break;
+            }
+            const uint8_t* K = smem + st * S::kStageBytes;
+            const uint8_t* V = K + S::kTileBytes;
+            const int key0 = d.key_begin + pi * kPage;
+            if (key0 + kPage <= d.key_end) {
+                decode_page<D, G, true>(ws, q2, K, V, pb, alpha_buf, warp, kk, seg, lane, 8);
+            } else {
+                const int nvalid_rows = min(8, d.key_end - (key0 + warp * 8));
+                decode_page<D, G, false>(ws, q2, K, V, pb, alpha_buf, warp, kk, seg, lane, nvalid_rows);
+            }
+            if (lane == 0) mbar_arrive(&empty[st]);
+        }
+        if (failed && lane == 0) flags[1] = 1;
+
+        // ---------------- merge the four warps' states of this unit ---------
+        // the lane's head sum over this warp's keys (rep lanes hold the terms)
+        ws.l += __shfl_xor_sync(0xffffffffu, ws.l, 8);
+        ws.l += __shfl_xor_sync(0xffffffffu, ws.l, 16);
+        if (kk == 0 && rep) {
+            red_m[warp * G + hg] = ws.m;
+            red_l[warp * G + hg] = ws.l;
+        }
+        const int bh = d.b * Hkv + d.kvh;
+        const bool partial = d.nsplit > 1;
+        constexpr int RH = S::kRedHeads;
+#pragma unroll
+        for (int g0 = 0; g0 < G; g0 += RH) {
+#pragma unroll
+            for (int gg = 0; gg < RH; ++gg)
+#pragma unroll
+                for (int j = 0; j < kDPL / 2; ++j)
+                    *reinterpret_cast<float2*>(&red_o[(warp * RH + gg) * D + lane * kDPL + 2 * j]) =
+                        ws.o2[g0 + gg][j];
+            consumer_sync();
+            for (int e = threadIdx.x; e < RH * D; e += kWarps * 32) {
+                const int gg = e / D, dd = e - (e / D) * D;
+                const int g = g0 + gg;
+                float M = -INFINITY;
+#pragma unroll
+                for (int w = 0; w < kWarps; ++w) M = fmaxf(M, red_m[w * G + g]);
+                float L = 0.f, O = 0.f;
+                if (M != -INFINITY) {
+#pragma unroll
+                    for (int w = 0; w < kWarps; ++w) {
+                        const float f = fast_exp2(red_m[w * G + g] - M);
+                        L = fmaf(f, red_l[w * G + g], L);
+                        O = fmaf(f, red_o[(w * RH + gg) * D + dd], O);
+                    }
                 }
-#pragma unroll
-                for (int g = 0; g < G; ++g)
-#pragma unroll
-                    for (int j = 0; j < kDPL; ++j) o[g][j] = fmaf(pg[g], v[j], o[g][j]);
+                O *= L > 0.f ? 1.0f / L : 0.f;
+                const float lse = L > 0.f ? (M + __log2f(L)) * kLn2 : -INFINITY;
+                const int64_t st = static_cast<int64_t>(d.r0) * Hq + d.kvh * G + g;
+                if (!partial) {
+                    if (p.out_f32) static_cast<float*>(p.out)[st * D + dd] = O;
+                    else static_cast<__nv_bfloat16*>(p.out)[st * D + dd] = __float2bfloat16_rn(O);
+                    if (p.lse && dd == 0) p.lse[st] = lse;
+                } else if (d.r0 < rows_bound) {
+                    p.ws_o[(st * S_ + d.split) * D + dd] = O;
+                    if (dd == 0) p.ws_lse[st * S_ + d.split] = lse;
+                }
             }
+            consumer_sync();  // red_o is rewritten by the next round
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[st]);
-    }
-    (void)ok;
-
-    // ---------------- merge the four warps' states ---------------------------
-#pragma unroll
-    for (int g = 0; g < G; ++g) l[g] = warp_sum(l[g]);
-    // every consumer is past its last shared read of the ring once all have
-    // arrived here; the producer only waits on barriers from now on.
-    asm volatile("bar.sync 1, %0;" ::"r"(kWarps * 32) : "memory");
-    if (lane == 0) {
-#pragma unroll
-        for (int g = 0; g < G; ++g) {
-            red_m[warp * G + g] = m[g];
-            red_l[warp * G + g] = l[g];
-        }
-    }
-#pragma unroll
-    for (int g = 0; g < G; ++g)
-#pragma unroll
-        for (int j = 0; j < kDPL; ++j) red_o[(warp * G + g) * D + lane * kDPL + j] = o[g][j];
-    asm volatile("bar.sync 1, %0;" ::"r"(kWarps * 32) : "memory");
-
-    const int S_ = p.num_splits;
-    for (int e = threadIdx.x; e < G * D; e += kWarps * 32) {
-        const int g = e / D, d = e - (e / D) * D;
-        float M = -INFINITY;
-#pragma unroll
-        for (int w = 0; w < kWarps; ++w) M = fmaxf(M, red_m[w * G + g]);
-        float L = 0.f, O = 0.f;
-        if (M != -INFINITY) {
-#pragma unroll
-            for (int w = 0; w < kWarps; ++w) {
-                const float f = fast_exp2(red_m[w * G + g] - M);
-                L = fmaf(f, red_l[w * G + g], L);
-                O = fmaf(f, red_o[(w * G + g) * D + d], O);
+        if (partial && d.r0 < rows_bound) {
+            // the last split of this (sequence, K/V head) to finish merges all
+            __threadfence();
+            consumer_sync();
+            if (threadIdx.x == 0) {
+                const int done = atomicAdd(&p.ws_counters[1 + bh], 1);
+                const int last = done == d.nsplit - 1;
+                if (last) atomicExch(&p.ws_counters[1 + bh], 0);
+                flags[0] = last;
             }
+            consumer_sync();
+            if (flags[0]) {
+                __threadfence();
+                for (int e = threadIdx.x; e < G * D; e += kWarps * 32) {
+                    const int g = e / D, dd = e - (e / D) * D;
+                    const int64_t st = static_cast<int64_t>(d.r0) * Hq + d.kvh * G + g;
+                    const float* lses = p.ws_lse + st * S_;
+                    float M = -INFINITY;
+                    for (int sp = 0; sp < d.nsplit; ++sp) M = fmaxf(M, __ldcg(lses + sp));
+                    float L = 0.f, O = 0.f;
+                    if (M != -INFINITY) {
+                        for (int sp = 0; sp < d.nsplit; ++sp) {
+                            const float w = __expf(__ldcg(lses + sp) - M);
+                            L += w;
+                            O = fmaf(w, __ldcg(p.ws_o + (st * S_ + sp) * D + dd), O);
+                        }
+                    }
+                    O *= L > 0.f ? 1.0f / L : 0.f;
+                    if (p.out_f32) static_cast<float*>(p.out)[st * D + dd] = O;
+                    else static_cast<__nv_bfloat16*>(p.out)[st * D + dd] = __float2bfloat16_rn(O);
+                    if (p.lse && dd == 0) p.lse[st] = L > 0.f ? M + __logf(L) : -INFINITY;
+                }
+            }
+            consumer_sync();  // flags[0] is rewritten by the next unit
         }
-        const float inv = L > 0.f ? 1.0f / L : 0.f;
-        O *= inv;
-        const float lse = L > 0.f ? (M + __log2f(L)) * kLn2 : -INFINITY;
-        const int h = kvh * G + g;
-        const int64_t st = static_cast<int64_t>(r0) * Hq + h;
-        if (S_ == 1) {
-            if (p.out_f32) static_cast<float*>(p.out)[st * D + d] = O;
-            else static_cast<__nv_bfloat16*>(p.out)[st * D + d] = __float2bfloat16_rn(O);
-            if (p.lse && d == 0) p.lse[st] = lse;
-        } else if (r0 < static_cast<int64_t>(p.batch) * p.max_q_rows) {  // workspace bound
-            p.ws_o[(st * S_ + split) * D + d] = O;
-            if (d == 0) p.ws_lse[st * S_ + split] = lse;
-        }
+        if (flags[1]) break;  // a wait timed out: every consumer warp stops here
     }
 }
 
 template <int D, int G>
-cudaError_t launch_dg(const AttnParams& p, const void* tk, const void* tv, cudaStream_t s) {
+cudaError_t launch_dg(const AttnParams& p, const void* tk, const void* tv, int sms, cudaStream_t s) {
     using S = DecodeSmem<D, G>;
     auto kern = decode_kernel<D, G>;
-    // per device context; cheap, and not a stream operation (safe under capture)
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         S::kAlloc);
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kBytes);
     if (e != cudaSuccess) return e;
-    dim3 grid(p.num_splits, p.num_kv_heads, p.batch);
-    kern<<<grid, kThreads, S::kAlloc, s>>>(*static_cast<const CUtensorMap*>(tk),
-                                           *static_cast<const CUtensorMap*>(tv), p);
+    int per_sm = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, S::kBytes);
+    if (e != cudaSuccess) return e;
+    const int64_t units = static_cast<int64_t>(p.batch) * p.num_kv_heads * p.num_splits;
+    const int64_t grid = std::min<int64_t>(units, static_cast<int64_t>(std::max(per_sm, 1)) * sms);
+    kern<<<static_cast<unsigned>(grid), kThreads, S::kBytes, s>>>(
+        *static_cast<const CUtensorMap*>(tk), *static_cast<const CUtensorMap*>(tv), p);
     return cudaGetLastError();
 }
 
@@ -379,10 +575,22 @@ bool decode_supported(int head_dim, int group) {
     return (head_dim == 64 || head_dim == 128) && (group == 1 || group == 2 || group == 4);
 }
 
+size_t decode_counter_bytes(int batch, int num_kv_heads) {
+    return (static_cast<size_t>(batch) * num_kv_heads + 1) * sizeof(int);
+}
+
 cudaError_t launch_decode(const AttnParams& p, const void* tk, const void* tv, cudaStream_t s) {
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    // the unit tickets and the per-(sequence, head) split counts start at zero
+    e = cudaMemsetAsync(p.ws_counters, 0, decode_counter_bytes(p.batch, p.num_kv_heads), s);
+    if (e != cudaSuccess) return e;
     const int G = p.num_q_heads / p.num_kv_heads;
 #define PKV_DEC(D_, G_) \
-    if (p.head_dim == D_ && G == G_) return launch_dg<D_, G_>(p, tk, tv, s);
+    if (p.head_dim == D_ && G == G_) return launch_dg<D_, G_>(p, tk, tv, sms, s);
     PKV_DEC(128, 4) PKV_DEC(128, 2) PKV_DEC(128, 1)
     PKV_DEC(64, 4) PKV_DEC(64, 2) PKV_DEC(64, 1)
 #undef PKV_DEC

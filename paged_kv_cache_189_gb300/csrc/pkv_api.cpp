@@ -117,9 +117,11 @@ Plan plan_attention(int batch, int max_q_rows, int Hq, int Hkv, int D, int max_k
     }
     pl.split_keys = keys;
     pl.splits = std::max(1, (max_kv_len + keys - 1) / keys);
+    // [scheduling counters][partial outputs][partial LSEs]
+    pl.ws_bytes = round_up(pkv::decode_counter_bytes(batch, Hkv), 256);
     if (pl.splits > 1) {
         const size_t states = static_cast<size_t>(batch) * max_q_rows * Hq * pl.splits;
-        pl.ws_bytes = round_up(states * D * sizeof(float), 256) + round_up(states * sizeof(float), 256);
+        pl.ws_bytes += round_up(states * D * sizeof(float), 256) + round_up(states * sizeof(float), 256);
     }
     return pl;
 }
@@ -270,11 +272,15 @@ pkv_status paged_attention(const void* q, int64_t q_token_stride, int64_t q_head
     p.split_keys = pl.split_keys;
     p.checked = (flags & PKV_FLAG_CHECKED) != 0;
     p.err = err;
-    if (pl.splits > 1) {
-        const size_t states = static_cast<size_t>(batch) * max_q_rows * num_q_heads * pl.splits;
-        p.ws_o = static_cast<float*>(workspace);
-        p.ws_lse = reinterpret_cast<float*>(static_cast<char*>(workspace) +
-                                            round_up(states * head_dim * sizeof(float), 256));
+    if (pl.kernel == Kernel::kDecode) {
+        char* w = static_cast<char*>(workspace);
+        p.ws_counters = reinterpret_cast<int*>(w);
+        w += round_up(pkv::decode_counter_bytes(batch, num_kv_heads), 256);
+        if (pl.splits > 1) {
+            const size_t states = static_cast<size_t>(batch) * max_q_rows * num_q_heads * pl.splits;
+            p.ws_o = reinterpret_cast<float*>(w);
+            p.ws_lse = reinterpret_cast<float*>(w + round_up(states * head_dim * sizeof(float), 256));
+        }
     }
     cudaStream_t s = static_cast<cudaStream_t>(stream);
 
@@ -285,10 +291,7 @@ pkv_status paged_attention(const void* q, int64_t q_token_stride, int64_t q_head
     if (st != PKV_OK) return st;
     st = make_pool_map(&tv, v_pool, head_dim, num_kv_heads, page_size, num_pages, page_stride);
     if (st != PKV_OK) return st;
-    cudaError_t e = pkv::launch_decode(p, &tk, &tv, s);
-    if (e != cudaSuccess) return from_cuda(e, "attention (decode)");
-    if (pl.splits > 1) return from_cuda(pkv::launch_split_reduce(p, s), "attention (split reduce)");
-    return ok();
+    return from_cuda(pkv::launch_decode(p, &tk, &tv, s), "attention (decode)");
 }
 
 pkv_status merge_attn_states(const void* o_a, const float* lse_a, const void* o_b,

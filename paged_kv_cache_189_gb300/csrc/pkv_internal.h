@@ -66,6 +66,7 @@ struct AttnParams {
     int split_keys;    // keys per split (multiple of the key tile)
     float* ws_o;       // [rows_bound][Hq][splits][D] partial outputs (splits > 1)
     float* ws_lse;     // [rows_bound][Hq][splits]
+    int* ws_counters;  // decode: [0] unit ticket, [1 + b*Hkv + h] finished splits
     bool checked;
     int32_t* err;
 };
@@ -75,6 +76,7 @@ struct AttnParams {
 cudaError_t launch_decode(const AttnParams& p, const void* tmap_k, const void* tmap_v,
                           cudaStream_t s);
 bool decode_supported(int head_dim, int group);
+size_t decode_counter_bytes(int batch, int num_kv_heads);
 
 // Generic SIMT kernel: any rows, masks, group sizes; no splits.  A slow
 // cross-check of the fast kernels and the path for shapes they do not cover.

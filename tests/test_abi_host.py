@@ -66,20 +66,25 @@ def test_attention_host_validation(L):
     assert _attn(L, q=None) == pkv.PKV_ERR_INVALID_ARG
     assert _attn(L, flags=pkv.PKV_FLAG_CHECKED, err=None) == pkv.PKV_ERR_INVALID_ARG
     assert _attn(L, odt=pkv.PKV_F16) == pkv.PKV_ERR_UNSUPPORTED
-    # split-KV needs a workspace: 3000 keys -> 6 splits of 512
+    # the decode kernel needs a workspace (counters; partials past 512 keys)
     assert _attn(L, mk=3000, bts=94) == pkv.PKV_ERR_WORKSPACE
+    assert _attn(L, mk=100) == pkv.PKV_ERR_WORKSPACE
     # empty problems return OK without touching the device
     assert _attn(L, batch=0) == pkv.PKV_OK
     assert _attn(L, mq=0) == pkv.PKV_OK
 
 
 def test_workspace_size(L):
-    # one split when everything fits in 512 keys: no workspace
-    assert pkv.paged_attention_workspace_size(64, 1, 32, 8, 128, 512) == 0
+    # one split when everything fits in 512 keys: only the scheduling counters
+    small = pkv.paged_attention_workspace_size(64, 1, 32, 8, 128, 512)
+    assert 64 * 8 * 4 < small <= 4096
     ws = pkv.paged_attention_workspace_size(64, 1, 32, 8, 128, 8193)
     splits = 17
     states = 64 * 32 * splits
-    assert ws >= states * 128 * 4 + states * 4
+    assert ws >= states * 128 * 4 + states * 4 + 64 * 8 * 4
+    # the generic kernel (several query rows) needs none
+    assert pkv.paged_attention_workspace_size(4, 16, 32, 8, 128, 8193,
+                                              flags=pkv.PKV_FLAG_SIMT_ONLY) == 0
     assert pkv.paged_attention_workspace_size(0, 1, 32, 8, 128, 8193) == 0
 
 

@@ -118,17 +118,18 @@ def test_decode_graph_capture_replay():
     rows, Hq, D = q.shape
     out = torch.empty(rows, Hq, D, dtype=torch.bfloat16, device=DEV)
     lse = torch.empty(rows, Hq, device=DEV)
-    ws = torch.empty(pkv.paged_attention_workspace_size(c.batch, 1, Hq, 8, D, 2000), dtype=torch.uint8,
+    mk = c.max_kv_len
+    ws = torch.empty(pkv.paged_attention_workspace_size(c.batch, 1, Hq, 8, D, mk), dtype=torch.uint8,
                      device=DEV)
     s = torch.cuda.Stream()
     g = torch.cuda.CUDAGraph()
     with torch.cuda.stream(s):
         pkv.paged_attention(q, k_pool, v_pool, bt, kl, qi, out, q_real=qr, lse=lse, max_q_rows=1,
-                            max_kv_len=2000, workspace=ws)  # warm-up outside capture
+                            max_kv_len=mk, workspace=ws)  # warm-up outside capture
         torch.cuda.synchronize()
         with torch.cuda.graph(g, stream=s):
             pkv.paged_attention(q, k_pool, v_pool, bt, kl, qi, out, q_real=qr, lse=lse,
-                                max_q_rows=1, max_kv_len=2000, workspace=ws)
+                                max_q_rows=1, max_kv_len=mk, workspace=ws)
     q2 = wl.randn_bf16(tuple(q.shape), torch.Generator().manual_seed(99))
     q.copy_(q2.to(DEV))
     g.replay()
