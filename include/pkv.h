@@ -170,6 +170,41 @@ pkv_status paged_attention(const void* q, int64_t q_token_stride, int64_t q_head
                            int32_t* err, void* stream);
 
 /*
+ * paged_attention_no_alloc -- paged_attention for callers that cannot allocate.
+ *
+ * The pages describe no such entry point; it exists for callers that have no
+ * workspace to give: code enqueuing work during CUDA-graph capture (where
+ * cudaMalloc is not allowed), servers that fix device memory at start-up and
+ * allow no allocator calls per request, and hosts that pass only input and
+ * output pointers.  Same arguments, results and errors as paged_attention,
+ * without workspace / workspace_bytes: the scratch is a device array inside
+ * the library of PKV_NO_ALLOC_SCRATCH_BYTES (32 MiB), present on every GPU
+ * that loads the library until the process exits.
+ *
+ *  - Nothing is allocated: no cudaMalloc, cudaFree or allocating library call.
+ *  - A call needing more scratch than the array holds (what
+ *    paged_attention_workspace_size reports for the same arguments) returns
+ *    PKV_ERR_WORKSPACE with a message, before anything is enqueued.
+ *  - The first call with a given device current looks up the array's address
+ *    on that device; make that first call before any stream capture.
+ *  - Every call on a device uses the same array and leaves its contents
+ *    behind (what must start at zero is cleared by each call), so calls that
+ *    can overlap on the GPU (unordered streams) race and must be serialised.
+ */
+#define PKV_NO_ALLOC_SCRATCH_BYTES ((size_t)32 << 20)
+
+pkv_status paged_attention_no_alloc(const void* q, int64_t q_token_stride, int64_t q_head_stride,
+                                    const void* k_pool, const void* v_pool, int64_t num_pages,
+                                    int page_size, int64_t page_stride,
+                                    const int32_t* block_table, int64_t block_table_stride,
+                                    const int32_t* kv_lens, const int32_t* q_indptr,
+                                    const int32_t* q_real, int batch, int max_q_rows,
+                                    int max_kv_len, int num_q_heads, int num_kv_heads,
+                                    int head_dim, pkv_mask mask, int causal_block, float scale,
+                                    void* out, pkv_dtype out_dtype, float* lse, int num_splits,
+                                    unsigned flags, int32_t* err, void* stream);
+
+/*
  * merge_attn_states -- exact merge of two attention states over disjoint key
  * sets (shared-prefix state with private-tail state).
  *

@@ -128,6 +128,11 @@ Plan plan_attention(int batch, int max_q_rows, int Hq, int Hkv, int D, int max_k
 
 }  // namespace
 
+pkv_status pkv::report(pkv_status status, const char* message) {
+    g_last_error = message;
+    return status;
+}
+
 extern "C" {
 
 const char* pkv_status_string(pkv_status s) {

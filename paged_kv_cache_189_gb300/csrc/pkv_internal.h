@@ -9,6 +9,9 @@
 
 namespace pkv {
 
+// Record a validation message for pkv_last_error() and return the status.
+pkv_status report(pkv_status status, const char* message);
+
 // ---------------------------- scatter --------------------------------------
 struct ScatterArgs {
     const void* k_src;

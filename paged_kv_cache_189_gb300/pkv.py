@@ -26,7 +26,8 @@ PKV_ERRBIT_SLOT, PKV_ERRBIT_SRC, PKV_ERRBIT_PAGE, PKV_ERRBIT_LEN, PKV_ERRBIT_TIM
 # every symbol include/pkv.h declares
 EXPORTED = ("pkv_status_string", "pkv_last_error", "kv_scatter_slots",
             "paged_attention_workspace_size", "paged_attention", "merge_attn_states",
-            "rotate_rows")
+            "rotate_rows", "paged_attention_no_alloc")
+NO_ALLOC_SCRATCH_BYTES = 32 << 20
 
 _vp, _i64, _i32, _u32, _f32, _sz = (ctypes.c_void_p, ctypes.c_int64, ctypes.c_int,
                                     ctypes.c_uint, ctypes.c_float, ctypes.c_size_t)
@@ -39,6 +40,9 @@ _SIGNATURES = {
     "paged_attention": (_i32, [_vp, _i64, _i64, _vp, _vp, _i64, _i32, _i64, _vp, _i64, _vp, _vp,
                                _vp, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _f32, _vp,
                                _i32, _vp, _vp, _sz, _i32, _u32, _vp, _vp]),
+    "paged_attention_no_alloc": (_i32, [_vp, _i64, _i64, _vp, _vp, _i64, _i32, _i64, _vp, _i64,
+                                        _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _i32,
+                                        _i32, _f32, _vp, _i32, _vp, _i32, _u32, _vp, _vp]),
     "merge_attn_states": (_i32, [_vp, _vp, _vp, _vp, _i32, _i64, _i32, _i32, _vp, _i32, _vp,
                                  _vp]),
     "rotate_rows": (_i32, [_vp, _i64, _i64, _i64, _i32, _i64, _vp]),
@@ -152,6 +156,28 @@ def paged_attention(q, k_pool, v_pool, block_table, kv_lens, q_indptr, out, *, q
         float(scale), _ptr(out), _dtype(out), _ptr(lse), _ptr(workspace), ws_bytes, num_splits,
         flags, _ptr(err), _stream(stream))
     _check("paged_attention", st)
+
+
+def paged_attention_no_alloc(q, k_pool, v_pool, block_table, kv_lens, q_indptr, out, *,
+                             q_real=None, lse=None, batch=None, max_q_rows, max_kv_len,
+                             mask="causal", causal_block=0, scale=0.0, num_splits=0, flags=0,
+                             err=None, stream=None):
+    """``paged_attention`` without a workspace argument, for callers that
+    cannot allocate: the scratch is the library's fixed device array of
+    ``NO_ALLOC_SCRATCH_BYTES`` (see include/pkv.h).  Calls on one device share
+    it, so they must not overlap on the GPU."""
+    n, P, H, D, page_stride = _pool_geometry(k_pool)
+    assert v_pool.shape == k_pool.shape and v_pool.stride() == k_pool.stride()
+    assert q.stride(2) == 1 and out.is_contiguous()
+    if batch is None:
+        batch = kv_lens.numel()
+    st = lib().paged_attention_no_alloc(
+        _ptr(q), q.stride(0), q.stride(1), _ptr(k_pool), _ptr(v_pool), n, P, page_stride,
+        _ptr(block_table), block_table.stride(0), _ptr(kv_lens), _ptr(q_indptr), _ptr(q_real),
+        batch, max_q_rows, max_kv_len, q.shape[1], H, D, MASKS[mask], causal_block,
+        float(scale), _ptr(out), _dtype(out), _ptr(lse), num_splits, flags, _ptr(err),
+        _stream(stream))
+    _check("paged_attention_no_alloc", st)
 
 
 def merge_attn_states(o_a, lse_a, o_b, lse_b, o_out, lse_out=None, stream=None):
