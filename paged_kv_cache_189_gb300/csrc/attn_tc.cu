@@ -1,0 +1,543 @@
+// attn_tc.cu -- paged attention for many query rows on the 5th-generation
+// tensor cores (tcgen05 MMA, accumulators in tensor memory, TMA-fed).
+//
+// "Paged causal K/V cache and cached attention for VisualGen", Description,
+// Attention and Cache (paged attention over per-block rows through the block
+// table, 32-token pages, frame-causal blocks, a real-token count with padding
+// rows returned as zeros), and "Support shared-prefix attention for n-sample
+// requests in FMHA" (the group's rows attend the shared pages once and return
+// output + LSE for the merge).  Prefill, block-causal and shared-prefix tiles
+// are dense contractions: enough query rows share each K/V page.
+//
+// One CTA = one tile of 128 query rows packed as (token, grouped head): token
+// t0 + r / G, query head kvh * G + r % G for tensor-memory lane r, so the G
+// query heads that share a K/V head share every K/V load.  Keys are walked in
+// tiles of 128 (four 32-token pages) within the CTA's key split.
+//
+// Roles (192 threads, one CTA per SM):
+//  * warps 0-3 (softmax): load the Q tile into swizzled shared memory; for
+//    each key tile read S = Q K^T from tensor memory (one row per thread),
+//    mask, online softmax in base 2 with a lazily moved maximum, write P as
+//    bf16 into shared memory in the MMA's K-major swizzled layout, rescale O
+//    in tensor memory when the maximum moved; finally normalise O and store it.
+//  * warp 4 lane 0 (producer): TMA loads of K pages (3-stage ring) and V
+//    pages (2-stage ring), 4 pages x 2 column halves per 128-key tile, through
+//    the block table; pages past the sequence are read out of bounds, which
+//    TMA fills with zeros.
+//  * warp 5 (MMA): allocates 512 tensor-memory columns (two S buffers and O),
+//    issues S_{j+2} = Q K_{j+2}^T and O += P_j V_j with tcgen05.mma
+//    (kind::f16, bf16 in, f32 accumulate, M = N = 128), and signals through
+//    tcgen05.commit on mbarriers.
+// Every mbarrier wait gives up after ~2 s (error bit, orderly exit).
+#include <cuda.h>
+
+#include "pkv_common.cuh"
+#include "pkv_internal.h"
+
+namespace pkv {
+namespace {
+
+constexpr int kD = 128;                 // head dim handled here
+constexpr int kTileM = 128;             // query rows per tile (tensor-memory lanes)
+constexpr int kTileN = 128;             // keys per tile
+constexpr int kKStages = 3;
+constexpr int kVStages = 2;
+constexpr int kThreads = 192;
+constexpr int kHalfBytes = kTileM * 128;           // 128 rows x 64 bf16 = 16 KiB
+constexpr int kTileBytes = 2 * kHalfBytes;         // 128 x 128 bf16 = 32 KiB
+constexpr int kQOff = 0;
+constexpr int kKOff = kQOff + kTileBytes;
+constexpr int kVOff = kKOff + kKStages * kTileBytes;
+constexpr int kPOff = kVOff + kVStages * kTileBytes;
+constexpr int kBarOff = kPOff + kTileBytes;
+// barriers: q_ready, k_full[3], k_empty[3], v_full[2], v_empty[2], s_full[2], p_full, p_free
+constexpr int kNumBars = 1 + 2 * kKStages + 2 * kVStages + 2 + 2;
+constexpr int kTmemSlotOff = kBarOff + kNumBars * 8;
+constexpr int kFlagOff = kTmemSlotOff + 8;
+constexpr int kSmemBytes = kFlagOff + 16;
+static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
+constexpr uint32_t kTmemCols = 512;     // S0 [0,128), S1 [128,256), O [256,384)
+constexpr float kLazyRescale = 8.0f;    // move the running max only past 2^8 growth
+
+// ---------------------------------------------------------------------------
+// tcgen05 wrappers
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void tmem_alloc(uint32_t* slot, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+                 ::"r"(smem_u32(slot)), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+// D[tmem] (+)= A[smem desc] * B[smem desc]
+__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                          uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+        ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate) : "memory");
+}
+// arrive on the mbarrier once all previously issued tcgen05 operations of this thread completed
+__device__ __forceinline__ void umma_commit(uint64_t* bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+                 ::"r"(smem_u32(bar)) : "memory");
+}
+
+#define PKV_R8(i) "=r"(v[i + 0]), "=r"(v[i + 1]), "=r"(v[i + 2]), "=r"(v[i + 3]), \
+                  "=r"(v[i + 4]), "=r"(v[i + 5]), "=r"(v[i + 6]), "=r"(v[i + 7])
+// 32 consecutive 32-bit columns of this thread's lane; waits for completion
+__device__ __forceinline__ void tmem_load32(uint32_t taddr, uint32_t (&v)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : PKV_R8(0), PKV_R8(8), PKV_R8(16), PKV_R8(24)
+        : "r"(taddr) : "memory");
+}
+#undef PKV_R8
+#define PKV_W8(i) "r"(v[i + 0]), "r"(v[i + 1]), "r"(v[i + 2]), "r"(v[i + 3]), \
+                  "r"(v[i + 4]), "r"(v[i + 5]), "r"(v[i + 6]), "r"(v[i + 7])
+__device__ __forceinline__ void tmem_store32(uint32_t taddr, const uint32_t (&v)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
+        "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};\n\t"
+        "tcgen05.wait::st.sync.aligned;"
+        ::"r"(taddr), PKV_W8(0), PKV_W8(8), PKV_W8(16), PKV_W8(24) : "memory");
+}
+#undef PKV_W8
+
+// Shared-memory matrix descriptor: 128-byte swizzle, start address, leading
+// and stride byte offsets (all in 16-byte units), descriptor version 1.
+__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    return static_cast<uint64_t>((saddr >> 4) & 0x3FFFu) |
+           (static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16) |
+           (static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
+}
+// Instruction descriptor, kind::f16: f32 accumulator, bf16 A and B, A K-major,
+// B K-major or MN-major, M and N.
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool b_mn_major) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn_major ? 1u : 0u) << 16) |
+           (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+__device__ __forceinline__ int visible_keys(int i, int qreal, int kv_len, int mask, int cb) {
+    if (i >= qreal) return 0;
+    const int first_new = kv_len - qreal;
+    if (mask == PKV_MASK_NONE) return kv_len;
+    if (mask == PKV_MASK_CAUSAL) return first_new + i + 1;
+    const int block_end = (i / cb + 1) * cb;
+    return first_new + min(qreal, block_end);
+}
+
+struct TileGeom {
+    int b, kvh, split, r0, nrows, qreal, kv_len, t0, kb, key_hi, nt;
+};
+
+__device__ __forceinline__ TileGeom tile_geometry(const AttnParams& p, int TQ) {
+    TileGeom g;
+    g.b = blockIdx.z / p.num_splits;
+    g.split = blockIdx.z - g.b * p.num_splits;
+    g.kvh = blockIdx.y;
+    g.r0 = p.q_indptr[g.b];
+    g.nrows = min(p.q_indptr[g.b + 1] - g.r0, p.max_q_rows);
+    g.t0 = blockIdx.x * TQ;
+    g.qreal = min(p.q_real ? p.q_real[g.b] : g.nrows, g.nrows);
+    g.kv_len = min(max(p.kv_lens[g.b], 0), p.max_kv_len);
+    g.kb = g.split * p.split_keys;
+    const int ke = min(g.kv_len, g.kb + p.split_keys);
+    // visibility is non-decreasing in the row, so the tile's last real row bounds it
+    const int last = min(g.t0 + TQ, g.nrows) - 1;
+    int lim = 0;
+    if (g.t0 < g.qreal)
+        lim = visible_keys(min(last, g.qreal - 1), g.qreal, g.kv_len, p.mask, max(p.causal_block, 1));
+    g.key_hi = min(ke, lim);
+    g.nt = g.key_hi > g.kb ? (g.key_hi - g.kb + kTileN - 1) / kTileN : 0;
+    return g;
+}
+
+// Write the state of one row (normalised O, LSE) to the output, or to the
+// split partials when the call has several key splits.
+__device__ __forceinline__ void store_row(const AttnParams& p, const TileGeom& g, int row_in_seq,
+                                          int h, const float* o, float inv_l, float lse) {
+    const int64_t st = static_cast<int64_t>(g.r0 + row_in_seq) * p.num_q_heads + h;
+    if (p.num_splits == 1) {
+        if (p.out_f32) {
+            float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) + st * kD);
+#pragma unroll
+            for (int c = 0; c < kD / 4; ++c)
+                dst[c] = make_float4(o[4 * c] * inv_l, o[4 * c + 1] * inv_l, o[4 * c + 2] * inv_l,
+                                     o[4 * c + 3] * inv_l);
+        } else {
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + st * kD);
+#pragma unroll
+            for (int c = 0; c < kD / 8; ++c)
+                dst[c] = make_uint4(pack_bf16x2(o[8 * c] * inv_l, o[8 * c + 1] * inv_l),
+                                    pack_bf16x2(o[8 * c + 2] * inv_l, o[8 * c + 3] * inv_l),
+                                    pack_bf16x2(o[8 * c + 4] * inv_l, o[8 * c + 5] * inv_l),
+                                    pack_bf16x2(o[8 * c + 6] * inv_l, o[8 * c + 7] * inv_l));
+        }
+        if (p.lse) p.lse[st] = lse;
+    } else {
+        if (g.r0 + row_in_seq >= static_cast<int64_t>(p.batch) * p.max_q_rows) return;
+        float4* dst = reinterpret_cast<float4*>(p.ws_o + (st * p.num_splits + g.split) * kD);
+#pragma unroll
+        for (int c = 0; c < kD / 4; ++c)
+            dst[c] = make_float4(o[4 * c] * inv_l, o[4 * c + 1] * inv_l, o[4 * c + 2] * inv_l,
+                                 o[4 * c + 3] * inv_l);
+        p.ws_lse[st * p.num_splits + g.split] = lse;
+    }
+}
+
+template <int G>
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                   const AttnParams p) {
+    constexpr int TQ = kTileM / G;
+    extern __shared__ __align__(1024) uint8_t smem[];
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    const TileGeom g = tile_geometry(p, TQ);
+    if (g.t0 >= g.nrows) return;  // tile past this sequence's rows (uniform)
+
+    if (g.nt == 0) {
+        // no visible key in this split for any row of the tile: empty states
+        if (threadIdx.x < kTileM) {
+            const int r = threadIdx.x;
+            const int i = g.t0 + r / G;
+            if (i < g.nrows) {
+                float zero[kD];
+#pragma unroll
+                for (int d = 0; d < kD; ++d) zero[d] = 0.f;
+                store_row(p, g, i, g.kvh * G + r % G, zero, 0.f, -INFINITY);
+            }
+        }
+        return;
+    }
+    if ((smem_u32(smem) & 1023u) != 0) {  // the swizzle needs 1024-byte aligned tiles
+        if (threadIdx.x == 0) set_err(p.err, PKV_ERRBIT_TIMEOUT);
+        return;
+    }
+
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kBarOff);
+    uint64_t* q_ready = bars;
+    uint64_t* k_full = bars + 1;
+    uint64_t* k_empty = k_full + kKStages;
+    uint64_t* v_full = k_empty + kKStages;
+    uint64_t* v_empty = v_full + kVStages;
+    uint64_t* s_full = v_empty + kVStages;
+    uint64_t* p_full = s_full + 2;
+    uint64_t* p_free = p_full + 1;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kTmemSlotOff);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kFlagOff);
+
+    if (threadIdx.x == 0) {
+        mbar_init(q_ready, kTileM);
+        for (int s = 0; s < kKStages; ++s) {
+            mbar_init(&k_full[s], 1);
+            mbar_init(&k_empty[s], 1);
+        }
+        for (int s = 0; s < kVStages; ++s) {
+            mbar_init(&v_full[s], 1);
+            mbar_init(&v_empty[s], 1);
+        }
+        mbar_init(&s_full[0], 1);
+        mbar_init(&s_full[1], 1);
+        mbar_init(p_full, kTileM);
+        mbar_init(p_free, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 5) {
+        tmem_alloc(tmem_slot, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const uint32_t sbase = smem_u32(smem);
+
+    // a wait that gives up marks the CTA aborted; later waits return at once
+    auto wait = [&](uint64_t* bar, uint32_t parity) -> bool {
+        if (*abort_flag) return false;
+        if (mbar_wait(bar, parity)) return true;
+        *abort_flag = 1;
+        set_err(p.err, PKV_ERRBIT_TIMEOUT);
+        return false;
+    };
+
+    if (warp == 4) {
+        // ============================ producer ==============================
+        if (lane == 0) {
+            prefetch_tmap(&tm_k);
+            prefetch_tmap(&tm_v);
+            const int32_t* bt = p.block_table + static_cast<int64_t>(g.b) * p.block_table_stride;
+            const int last_page = (g.kv_len + 31) / 32;  // pages at or past it are never read
+            int k_issued = 0, v_issued = 0;
+            auto load_tile = [&](const CUtensorMap* tm, uint8_t* dst, uint64_t* bar, int j) {
+                mbar_arrive_expect_tx(bar, kTileBytes);
+#pragma unroll
+                for (int pg = 0; pg < 4; ++pg) {
+                    const int lp = (g.kb + j * kTileN) / 32 + pg;
+                    int phys = lp < last_page ? bt[lp] : static_cast<int>(p.num_pages);
+                    if (p.checked && lp < last_page && (phys < 0 || phys >= p.num_pages)) {
+                        set_err(p.err, PKV_ERRBIT_PAGE);
+                        phys = static_cast<int>(p.num_pages);
+                    }
+#pragma unroll
+                    for (int h = 0; h < 2; ++h)
+                        tma_load_4d(dst + h * kHalfBytes + pg * 4096, tm, bar, h * 64, g.kvh, 0, phys);
+                }
+            };
+            // K runs ahead of V by the depth of its ring
+            for (int j = 0; j < g.nt || v_issued < g.nt;) {
+                bool progressed = false;
+                if (k_issued < g.nt && k_issued < v_issued + kKStages) {
+                    const int s = k_issued % kKStages;
+                    if (k_issued >= kKStages && !wait(&k_empty[s], ((k_issued / kKStages) - 1) & 1)) break;
+                    load_tile(&tm_k, smem + kKOff + s * kTileBytes, &k_full[s], k_issued);
+                    ++k_issued;
+                    progressed = true;
+                }
+                if (v_issued < g.nt && v_issued < k_issued) {
+                    const int s = v_issued % kVStages;
+                    if (v_issued >= kVStages && !wait(&v_empty[s], ((v_issued / kVStages) - 1) & 1)) break;
+                    load_tile(&tm_v, smem + kVOff + s * kTileBytes, &v_full[s], v_issued);
+                    ++v_issued;
+                    progressed = true;
+                }
+                j = k_issued;
+                if (!progressed) break;
+            }
+            // do not leave with copies into this CTA's shared memory in flight
+            for (int j = max(0, k_issued - kKStages); j < k_issued; ++j)
+                mbar_wait(&k_full[j % kKStages], (j / kKStages) & 1);
+            for (int j = max(0, v_issued - kVStages); j < v_issued; ++j)
+                mbar_wait(&v_full[j % kVStages], (j / kVStages) & 1);
+        }
+    } else if (warp == 5) {
+        // ============================== MMA ================================
+        if (lane == 0) {
+            constexpr uint32_t kIdescS = idesc_bf16(kTileM, kTileN, false);  // K rows are K-major
+            constexpr uint32_t kIdescO = idesc_bf16(kTileM, kD, true);       // V rows are MN-major
+            const uint32_t tmem_o = tmem + 256;
+            auto issue_s = [&](int j) -> bool {
+                const int s = j % kKStages;
+                if (!wait(&k_full[s], (j / kKStages) & 1)) return false;
+                tc_fence_after();
+                const uint32_t qa = sbase + kQOff, kbse = sbase + kKOff + s * kTileBytes;
+#pragma unroll
+                for (int kk = 0; kk < kD / 16; ++kk) {
+                    const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
+                    umma_bf16(tmem + (j & 1) * 128, sdesc_sw128(qa + off, 16, 1024),
+                              sdesc_sw128(kbse + off, 16, 1024), kIdescS, kk > 0);
+                }
+                umma_commit(&s_full[j & 1]);
+                umma_commit(&k_empty[s]);
+                return true;
+            };
+            bool ok = wait(q_ready, 0);
+            if (ok) ok = issue_s(0);
+            if (ok && g.nt > 1) ok = issue_s(1);
+            for (int j = 0; ok && j < g.nt; ++j) {
+                if (!wait(p_full, j & 1) || !wait(&v_full[j % kVStages], (j / kVStages) & 1)) break;
+                tc_fence_after();
+                const uint32_t pa = sbase + kPOff;
+                const uint32_t vb = sbase + kVOff + (j % kVStages) * kTileBytes;
+#pragma unroll
+                for (int kk = 0; kk < kTileN / 16; ++kk) {
+                    // A = P (K-major over keys), B = V (rows = keys, columns = dims: MN-major);
+                    // the two 64-column halves of V are LBO apart, 8-key groups SBO apart
+                    const uint64_t a = sdesc_sw128(pa + (kk >> 2) * kHalfBytes + (kk & 3) * 32, 16, 1024);
+                    const uint64_t bdesc = sdesc_sw128(vb + kk * 16 * 128, kHalfBytes, 1024);
+                    umma_bf16(tmem_o, a, bdesc, kIdescO, (j > 0 || kk > 0) ? 1u : 0u);
+                }
+                umma_commit(&v_empty[j % kVStages]);
+                umma_commit(p_free);
+                if (j + 2 < g.nt && !issue_s(j + 2)) break;
+            }
+        }
+    } else {
+        // ============================ softmax ===============================
+        const int r = threadIdx.x;             // tile row = tensor-memory lane
+        const int t = r / G, hg = r % G;
+        const int i = g.t0 + t;                // query row within the sequence
+        const int h = g.kvh * G + hg;
+        const bool row_exists = i < g.nrows;
+        const int limit = row_exists ? visible_keys(i, g.qreal, g.kv_len, p.mask, max(p.causal_block, 1))
+                                     : 0;
+        // ---- Q tile -> swizzled shared memory (rows past the sequence: zeros)
+        {
+            const uint4* src = reinterpret_cast<const uint4*>(
+                static_cast<const __nv_bfloat16*>(p.q) + static_cast<int64_t>(g.r0 + i) * p.q_token_stride +
+                static_cast<int64_t>(h) * p.q_head_stride);
+#pragma unroll
+            for (int c = 0; c < 16; ++c) {
+                const uint4 v = row_exists ? src[c] : make_uint4(0u, 0u, 0u, 0u);
+                *reinterpret_cast<uint4*>(smem + kQOff + (c >> 3) * kHalfBytes +
+                                          sw128_offset(r, c & 7)) = v;
+            }
+            fence_proxy_async_smem();
+            mbar_arrive(q_ready);
+        }
+        const uint32_t lane_addr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+        float m_used = -INFINITY;   // base-2 running maximum used for the exponentials
+        float l = 0.f;
+        uint8_t* prow = smem + kPOff;
+        // warp-collective tensor-memory accesses follow every wait, so a wait
+        // counts as passed only if it passed in every lane of the warp
+        auto wait_warp = [&](uint64_t* bar, uint32_t parity) -> bool {
+            return __all_sync(0xffffffffu, wait(bar, parity));
+        };
+        for (int j = 0; j < g.nt; ++j) {
+            if (!wait_warp(&s_full[j & 1], (j >> 1) & 1)) break;
+            tc_fence_after();
+            const int key0 = g.kb + j * kTileN;
+            float s[kTileN];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                uint32_t v[32];
+                tmem_load32(lane_addr + (j & 1) * 128 + c * 32, v);
+#pragma unroll
+                for (int e = 0; e < 32; ++e) s[c * 32 + e] = __uint_as_float(v[e]) * p.scale_log2;
+            }
+            // mask keys at or past this row's visible limit
+            const int nvis = limit - key0;
+            float mx = -INFINITY;
+            if (nvis < kTileN) {
+#pragma unroll
+                for (int e = 0; e < kTileN; ++e) s[e] = e < nvis ? s[e] : -INFINITY;
+            }
+#pragma unroll
+            for (int e = 0; e < kTileN; ++e) mx = fmaxf(mx, s[e]);
+            float alpha = 1.f;
+            if (mx > m_used + kLazyRescale) {   // also true the first time a key is visible
+                alpha = fast_exp2(m_used - mx);  // 0 when m_used was -inf
+                m_used = mx;
+            }
+            const float mref = m_used == -INFINITY ? 0.f : m_used;
+            uint32_t pk[kTileN / 2];
+            float rs = 0.f;
+#pragma unroll
+            for (int e = 0; e < kTileN; e += 2) {
+                const float p0 = fast_exp2(s[e] - mref), p1 = fast_exp2(s[e + 1] - mref);
+                pk[e / 2] = pack_bf16x2(p0, p1);
+                // the row sum uses the bf16 probabilities the P.V product uses, so
+                // numerator and denominator carry the same rounding
+                rs += bf16lo(pk[e / 2]) + bf16hi(pk[e / 2]);
+            }
+            l = l * alpha + rs;
+            // P buffer and O are free once the previous P.V finished
+            if (j > 0 && !wait_warp(p_free, (j - 1) & 1)) break;
+            tc_fence_after();
+            if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+                // O *= alpha for this row (warp-collective tensor-memory access)
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t v[32];
+                    tmem_load32(lane_addr + 256 + c * 32, v);
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
+                    tmem_store32(lane_addr + 256 + c * 32, v);
+                }
+            }
+            // P row -> shared memory, K-major 128-byte swizzle, two 64-key halves
+#pragma unroll
+            for (int c = 0; c < 16; ++c)
+                *reinterpret_cast<uint4*>(prow + (c >> 3) * kHalfBytes + sw128_offset(r, c & 7)) =
+                    make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+            // V rows of keys past the sequence's length inside its last page hold
+            // whatever the pool holds there; zero them so 0 * garbage cannot make NaN
+            if (key0 + kTileN > g.kv_len && g.kv_len > key0) {
+                const int vs = j % kVStages;
+                if (!wait_warp(&v_full[vs], (j / kVStages) & 1)) break;
+                const int first = g.kv_len - key0;
+                const int last = min(kTileN, (first + 31) / 32 * 32);
+                uint8_t* vt = smem + kVOff + vs * kTileBytes;
+                for (int idx = r; idx < (last - first) * 16; idx += kTileM) {
+                    const int row = first + idx / 16, c = idx % 16;
+                    *reinterpret_cast<uint4*>(vt + (c >> 3) * kHalfBytes + sw128_offset(row, c & 7)) =
+                        make_uint4(0u, 0u, 0u, 0u);
+                }
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(p_full);
+        }
+        // ---- epilogue: O / l
+        const bool ok = wait_warp(p_free, (g.nt - 1) & 1);
+        tc_fence_after();
+        float o[kD];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            uint32_t v[32];
+            tmem_load32(lane_addr + 256 + c * 32, v);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) o[c * 32 + e] = __uint_as_float(v[e]);
+        }
+        if (ok && row_exists) {
+            const bool any = l > 0.f;
+            const float inv_l = any ? 1.0f / l : 0.f;
+            const float lse = any ? (m_used + __log2f(l)) * kLn2 : -INFINITY;
+            if (!any) {
+#pragma unroll
+                for (int d = 0; d < kD; ++d) o[d] = 0.f;
+            }
+            store_row(p, g, i, h, o, inv_l, lse);
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 5) tmem_dealloc(tmem, kTmemCols);
+}
+
+template <int G>
+cudaError_t launch_g(const AttnParams& p, const void* tk, const void* tv, cudaStream_t s) {
+    auto kern = attn_tc_kernel<G>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e != cudaSuccess) return e;
+    const int TQ = kTileM / G;
+    dim3 grid((p.max_q_rows + TQ - 1) / TQ, p.num_kv_heads, p.batch * p.num_splits);
+    kern<<<grid, kThreads, kSmemBytes, s>>>(*static_cast<const CUtensorMap*>(tk),
+                                            *static_cast<const CUtensorMap*>(tv), p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+bool attn_tc_supported(int head_dim, int group) {
+    return head_dim == kD && (group == 1 || group == 2 || group == 4 || group == 8 || group == 16);
+}
+
+int attn_tc_rows_per_tile(int group) { return kTileM / group; }
+
+cudaError_t launch_attn_tc(const AttnParams& p, const void*, const void* tk, const void* tv,
+                           cudaStream_t s) {
+    const int G = p.num_q_heads / p.num_kv_heads;
+    switch (G) {
+        case 1: return launch_g<1>(p, tk, tv, s);
+        case 2: return launch_g<2>(p, tk, tv, s);
+        case 4: return launch_g<4>(p, tk, tv, s);
+        case 8: return launch_g<8>(p, tk, tv, s);
+        case 16: return launch_g<16>(p, tk, tv, s);
+    }
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace pkv

@@ -88,7 +88,7 @@ pkv_status make_pool_map(CUtensorMap* m, const void* base, int D, int Hkv, int p
     return PKV_OK;
 }
 
-enum class Kernel { kNone, kDecode, kSimt };
+enum class Kernel { kNone, kDecode, kSimt, kTile };
 
 struct Plan {
     Kernel kernel = Kernel::kNone;
@@ -101,10 +101,34 @@ constexpr int kDecodeSplitKeys = 512;  // 16 pages: the pages' minimum split of 
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+constexpr int kPlanSMs = 152;          // GB300; only shapes the split choice
+constexpr int kTileKeys = 128;         // key tile of the tensor-core kernel
+
 Plan plan_attention(int batch, int max_q_rows, int Hq, int Hkv, int D, int max_kv_len,
                     int num_splits, unsigned flags) {
     Plan pl;
     const int G = Hkv > 0 ? Hq / Hkv : 0;
+    if (!(flags & PKV_FLAG_SIMT_ONLY) && max_q_rows > 1 && pkv::attn_tc_supported(D, G)) {
+        // tensor-core tiles; split the keys only when the tiles cannot half-fill the GPU
+        pl.kernel = Kernel::kTile;
+        const int64_t tiles = static_cast<int64_t>((max_q_rows + pkv::attn_tc_rows_per_tile(G) - 1) /
+                                                   pkv::attn_tc_rows_per_tile(G)) * Hkv * batch;
+        int s = 1;
+        if (num_splits > 0) {
+            s = num_splits;
+        } else if (tiles * 2 < kPlanSMs) {
+            s = static_cast<int>(std::min<int64_t>(8, (kPlanSMs + tiles - 1) / tiles));
+            s = std::max(1, std::min(s, (max_kv_len + 511) / 512));
+        }
+        const int per = (max_kv_len + s - 1) / std::max(s, 1);
+        pl.split_keys = std::max(kTileKeys, (per + kTileKeys - 1) / kTileKeys * kTileKeys);
+        pl.splits = std::max(1, (max_kv_len + pl.split_keys - 1) / pl.split_keys);
+        if (pl.splits > 1) {
+            const size_t states = static_cast<size_t>(batch) * max_q_rows * Hq * pl.splits;
+            pl.ws_bytes = round_up(states * D * sizeof(float), 256) + round_up(states * sizeof(float), 256);
+        }
+        return pl;
+    }
     if ((flags & PKV_FLAG_SIMT_ONLY) || max_q_rows != 1 || !pkv::decode_supported(D, G)) {
         pl.kernel = Kernel::kSimt;
         return pl;
@@ -230,8 +254,8 @@ pkv_status paged_attention(const void* q, int64_t q_token_stride, int64_t q_head
         q_head_stride % 8 || q_token_stride < 0 || q_head_stride < 0)
         return fail(PKV_ERR_INVALID_ARG,
                     "attention: q / pools must be 16-byte aligned with strides multiple of 8");
-    if (!aligned(out, out_dtype == PKV_F32 ? 16 : 8) || (lse && !aligned(lse, 4)))
-        return fail(PKV_ERR_INVALID_ARG, "attention: output misaligned");
+    if (!aligned(out, 16) || (lse && !aligned(lse, 4)))
+        return fail(PKV_ERR_INVALID_ARG, "attention: output must be 16-byte aligned");
     const int64_t pages_needed = (static_cast<int64_t>(max_kv_len) + page_size - 1) / page_size;
     if (block_table_stride < pages_needed)
         return fail(PKV_ERR_INVALID_ARG, "attention: block_table_stride %lld < %lld pages for max_kv_len",
@@ -277,6 +301,14 @@ pkv_status paged_attention(const void* q, int64_t q_token_stride, int64_t q_head
     p.split_keys = pl.split_keys;
     p.checked = (flags & PKV_FLAG_CHECKED) != 0;
     p.err = err;
+    if (pl.kernel == Kernel::kTile && static_cast<int64_t>(batch) * pl.splits > 65535)
+        return fail(PKV_ERR_UNSUPPORTED, "attention: batch x key splits above 65535");
+    if (pl.kernel == Kernel::kTile && pl.splits > 1) {
+        const size_t states = static_cast<size_t>(batch) * max_q_rows * num_q_heads * pl.splits;
+        p.ws_o = static_cast<float*>(workspace);
+        p.ws_lse = reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                            round_up(states * head_dim * sizeof(float), 256));
+    }
     if (pl.kernel == Kernel::kDecode) {
         char* w = static_cast<char*>(workspace);
         p.ws_counters = reinterpret_cast<int*>(w);
@@ -296,6 +328,12 @@ pkv_status paged_attention(const void* q, int64_t q_token_stride, int64_t q_head
     if (st != PKV_OK) return st;
     st = make_pool_map(&tv, v_pool, head_dim, num_kv_heads, page_size, num_pages, page_stride);
     if (st != PKV_OK) return st;
+    if (pl.kernel == Kernel::kTile) {
+        cudaError_t e = pkv::launch_attn_tc(p, nullptr, &tk, &tv, s);
+        if (e != cudaSuccess) return from_cuda(e, "attention (tensor-core tiles)");
+        if (pl.splits > 1) return from_cuda(pkv::launch_split_reduce(p, s), "attention (split reduce)");
+        return ok();
+    }
     return from_cuda(pkv::launch_decode(p, &tk, &tv, s), "attention (decode)");
 }
 
