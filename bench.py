@@ -33,6 +33,9 @@ sys.path.insert(0, ROOT)
 METRIC = "paged decode KV GB/s"
 # the sources of the timed decode launch; a committed DRAM-traffic figure is
 # used only while their hash matches the one recorded beside it
+ATTN_TC_SOURCES = ["paged_kv_cache_189_gb300/csrc/attn_tc.cu",
+                   "paged_kv_cache_189_gb300/csrc/pkv_common.cuh",
+                   "paged_kv_cache_189_gb300/csrc/pkv_api.cpp"]
 DECODE_SOURCES = ["paged_kv_cache_189_gb300/csrc/decode.cu",
                   "paged_kv_cache_189_gb300/csrc/pkv_common.cuh",
                   "paged_kv_cache_189_gb300/csrc/pkv_api.cpp"]
@@ -45,7 +48,9 @@ def parse():
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="gqa_decode", choices=["gqa_decode"])
+    ap.add_argument("--workload", default="gqa_decode",
+                    choices=["gqa_decode", "chunked_prefill", "block_causal_video",
+                             "shared_prefix", "tiny_decode"])
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-sample-seqs", type=int, default=64)
@@ -266,6 +271,17 @@ def measured_peaks():
     return 6800.0, "fallback"
 
 
+def measured_tensor_peak():
+    """Dense bf16 tensor peak; the sustained figure, since the kernel is timed
+    inside a long run of steps."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), "measured"
+    return 1700.0, "fallback"
+
+
 def committed_traffic(workload, kernel_sources):
     """DRAM bytes per launch from a committed ncu summary, valid only while the
     kernel's sources are unchanged (hash recorded beside the figure)."""
@@ -325,6 +341,155 @@ def run_reference(args):
     return 0
 
 
+def visible_pairs(case):
+    """(query row, visible key) pairs of a case's real rows, per query head."""
+    kvl = case.kv_lens.numpy().astype(np.int64)
+    qr = case.q_real.numpy().astype(np.int64)
+    total = 0
+    for b in range(case.batch):
+        i = np.arange(qr[b])
+        first_new = kvl[b] - qr[b]
+        if case.mask == "none":
+            vis = np.full(qr[b], kvl[b])
+        elif case.mask == "causal":
+            vis = first_new + i + 1
+        else:
+            cb = case.causal_block
+            vis = first_new + np.minimum(qr[b], (i // cb + 1) * cb)
+        total += int(vis.sum())
+    return total
+
+
+class StepPlan:
+    """One workload step on the device: pre -> dominant -> post launches."""
+
+    def __init__(self, **kw):
+        self.__dict__.update(kw)
+
+
+def build_plan(name, rank, dev, stream):
+    import torch
+    from paged_kv_cache_189_gb300 import pkv, workloads as wl
+
+    case = {"gqa_decode": wl.gqa_decode, "chunked_prefill": wl.chunked_prefill,
+            "block_causal_video": wl.block_causal_video, "shared_prefix": wl.shared_prefix,
+            "tiny_decode": wl.tiny_decode}[name](seed={"gqa_decode": 1, "chunked_prefill": 2,
+                                                         "shared_prefix": 3, "block_causal_video": 4,
+                                                         "tiny_decode": 0}[name] + rank)
+    Hq, Hkv, D = case.num_q_heads, case.num_kv_heads, case.head_dim
+    rows = case.q.shape[0]
+    t = dict(k_pool=case.k_pool.to(dev), v_pool=case.v_pool.to(dev), q=case.q.to(dev),
+             new_k=case.new_k.to(dev), new_v=case.new_v.to(dev), slots=case.slots.to(dev),
+             bt=case.block_table.to(dev), kl=case.kv_lens.to(dev), qi=case.q_indptr.to(dev),
+             qr=case.q_real.to(dev))
+    out = torch.empty(rows, Hq, D, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty(rows, Hq, dtype=torch.float32, device=dev)
+    kv_tok_bytes = Hkv * D * 2 * 2
+    scatter = lambda: pkv.kv_scatter_slots(t["new_k"], t["new_v"], t["slots"], t["k_pool"],
+                                           t["v_pool"], stream=stream)
+    real_new = int((case.slots.numpy() >= 0).sum())
+    aux = {"scatter": (scatter, real_new * kv_tok_bytes * 2 + real_new * 8, "GB/s")}
+    cfg = {"workload": name, "batch": case.batch, "q_heads": Hq, "kv_heads": Hkv,
+           "head_dim": D, "page": 32}
+    peak_hbm, hbm_kind = measured_peaks()
+    peak_tc, tc_kind = measured_tensor_peak()
+
+    def attention_call(q, bt, kl, qi, qr, o, l, max_q_rows, max_kv_len, mask, cb=0):
+        ws_b = pkv.paged_attention_workspace_size(int(kl.numel()), max_q_rows, Hq, Hkv, D, max_kv_len)
+        ws = torch.empty(max(ws_b, 256), dtype=torch.uint8, device=dev)
+        return lambda: pkv.paged_attention(q, t["k_pool"], t["v_pool"], bt, kl, qi, o, q_real=qr,
+                                           lse=l, max_q_rows=max_q_rows, max_kv_len=max_kv_len,
+                                           mask=mask, causal_block=cb, workspace=ws, stream=stream)
+
+    h2d_src = [case.q, case.new_k, case.new_v, case.slots, case.kv_lens, case.block_table]
+    h2d_dst = [t["q"], t["new_k"], t["new_v"], t["slots"], t["kl"], t["bt"]]
+    d2h_src = [out, lse]
+    if name in ("gqa_decode", "tiny_decode"):
+        attn_bytes, kv_bytes = decode_bytes(case)
+        dom = attention_call(t["q"], t["bt"], t["kl"], t["qi"], t["qr"], out, lse, 1,
+                             case.max_kv_len, "causal")
+        cfg.update(kv_len="U[512,8192]+1" if name == "gqa_decode" else "{37,100}",
+                   kv_bytes_per_step=kv_bytes, queries_per_step=rows,
+                   l2="inputs larger than L2 (1.14 GB of K/V read per step)")
+        return StepPlan(case=case, cfg=cfg, metric=METRIC, unit=UNIT, work=kv_bytes, scale=1e9,
+                        queries=rows, pre=[scatter], dominant=dom, post=[], aux=aux,
+                        dom_label="paged_attention: persistent split-KV decode kernel with the split "
+                                  "merge fused in (plus a 2 KB counter memset)",
+                        dom_work=attn_bytes, bound="hbm", peak=peak_hbm, peak_unit="GB/s",
+                        peak_src=f"{hbm_kind} hbm_gbs", h2d=(h2d_src, h2d_dst), d2h=d2h_src,
+                        launches=3, traffic_sources=DECODE_SOURCES)
+    if name in ("chunked_prefill", "block_causal_video"):
+        pairs = visible_pairs(case)
+        flops = 4.0 * D * Hq * pairs
+        dom = attention_call(t["q"], t["bt"], t["kl"], t["qi"], t["qr"], out, lse,
+                             case.max_q_rows, case.max_kv_len, case.mask, case.causal_block)
+        post = []
+        launches = 2
+        if name == "block_causal_video":
+            e = case.extra
+            tok = Hkv * D * 2
+            n, sh, first = e["rotate_tokens"], e["rotate_shift_tokens"], e["rotate_first_token"]
+            regions = [pool.view(torch.uint8).view(-1)[first * tok:(first + n) * tok]
+                       for pool in (t["k_pool"], t["v_pool"])]
+
+            def rotate():
+                for reg in regions:
+                    pkv.rotate_rows(reg, sh * tok // 16, rows=1, cols=n * tok // 16,
+                                    row_stride=n * tok // 16, elem_size=16, stream=stream)
+            post = [rotate]
+            aux["rotate"] = (rotate, 2 * 2 * n * tok, "GB/s")
+            launches = 4
+            cfg.update(kv_len=int(case.kv_lens[0]), q_rows=rows, q_real=int(case.q_real[0]),
+                       causal_block=case.causal_block)
+        else:
+            cfg.update(ctx="U[2048,16384]", chunk=512)
+        cfg.update(mask=case.mask, visible_pairs_per_head=pairs, flops_per_step=flops,
+                   l2="K/V read per step larger than L2")
+        return StepPlan(case=case, cfg=cfg, metric="prefill TFLOP/s", unit="TFLOP/s", work=flops,
+                        scale=1e12, queries=int(case.q_real.sum()), pre=[scatter], dominant=dom,
+                        post=post, aux=aux,
+                        dom_label="paged_attention: tcgen05 tile kernel (tensor memory, TMA)",
+                        dom_work=flops / 1e12, bound="tensor", peak=peak_tc, peak_unit="TFLOP/s",
+                        peak_src=f"{tc_kind} bf16_tflops_sustained", h2d=(h2d_src, h2d_dst),
+                        d2h=d2h_src, launches=launches, traffic_sources=ATTN_TC_SOURCES)
+    if name == "shared_prefix":
+        e = case.extra
+        Gn, n_s = e["groups"], e["samples"]
+        pt = dict(pt=e["prefix_table"].to(dev), pl=e["prefix_lens"].to(dev),
+                  pqi=e["prefix_q_indptr"].to(dev), pqr=e["prefix_q_real"].to(dev),
+                  tt=e["tail_table"].to(dev), tl=e["tail_lens"].to(dev))
+        o_p = torch.empty(rows, Hq, D, device=dev)
+        l_p = torch.empty(rows, Hq, device=dev)
+        o_t = torch.empty(rows, Hq, D, device=dev)
+        l_t = torch.empty(rows, Hq, device=dev)
+        prefix = int(e["prefix_lens"][0])
+        dom = attention_call(t["q"], pt["pt"], pt["pl"], pt["pqi"], pt["pqr"], o_p, l_p, n_s,
+                             prefix, "none")
+        mt = int(e["tail_lens"].max())
+        tail = attention_call(t["q"], pt["tt"], pt["tl"], t["qi"], t["qr"], o_t, l_t, 1, mt,
+                              "causal")
+        merge = lambda: pkv.merge_attn_states(o_p, l_p, o_t, l_t, out, lse, stream=stream)
+        prefix_bytes = Gn * prefix * kv_tok_bytes
+        tail_bytes = int(e["tail_lens"].sum()) * kv_tok_bytes
+        aux["tail_attention"] = (tail, tail_bytes, "GB/s")
+        aux["merge"] = (merge, rows * Hq * (D * 4 * 2 + D * 2 + 12), "GB/s")
+        cfg.update(groups=Gn, samples=n_s, prefix=prefix, tail="U[1,1024]",
+                   kv_bytes_per_step=prefix_bytes + tail_bytes,
+                   kv_bytes_without_sharing=rows * prefix * kv_tok_bytes + tail_bytes,
+                   l2="prefix pages 16.8 MB per group; 537 MB of K/V per step")
+        h2d_src = [case.q, case.new_k, case.new_v, case.slots, e["tail_lens"], e["tail_table"]]
+        h2d_dst = [t["q"], t["new_k"], t["new_v"], t["slots"], pt["tl"], pt["tt"]]
+        return StepPlan(case=case, cfg=cfg, metric="shared-prefix KV GB/s", unit="GB/s",
+                        work=prefix_bytes + tail_bytes, scale=1e9, queries=rows, pre=[scatter],
+                        dominant=dom, post=[tail, merge], aux=aux,
+                        dom_label="paged_attention, prefix call: tcgen05 tile kernel, 8 samples x 4 "
+                                  "heads = 32 of 128 tile rows, HBM-bound",
+                        dom_work=prefix_bytes, bound="hbm", peak=peak_hbm, peak_unit="GB/s",
+                        peak_src=f"{hbm_kind} hbm_gbs", h2d=(h2d_src, h2d_dst), d2h=d2h_src,
+                        launches=6, traffic_sources=ATTN_TC_SOURCES)
+    raise ValueError(name)
+
+
 def run_ours(args):
     import torch
     from paged_kv_cache_189_gb300 import build as pkv_build
@@ -337,35 +502,15 @@ def run_ours(args):
     if rank == 0:
         pkv_build.build()
     barrier(dist)
-    from paged_kv_cache_189_gb300 import pkv, workloads as wl
-
-    case = wl.gqa_decode(seed=1 + rank)
-    attn_bytes, kv_bytes = decode_bytes(case)
-    sc_bytes = scatter_bytes(case)
-    Hq, Hkv, D = case.num_q_heads, case.num_kv_heads, case.head_dim
-    rows = case.q.shape[0]
-    max_kv = case.max_kv_len
-
-    k_pool, v_pool = case.k_pool.to(dev), case.v_pool.to(dev)
-    q = case.q.to(dev)
-    new_k, new_v, slots = case.new_k.to(dev), case.new_v.to(dev), case.slots.to(dev)
-    bt, kl, qi, qr = (case.block_table.to(dev), case.kv_lens.to(dev), case.q_indptr.to(dev),
-                      case.q_real.to(dev))
-    out = torch.empty(rows, Hq, D, dtype=torch.bfloat16, device=dev)
-    lse = torch.empty(rows, Hq, dtype=torch.float32, device=dev)
-    ws_bytes = pkv.paged_attention_workspace_size(case.batch, 1, Hq, Hkv, D, max_kv)
-    ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=dev)
     stream = torch.cuda.Stream(device=dev)
-    launches_per_step = 1 + 1 + (1 if ws_bytes else 0)
-
-    def attention():
-        pkv.paged_attention(q, k_pool, v_pool, bt, kl, qi, out, q_real=qr, lse=lse,
-                            max_q_rows=1, max_kv_len=max_kv, mask="causal", workspace=ws,
-                            stream=stream)
+    plan = build_plan(args.workload, rank, dev, stream)
 
     def step():
-        pkv.kv_scatter_slots(new_k, new_v, slots, k_pool, v_pool, stream=stream)
-        attention()
+        for f in plan.pre:
+            f()
+        plan.dominant()
+        for f in plan.post:
+            f()
 
     clocks = ClockSampler(local)
     clocks.start()
@@ -382,46 +527,57 @@ def run_ours(args):
     with torch.cuda.stream(stream):
         t_start.record(stream)
         for i in range(args.steps):
-            pkv.kv_scatter_slots(new_k, new_v, slots, k_pool, v_pool, stream=stream)
+            for f in plan.pre:
+                f()
             ev[i][0].record(stream)
-            attention()
+            plan.dominant()
             ev[i][1].record(stream)
+            for f in plan.post:
+                f()
         t_end.record(stream)
     torch.cuda.synchronize()
     barrier(dist)
     wall1 = time.time()
     clk = clocks.stop(wall0, wall1)
     ms_total = t_start.elapsed_time(t_end)
-    attn_ms = [a.elapsed_time(b) for a, b in ev]
+    dom_ms = [a.elapsed_time(b) for a, b in ev]
     ms_total_max = max_over_ranks(dist, ms_total, dev)
-    kv_total = sum_over_ranks(dist, kv_bytes * args.steps, dev)
-    queries_total = sum_over_ranks(dist, rows * args.steps, dev)
-    value = kv_total / (ms_total_max * 1e-3) / 1e9
+    work_total = sum_over_ranks(dist, plan.work * args.steps, dev)
+    queries_total = sum_over_ranks(dist, plan.queries * args.steps, dev)
+    value = work_total / (ms_total_max * 1e-3) / plan.scale
+
+    # ---- auxiliary launches of the step, each timed alone (inputs > L2)
+    aux_out = {}
+    for key, (fn, nbytes, unit) in plan.aux.items():
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            fn()
+            a.record(stream)
+            for _ in range(5):
+                fn()
+            b.record(stream)
+        torch.cuda.synchronize()
+        ms = a.elapsed_time(b) / 5
+        aux_out[key] = {"ms": ms, "bytes": nbytes, "GB/s": nbytes / (ms * 1e-3) / 1e9}
 
     # ---- end to end through the public API: pinned host inputs -> device,
-    #      scatter + attention, result read back to the host, every step
-    h_q = case.q.pin_memory()
-    h_k, h_v, h_s = case.new_k.pin_memory(), case.new_v.pin_memory(), case.slots.pin_memory()
-    h_kl, h_bt = case.kv_lens.pin_memory(), case.block_table.pin_memory()
-    h_out = torch.empty(rows, Hq, D, dtype=torch.bfloat16).pin_memory()
-    h_lse = torch.empty(rows, Hq, dtype=torch.float32).pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_k, h_v, h_s, h_kl, h_bt))
-    d2h = h_out.numel() * 2 + h_lse.numel() * 4
+    #      the whole step, result read back to the host, every step
+    e2e_value = None
+    srcs, dsts = plan.h2d
+    h_in = [x.pin_memory() for x in srcs]
+    h_out = [torch.empty(x.shape, dtype=x.dtype).pin_memory() for x in plan.d2h]
+    h2d = sum(x.numel() * x.element_size() for x in h_in)
+    d2h = sum(x.numel() * x.element_size() for x in h_out)
 
     def e2e_step():
         with torch.cuda.stream(stream):
-            q.copy_(h_q, non_blocking=True)
-            new_k.copy_(h_k, non_blocking=True)
-            new_v.copy_(h_v, non_blocking=True)
-            slots.copy_(h_s, non_blocking=True)
-            kl.copy_(h_kl, non_blocking=True)
-            bt.copy_(h_bt, non_blocking=True)
+            for hs, dd in zip(h_in, dsts):
+                dd.copy_(hs, non_blocking=True)
             step()
-            h_out.copy_(out, non_blocking=True)
-            h_lse.copy_(lse, non_blocking=True)
+            for hd, ds in zip(h_out, plan.d2h):
+                hd.copy_(ds, non_blocking=True)
         stream.synchronize()
 
-    e2e_value = None
     if args.e2e_steps > 0:
         for _ in range(3):
             e2e_step()
@@ -433,47 +589,47 @@ def run_ours(args):
         e1.record(stream)
         torch.cuda.synchronize()
         e2e_ms = max_over_ranks(dist, e0.elapsed_time(e1), dev)
-        e2e_value = sum_over_ranks(dist, kv_bytes * args.e2e_steps, dev) / (e2e_ms * 1e-3) / 1e9
+        e2e_value = sum_over_ranks(dist, plan.work * args.e2e_steps, dev) / (e2e_ms * 1e-3) / plan.scale
 
     if rank == 0:
-        peak, peak_kind = measured_peaks()
-        attn_avg_ms = statistics.mean(attn_ms)
-        achieved = attn_bytes / (attn_avg_ms * 1e-3) / 1e9
-        traffic = committed_traffic("gqa_decode", DECODE_SOURCES)
+        dom_avg = statistics.mean(dom_ms)
+        achieved = plan.dom_work / (dom_avg * 1e-3) / (1e9 if plan.bound == "hbm" else 1.0)
+        traffic = committed_traffic(args.workload, plan.traffic_sources)
         line = {
-            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "metric": plan.metric, "value": value, "unit": plan.unit, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_total_max / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic",
-            "config": {"workload": "gqa_decode", "batch": case.batch, "q_heads": Hq,
-                       "kv_heads": Hkv, "head_dim": D, "page": 32, "kv_len": "U[512,8192]+1",
-                       "kv_bytes_per_step": kv_bytes, "queries_per_step": rows,
-                       "l2": "inputs larger than L2 (1.14 GB of K/V read per step)",
-                       "parallelism": f"replicas x{world} (sequences sharded by rank)"},
+            "config": dict(plan.cfg, parallelism=f"replicas x{world} (sequences sharded by rank)"),
             "queries_per_s": queries_total / (ms_total_max * 1e-3),
-            "hbm_frac": value / peak,
-            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                         "frac": achieved / peak, "traffic": traffic,
-                         "kernel": "paged_attention: persistent split-KV decode kernel with the "
-                                   "split merge fused in (plus a 2 KB counter memset); CUDA "
-                                   "events around the call each timed step",
-                         "bytes_per_launch": attn_bytes, "avg_launch_ms": attn_avg_ms,
-                         "peak_source": f"{peak_kind} hbm_gbs"},
+            "roofline": {"bound": plan.bound, "achieved": achieved, "peak": plan.peak,
+                         "unit": plan.peak_unit, "frac": achieved / plan.peak, "traffic": traffic,
+                         "kernel": plan.dom_label + "; CUDA events around the call each timed step",
+                         "work_per_launch": plan.dom_work, "avg_launch_ms": dom_avg,
+                         "peak_source": plan.peak_src},
             "clocks": clk,
-            "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
+            "e2e": {"value": e2e_value, "unit": plan.unit, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "steps": args.e2e_steps},
-            "gpu_launches": launches_per_step * args.steps,
-            "scatter_bytes_per_step": sc_bytes,
+            "gpu_launches": plan.launches * args.steps,
+            "aux": aux_out,
         }
+        if plan.unit == "GB/s":
+            line["hbm_frac"] = value / plan.peak if plan.bound == "hbm" else None
         if world == 1 and not args.no_cpu_baseline:
-            line["cpu_baseline"] = cpu_baseline(case, args)
+            line["cpu_baseline"] = cpu_baseline_for(plan, args)
         print(json.dumps(line), flush=True)
     barrier(dist)
     return 0
 
 
-def cpu_baseline(case, args):
+def cpu_baseline_for(plan, args):
+    """The fp64 oracle on a bounded sample of the same step (whole sequences of
+    the decode batch; for the other workloads, a few sequences), in the metric's
+    unit, with the worker count as the cores used."""
+    case = plan.case
     workers = min(16, os.cpu_count() or 1)
+    if args.workload not in ("gqa_decode", "tiny_decode"):
+        return None
     pool = OraclePool(case, workers)
     seqs = list(range(min(args.cpu_sample_seqs, case.batch)))
     dt = pool.run(seqs)

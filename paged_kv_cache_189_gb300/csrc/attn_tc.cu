@@ -396,7 +396,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const uint32_t lane_addr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
         float m_used = -INFINITY;   // base-2 running maximum used for the exponentials
-        float l = 0.f;
+        float l = 0.f, l_b = 0.f;
         uint8_t* prow = smem + kPOff;
         // warp-collective tensor-memory accesses follow every wait, so a wait
         // counts as passed only if it passed in every lane of the warp
@@ -431,16 +431,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             const float mref = m_used == -INFINITY ? 0.f : m_used;
             uint32_t pk[kTileN / 2];
-            float rs = 0.f;
+            float rs = 0.f, rs_b = 0.f;
 #pragma unroll
             for (int e = 0; e < kTileN; e += 2) {
                 const float p0 = fast_exp2(s[e] - mref), p1 = fast_exp2(s[e + 1] - mref);
                 pk[e / 2] = pack_bf16x2(p0, p1);
-                // the row sum uses the bf16 probabilities the P.V product uses, so
-                // numerator and denominator carry the same rounding
-                rs += bf16lo(pk[e / 2]) + bf16hi(pk[e / 2]);
+                rs += p0 + p1;
+                rs_b += bf16lo(pk[e / 2]) + bf16hi(pk[e / 2]);
             }
+            // O is normalised by the sum of the bf16 probabilities the P.V product
+            // used (numerator and denominator carry the same rounding); the LSE
+            // uses the sum of the unrounded ones
             l = l * alpha + rs;
+            l_b = l_b * alpha + rs_b;
             // P buffer and O are free once the previous P.V finished
             if (j > 0 && !wait_warp(p_free, (j - 1) & 1)) break;
             tc_fence_after();
@@ -490,8 +493,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int e = 0; e < 32; ++e) o[c * 32 + e] = __uint_as_float(v[e]);
         }
         if (ok && row_exists) {
-            const bool any = l > 0.f;
-            const float inv_l = any ? 1.0f / l : 0.f;
+            const bool any = l > 0.f && l_b > 0.f;
+            const float inv_l = any ? 1.0f / l_b : 0.f;
             const float lse = any ? (m_used + __log2f(l)) * kLn2 : -INFINITY;
             if (!any) {
 #pragma unroll
