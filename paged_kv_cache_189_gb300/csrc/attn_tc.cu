@@ -106,6 +106,28 @@ __device__ __forceinline__ void tmem_load32(uint32_t taddr, uint32_t (&v)[32]) {
         : PKV_R8(0), PKV_R8(8), PKV_R8(16), PKV_R8(24)
         : "r"(taddr) : "memory");
 }
+// 128 consecutive 32-bit columns (four 32-column loads, one wait)
+__device__ __forceinline__ void tmem_load128(uint32_t taddr, uint32_t (&v)[128]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%128];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, "
+        "%48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63}, [%129];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%64, %65, %66, %67, %68, %69, %70, %71, %72, %73, %74, %75, %76, %77, %78, %79, "
+        "%80, %81, %82, %83, %84, %85, %86, %87, %88, %89, %90, %91, %92, %93, %94, %95}, [%130];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%96, %97, %98, %99, %100, %101, %102, %103, %104, %105, %106, %107, %108, %109, %110, "
+        "%111, %112, %113, %114, %115, %116, %117, %118, %119, %120, %121, %122, %123, %124, %125, "
+        "%126, %127}, [%131];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : PKV_R8(0), PKV_R8(8), PKV_R8(16), PKV_R8(24), PKV_R8(32), PKV_R8(40), PKV_R8(48),
+          PKV_R8(56), PKV_R8(64), PKV_R8(72), PKV_R8(80), PKV_R8(88), PKV_R8(96), PKV_R8(104),
+          PKV_R8(112), PKV_R8(120)
+        : "r"(taddr), "r"(taddr + 32), "r"(taddr + 64), "r"(taddr + 96) : "memory");
+}
 #undef PKV_R8
 #define PKV_W8(i) "r"(v[i + 0]), "r"(v[i + 1]), "r"(v[i + 2]), "r"(v[i + 3]), \
                   "r"(v[i + 4]), "r"(v[i + 5]), "r"(v[i + 6]), "r"(v[i + 7])
@@ -407,43 +429,47 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!wait_warp(&s_full[j & 1], (j >> 1) & 1)) break;
             tc_fence_after();
             const int key0 = g.kb + j * kTileN;
-            float s[kTileN];
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                uint32_t v[32];
-                tmem_load32(lane_addr + (j & 1) * 128 + c * 32, v);
-#pragma unroll
-                for (int e = 0; e < 32; ++e) s[c * 32 + e] = __uint_as_float(v[e]) * p.scale_log2;
-            }
-            // mask keys at or past this row's visible limit
+            uint32_t sv[kTileN];  // raw scores of this row (f32 bits)
+            tmem_load128(lane_addr + (j & 1) * 128, sv);
+            // keys at or past this row's visible limit are masked (diagonal tiles only)
             const int nvis = limit - key0;
-            float mx = -INFINITY;
             if (nvis < kTileN) {
 #pragma unroll
-                for (int e = 0; e < kTileN; ++e) s[e] = e < nvis ? s[e] : -INFINITY;
+                for (int e = 0; e < kTileN; ++e)
+                    sv[e] = e < nvis ? sv[e] : __float_as_uint(-INFINITY);
             }
+            // row maximum of the raw scores (the scale is positive), three at a time
+            float mx = __uint_as_float(sv[0]);
 #pragma unroll
-            for (int e = 0; e < kTileN; ++e) mx = fmaxf(mx, s[e]);
+            for (int e = 1; e + 1 < kTileN; e += 2)
+                mx = fmaxf(mx, fmaxf(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])));
+            mx = fmaxf(mx, __uint_as_float(sv[kTileN - 1]));
+            mx *= p.scale_log2;
             float alpha = 1.f;
             if (mx > m_used + kLazyRescale) {   // also true the first time a key is visible
                 alpha = fast_exp2(m_used - mx);  // 0 when m_used was -inf
                 m_used = mx;
             }
-            const float mref = m_used == -INFINITY ? 0.f : m_used;
+            const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
+            const float nm = m_used == -INFINITY ? 0.f : -m_used;
+            const float2 nm2 = make_float2(nm, nm);
             uint32_t pk[kTileN / 2];
-            float rs = 0.f, rs_b = 0.f;
+            float2 rs2 = make_float2(0.f, 0.f), rsb2 = make_float2(0.f, 0.f);
 #pragma unroll
             for (int e = 0; e < kTileN; e += 2) {
-                const float p0 = fast_exp2(s[e] - mref), p1 = fast_exp2(s[e + 1] - mref);
+                // exponent argument s * scale - m for two keys in one packed FMA
+                const float2 x = __ffma2_rn(make_float2(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])),
+                                            sc2, nm2);
+                const float p0 = fast_exp2(x.x), p1 = fast_exp2(x.y);
                 pk[e / 2] = pack_bf16x2(p0, p1);
-                rs += p0 + p1;
-                rs_b += bf16lo(pk[e / 2]) + bf16hi(pk[e / 2]);
+                rs2 = __fadd2_rn(rs2, make_float2(p0, p1));
+                rsb2 = __fadd2_rn(rsb2, make_float2(bf16lo(pk[e / 2]), bf16hi(pk[e / 2])));
             }
             // O is normalised by the sum of the bf16 probabilities the P.V product
             // used (numerator and denominator carry the same rounding); the LSE
             // uses the sum of the unrounded ones
-            l = l * alpha + rs;
-            l_b = l_b * alpha + rs_b;
+            l = l * alpha + (rs2.x + rs2.y);
+            l_b = l_b * alpha + (rsb2.x + rsb2.y);
             // P buffer and O are free once the previous P.V finished
             if (j > 0 && !wait_warp(p_free, (j - 1) & 1)) break;
             tc_fence_after();
@@ -454,7 +480,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     uint32_t v[32];
                     tmem_load32(lane_addr + 256 + c * 32, v);
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
+                    for (int e = 0; e < 32; e += 2) {
+                        const float2 o2 = __fmul2_rn(make_float2(__uint_as_float(v[e]), __uint_as_float(v[e + 1])),
+                                                     make_float2(alpha, alpha));
+                        v[e] = __float_as_uint(o2.x);
+                        v[e + 1] = __float_as_uint(o2.y);
+                    }
                     tmem_store32(lane_addr + 256 + c * 32, v);
                 }
             }
@@ -484,14 +515,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ---- epilogue: O / l
         const bool ok = wait_warp(p_free, (g.nt - 1) & 1);
         tc_fence_after();
-        float o[kD];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            uint32_t v[32];
-            tmem_load32(lane_addr + 256 + c * 32, v);
-#pragma unroll
-            for (int e = 0; e < 32; ++e) o[c * 32 + e] = __uint_as_float(v[e]);
-        }
+        uint32_t ov[kD];
+        tmem_load128(lane_addr + 256, ov);
+        float* o = reinterpret_cast<float*>(ov);
         if (ok && row_exists) {
             const bool any = l > 0.f && l_b > 0.f;
             const float inv_l = any ? 1.0f / l_b : 0.f;
