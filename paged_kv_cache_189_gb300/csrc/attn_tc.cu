@@ -164,6 +164,29 @@ __device__ __forceinline__ int visible_keys(int i, int qreal, int kv_len, int ma
     return first_new + min(qreal, block_end);
 }
 
+// 2^x for two values on the FMA pipes, to share the exponentials of a tile
+// between the special-function unit and the FMA units.  Range reduction
+// x = n + f with n the nearest integer (added through the 1.5 * 2^23 rounding
+// constant) and f in [-0.5, 0.5]; 2^f by a cubic fitted here to minimise the
+// relative error on that interval (Lawson's iteratively reweighted least
+// squares; max relative error 8.4e-5, well below bf16's 2^-9); 2^n added to
+// the exponent field.  Inputs below -126 are clamped (the result is then
+// ~1e-38 instead of a smaller number).
+__device__ __forceinline__ float2 exp2_poly2(float2 x) {
+    constexpr float kRound = 12582912.0f;  // 1.5 * 2^23
+    x = make_float2(fmaxf(x.x, -126.f), fmaxf(x.y, -126.f));
+    const float2 t = __fadd2_rn(x, make_float2(kRound, kRound));
+    const float2 n = __fadd2_rn(t, make_float2(-kRound, -kRound));
+    const float2 f = __ffma2_rn(n, make_float2(-1.f, -1.f), x);
+    float2 q = __ffma2_rn(f, make_float2(0.055213093757629395f, 0.055213093757629395f),
+                          make_float2(0.24271467328071594f, 0.24271467328071594f));
+    q = __ffma2_rn(q, f, make_float2(0.6932622194290161f, 0.6932622194290161f));
+    q = __ffma2_rn(q, f, make_float2(0.9999195337295532f, 0.9999195337295532f));
+    // the low bits of t hold n; shifted into the exponent field they scale q by 2^n
+    return make_float2(__int_as_float(__float_as_int(q.x) + (__float_as_int(t.x) << 23)),
+                       __int_as_float(__float_as_int(q.y) + (__float_as_int(t.y) << 23)));
+}
+
 struct TileGeom {
     int b, kvh, split, r0, nrows, qreal, kv_len, t0, kb, key_hi, nt;
 };
@@ -190,35 +213,38 @@ __device__ __forceinline__ TileGeom tile_geometry(const AttnParams& p, int TQ) {
     return g;
 }
 
-// Write the state of one row (normalised O, LSE) to the output, or to the
-// split partials when the call has several key splits.
-__device__ __forceinline__ void store_row(const AttnParams& p, const TileGeom& g, int row_in_seq,
-                                          int h, const float* o, float inv_l, float lse) {
+// Columns [32c, 32c + 32) of one row's normalised output (or split partial).
+__device__ __forceinline__ void store_row_chunk(const AttnParams& p, const TileGeom& g, int row_in_seq,
+                                                int h, int c, const uint32_t (&v)[32], float inv_l) {
     const int64_t st = static_cast<int64_t>(g.r0 + row_in_seq) * p.num_q_heads + h;
+    float o[32];
+#pragma unroll
+    for (int e = 0; e < 32; ++e) o[e] = __uint_as_float(v[e]) * inv_l;
+    if (p.num_splits == 1 && !p.out_f32) {
+        uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + st * kD + c * 32);
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+            dst[q] = make_uint4(pack_bf16x2(o[8 * q], o[8 * q + 1]), pack_bf16x2(o[8 * q + 2], o[8 * q + 3]),
+                                pack_bf16x2(o[8 * q + 4], o[8 * q + 5]), pack_bf16x2(o[8 * q + 6], o[8 * q + 7]));
+        return;
+    }
+    float* base;
     if (p.num_splits == 1) {
-        if (p.out_f32) {
-            float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) + st * kD);
-#pragma unroll
-            for (int c = 0; c < kD / 4; ++c)
-                dst[c] = make_float4(o[4 * c] * inv_l, o[4 * c + 1] * inv_l, o[4 * c + 2] * inv_l,
-                                     o[4 * c + 3] * inv_l);
-        } else {
-            uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + st * kD);
-#pragma unroll
-            for (int c = 0; c < kD / 8; ++c)
-                dst[c] = make_uint4(pack_bf16x2(o[8 * c] * inv_l, o[8 * c + 1] * inv_l),
-                                    pack_bf16x2(o[8 * c + 2] * inv_l, o[8 * c + 3] * inv_l),
-                                    pack_bf16x2(o[8 * c + 4] * inv_l, o[8 * c + 5] * inv_l),
-                                    pack_bf16x2(o[8 * c + 6] * inv_l, o[8 * c + 7] * inv_l));
-        }
-        if (p.lse) p.lse[st] = lse;
+        base = static_cast<float*>(p.out) + st * kD;
     } else {
         if (g.r0 + row_in_seq >= static_cast<int64_t>(p.batch) * p.max_q_rows) return;
-        float4* dst = reinterpret_cast<float4*>(p.ws_o + (st * p.num_splits + g.split) * kD);
+        base = p.ws_o + (st * p.num_splits + g.split) * kD;
+    }
+    float4* dst = reinterpret_cast<float4*>(base + c * 32);
 #pragma unroll
-        for (int c = 0; c < kD / 4; ++c)
-            dst[c] = make_float4(o[4 * c] * inv_l, o[4 * c + 1] * inv_l, o[4 * c + 2] * inv_l,
-                                 o[4 * c + 3] * inv_l);
+    for (int q = 0; q < 8; ++q) dst[q] = make_float4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+}
+__device__ __forceinline__ void store_row_lse(const AttnParams& p, const TileGeom& g, int row_in_seq,
+                                              int h, float lse) {
+    const int64_t st = static_cast<int64_t>(g.r0 + row_in_seq) * p.num_q_heads + h;
+    if (p.num_splits == 1) {
+        if (p.lse) p.lse[st] = lse;
+    } else if (g.r0 + row_in_seq < static_cast<int64_t>(p.batch) * p.max_q_rows) {
         p.ws_lse[st * p.num_splits + g.split] = lse;
     }
 }
@@ -241,10 +267,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int r = threadIdx.x;
             const int i = g.t0 + r / G;
             if (i < g.nrows) {
-                float zero[kD];
+                uint32_t zero[32];
 #pragma unroll
-                for (int d = 0; d < kD; ++d) zero[d] = 0.f;
-                store_row(p, g, i, g.kvh * G + r % G, zero, 0.f, -INFINITY);
+                for (int e = 0; e < 32; ++e) zero[e] = 0u;
+#pragma unroll
+                for (int c = 0; c < 4; ++c) store_row_chunk(p, g, i, g.kvh * G + r % G, c, zero, 0.f);
+                store_row_lse(p, g, i, g.kvh * G + r % G, -INFINITY);
             }
         }
         return;
@@ -460,9 +488,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // exponent argument s * scale - m for two keys in one packed FMA
                 const float2 x = __ffma2_rn(make_float2(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])),
                                             sc2, nm2);
-                const float p0 = fast_exp2(x.x), p1 = fast_exp2(x.y);
-                pk[e / 2] = pack_bf16x2(p0, p1);
-                rs2 = __fadd2_rn(rs2, make_float2(p0, p1));
+                const float2 pp = make_float2(fast_exp2(x.x), fast_exp2(x.y));
+                pk[e / 2] = pack_bf16x2(pp.x, pp.y);
+                rs2 = __fadd2_rn(rs2, pp);
                 rsb2 = __fadd2_rn(rsb2, make_float2(bf16lo(pk[e / 2]), bf16hi(pk[e / 2])));
             }
             // O is normalised by the sum of the bf16 probabilities the P.V product
@@ -512,28 +540,428 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_before();
             mbar_arrive(p_full);
         }
-        // ---- epilogue: O / l
+        // ---- epilogue: O / l, 32 columns at a time
         const bool ok = wait_warp(p_free, (g.nt - 1) & 1);
         tc_fence_after();
-        uint32_t ov[kD];
-        tmem_load128(lane_addr + 256, ov);
-        float* o = reinterpret_cast<float*>(ov);
-        if (ok && row_exists) {
-            const bool any = l > 0.f && l_b > 0.f;
-            const float inv_l = any ? 1.0f / l_b : 0.f;
-            const float lse = any ? (m_used + __log2f(l)) * kLn2 : -INFINITY;
-            if (!any) {
+        const bool any = l > 0.f && l_b > 0.f;
+        const float inv_l = any ? 1.0f / l_b : 0.f;
 #pragma unroll
-                for (int d = 0; d < kD; ++d) o[d] = 0.f;
-            }
-            store_row(p, g, i, h, o, inv_l, lse);
+        for (int c = 0; c < 4; ++c) {
+            uint32_t v[32];
+            tmem_load32(lane_addr + 256 + c * 32, v);
+            if (ok && row_exists) store_row_chunk(p, g, i, h, c, v, inv_l);
         }
+        if (ok && row_exists) store_row_lse(p, g, i, h, any ? (m_used + __log2f(l)) * kLn2 : -INFINITY);
     }
 
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     if (warp == 5) tmem_dealloc(tmem, kTmemCols);
+}
+
+// ===========================================================================
+// Two query tiles per CTA (tile A = rows [0,128), tile B = rows [128,256) of
+// the CTA's 2 x TQ tokens), one softmax warpgroup each, sharing every K/V
+// load.  While one warpgroup runs its softmax the tensor core works on the
+// other tile, so the exponentials and the MMAs overlap.  P is written back
+// into tensor memory over the tile's S columns (packed bf16 pairs) and the
+// P.V product reads its A operand from tensor memory, which leaves shared
+// memory for the two Q tiles and the K/V rings.
+// Tensor memory: S_A [0,128) O_A [128,256) S_B [256,384) O_B [384,512).
+// Roles (320 threads): warps 0-3 softmax A, warps 4-7 softmax B, warp 8 TMA
+// producer, warp 9 MMA.
+// ===========================================================================
+constexpr int kThreads2 = 320;
+constexpr int kQ2Off = 0;                                   // Q_A, Q_B
+constexpr int kK2Off = kQ2Off + 2 * kTileBytes;
+constexpr int kV2Off = kK2Off + kKStages * kTileBytes;
+constexpr int kBar2Off = kV2Off + kVStages * kTileBytes;
+// barriers: q_ready, k_full[3], k_empty[3], v_full[2], v_empty[2], s_full[2], p_full[2], o_full[2]
+constexpr int kNumBars2 = 1 + 2 * kKStages + 2 * kVStages + 6;
+constexpr int kTmemSlot2Off = kBar2Off + kNumBars2 * 8;
+constexpr int kFlag2Off = kTmemSlot2Off + 8;
+constexpr int kSmemBytes2 = kFlag2Off + 16;
+static_assert(kSmemBytes2 <= 227 * 1024, "shared memory per CTA");
+
+#define PKV_W4(i) "r"(v[i + 0]), "r"(v[i + 1]), "r"(v[i + 2]), "r"(v[i + 3])
+// 16 consecutive 32-bit columns of this thread's lane
+__device__ __forceinline__ void tmem_store16(uint32_t taddr, const uint32_t (&v)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};"
+        ::"r"(taddr), PKV_W4(0), PKV_W4(4), PKV_W4(8), PKV_W4(12) : "memory");
+}
+#undef PKV_W4
+__device__ __forceinline__ void tmem_store_wait() {
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+// D[tmem] (+)= A[tmem] * B[smem desc]
+__device__ __forceinline__ void umma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                             uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
+        ::"r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate) : "memory");
+}
+
+template <int G>
+__global__ void __launch_bounds__(kThreads2, 1)
+    attn_tc2_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                    const AttnParams p) {
+    constexpr int TQ = kTileM / G;
+    extern __shared__ __align__(1024) uint8_t smem[];
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    // geometry of the CTA's 2 x TQ tokens (tile A then tile B)
+    TileGeom g;
+    g.b = blockIdx.z / p.num_splits;
+    g.split = blockIdx.z - g.b * p.num_splits;
+    g.kvh = blockIdx.y;
+    g.r0 = p.q_indptr[g.b];
+    g.nrows = min(p.q_indptr[g.b + 1] - g.r0, p.max_q_rows);
+    g.t0 = blockIdx.x * 2 * TQ;
+    g.qreal = min(p.q_real ? p.q_real[g.b] : g.nrows, g.nrows);
+    g.kv_len = min(max(p.kv_lens[g.b], 0), p.max_kv_len);
+    g.kb = g.split * p.split_keys;
+    {
+        const int ke = min(g.kv_len, g.kb + p.split_keys);
+        const int last = min(g.t0 + 2 * TQ, g.nrows) - 1;
+        int lim = 0;
+        if (g.t0 < g.qreal)
+            lim = visible_keys(min(last, g.qreal - 1), g.qreal, g.kv_len, p.mask, max(p.causal_block, 1));
+        g.key_hi = min(ke, lim);
+        g.nt = g.key_hi > g.kb ? (g.key_hi - g.kb + kTileN - 1) / kTileN : 0;
+    }
+    if (g.t0 >= g.nrows) return;  // uniform
+
+    if (g.nt == 0) {
+        if (threadIdx.x < 2 * kTileM) {
+            const int x = threadIdx.x / kTileM, r = threadIdx.x % kTileM;
+            const int i = g.t0 + x * TQ + r / G;
+            if (i < g.nrows) {
+                uint32_t zero[32];
+#pragma unroll
+                for (int e = 0; e < 32; ++e) zero[e] = 0u;
+#pragma unroll
+                for (int c = 0; c < 4; ++c) store_row_chunk(p, g, i, g.kvh * G + r % G, c, zero, 0.f);
+                store_row_lse(p, g, i, g.kvh * G + r % G, -INFINITY);
+            }
+        }
+        return;
+    }
+    if ((smem_u32(smem) & 1023u) != 0) {
+        if (threadIdx.x == 0) set_err(p.err, PKV_ERRBIT_TIMEOUT);
+        return;
+    }
+
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kBar2Off);
+    uint64_t* q_ready = bars;
+    uint64_t* k_full = bars + 1;
+    uint64_t* k_empty = k_full + kKStages;
+    uint64_t* v_full = k_empty + kKStages;
+    uint64_t* v_empty = v_full + kVStages;
+    uint64_t* s_full = v_empty + kVStages;  // [tile]
+    uint64_t* p_full = s_full + 2;          // [tile]
+    uint64_t* o_full = p_full + 2;          // [tile]
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kTmemSlot2Off);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kFlag2Off);
+
+    if (threadIdx.x == 0) {
+        mbar_init(q_ready, 2 * kTileM);
+        for (int s = 0; s < kKStages; ++s) {
+            mbar_init(&k_full[s], 1);
+            mbar_init(&k_empty[s], 1);
+        }
+        for (int s = 0; s < kVStages; ++s) {
+            mbar_init(&v_full[s], 1);
+            mbar_init(&v_empty[s], 1);
+        }
+        for (int x = 0; x < 2; ++x) {
+            mbar_init(&s_full[x], 1);
+            mbar_init(&p_full[x], kTileM);
+            mbar_init(&o_full[x], 1);
+        }
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 9) {
+        tmem_alloc(tmem_slot, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const uint32_t sbase = smem_u32(smem);
+
+    auto wait = [&](uint64_t* bar, uint32_t parity) -> bool {
+        if (*abort_flag) return false;
+        if (mbar_wait(bar, parity)) return true;
+        *abort_flag = 1;
+        set_err(p.err, PKV_ERRBIT_TIMEOUT);
+        return false;
+    };
+
+    if (warp == 8) {
+        // ============================ producer ==============================
+        if (lane == 0) {
+            prefetch_tmap(&tm_k);
+            prefetch_tmap(&tm_v);
+            const int32_t* bt = p.block_table + static_cast<int64_t>(g.b) * p.block_table_stride;
+            const int last_page = (g.kv_len + 31) / 32;
+            auto load_tile = [&](const CUtensorMap* tm, uint8_t* dst, uint64_t* bar, int j) {
+                mbar_arrive_expect_tx(bar, kTileBytes);
+#pragma unroll
+                for (int pg = 0; pg < 4; ++pg) {
+                    const int lp = (g.kb + j * kTileN) / 32 + pg;
+                    int phys = lp < last_page ? bt[lp] : static_cast<int>(p.num_pages);
+                    if (p.checked && lp < last_page && (phys < 0 || phys >= p.num_pages)) {
+                        set_err(p.err, PKV_ERRBIT_PAGE);
+                        phys = static_cast<int>(p.num_pages);
+                    }
+#pragma unroll
+                    for (int h = 0; h < 2; ++h)
+                        tma_load_4d(dst + h * kHalfBytes + pg * 4096, tm, bar, h * 64, g.kvh, 0, phys);
+                }
+            };
+            int k_issued = 0, v_issued = 0;
+            while (k_issued < g.nt || v_issued < g.nt) {
+                if (k_issued < g.nt) {
+                    const int s = k_issued % kKStages;
+                    if (k_issued >= kKStages && !wait(&k_empty[s], ((k_issued / kKStages) - 1) & 1)) break;
+                    load_tile(&tm_k, smem + kK2Off + s * kTileBytes, &k_full[s], k_issued);
+                    ++k_issued;
+                }
+                if (v_issued < k_issued) {
+                    const int s = v_issued % kVStages;
+                    if (v_issued >= kVStages && !wait(&v_empty[s], ((v_issued / kVStages) - 1) & 1)) break;
+                    load_tile(&tm_v, smem + kV2Off + s * kTileBytes, &v_full[s], v_issued);
+                    ++v_issued;
+                }
+            }
+            for (int j = max(0, k_issued - kKStages); j < k_issued; ++j)
+                mbar_wait(&k_full[j % kKStages], (j / kKStages) & 1);
+            for (int j = max(0, v_issued - kVStages); j < v_issued; ++j)
+                mbar_wait(&v_full[j % kVStages], (j / kVStages) & 1);
+        }
+    } else if (warp == 9) {
+        // ============================== MMA ================================
+        if (lane == 0) {
+            constexpr uint32_t kIdescS = idesc_bf16(kTileM, kTileN, false);
+            constexpr uint32_t kIdescO = idesc_bf16(kTileM, kD, true);
+            auto issue_s = [&](int x, int j) {
+                const uint32_t qa = sbase + kQ2Off + x * kTileBytes;
+                const uint32_t kbse = sbase + kK2Off + (j % kKStages) * kTileBytes;
+#pragma unroll
+                for (int kk = 0; kk < kD / 16; ++kk) {
+                    const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
+                    umma_bf16(tmem + x * 256, sdesc_sw128(qa + off, 16, 1024),
+                              sdesc_sw128(kbse + off, 16, 1024), kIdescS, kk > 0);
+                }
+                umma_commit(&s_full[x]);
+            };
+            auto issue_pv = [&](int x, int j) {
+                const uint32_t vb = sbase + kV2Off + (j % kVStages) * kTileBytes;
+#pragma unroll
+                for (int kk = 0; kk < kTileN / 16; ++kk) {
+                    // A = P in tensor memory (16 keys = 8 packed columns per step),
+                    // B = V (rows = keys, MN-major; 64-column halves LBO apart)
+                    const uint64_t bdesc = sdesc_sw128(vb + kk * 16 * 128, kHalfBytes, 1024);
+                    umma_bf16_ts(tmem + x * 256 + 128, tmem + x * 256 + kk * 8, bdesc, kIdescO,
+                                 (j > 0 || kk > 0) ? 1u : 0u);
+                }
+            };
+            bool ok = wait(q_ready, 0) && wait(&k_full[0], 0);
+            if (ok) {
+                tc_fence_after();
+                issue_s(0, 0);
+                issue_s(1, 0);
+                umma_commit(&k_empty[0]);
+            }
+            for (int j = 0; ok && j < g.nt; ++j) {
+                const bool more = j + 1 < g.nt;
+                // tile A
+                if (!wait(&p_full[0], j & 1) || !wait(&v_full[j % kVStages], (j / kVStages) & 1)) break;
+                tc_fence_after();
+                issue_pv(0, j);
+                if (more) {
+                    if (!wait(&k_full[(j + 1) % kKStages], ((j + 1) / kKStages) & 1)) break;
+                    tc_fence_after();
+                    issue_s(0, j + 1);
+                } else {
+                    umma_commit(&o_full[0]);
+                }
+                // tile B
+                if (!wait(&p_full[1], j & 1)) break;
+                tc_fence_after();
+                issue_pv(1, j);
+                umma_commit(&v_empty[j % kVStages]);
+                if (more) {
+                    issue_s(1, j + 1);
+                    umma_commit(&k_empty[(j + 1) % kKStages]);
+                } else {
+                    umma_commit(&o_full[1]);
+                }
+            }
+        }
+    } else {
+        // ============================ softmax ===============================
+        const int x = warp >> 2;              // tile of this warpgroup
+        const int r = threadIdx.x & 127;       // row in the tile = tensor-memory lane
+        const int t = r / G, hg = r % G;
+        const int i = g.t0 + x * TQ + t;       // query row within the sequence
+        const int h = g.kvh * G + hg;
+        const bool row_exists = i < g.nrows;
+        const int limit = row_exists ? visible_keys(i, g.qreal, g.kv_len, p.mask, max(p.causal_block, 1))
+                                     : 0;
+        {
+            const uint4* src = reinterpret_cast<const uint4*>(
+                static_cast<const __nv_bfloat16*>(p.q) + static_cast<int64_t>(g.r0 + i) * p.q_token_stride +
+                static_cast<int64_t>(h) * p.q_head_stride);
+            uint8_t* qt = smem + kQ2Off + x * kTileBytes;
+#pragma unroll
+            for (int c = 0; c < 16; ++c) {
+                const uint4 v = row_exists ? src[c] : make_uint4(0u, 0u, 0u, 0u);
+                *reinterpret_cast<uint4*>(qt + (c >> 3) * kHalfBytes + sw128_offset(r, c & 7)) = v;
+            }
+            fence_proxy_async_smem();
+            mbar_arrive(q_ready);
+        }
+        auto wait_warp = [&](uint64_t* bar, uint32_t parity) -> bool {
+            return __all_sync(0xffffffffu, wait(bar, parity));
+        };
+        const uint32_t lane_addr = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16) + x * 256;
+        const uint32_t s_addr = lane_addr, o_addr = lane_addr + 128;
+        float m_used = -INFINITY;
+        float l = 0.f, l_b = 0.f;
+        const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
+        for (int j = 0; j < g.nt; ++j) {
+            if (!wait_warp(&s_full[x], j & 1)) break;
+            tc_fence_after();
+            const int nvis = limit - (g.kb + j * kTileN);
+            // pass 1: row maximum of the raw scores over the visible keys
+            float mx = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                uint32_t v[32];
+                tmem_load32(s_addr + c * 32, v);
+                if (nvis < (c + 1) * 32) {
+#pragma unroll
+                    for (int e = 0; e < 32; ++e)
+                        v[e] = c * 32 + e < nvis ? v[e] : __float_as_uint(-INFINITY);
+                }
+                float m0 = __uint_as_float(v[0]), m1 = __uint_as_float(v[1]);
+#pragma unroll
+                for (int e = 2; e < 32; e += 2) {
+                    m0 = fmaxf(m0, __uint_as_float(v[e]));
+                    m1 = fmaxf(m1, __uint_as_float(v[e + 1]));
+                }
+                mx = fmaxf(mx, fmaxf(m0, m1));
+            }
+            mx *= p.scale_log2;
+            float alpha = 1.f;
+            if (mx > m_used + kLazyRescale) {
+                alpha = fast_exp2(m_used - mx);
+                m_used = mx;
+            }
+            // O *= alpha (O is stable: S of this tile was issued after the previous P.V)
+            if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t v[32];
+                    tmem_load32(o_addr + c * 32, v);
+#pragma unroll
+                    for (int e = 0; e < 32; e += 2) {
+                        const float2 o2 = __fmul2_rn(make_float2(__uint_as_float(v[e]), __uint_as_float(v[e + 1])),
+                                                     make_float2(alpha, alpha));
+                        v[e] = __float_as_uint(o2.x);
+                        v[e + 1] = __float_as_uint(o2.y);
+                    }
+                    tmem_store32(o_addr + c * 32, v);
+                }
+            }
+            // pass 2: probabilities, 32 keys at a time, written back as packed
+            // bf16 over the columns of S already read
+            const float nm = m_used == -INFINITY ? 0.f : -m_used;
+            const float2 nm2 = make_float2(nm, nm);
+            float2 rs2 = make_float2(0.f, 0.f), rsb2 = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                uint32_t v[32];
+                tmem_load32(s_addr + c * 32, v);
+                if (nvis < (c + 1) * 32) {
+#pragma unroll
+                    for (int e = 0; e < 32; ++e)
+                        v[e] = c * 32 + e < nvis ? v[e] : __float_as_uint(-INFINITY);
+                }
+                uint32_t pk[16];
+#pragma unroll
+                for (int e = 0; e < 32; e += 2) {
+                    const float2 xx = __ffma2_rn(make_float2(__uint_as_float(v[e]), __uint_as_float(v[e + 1])),
+                                                 sc2, nm2);
+                    const float2 pp = make_float2(fast_exp2(xx.x), fast_exp2(xx.y));
+                    pk[e / 2] = pack_bf16x2(pp.x, pp.y);
+                    rs2 = __fadd2_rn(rs2, pp);
+                    rsb2 = __fadd2_rn(rsb2, make_float2(bf16lo(pk[e / 2]), bf16hi(pk[e / 2])));
+                }
+                tmem_store16(s_addr + c * 16, pk);
+            }
+            tmem_store_wait();
+            l = l * alpha + (rs2.x + rs2.y);
+            l_b = l_b * alpha + (rsb2.x + rsb2.y);
+            // keys past the sequence's length inside its last page: zero their V
+            // rows so that 0 * whatever the pool holds there cannot give NaN
+            const int key0 = g.kb + j * kTileN;
+            if (x == 0 && key0 + kTileN > g.kv_len && g.kv_len > key0) {
+                // tile A's warpgroup does it; tile B's P.V is issued after tile A's
+                const int vs = j % kVStages;
+                if (!wait_warp(&v_full[vs], (j / kVStages) & 1)) break;
+                const int first = g.kv_len - key0;
+                const int lastr = min(kTileN, (first + 31) / 32 * 32);
+                uint8_t* vt = smem + kV2Off + vs * kTileBytes;
+                for (int idx = r; idx < (lastr - first) * 16; idx += kTileM) {
+                    const int row = first + idx / 16, cc = idx % 16;
+                    *reinterpret_cast<uint4*>(vt + (cc >> 3) * kHalfBytes + sw128_offset(row, cc & 7)) =
+                        make_uint4(0u, 0u, 0u, 0u);
+                }
+                fence_proxy_async_smem();
+            }
+            tc_fence_before();
+            mbar_arrive(&p_full[x]);
+        }
+        // ---- epilogue: O / l, 32 columns at a time
+        const bool ok = wait_warp(&o_full[x], 0);
+        tc_fence_after();
+        const bool any = l > 0.f && l_b > 0.f;
+        const float inv_l = any ? 1.0f / l_b : 0.f;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            uint32_t v[32];
+            tmem_load32(o_addr + c * 32, v);
+            if (ok && row_exists) store_row_chunk(p, g, i, h, c, v, inv_l);
+        }
+        if (ok && row_exists) store_row_lse(p, g, i, h, any ? (m_used + __log2f(l)) * kLn2 : -INFINITY);
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 9) tmem_dealloc(tmem, kTmemCols);
+}
+
+template <int G>
+cudaError_t launch_g2(const AttnParams& p, const void* tk, const void* tv, cudaStream_t s) {
+    auto kern = attn_tc2_kernel<G>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes2);
+    if (e != cudaSuccess) return e;
+    const int TQ = kTileM / G;
+    dim3 grid((p.max_q_rows + 2 * TQ - 1) / (2 * TQ), p.num_kv_heads, p.batch * p.num_splits);
+    kern<<<grid, kThreads2, kSmemBytes2, s>>>(*static_cast<const CUtensorMap*>(tk),
+                                              *static_cast<const CUtensorMap*>(tv), p);
+    return cudaGetLastError();
 }
 
 template <int G>
@@ -559,6 +987,16 @@ int attn_tc_rows_per_tile(int group) { return kTileM / group; }
 cudaError_t launch_attn_tc(const AttnParams& p, const void*, const void* tk, const void* tv,
                            cudaStream_t s) {
     const int G = p.num_q_heads / p.num_kv_heads;
+    if (p.max_q_rows > kTileM / G) {
+        switch (G) {
+            case 1: return launch_g2<1>(p, tk, tv, s);
+            case 2: return launch_g2<2>(p, tk, tv, s);
+            case 4: return launch_g2<4>(p, tk, tv, s);
+            case 8: return launch_g2<8>(p, tk, tv, s);
+            case 16: return launch_g2<16>(p, tk, tv, s);
+        }
+        return cudaErrorInvalidValue;
+    }
     switch (G) {
         case 1: return launch_g<1>(p, tk, tv, s);
         case 2: return launch_g<2>(p, tk, tv, s);
