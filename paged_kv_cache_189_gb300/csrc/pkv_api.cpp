@@ -98,11 +98,11 @@ struct Plan {
 };
 
 constexpr int kDecodeSplitKeys = 512;  // 16 pages: the pages' minimum split of 512 tokens
+constexpr int kPlanSMs = 152;          // GB300; only shapes the split choice
+constexpr int kTileKeys = 128;         // key tile of the tensor-core kernel
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-constexpr int kPlanSMs = 152;          // GB300; only shapes the split choice
-constexpr int kTileKeys = 128;         // key tile of the tensor-core kernel
 
 Plan plan_attention(int batch, int max_q_rows, int Hq, int Hkv, int D, int max_kv_len,
                     int num_splits, unsigned flags) {
@@ -134,10 +134,19 @@ Plan plan_attention(int batch, int max_q_rows, int Hq, int Hkv, int D, int max_k
         return pl;
     }
     pl.kernel = Kernel::kDecode;
+    // Work units (split, K/V head, sequence) are handed out dynamically to the
+    // persistent CTAs (3 per SM); each unit ends with a merge of its warps'
+    // states, so units should be long, but numerous enough to balance ragged
+    // lengths: aim for ~6 units per resident CTA at the host's length bound,
+    // never below the pages' minimum split of 512 keys.
     int keys = kDecodeSplitKeys;
     if (num_splits > 0) {
         const int per = (max_kv_len + num_splits - 1) / num_splits;
         keys = std::max(32, (per + 31) / 32 * 32);
+    } else {
+        const int64_t target_units = 6 * 3 * kPlanSMs;
+        const int64_t per = (static_cast<int64_t>(max_kv_len) * batch * Hkv + target_units - 1) / target_units;
+        keys = static_cast<int>(std::max<int64_t>(kDecodeSplitKeys, (per + 31) / 32 * 32));
     }
     pl.split_keys = keys;
     pl.splits = std::max(1, (max_kv_len + keys - 1) / keys);

@@ -78,10 +78,16 @@ def test_workspace_size(L):
     # one split when everything fits in 512 keys: only the scheduling counters
     small = pkv.paged_attention_workspace_size(64, 1, 32, 8, 128, 512)
     assert 64 * 8 * 4 < small <= 4096
+    # the automatic split size aims at ~6 work units per resident CTA (3 per SM
+    # on 152 SMs): 8193 keys x 512 (sequence, head) pairs / 2736 -> 1536 keys,
+    # i.e. 6 splits
     ws = pkv.paged_attention_workspace_size(64, 1, 32, 8, 128, 8193)
-    splits = 17
+    splits = 6
     states = 64 * 32 * splits
     assert ws >= states * 128 * 4 + states * 4 + 64 * 8 * 4
+    # an explicit split count overrides it
+    ws17 = pkv.paged_attention_workspace_size(64, 1, 32, 8, 128, 8193, num_splits=17)
+    assert ws17 >= 64 * 32 * 17 * 129 * 4
     # the generic kernel (several query rows) needs none
     assert pkv.paged_attention_workspace_size(4, 16, 32, 8, 128, 8193,
                                               flags=pkv.PKV_FLAG_SIMT_ONLY) == 0
