@@ -842,24 +842,28 @@ __global__ void __launch_bounds__(kThreads2, 1)
             if (!wait_warp(&s_full[x], j & 1)) break;
             tc_fence_after();
             const int nvis = limit - (g.kb + j * kTileN);
-            // pass 1: row maximum of the raw scores over the visible keys
-            float mx = -INFINITY;
+            // pass 1: row maximum over the visible keys, from one 128-column read
+            float mx;
+            {
+                uint32_t sv[kTileN];
+                tmem_load128(s_addr, sv);
+                if (nvis < kTileN) {
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                uint32_t v[32];
-                tmem_load32(s_addr + c * 32, v);
-                if (nvis < (c + 1) * 32) {
-#pragma unroll
-                    for (int e = 0; e < 32; ++e)
-                        v[e] = c * 32 + e < nvis ? v[e] : __float_as_uint(-INFINITY);
+                    for (int e = 0; e < kTileN; ++e)
+                        sv[e] = e < nvis ? sv[e] : __float_as_uint(-INFINITY);
                 }
-                float m0 = __uint_as_float(v[0]), m1 = __uint_as_float(v[1]);
+                float m4[4];
 #pragma unroll
-                for (int e = 2; e < 32; e += 2) {
-                    m0 = fmaxf(m0, __uint_as_float(v[e]));
-                    m1 = fmaxf(m1, __uint_as_float(v[e + 1]));
+                for (int q = 0; q < 4; ++q) {
+                    float a0 = __uint_as_float(sv[q]), a1 = __uint_as_float(sv[q + 4]);
+#pragma unroll
+                    for (int e = q + 8; e < kTileN; e += 8) {
+                        a0 = fmaxf(a0, __uint_as_float(sv[e]));
+                        a1 = fmaxf(a1, __uint_as_float(sv[e + 4]));
+                    }
+                    m4[q] = fmaxf(a0, a1);
                 }
-                mx = fmaxf(mx, fmaxf(m0, m1));
+                mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
             }
             mx *= p.scale_log2;
             float alpha = 1.f;
@@ -883,11 +887,11 @@ __global__ void __launch_bounds__(kThreads2, 1)
                     tmem_store32(o_addr + c * 32, v);
                 }
             }
-            // pass 2: probabilities, 32 keys at a time, written back as packed
-            // bf16 over the columns of S already read
+            // probabilities written back as packed bf16 over the columns of S
             const float nm = m_used == -INFINITY ? 0.f : -m_used;
             const float2 nm2 = make_float2(nm, nm);
             float2 rs2 = make_float2(0.f, 0.f), rsb2 = make_float2(0.f, 0.f);
+            // pass 2: 32 keys at a time (re-read: keeps the registers of a pass low)
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
                 uint32_t v[32];

@@ -55,12 +55,14 @@ def test_no_alloc_matches_paged_attention_on_two_calls():
 def test_no_alloc_rejects_calls_beyond_its_scratch():
     case = wl.random_case(33, batch=2, Hq=32, Hkv=8, D=128, kv_range=(10, 40))
     out = torch.empty(2, 32, 128, dtype=torch.bfloat16, device=DEV)
-    big = 1 << 20  # keys: the split partials would need far more than the scratch holds
-    assert pkv.paged_attention_workspace_size(64, 1, 32, 8, 128, big) > pkv.NO_ALLOC_SCRATCH_BYTES
+    # 64 sequences x 32 heads x 64 key splits of partial states: far more than the
+    # scratch holds
+    big, splits = 1 << 20, 64
+    assert pkv.paged_attention_workspace_size(64, 1, 32, 8, 128, big, splits) > pkv.NO_ALLOC_SCRATCH_BYTES
     with pytest.raises(pkv.PkvError) as e:
         pkv.paged_attention_no_alloc(case.q.to(DEV), case.k_pool.to(DEV), case.v_pool.to(DEV),
                                      case.block_table.to(DEV), case.kv_lens.to(DEV),
                                      case.q_indptr.to(DEV), out, batch=64, max_q_rows=1,
-                                     max_kv_len=big)
+                                     max_kv_len=big, num_splits=splits)
     assert e.value.status == pkv.PKV_ERR_WORKSPACE
     assert "scratch" in str(e.value)
