@@ -453,55 +453,63 @@ __global__ void __launch_bounds__(kThreads, 1)
         auto wait_warp = [&](uint64_t* bar, uint32_t parity) -> bool {
             return __all_sync(0xffffffffu, wait(bar, parity));
         };
+        // a warp none of whose rows sees a key (rows past the sequence, padding
+        // rows) writes zero probabilities and skips the softmax arithmetic
+        const bool warp_live = __any_sync(0xffffffffu, limit > 0);
         for (int j = 0; j < g.nt; ++j) {
             if (!wait_warp(&s_full[j & 1], (j >> 1) & 1)) break;
             tc_fence_after();
-            const int key0 = g.kb + j * kTileN;
-            uint32_t sv[kTileN];  // raw scores of this row (f32 bits)
-            tmem_load128(lane_addr + (j & 1) * 128, sv);
-            // keys at or past this row's visible limit are masked (diagonal tiles only)
-            const int nvis = limit - key0;
-            if (nvis < kTileN) {
-#pragma unroll
-                for (int e = 0; e < kTileN; ++e)
-                    sv[e] = e < nvis ? sv[e] : __float_as_uint(-INFINITY);
-            }
-            // row maximum of the raw scores (the scale is positive), three at a time
-            float mx = __uint_as_float(sv[0]);
-#pragma unroll
-            for (int e = 1; e + 1 < kTileN; e += 2)
-                mx = fmaxf(mx, fmaxf(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])));
-            mx = fmaxf(mx, __uint_as_float(sv[kTileN - 1]));
-            mx *= p.scale_log2;
-            float alpha = 1.f;
-            if (mx > m_used + kLazyRescale) {   // also true the first time a key is visible
-                alpha = fast_exp2(m_used - mx);  // 0 when m_used was -inf
-                m_used = mx;
-            }
-            const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
-            const float nm = m_used == -INFINITY ? 0.f : -m_used;
-            const float2 nm2 = make_float2(nm, nm);
             uint32_t pk[kTileN / 2];
-            float2 rs2 = make_float2(0.f, 0.f), rsb2 = make_float2(0.f, 0.f);
+            float alpha = 1.f;
+            if (warp_live) {
+                const int key0 = g.kb + j * kTileN;
+                uint32_t sv[kTileN];  // raw scores of this row (f32 bits)
+                tmem_load128(lane_addr + (j & 1) * 128, sv);
+                // keys at or past this row's visible limit are masked (diagonal tiles only)
+                const int nvis = limit - key0;
+                if (nvis < kTileN) {
 #pragma unroll
-            for (int e = 0; e < kTileN; e += 2) {
-                // exponent argument s * scale - m for two keys in one packed FMA
-                const float2 x = __ffma2_rn(make_float2(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])),
-                                            sc2, nm2);
-                const float2 pp = make_float2(fast_exp2(x.x), fast_exp2(x.y));
-                pk[e / 2] = pack_bf16x2(pp.x, pp.y);
-                rs2 = __fadd2_rn(rs2, pp);
-                rsb2 = __fadd2_rn(rsb2, make_float2(bf16lo(pk[e / 2]), bf16hi(pk[e / 2])));
+                    for (int e = 0; e < kTileN; ++e)
+                        sv[e] = e < nvis ? sv[e] : __float_as_uint(-INFINITY);
+                }
+                // row maximum of the raw scores (the scale is positive)
+                float mx = __uint_as_float(sv[0]);
+#pragma unroll
+                for (int e = 1; e + 1 < kTileN; e += 2)
+                    mx = fmaxf(mx, fmaxf(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])));
+                mx = fmaxf(mx, __uint_as_float(sv[kTileN - 1]));
+                mx *= p.scale_log2;
+                if (mx > m_used + kLazyRescale) {   // also true the first time a key is visible
+                    alpha = fast_exp2(m_used - mx);  // 0 when m_used was -inf
+                    m_used = mx;
+                }
+                const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
+                const float nm = m_used == -INFINITY ? 0.f : -m_used;
+                const float2 nm2 = make_float2(nm, nm);
+                float2 rs2 = make_float2(0.f, 0.f), rsb2 = make_float2(0.f, 0.f);
+#pragma unroll
+                for (int e = 0; e < kTileN; e += 2) {
+                    // exponent argument s * scale - m for two keys in one packed FMA
+                    const float2 xx = __ffma2_rn(make_float2(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])),
+                                                 sc2, nm2);
+                    const float2 pp = make_float2(fast_exp2(xx.x), fast_exp2(xx.y));
+                    pk[e / 2] = pack_bf16x2(pp.x, pp.y);
+                    rs2 = __fadd2_rn(rs2, pp);
+                    rsb2 = __fadd2_rn(rsb2, make_float2(bf16lo(pk[e / 2]), bf16hi(pk[e / 2])));
+                }
+                // O is normalised by the sum of the bf16 probabilities the P.V product
+                // used (numerator and denominator carry the same rounding); the LSE
+                // uses the sum of the unrounded ones
+                l = l * alpha + (rs2.x + rs2.y);
+                l_b = l_b * alpha + (rsb2.x + rsb2.y);
+            } else {
+#pragma unroll
+                for (int e = 0; e < kTileN / 2; ++e) pk[e] = 0u;
             }
-            // O is normalised by the sum of the bf16 probabilities the P.V product
-            // used (numerator and denominator carry the same rounding); the LSE
-            // uses the sum of the unrounded ones
-            l = l * alpha + (rs2.x + rs2.y);
-            l_b = l_b * alpha + (rsb2.x + rsb2.y);
             // P buffer and O are free once the previous P.V finished
             if (j > 0 && !wait_warp(p_free, (j - 1) & 1)) break;
             tc_fence_after();
-            if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+            if (warp_live && j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
                 // O *= alpha for this row (warp-collective tensor-memory access)
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
@@ -517,6 +525,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tmem_store32(lane_addr + 256 + c * 32, v);
                 }
             }
+            const int key0 = g.kb + j * kTileN;
             // P row -> shared memory, K-major 128-byte swizzle, two 64-key halves
 #pragma unroll
             for (int c = 0; c < 16; ++c)
@@ -838,84 +847,96 @@ __global__ void __launch_bounds__(kThreads2, 1)
         float m_used = -INFINITY;
         float l = 0.f, l_b = 0.f;
         const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
+        // a warp none of whose rows sees a key (rows past the sequence, padding
+        // rows) writes zero probabilities and skips the softmax arithmetic
+        const bool warp_live = __any_sync(0xffffffffu, limit > 0);
         for (int j = 0; j < g.nt; ++j) {
             if (!wait_warp(&s_full[x], j & 1)) break;
             tc_fence_after();
-            const int nvis = limit - (g.kb + j * kTileN);
-            // pass 1: row maximum over the visible keys, from one 128-column read
-            float mx;
-            {
-                uint32_t sv[kTileN];
-                tmem_load128(s_addr, sv);
-                if (nvis < kTileN) {
+            if (warp_live) {
+                const int nvis = limit - (g.kb + j * kTileN);
+                // pass 1: row maximum over the visible keys, from one 128-column read
+                float mx;
+                {
+                    uint32_t sv[kTileN];
+                    tmem_load128(s_addr, sv);
+                    if (nvis < kTileN) {
 #pragma unroll
-                    for (int e = 0; e < kTileN; ++e)
-                        sv[e] = e < nvis ? sv[e] : __float_as_uint(-INFINITY);
-                }
-                float m4[4];
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    float a0 = __uint_as_float(sv[q]), a1 = __uint_as_float(sv[q + 4]);
-#pragma unroll
-                    for (int e = q + 8; e < kTileN; e += 8) {
-                        a0 = fmaxf(a0, __uint_as_float(sv[e]));
-                        a1 = fmaxf(a1, __uint_as_float(sv[e + 4]));
+                        for (int e = 0; e < kTileN; ++e)
+                            sv[e] = e < nvis ? sv[e] : __float_as_uint(-INFINITY);
                     }
-                    m4[q] = fmaxf(a0, a1);
+                    float m4[4];
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        float a0 = __uint_as_float(sv[q]), a1 = __uint_as_float(sv[q + 4]);
+#pragma unroll
+                        for (int e = q + 8; e < kTileN; e += 8) {
+                            a0 = fmaxf(a0, __uint_as_float(sv[e]));
+                            a1 = fmaxf(a1, __uint_as_float(sv[e + 4]));
+                        }
+                        m4[q] = fmaxf(a0, a1);
+                    }
+                    mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
                 }
-                mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
-            }
-            mx *= p.scale_log2;
-            float alpha = 1.f;
-            if (mx > m_used + kLazyRescale) {
-                alpha = fast_exp2(m_used - mx);
-                m_used = mx;
-            }
-            // O *= alpha (O is stable: S of this tile was issued after the previous P.V)
-            if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+                mx *= p.scale_log2;
+                float alpha = 1.f;
+                if (mx > m_used + kLazyRescale) {
+                    alpha = fast_exp2(m_used - mx);
+                    m_used = mx;
+                }
+                // O *= alpha (O is stable: S of this tile was issued after the previous P.V)
+                if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        uint32_t v[32];
+                        tmem_load32(o_addr + c * 32, v);
+#pragma unroll
+                        for (int e = 0; e < 32; e += 2) {
+                            const float2 o2 = __fmul2_rn(make_float2(__uint_as_float(v[e]), __uint_as_float(v[e + 1])),
+                                                         make_float2(alpha, alpha));
+                            v[e] = __float_as_uint(o2.x);
+                            v[e + 1] = __float_as_uint(o2.y);
+                        }
+                        tmem_store32(o_addr + c * 32, v);
+                    }
+                }
+                // probabilities written back as packed bf16 over the columns of S
+                const float nm = m_used == -INFINITY ? 0.f : -m_used;
+                const float2 nm2 = make_float2(nm, nm);
+                float2 rs2 = make_float2(0.f, 0.f), rsb2 = make_float2(0.f, 0.f);
+                // pass 2: 32 keys at a time (re-read: keeps the registers of a pass low)
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
                     uint32_t v[32];
-                    tmem_load32(o_addr + c * 32, v);
+                    tmem_load32(s_addr + c * 32, v);
+                    if (nvis < (c + 1) * 32) {
+#pragma unroll
+                        for (int e = 0; e < 32; ++e)
+                            v[e] = c * 32 + e < nvis ? v[e] : __float_as_uint(-INFINITY);
+                    }
+                    uint32_t pk[16];
 #pragma unroll
                     for (int e = 0; e < 32; e += 2) {
-                        const float2 o2 = __fmul2_rn(make_float2(__uint_as_float(v[e]), __uint_as_float(v[e + 1])),
-                                                     make_float2(alpha, alpha));
-                        v[e] = __float_as_uint(o2.x);
-                        v[e + 1] = __float_as_uint(o2.y);
+                        const float2 xx = __ffma2_rn(make_float2(__uint_as_float(v[e]), __uint_as_float(v[e + 1])),
+                                                     sc2, nm2);
+                        const float2 pp = make_float2(fast_exp2(xx.x), fast_exp2(xx.y));
+                        pk[e / 2] = pack_bf16x2(pp.x, pp.y);
+                        rs2 = __fadd2_rn(rs2, pp);
+                        rsb2 = __fadd2_rn(rsb2, make_float2(bf16lo(pk[e / 2]), bf16hi(pk[e / 2])));
                     }
-                    tmem_store32(o_addr + c * 32, v);
+                    tmem_store16(s_addr + c * 16, pk);
                 }
+                tmem_store_wait();
+                l = l * alpha + (rs2.x + rs2.y);
+                l_b = l_b * alpha + (rsb2.x + rsb2.y);
+            } else {
+                uint32_t zero[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e) zero[e] = 0u;
+#pragma unroll
+                for (int c = 0; c < 4; ++c) tmem_store16(s_addr + c * 16, zero);
+                tmem_store_wait();
             }
-            // probabilities written back as packed bf16 over the columns of S
-            const float nm = m_used == -INFINITY ? 0.f : -m_used;
-            const float2 nm2 = make_float2(nm, nm);
-            float2 rs2 = make_float2(0.f, 0.f), rsb2 = make_float2(0.f, 0.f);
-            // pass 2: 32 keys at a time (re-read: keeps the registers of a pass low)
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                uint32_t v[32];
-                tmem_load32(s_addr + c * 32, v);
-                if (nvis < (c + 1) * 32) {
-#pragma unroll
-                    for (int e = 0; e < 32; ++e)
-                        v[e] = c * 32 + e < nvis ? v[e] : __float_as_uint(-INFINITY);
-                }
-                uint32_t pk[16];
-#pragma unroll
-                for (int e = 0; e < 32; e += 2) {
-                    const float2 xx = __ffma2_rn(make_float2(__uint_as_float(v[e]), __uint_as_float(v[e + 1])),
-                                                 sc2, nm2);
-                    const float2 pp = make_float2(fast_exp2(xx.x), fast_exp2(xx.y));
-                    pk[e / 2] = pack_bf16x2(pp.x, pp.y);
-                    rs2 = __fadd2_rn(rs2, pp);
-                    rsb2 = __fadd2_rn(rsb2, make_float2(bf16lo(pk[e / 2]), bf16hi(pk[e / 2])));
-                }
-                tmem_store16(s_addr + c * 16, pk);
-            }
-            tmem_store_wait();
-            l = l * alpha + (rs2.x + rs2.y);
-            l_b = l_b * alpha + (rsb2.x + rsb2.y);
             // keys past the sequence's length inside its last page: zero their V
             // rows so that 0 * whatever the pool holds there cannot give NaN
             const int key0 = g.kb + j * kTileN;
