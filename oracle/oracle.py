@@ -285,3 +285,93 @@ def merge_many(os_, lses):
     for o_i, l_i in zip(os_[1:], lses[1:]):
         o, lse = merge_attn_states(o, lse, o_i, l_i)
     return np.asarray(o, dtype=np.float64), np.asarray(lse, dtype=np.float64)
+
+
+# ----------------------------------------------------------------------------
+# fused rotary embedding + paged K/V write (the step before the scatter)
+# ----------------------------------------------------------------------------
+
+def rope_rotate(x, cos, sin):
+    """NeoX-style rotary embedding of one vector set: the two halves of the
+    head dimension form the pairs (x[i], x[i + D/2]), each rotated by its own
+    angle: ``out[i] = x[i] cos_i - x[i+D/2] sin_i``,
+    ``out[i+D/2] = x[i+D/2] cos_i + x[i] sin_i``.
+
+    [SP] commit notes: the library rotates Q and K with NeoX RoPE (no or
+    linear scaling); the kernel rope_write_kv_paged rotates Q in place and
+    writes the rotated K and the V straight to the pool, RoPE at the absolute
+    positions.  READING: the caller supplies the cos/sin of every (position,
+    pair) as a table, so that scaling variants live in the table.
+
+    ``x``: ``[..., D]`` float64; ``cos``, ``sin``: broadcastable ``[..., D/2]``.
+    """
+    x = np.asarray(x, dtype=np.float64)
+    h = x.shape[-1] // 2
+    x1, x2 = x[..., :h], x[..., h:]
+    return np.concatenate([x1 * cos - x2 * sin, x2 * cos + x1 * sin], axis=-1)
+
+
+def rope_write_kv_paged(q, k_src, v_src, positions, cos_sin, slots, k_pool, v_pool):
+    """Rotate every query head of token t at ``positions[t]`` (in place in the
+    result), rotate its K heads the same way and write them, with its V heads
+    unrotated, into pool slot ``slots[t]`` (negative: no write).
+
+    ``q``: ``[T, Hq, D]`` bf16 bits; ``k_src``/``v_src``: ``[T, Hkv, D]`` bf16
+    bits; ``cos_sin``: ``[max_pos, D]`` float (cos of the D/2 pairs, then their
+    sin); pools ``[pages, P, Hkv, D]`` bf16 bits.
+
+    Returns ``(q_rot float64 [T, Hq, D], k_rot float64 [T, Hkv, D],
+    k_pool_out, v_pool_out)``: the rotated values exactly (the device rounds
+    them to bf16), and the pools with V copied bit for bit and the K slots
+    marked by the rows of ``k_rot`` (compare K through ``k_rot``).
+    """
+    qf = bf16_to_f64(bf16_bits(q))
+    kf = bf16_to_f64(bf16_bits(k_src))
+    cs = np.asarray(cos_sin, dtype=np.float64)
+    h = qf.shape[-1] // 2
+    pos = np.asarray(positions, dtype=np.int64)
+    cos = cs[pos, :h][:, None, :]
+    sin = cs[pos, h:][:, None, :]
+    q_rot = rope_rotate(qf, cos, sin)
+    k_rot = rope_rotate(kf, cos, sin)
+    k_out = np.array(bf16_bits(k_pool), copy=True)
+    v_out = np.array(bf16_bits(v_pool), copy=True)
+    vb = bf16_bits(v_src)
+    P = k_out.shape[1]
+    for t, s_ in enumerate(np.asarray(slots)):
+        s_ = int(s_)
+        if s_ < 0:
+            continue
+        v_out[s_ // P, s_ % P] = vb[t]
+    return q_rot, k_rot, k_out, v_out
+
+
+# ----------------------------------------------------------------------------
+# pool-to-pool slot copy (fills private pages at commit)
+# ----------------------------------------------------------------------------
+
+def copy_kv_slots(k_pools, v_pools, src_slots, dst_slots):
+    """Copy whole slot rows (every K/V head) from slot ``src[c]`` to slot
+    ``dst[c]`` in every layer's K and V pool; an entry with a negative source
+    or destination is a sentinel and is skipped.
+
+    [VG] Description, Cache (one pool-to-pool copy, copy_kv_slots_, fills the
+    private pages at commit) and the per-file notes on causalLayout.cu (the
+    pool-to-pool copy with sentinel entries; copies across layers, K/V and
+    heads).  READING: all sources are read before any destination is written
+    (the device kernel requires source and destination slots to be disjoint
+    for this to hold).
+
+    ``k_pools``/``v_pools``: ``[layers, pages, P, Hkv, D]`` bit arrays.
+    Returns new arrays.
+    """
+    k_out = np.array(k_pools, copy=True)
+    v_out = np.array(v_pools, copy=True)
+    P = k_out.shape[2]
+    pairs = [(int(s_), int(d_)) for s_, d_ in zip(src_slots, dst_slots) if s_ >= 0 and d_ >= 0]
+    k_rows = [np.array(k_pools[:, s_ // P, s_ % P]) for s_, _ in pairs]
+    v_rows = [np.array(v_pools[:, s_ // P, s_ % P]) for s_, _ in pairs]
+    for (s_, d_), kr, vr in zip(pairs, k_rows, v_rows):
+        k_out[:, d_ // P, d_ % P] = kr
+        v_out[:, d_ // P, d_ % P] = vr
+    return k_out, v_out

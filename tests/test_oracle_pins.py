@@ -389,3 +389,81 @@ def test_rotate_three_reversal_identity():
     s = 9
     y = np.concatenate([x[:, :s][:, ::-1], x[:, s:][:, ::-1]], axis=1)[:, ::-1]
     np.testing.assert_array_equal(orc.rotate_rows(x, s), y)
+
+
+# ----------------------------------------------------------------------------
+# rotary embedding + paged write, slot copy
+# ----------------------------------------------------------------------------
+
+def _cos_sin_table(max_pos, D, base=10000.0):
+    """cos/sin of angle pos * base^(-2i/D) for the D/2 pairs (the usual RoPE
+    frequencies), as the caller-supplied table the kernel reads."""
+    i = np.arange(D // 2)
+    ang = np.arange(max_pos)[:, None] * base ** (-2.0 * i / D)[None, :]
+    return np.concatenate([np.cos(ang), np.sin(ang)], axis=1), ang
+
+
+def test_rope_matches_complex_multiplication():
+    """Each pair (x_i, x_{i+D/2}) is the complex number x_i + j x_{i+D/2}
+    multiplied by e^{j angle}: numpy complex arithmetic, a different
+    formulation."""
+    rng = np.random.default_rng(0)
+    D = 16
+    x = rng.standard_normal((5, 3, D))
+    table, ang = _cos_sin_table(50, D)
+    pos = np.array([0, 1, 7, 31, 49])
+    out = orc.rope_rotate(x, table[pos, :D // 2][:, None], table[pos, D // 2:][:, None])
+    z = (x[..., :D // 2] + 1j * x[..., D // 2:]) * np.exp(1j * ang[pos])[:, None, :]
+    np.testing.assert_allclose(out, np.concatenate([z.real, z.imag], axis=-1), rtol=1e-13, atol=1e-13)
+
+
+def test_rope_identity_norm_and_composition():
+    rng = np.random.default_rng(1)
+    D = 8
+    x = rng.standard_normal((4, D))
+    table, ang = _cos_sin_table(20, D)
+    h = D // 2
+    # position 0: the identity
+    np.testing.assert_allclose(orc.rope_rotate(x, table[0, :h], table[0, h:]), x, rtol=0, atol=1e-15)
+    # every pair keeps its length
+    y = orc.rope_rotate(x, table[13, :h], table[13, h:])
+    np.testing.assert_allclose(x[:, :h] ** 2 + x[:, h:] ** 2, y[:, :h] ** 2 + y[:, h:] ** 2, rtol=1e-13)
+    # rotating by 5 then by 8 equals rotating by 13
+    z = orc.rope_rotate(orc.rope_rotate(x, table[5, :h], table[5, h:]), table[8, :h], table[8, h:])
+    np.testing.assert_allclose(z, y, rtol=1e-12, atol=1e-13)
+
+
+def test_rope_write_kv_paged_writes_v_exactly_and_skips_sentinels():
+    gen = torch.Generator().manual_seed(2)
+    T, Hq, Hkv, D, pages = 6, 4, 2, 16, 3
+    q = wl.randn_bf16((T, Hq, D), gen)
+    k = wl.randn_bf16((T, Hkv, D), gen)
+    v = wl.randn_bf16((T, Hkv, D), gen)
+    kp = wl.randn_bf16((pages, 32, Hkv, D), gen)
+    vp = wl.randn_bf16((pages, 32, Hkv, D), gen)
+    table, _ = _cos_sin_table(64, D)
+    pos = np.array([3, 0, 63, 10, 11, 12])
+    slots = np.array([5, 40, -1, 70, 2, 33], dtype=np.int64)
+    q_rot, k_rot, k_out, v_out = orc.rope_write_kv_paged(q, k, v, pos, table, slots, kp, vp)
+    ref_v = bits(vp).reshape(-1, Hkv, D).copy()
+    ok = slots >= 0
+    ref_v[slots[ok]] = bits(v)[ok]
+    np.testing.assert_array_equal(v_out.reshape(-1, Hkv, D), ref_v)
+    # token 1 sits at position 0: unrotated
+    np.testing.assert_array_equal(q_rot[1], f64(q)[1])
+    np.testing.assert_array_equal(k_rot[1], f64(k)[1])
+
+
+def test_copy_kv_slots_matches_fancy_indexing_across_layers():
+    gen = torch.Generator().manual_seed(3)
+    layers, pages, H, D = 3, 4, 2, 8
+    k = bits(wl.randn_bf16((layers, pages, 32, H, D), gen))
+    v = bits(wl.randn_bf16((layers, pages, 32, H, D), gen))
+    src = np.array([1, 5, -1, 40, 77, 9], dtype=np.int64)
+    dst = np.array([100, 64, 3, -1, 90, 120], dtype=np.int64)
+    k_o, v_o = orc.copy_kv_slots(k, v, src, dst)
+    ok = (src >= 0) & (dst >= 0)
+    for pool, out in ((k, k_o), (v, v_o)):
+        ref = pool.reshape(layers, -1, H, D).copy()
+        ref[:, dst[ok]] = pool.reshape(layers, -1, H, D)[:, src[ok]]
+        np.testing.assert_array_equal(out.reshape(layers, -1, H, D), ref)
