@@ -170,6 +170,65 @@ pkv_status paged_attention(const void* q, int64_t q_token_stride, int64_t q_head
                            int32_t* err, void* stream);
 
 /*
+ * rope_write_kv_paged -- rotary embedding of this step's queries (in place)
+ * and keys, with the rotated keys and the values written into pool slots, in
+ * one launch (the step that precedes paged_attention).
+ *
+ * [SP] commit notes: RoPE and the K/V write are one kernel (rope_write_kv_paged:
+ * Q rotated in place, the rotated K and V written straight to the pool; NeoX
+ * RoPE with no or linear scaling; RoPE at the absolute positions, the write at
+ * the slot of the table).  NeoX pairs are (x[i], x[i + D/2]):
+ *     out[i]       = x[i] cos - x[i + D/2] sin
+ *     out[i + D/2] = x[i + D/2] cos + x[i] sin
+ * with the angle of token t's position positions[t] and pair i read from the
+ * caller's table cos_sin[positions[t]][i] (cos) and [D/2 + i] (sin), so any
+ * frequency base or linear scaling lives in the table.
+ *
+ * For t in [0, num_tokens): every query head of row t is rotated in place
+ * (q: bf16, q_token_stride / q_head_stride); if slots[t] >= 0, the rotated K
+ * heads of source row t are written to pool slot slots[t] of k_pool and the V
+ * heads, unrotated and bit for bit, to v_pool (k_src / v_src are not
+ * modified).  Results are rounded to bf16 from fp32 arithmetic.
+ *
+ *  cos_sin       device f32 [max_position][head_dim], 16-byte aligned
+ *  positions     device int64 [num_tokens]; outside [0, max_position) they are
+ *                clamped (and flagged with PKV_FLAG_CHECKED)
+ *  head_dim      a multiple of 16; q / sources 16-byte aligned, strides
+ *                multiples of 8 elements
+ */
+pkv_status rope_write_kv_paged(void* q, int64_t q_token_stride, int64_t q_head_stride,
+                               int num_q_heads, const void* k_src, const void* v_src,
+                               int64_t src_token_stride, int64_t src_head_stride,
+                               int64_t num_tokens, int num_kv_heads, int head_dim,
+                               const int64_t* positions, const float* cos_sin,
+                               int64_t max_position, const int64_t* slots, void* k_pool,
+                               void* v_pool, int64_t num_pages, int page_size,
+                               int64_t page_stride, unsigned flags, int32_t* err, void* stream);
+
+/*
+ * copy_kv_slots -- copy whole slot rows from one pool slot to another, in
+ * every layer's K and V pool.
+ *
+ * [VG] Description, Cache (a pool-to-pool copy, copy_kv_slots_, fills the
+ * private pages of the causal blocks at commit) and the per-file notes on
+ * causalLayout.cu (copies across layers, K/V and heads; sentinel entries).
+ * For c in [0, num_copies) with src_slots[c] >= 0 and dst_slots[c] >= 0, and
+ * every layer l in [0, num_layers): slot dst_slots[c] of layer l's K pool (at
+ * k_pool + l * layer_stride elements) <- its slot src_slots[c]; same for V.
+ * A negative entry is a sentinel and is skipped.  Source and destination slots
+ * must be disjoint and destinations distinct: otherwise the result is
+ * unspecified (copies run concurrently).
+ *
+ *  dtype      element type (only its size matters); a slot row
+ *             (num_kv_heads * head_dim elements) must be a multiple of 16 bytes
+ */
+pkv_status copy_kv_slots(void* k_pool, void* v_pool, int num_layers, int64_t layer_stride,
+                         int64_t num_pages, int page_size, int64_t page_stride, int num_kv_heads,
+                         int head_dim, pkv_dtype dtype, const int64_t* src_slots,
+                         const int64_t* dst_slots, int64_t num_copies, unsigned flags,
+                         int32_t* err, void* stream);
+
+/*
  * paged_attention_no_alloc -- paged_attention for callers that cannot allocate.
  *
  * The pages describe no such entry point; it exists for callers that have no

@@ -3,4 +3,4 @@
 from . import workloads  # noqa: F401  (seeded input generators)
 from .pkv import (  # noqa: F401
     kv_scatter_slots, paged_attention, paged_attention_workspace_size, merge_attn_states,
-    rotate_rows, lib, PkvError)
+    rotate_rows, rope_write_kv_paged, copy_kv_slots, paged_attention_no_alloc, lib, PkvError)

@@ -369,6 +369,71 @@ pkv_status merge_attn_states(const void* o_a, const float* lse_a, const void* o_
                      "merge launch");
 }
 
+pkv_status rope_write_kv_paged(void* q, int64_t q_token_stride, int64_t q_head_stride,
+                               int num_q_heads, const void* k_src, const void* v_src,
+                               int64_t src_token_stride, int64_t src_head_stride,
+                               int64_t num_tokens, int num_kv_heads, int head_dim,
+                               const int64_t* positions, const float* cos_sin,
+                               int64_t max_position, const int64_t* slots, void* k_pool,
+                               void* v_pool, int64_t num_pages, int page_size,
+                               int64_t page_stride, unsigned flags, int32_t* err, void* stream) {
+    if (num_tokens < 0 || num_q_heads < 0 || num_kv_heads < 0 || head_dim < 0 || num_pages < 0 ||
+        max_position < 0)
+        return fail(PKV_ERR_INVALID_ARG, "rope: negative size");
+    if (num_tokens == 0) return ok();
+    if (!q || !k_src || !v_src || !positions || !cos_sin || !slots || !k_pool || !v_pool)
+        return fail(PKV_ERR_INVALID_ARG, "rope: null pointer");
+    if (head_dim <= 0 || head_dim % 16)
+        return fail(PKV_ERR_UNSUPPORTED, "rope: head_dim %d (a multiple of 16)", head_dim);
+    if (max_position == 0) return fail(PKV_ERR_INVALID_ARG, "rope: empty cos/sin table");
+    if (page_size <= 0 || page_stride < static_cast<int64_t>(page_size) * num_kv_heads * head_dim ||
+        page_stride % 8)
+        return fail(PKV_ERR_INVALID_ARG, "rope: page_stride must cover a page, a multiple of 8");
+    if (!aligned(q, 16) || !aligned(k_src, 16) || !aligned(v_src, 16) || !aligned(k_pool, 16) ||
+        !aligned(v_pool, 16) || !aligned(cos_sin, 16) || q_token_stride % 8 || q_head_stride % 8 ||
+        src_token_stride % 8 || src_head_stride % 8 || q_token_stride < 0 || q_head_stride < 0 ||
+        src_token_stride < 0 || src_head_stride < 0)
+        return fail(PKV_ERR_INVALID_ARG, "rope: 16-byte aligned pointers and strides multiple of 8");
+    if ((flags & PKV_FLAG_CHECKED) && !err)
+        return fail(PKV_ERR_INVALID_ARG, "rope: checked mode needs an error flag");
+    pkv::RopeArgs a{q, q_token_stride, q_head_stride, num_q_heads, k_src, v_src, src_token_stride,
+                    src_head_stride, num_tokens, num_kv_heads, head_dim, positions, cos_sin,
+                    max_position, slots, k_pool, v_pool, num_pages, page_size, page_stride,
+                    (flags & PKV_FLAG_CHECKED) != 0, err};
+    return from_cuda(pkv::launch_rope_write(a, static_cast<cudaStream_t>(stream)), "rope launch");
+}
+
+pkv_status copy_kv_slots(void* k_pool, void* v_pool, int num_layers, int64_t layer_stride,
+                         int64_t num_pages, int page_size, int64_t page_stride, int num_kv_heads,
+                         int head_dim, pkv_dtype dtype, const int64_t* src_slots,
+                         const int64_t* dst_slots, int64_t num_copies, unsigned flags,
+                         int32_t* err, void* stream) {
+    const int esz = elem_size(dtype);
+    if (esz == 0) return fail(PKV_ERR_INVALID_ARG, "copy: unknown dtype %d", (int)dtype);
+    if (num_copies < 0 || num_layers < 0 || num_pages < 0 || num_kv_heads < 0 || head_dim < 0)
+        return fail(PKV_ERR_INVALID_ARG, "copy: negative size");
+    if (num_copies == 0 || num_layers == 0 || num_kv_heads == 0 || head_dim == 0) return ok();
+    if (!k_pool || !v_pool || !src_slots || !dst_slots)
+        return fail(PKV_ERR_INVALID_ARG, "copy: null pointer");
+    const int64_t row_bytes = static_cast<int64_t>(num_kv_heads) * head_dim * esz;
+    if (row_bytes % 16)
+        return fail(PKV_ERR_UNSUPPORTED, "copy: a slot row must be a multiple of 16 bytes");
+    if (page_size <= 0 || page_stride < static_cast<int64_t>(page_size) * num_kv_heads * head_dim ||
+        (page_stride * esz) % 16)
+        return fail(PKV_ERR_INVALID_ARG, "copy: page_stride must cover a page, 16-byte multiple");
+    if (num_layers > 1 && (layer_stride < num_pages * page_stride || (layer_stride * esz) % 16))
+        return fail(PKV_ERR_INVALID_ARG, "copy: layer_stride must cover a layer's pool, 16-byte multiple");
+    if (num_layers > 65535) return fail(PKV_ERR_UNSUPPORTED, "copy: more than 65535 layers");
+    if (!aligned(k_pool, 16) || !aligned(v_pool, 16))
+        return fail(PKV_ERR_INVALID_ARG, "copy: pools must be 16-byte aligned");
+    if ((flags & PKV_FLAG_CHECKED) && !err)
+        return fail(PKV_ERR_INVALID_ARG, "copy: checked mode needs an error flag");
+    pkv::CopySlotsArgs a{k_pool, v_pool, num_layers, layer_stride, num_pages, page_size, page_stride,
+                         num_kv_heads, head_dim, esz, src_slots, dst_slots, num_copies,
+                         (flags & PKV_FLAG_CHECKED) != 0, err};
+    return from_cuda(pkv::launch_copy_slots(a, static_cast<cudaStream_t>(stream)), "copy launch");
+}
+
 pkv_status rotate_rows(void* x, int64_t rows, int64_t cols, int64_t row_stride, int elem_size_b,
                        int64_t shift, void* stream) {
     if (rows < 0 || cols < 0) return fail(PKV_ERR_INVALID_ARG, "rotate: negative size");

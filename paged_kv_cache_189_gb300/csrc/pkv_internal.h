@@ -32,6 +32,48 @@ struct ScatterArgs {
 };
 cudaError_t launch_scatter(const ScatterArgs& a, cudaStream_t s);
 
+// ---------------------------- rope + paged write -----------------------------
+struct RopeArgs {
+    void* q;
+    int64_t q_token_stride, q_head_stride;
+    int num_q_heads;
+    const void* k_src;
+    const void* v_src;
+    int64_t src_token_stride, src_head_stride;
+    int64_t num_tokens;
+    int num_kv_heads, head_dim;
+    const int64_t* positions;
+    const float* cos_sin;  // [max_position][head_dim]: cos of the D/2 pairs, then their sin
+    int64_t max_position;
+    const int64_t* slots;
+    void* k_pool;
+    void* v_pool;
+    int64_t num_pages;
+    int page_size;
+    int64_t page_stride;
+    bool checked;
+    int32_t* err;
+};
+cudaError_t launch_rope_write(const RopeArgs& a, cudaStream_t s);
+
+// ---------------------------- pool-to-pool slot copy --------------------------
+struct CopySlotsArgs {
+    void* k_pool;
+    void* v_pool;
+    int num_layers;
+    int64_t layer_stride;  // elements between layers' pools
+    int64_t num_pages;
+    int page_size;
+    int64_t page_stride;
+    int num_kv_heads, head_dim, elem_size;
+    const int64_t* src_slots;
+    const int64_t* dst_slots;
+    int64_t num_copies;
+    bool checked;
+    int32_t* err;
+};
+cudaError_t launch_copy_slots(const CopySlotsArgs& a, cudaStream_t s);
+
 // ---------------------------- rotate ---------------------------------------
 // Rotation in units of `unit` bytes (1, 2, 4, 8 or 16); cols, shift and
 // row_stride are already expressed in units, 0 < shift < cols.

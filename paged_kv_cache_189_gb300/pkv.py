@@ -26,7 +26,7 @@ PKV_ERRBIT_SLOT, PKV_ERRBIT_SRC, PKV_ERRBIT_PAGE, PKV_ERRBIT_LEN, PKV_ERRBIT_TIM
 # every symbol include/pkv.h declares
 EXPORTED = ("pkv_status_string", "pkv_last_error", "kv_scatter_slots",
             "paged_attention_workspace_size", "paged_attention", "merge_attn_states",
-            "rotate_rows", "paged_attention_no_alloc")
+            "rotate_rows", "paged_attention_no_alloc", "rope_write_kv_paged", "copy_kv_slots")
 NO_ALLOC_SCRATCH_BYTES = 32 << 20
 
 _vp, _i64, _i32, _u32, _f32, _sz = (ctypes.c_void_p, ctypes.c_int64, ctypes.c_int,
@@ -46,6 +46,11 @@ _SIGNATURES = {
     "merge_attn_states": (_i32, [_vp, _vp, _vp, _vp, _i32, _i64, _i32, _i32, _vp, _i32, _vp,
                                  _vp]),
     "rotate_rows": (_i32, [_vp, _i64, _i64, _i64, _i32, _i64, _vp]),
+    "rope_write_kv_paged": (_i32, [_vp, _i64, _i64, _i32, _vp, _vp, _i64, _i64, _i64, _i32, _i32,
+                                   _vp, _vp, _i64, _vp, _vp, _vp, _i64, _i32, _i64, _u32, _vp,
+                                   _vp]),
+    "copy_kv_slots": (_i32, [_vp, _vp, _i32, _i64, _i64, _i32, _i64, _i32, _i32, _i32, _vp, _vp,
+                             _i64, _u32, _vp, _vp]),
 }
 
 _lib = None
@@ -202,3 +207,36 @@ def rotate_rows(x, shift, rows=None, cols=None, row_stride=None, elem_size=None,
         elem_size = x.element_size()
     st = lib().rotate_rows(_ptr(x), rows, cols, row_stride, elem_size, shift, _stream(stream))
     _check("rotate_rows", st)
+
+
+def rope_write_kv_paged(q, k_src, v_src, positions, cos_sin, slots, k_pool, v_pool,
+                        checked=False, err=None, stream=None):
+    """Rotate ``q [T, Hq, D]`` in place and write the rotated ``k_src`` and the
+    ``v_src`` rows ``[T, Hkv, D]`` into pool slots ``slots`` (NeoX pairs,
+    angles from the table ``cos_sin [max_position, D]``)."""
+    assert q.stride(2) == 1 and k_src.stride(2) == 1 and k_src.stride() == v_src.stride()
+    n, P, H, D, page_stride = _pool_geometry(k_pool)
+    assert v_pool.shape == k_pool.shape and v_pool.stride() == k_pool.stride()
+    assert cos_sin.dtype == torch.float32 and cos_sin.is_contiguous() and cos_sin.shape[1] == D
+    st = lib().rope_write_kv_paged(
+        _ptr(q), q.stride(0), q.stride(1), q.shape[1], _ptr(k_src), _ptr(v_src), k_src.stride(0),
+        k_src.stride(1), q.shape[0], H, D, _ptr(positions), _ptr(cos_sin), cos_sin.shape[0],
+        _ptr(slots), _ptr(k_pool), _ptr(v_pool), n, P, page_stride,
+        PKV_FLAG_CHECKED if checked else 0, _ptr(err), _stream(stream))
+    _check("rope_write_kv_paged", st)
+
+
+def copy_kv_slots(k_pools, v_pools, src_slots, dst_slots, checked=False, err=None, stream=None):
+    """Copy slot rows ``src -> dst`` in every layer of ``k_pools``/``v_pools``
+    ``[layers, pages, P, Hkv, D]`` (a 4-D pool is one layer); negative entries
+    are skipped."""
+    if k_pools.dim() == 4:
+        k_pools, v_pools = k_pools.unsqueeze(0), v_pools.unsqueeze(0)
+    layers = k_pools.shape[0]
+    n, P, H, D, page_stride = _pool_geometry(k_pools[0])
+    assert v_pools.shape == k_pools.shape and v_pools.stride() == k_pools.stride()
+    st = lib().copy_kv_slots(_ptr(k_pools), _ptr(v_pools), layers, k_pools.stride(0), n, P,
+                             page_stride, H, D, _dtype(k_pools), _ptr(src_slots), _ptr(dst_slots),
+                             src_slots.numel(), PKV_FLAG_CHECKED if checked else 0, _ptr(err),
+                             _stream(stream))
+    _check("copy_kv_slots", st)
