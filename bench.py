@@ -50,7 +50,7 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="gqa_decode",
                     choices=["gqa_decode", "chunked_prefill", "block_causal_video",
-                             "shared_prefix", "tiny_decode"])
+                             "shared_prefix", "tiny_decode", "multi_token_decode"])
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-sample-seqs", type=int, default=64)
@@ -373,9 +373,9 @@ def build_plan(name, rank, dev, stream):
 
     case = {"gqa_decode": wl.gqa_decode, "chunked_prefill": wl.chunked_prefill,
             "block_causal_video": wl.block_causal_video, "shared_prefix": wl.shared_prefix,
-            "tiny_decode": wl.tiny_decode}[name](seed={"gqa_decode": 1, "chunked_prefill": 2,
-                                                         "shared_prefix": 3, "block_causal_video": 4,
-                                                         "tiny_decode": 0}[name] + rank)
+            "tiny_decode": wl.tiny_decode, "multi_token_decode": wl.multi_token_decode}[name](
+        seed={"gqa_decode": 1, "chunked_prefill": 2, "shared_prefix": 3, "block_causal_video": 4,
+              "tiny_decode": 0, "multi_token_decode": 5}[name] + rank)
     Hq, Hkv, D = case.num_q_heads, case.num_kv_heads, case.head_dim
     rows = case.q.shape[0]
     t = dict(k_pool=case.k_pool.to(dev), v_pool=case.v_pool.to(dev), q=case.q.to(dev),
@@ -418,6 +418,19 @@ def build_plan(name, rank, dev, stream):
                         dom_work=attn_bytes, bound="hbm", peak=peak_hbm, peak_unit="GB/s",
                         peak_src=f"{hbm_kind} hbm_gbs", h2d=(h2d_src, h2d_dst), d2h=d2h_src,
                         launches=3, traffic_sources=DECODE_SOURCES)
+    if name == "multi_token_decode":
+        attn_bytes, kv_bytes = decode_bytes(case)
+        dom = attention_call(t["q"], t["bt"], t["kl"], t["qi"], t["qr"], out, lse, case.max_q_rows,
+                             case.max_kv_len, "causal")
+        cfg.update(kv_len="U[512,8192]+4", q_len=case.max_q_rows, kv_bytes_per_step=kv_bytes,
+                   queries_per_step=rows, l2="inputs larger than L2")
+        return StepPlan(case=case, cfg=cfg, metric="multi-token decode KV GB/s", unit=UNIT,
+                        work=kv_bytes, scale=1e9, queries=rows, pre=[scatter], dominant=dom, post=[],
+                        aux=aux, dom_label="paged_attention: tensor-core tile kernel, 4 tokens x 4 "
+                                           "grouped heads = 16 of 128 tile rows",
+                        dom_work=attn_bytes, bound="hbm", peak=peak_hbm, peak_unit="GB/s",
+                        peak_src=f"{hbm_kind} hbm_gbs", h2d=(h2d_src, h2d_dst), d2h=d2h_src,
+                        launches=2, traffic_sources=ATTN_TC_SOURCES)
     if name in ("chunked_prefill", "block_causal_video"):
         pairs = visible_pairs(case)
         flops = 4.0 * D * Hq * pairs
@@ -546,19 +559,30 @@ def run_ours(args):
     queries_total = sum_over_ranks(dist, plan.queries * args.steps, dev)
     value = work_total / (ms_total_max * 1e-3) / plan.scale
 
-    # ---- auxiliary launches of the step, each timed alone (inputs > L2)
+    # ---- auxiliary launches of the step, each timed alone: 20 calls captured
+    #      in a CUDA graph and replayed, so host call overhead is not measured
     aux_out = {}
     for key, (fn, nbytes, unit) in plan.aux.items():
+        reps = 20
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            fn()  # warm (first-call set-up happens outside the capture)
+            torch.cuda.synchronize()
+            with torch.cuda.graph(graph, stream=stream):
+                for _ in range(reps):
+                    fn()
+            graph.replay()
+        torch.cuda.synchronize()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         with torch.cuda.stream(stream):
-            fn()
             a.record(stream)
-            for _ in range(5):
-                fn()
+            graph.replay()
             b.record(stream)
         torch.cuda.synchronize()
-        ms = a.elapsed_time(b) / 5
-        aux_out[key] = {"ms": ms, "bytes": nbytes, "GB/s": nbytes / (ms * 1e-3) / 1e9}
+        ms = a.elapsed_time(b) / reps
+        aux_out[key] = {"ms": ms, "bytes": nbytes, "GB/s": nbytes / (ms * 1e-3) / 1e9,
+                        "timing": f"{reps} calls in one CUDA graph replay"}
+        del graph
 
     # ---- end to end through the public API: pinned host inputs -> device,
     #      the whole step, result read back to the host, every step

@@ -32,7 +32,7 @@ PAGE_SIZE = 32
 
 __all__ = [
     "PAGE_SIZE", "PagedCase", "randn_bf16", "slot_of", "build_pool_case",
-    "tiny_decode", "gqa_decode", "chunked_prefill", "shared_prefix",
+    "tiny_decode", "gqa_decode", "multi_token_decode", "chunked_prefill", "shared_prefix",
     "block_causal_video", "random_case", "WORKLOADS",
 ]
 
@@ -193,6 +193,17 @@ def gqa_decode(seed: int = 1, batch: int = 64, lo: int = 512, hi: int = 8192,
                            Hq, Hkv, D, mask="causal")
 
 
+def multi_token_decode(seed: int = 5, batch: int = 64, q_len: int = 4, lo: int = 512,
+                       hi: int = 8192, Hq: int = 32, Hkv: int = 8, D: int = 128) -> PagedCase:
+    """Speculative verification: each of 64 sequences with a cached length
+    L ~ U[512, 8192] appends q_len = 4 new tokens (the last accepted token and
+    the drafts), scattered first, and attends causally over L + q_len keys."""
+    rng = np.random.default_rng(seed)
+    L = rng.integers(lo, hi, size=batch, endpoint=True)
+    return build_pool_case("multi_token_decode", seed, L + q_len, np.full(batch, q_len),
+                           np.full(batch, q_len), Hq, Hkv, D, mask="causal")
+
+
 def chunked_prefill(seed: int = 2, batch: int = 8, chunk: int = 512, lo: int = 2048,
                     hi: int = 16384, Hq: int = 32, Hkv: int = 8, D: int = 128) -> PagedCase:
     """Batch 8, 512 new query tokens appended to a cached context of
@@ -309,4 +320,5 @@ WORKLOADS = {
     "chunked_prefill": chunked_prefill,
     "shared_prefix": shared_prefix,
     "block_causal_video": block_causal_video,
+    "multi_token_decode": multi_token_decode,
 }

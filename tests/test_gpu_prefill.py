@@ -20,13 +20,31 @@ DEV = "cuda"
 
 @pytest.mark.parametrize("mask,cb", [("causal", 0), ("block_causal", 7), ("block_causal", 64),
                                      ("none", 0)])
-@pytest.mark.parametrize("Hq,Hkv", [(32, 8), (8, 8), (16, 2), (4, 2)])
+@pytest.mark.parametrize("Hq,Hkv", [(32, 8), (8, 8), (16, 2), (4, 2), (32, 2)])
 def test_tile_kernel_random(mask, cb, Hq, Hkv):
     c = wl.random_case(300 + Hq + cb, batch=3, Hq=Hq, Hkv=Hkv, D=128, kv_range=(40, 700),
                        q_range=(2, 150), pad_range=(0, 9), mask=mask, causal_block=cb)
     out, lse, *_ , err = gpu_step(c)
     O, L, *_ = oracle_step(c)
     assert err == 0
+    assert_attention_close(out, lse, O, L, c)
+
+
+def test_multi_token_decode_workload():
+    """Speculative verification rows: 4 new tokens per sequence, causal."""
+    c = wl.multi_token_decode(batch=16)
+    out, lse, *_ , err = gpu_step(c)
+    O, L, *_ = oracle_step(c)
+    assert err == 0
+    assert_attention_close(out, lse, O, L, c)
+
+
+@pytest.mark.parametrize("q_len", [2, 3, 9, 16])
+def test_few_rows_per_sequence(q_len):
+    c = wl.random_case(500 + q_len, batch=6, Hq=32, Hkv=8, D=128, kv_range=(q_len, 900),
+                       q_range=(q_len, q_len), pad_range=(0, 1), mask="causal")
+    out, lse, *_ = gpu_step(c)
+    O, L, *_ = oracle_step(c)
     assert_attention_close(out, lse, O, L, c)
 
 
