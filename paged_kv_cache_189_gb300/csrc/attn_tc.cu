@@ -164,29 +164,6 @@ __device__ __forceinline__ int visible_keys(int i, int qreal, int kv_len, int ma
     return first_new + min(qreal, block_end);
 }
 
-// 2^x for two values on the FMA pipes, to share the exponentials of a tile
-// between the special-function unit and the FMA units.  Range reduction
-// x = n + f with n the nearest integer (added through the 1.5 * 2^23 rounding
-// constant) and f in [-0.5, 0.5]; 2^f by a cubic fitted here to minimise the
-// relative error on that interval (Lawson's iteratively reweighted least
-// squares; max relative error 8.4e-5, well below bf16's 2^-9); 2^n added to
-// the exponent field.  Inputs below -126 are clamped (the result is then
-// ~1e-38 instead of a smaller number).
-__device__ __forceinline__ float2 exp2_poly2(float2 x) {
-    constexpr float kRound = 12582912.0f;  // 1.5 * 2^23
-    x = make_float2(fmaxf(x.x, -126.f), fmaxf(x.y, -126.f));
-    const float2 t = __fadd2_rn(x, make_float2(kRound, kRound));
-    const float2 n = __fadd2_rn(t, make_float2(-kRound, -kRound));
-    const float2 f = __ffma2_rn(n, make_float2(-1.f, -1.f), x);
-    float2 q = __ffma2_rn(f, make_float2(0.055213093757629395f, 0.055213093757629395f),
-                          make_float2(0.24271467328071594f, 0.24271467328071594f));
-    q = __ffma2_rn(q, f, make_float2(0.6932622194290161f, 0.6932622194290161f));
-    q = __ffma2_rn(q, f, make_float2(0.9999195337295532f, 0.9999195337295532f));
-    // the low bits of t hold n; shifted into the exponent field they scale q by 2^n
-    return make_float2(__int_as_float(__float_as_int(q.x) + (__float_as_int(t.x) << 23)),
-                       __int_as_float(__float_as_int(q.y) + (__float_as_int(t.y) << 23)));
-}
-
 struct TileGeom {
     int b, kvh, split, r0, nrows, qreal, kv_len, t0, kb, key_hi, nt;
 };
@@ -569,29 +546,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 5) tmem_dealloc(tmem, kTmemCols);
 }
 
-// ===========================================================================
-// Two query tiles per CTA (tile A = rows [0,128), tile B = rows [128,256) of
-// the CTA's 2 x TQ tokens), one softmax warpgroup each, sharing every K/V
-// load.  While one warpgroup runs its softmax the tensor core works on the
-// other tile, so the exponentials and the MMAs overlap.  P is written back
-// into tensor memory over the tile's S columns (packed bf16 pairs) and the
-// P.V product reads its A operand from tensor memory, which leaves shared
-// memory for the two Q tiles and the K/V rings.
-// Tensor memory: S_A [0,128) O_A [128,256) S_B [256,384) O_B [384,512).
-// Roles (320 threads): warps 0-3 softmax A, warps 4-7 softmax B, warp 8 TMA
-// producer, warp 9 MMA.
-// ===========================================================================
-constexpr int kThreads2 = 320;
 constexpr int kQ2Off = 0;                                   // Q_A, Q_B
 constexpr int kK2Off = kQ2Off + 2 * kTileBytes;
 constexpr int kV2Off = kK2Off + kKStages * kTileBytes;
 constexpr int kBar2Off = kV2Off + kVStages * kTileBytes;
 // barriers: q_ready, k_full[3], k_empty[3], v_full[2], v_empty[2], s_full[2], p_full[2], o_full[2]
 constexpr int kNumBars2 = 1 + 2 * kKStages + 2 * kVStages + 6;
-constexpr int kTmemSlot2Off = kBar2Off + kNumBars2 * 8;
-constexpr int kFlag2Off = kTmemSlot2Off + 8;
-constexpr int kSmemBytes2 = kFlag2Off + 16;
-static_assert(kSmemBytes2 <= 227 * 1024, "shared memory per CTA");
 
 #define PKV_W4(i) "r"(v[i + 0]), "r"(v[i + 1]), "r"(v[i + 2]), "r"(v[i + 3])
 // 16 consecutive 32-bit columns of this thread's lane
@@ -615,8 +575,52 @@ __device__ __forceinline__ void umma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, u
         ::"r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate) : "memory");
 }
 
+// ===========================================================================
+// Two query tiles per CTA (tile A = rows [0,128), tile B = rows [128,256) of
+// the CTA's 2 x TQ tokens) sharing every K/V load.  While one tile's softmax
+// runs, the tensor core works on the other tile, so the exponentials and the
+// MMAs overlap.  P is written back into tensor memory over the tile's S
+// columns (packed bf16 pairs) and the P.V product reads its A operand from
+// tensor memory, which leaves shared memory for the two Q tiles and the K/V
+// rings.  Tensor memory: S_A [0,128) O_A [128,256) S_B [256,384) O_B [384,512).
+//
+// Eight softmax warps per tile: the two warps that share a tensor-memory lane
+// quadrant (the same 32 rows) take one 64-key half of each 128-key tile each
+// and exchange their partial row maxima through shared memory, which halves
+// each warp's serial work per key tile (the chain softmax -> P.V -> next S
+// that the other tile's MMAs have to cover).  Packed P of the first key half
+// goes to columns [0,32) of the tile's S region, that of the second half to
+// columns [96,128) (written from its last 32 keys backwards), so neither half
+// overwrites S values the other has not read yet.
+// Roles (576 threads): warps 0-7 softmax A, warps 8-15 softmax B (quadrant
+// warp & 3, key half (warp >> 2) & 1), warp 16 TMA producer, warp 17 MMA.
+// Every wait gives up after ~2 s; the per-tile exchange barrier also ANDs the
+// waits' results, so the 256 threads of a tile leave the key loop together.
+// ===========================================================================
+constexpr int kThreads2 = 576;
+constexpr int kXch2Off = kBar2Off + kNumBars2 * 8;            // float [2 tiles][2 halves][128 rows]
+constexpr int kTmemSlot2Off = kXch2Off + 2 * 2 * kTileM * 4;
+constexpr int kFlag2Off = kTmemSlot2Off + 8;
+constexpr int kSmemBytes2 = kFlag2Off + 16;
+static_assert(kSmemBytes2 <= 227 * 1024, "shared memory per CTA");
+
+// named barrier `id` over `count` threads that also returns the AND of `pred`
+__device__ __forceinline__ bool bar_and(int id, int count, bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 q, %1, 0;\n\t"
+        "bar.red.and.pred p, %2, %3, q;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(r) : "r"(static_cast<uint32_t>(pred)), "r"(id), "r"(count) : "memory");
+    return r != 0;
+}
+__device__ __forceinline__ void bar_sync_n(int id, int count) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
 template <int G>
-__global__ void __launch_bounds__(kThreads2, 1)
+__global__ void __maxnreg__(96)
     attn_tc2_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                     const AttnParams p) {
     constexpr int TQ = kTileM / G;
@@ -624,7 +628,6 @@ __global__ void __launch_bounds__(kThreads2, 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
-    // geometry of the CTA's 2 x TQ tokens (tile A then tile B)
     TileGeom g;
     g.b = blockIdx.z / p.num_splits;
     g.split = blockIdx.z - g.b * p.num_splits;
@@ -675,11 +678,12 @@ __global__ void __launch_bounds__(kThreads2, 1)
     uint64_t* s_full = v_empty + kVStages;  // [tile]
     uint64_t* p_full = s_full + 2;          // [tile]
     uint64_t* o_full = p_full + 2;          // [tile]
+    float* xch = reinterpret_cast<float*>(smem + kXch2Off);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kTmemSlot2Off);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kFlag2Off);
 
     if (threadIdx.x == 0) {
-        mbar_init(q_ready, 2 * kTileM);
+        mbar_init(q_ready, 4 * kTileM);
         for (int s = 0; s < kKStages; ++s) {
             mbar_init(&k_full[s], 1);
             mbar_init(&k_empty[s], 1);
@@ -690,13 +694,13 @@ __global__ void __launch_bounds__(kThreads2, 1)
         }
         for (int x = 0; x < 2; ++x) {
             mbar_init(&s_full[x], 1);
-            mbar_init(&p_full[x], kTileM);
+            mbar_init(&p_full[x], 2 * kTileM);
             mbar_init(&o_full[x], 1);
         }
         *abort_flag = 0;
         fence_mbar_init();
     }
-    if (warp == 9) {
+    if (warp == 17) {
         tmem_alloc(tmem_slot, kTmemCols);
         tmem_relinquish();
     }
@@ -714,7 +718,7 @@ __global__ void __launch_bounds__(kThreads2, 1)
         return false;
     };
 
-    if (warp == 8) {
+    if (warp == 16) {
         // ============================ producer ==============================
         if (lane == 0) {
             prefetch_tmap(&tm_k);
@@ -756,7 +760,7 @@ __global__ void __launch_bounds__(kThreads2, 1)
             for (int j = max(0, v_issued - kVStages); j < v_issued; ++j)
                 mbar_wait(&v_full[j % kVStages], (j / kVStages) & 1);
         }
-    } else if (warp == 9) {
+    } else if (warp == 17) {
         // ============================== MMA ================================
         if (lane == 0) {
             constexpr uint32_t kIdescS = idesc_bf16(kTileM, kTileN, false);
@@ -776,10 +780,11 @@ __global__ void __launch_bounds__(kThreads2, 1)
                 const uint32_t vb = sbase + kV2Off + (j % kVStages) * kTileBytes;
 #pragma unroll
                 for (int kk = 0; kk < kTileN / 16; ++kk) {
-                    // A = P in tensor memory (16 keys = 8 packed columns per step),
-                    // B = V (rows = keys, MN-major; 64-column halves LBO apart)
+                    // A = P in tensor memory: keys [0,64) packed in columns [0,32),
+                    // keys [64,128) in columns [96,128); 16 keys = 8 columns per step
+                    const uint32_t pcol = kk < 4 ? kk * 8 : 64 + kk * 8;
                     const uint64_t bdesc = sdesc_sw128(vb + kk * 16 * 128, kHalfBytes, 1024);
-                    umma_bf16_ts(tmem + x * 256 + 128, tmem + x * 256 + kk * 8, bdesc, kIdescO,
+                    umma_bf16_ts(tmem + x * 256 + 128, tmem + x * 256 + pcol, bdesc, kIdescO,
                                  (j > 0 || kk > 0) ? 1u : 0u);
                 }
             };
@@ -792,7 +797,6 @@ __global__ void __launch_bounds__(kThreads2, 1)
             }
             for (int j = 0; ok && j < g.nt; ++j) {
                 const bool more = j + 1 < g.nt;
-                // tile A
                 if (!wait(&p_full[0], j & 1) || !wait(&v_full[j % kVStages], (j / kVStages) & 1)) break;
                 tc_fence_after();
                 issue_pv(0, j);
@@ -803,7 +807,6 @@ __global__ void __launch_bounds__(kThreads2, 1)
                 } else {
                     umma_commit(&o_full[0]);
                 }
-                // tile B
                 if (!wait(&p_full[1], j & 1)) break;
                 tc_fence_after();
                 issue_pv(1, j);
@@ -818,76 +821,83 @@ __global__ void __launch_bounds__(kThreads2, 1)
         }
     } else {
         // ============================ softmax ===============================
-        const int x = warp >> 2;              // tile of this warpgroup
-        const int r = threadIdx.x & 127;       // row in the tile = tensor-memory lane
+        const int x = warp >> 3;               // tile
+        const int hf = (warp >> 2) & 1;        // key half of each tile (and O column half)
+        const int r = (warp & 3) * 32 + lane;  // row in the tile = tensor-memory lane
         const int t = r / G, hg = r % G;
-        const int i = g.t0 + x * TQ + t;       // query row within the sequence
+        const int i = g.t0 + x * TQ + t;
         const int h = g.kvh * G + hg;
+        const int bar_id = 1 + x;
         const bool row_exists = i < g.nrows;
         const int limit = row_exists ? visible_keys(i, g.qreal, g.kv_len, p.mask, max(p.causal_block, 1))
                                      : 0;
         {
+            // this thread's half of the row's 16-byte chunks
             const uint4* src = reinterpret_cast<const uint4*>(
                 static_cast<const __nv_bfloat16*>(p.q) + static_cast<int64_t>(g.r0 + i) * p.q_token_stride +
-                static_cast<int64_t>(h) * p.q_head_stride);
-            uint8_t* qt = smem + kQ2Off + x * kTileBytes;
+                static_cast<int64_t>(h) * p.q_head_stride) + hf * 8;
+            uint8_t* qt = smem + kQ2Off + x * kTileBytes + hf * kHalfBytes;
 #pragma unroll
-            for (int c = 0; c < 16; ++c) {
+            for (int c = 0; c < 8; ++c) {
                 const uint4 v = row_exists ? src[c] : make_uint4(0u, 0u, 0u, 0u);
-                *reinterpret_cast<uint4*>(qt + (c >> 3) * kHalfBytes + sw128_offset(r, c & 7)) = v;
+                *reinterpret_cast<uint4*>(qt + sw128_offset(r, c)) = v;
             }
             fence_proxy_async_smem();
             mbar_arrive(q_ready);
         }
-        auto wait_warp = [&](uint64_t* bar, uint32_t parity) -> bool {
-            return __all_sync(0xffffffffu, wait(bar, parity));
-        };
         const uint32_t lane_addr = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16) + x * 256;
-        const uint32_t s_addr = lane_addr, o_addr = lane_addr + 128;
+        const uint32_t s_addr = lane_addr + hf * 64;     // this half's S columns
+        const uint32_t o_addr = lane_addr + 128 + hf * 64;  // this half's O columns
+        float* xmine = xch + (x * 2 + hf) * kTileM + r;
+        const float* xother = xch + (x * 2 + (hf ^ 1)) * kTileM + r;
         float m_used = -INFINITY;
         float l = 0.f, l_b = 0.f;
         const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
-        // a warp none of whose rows sees a key (rows past the sequence, padding
-        // rows) writes zero probabilities and skips the softmax arithmetic
         const bool warp_live = __any_sync(0xffffffffu, limit > 0);
+        bool ok = true;
         for (int j = 0; j < g.nt; ++j) {
-            if (!wait_warp(&s_full[x], j & 1)) break;
+            bool ok_t = __all_sync(0xffffffffu, wait(&s_full[x], j & 1));
             tc_fence_after();
-            if (warp_live) {
-                const int nvis = limit - (g.kb + j * kTileN);
-                // pass 1: row maximum over the visible keys, from one 128-column read
-                float mx;
-                {
-                    uint32_t sv[kTileN];
-                    tmem_load128(s_addr, sv);
-                    if (nvis < kTileN) {
+            const int nvis = limit - (g.kb + j * kTileN) - hf * 64;  // visible columns of this half
+            float mpart = -INFINITY;
+            if (ok_t && warp_live) {
+                uint32_t sv[32];
 #pragma unroll
-                        for (int e = 0; e < kTileN; ++e)
-                            sv[e] = e < nvis ? sv[e] : __float_as_uint(-INFINITY);
+                for (int c = 0; c < 2; ++c) {
+                    tmem_load32(s_addr + c * 32, sv);
+                    if (nvis < (c + 1) * 32) {
+#pragma unroll
+                        for (int e = 0; e < 32; ++e)
+                            sv[e] = c * 32 + e < nvis ? sv[e] : __float_as_uint(-INFINITY);
                     }
-                    float m4[4];
+                    float a[4];
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        float a0 = __uint_as_float(sv[q]), a1 = __uint_as_float(sv[q + 4]);
+                    for (int q = 0; q < 4; ++q) a[q] = __uint_as_float(sv[q]);
 #pragma unroll
-                        for (int e = q + 8; e < kTileN; e += 8) {
-                            a0 = fmaxf(a0, __uint_as_float(sv[e]));
-                            a1 = fmaxf(a1, __uint_as_float(sv[e + 4]));
-                        }
-                        m4[q] = fmaxf(a0, a1);
+                    for (int e = 4; e < 32; e += 4) {
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) a[q] = fmaxf(a[q], __uint_as_float(sv[e + q]));
                     }
-                    mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+                    mpart = fmaxf(mpart, fmaxf(fmaxf(a[0], a[1]), fmaxf(a[2], a[3])));
                 }
-                mx *= p.scale_log2;
+            }
+            // exchange the two halves' maxima; also agree on whether every wait succeeded
+            *xmine = mpart;
+            if (!bar_and(bar_id, 8 * 32, ok_t)) {
+                ok = false;
+                break;
+            }
+            if (warp_live) {
+                const float mx = fmaxf(mpart, *xother) * p.scale_log2;
                 float alpha = 1.f;
                 if (mx > m_used + kLazyRescale) {
                     alpha = fast_exp2(m_used - mx);
                     m_used = mx;
                 }
-                // O *= alpha (O is stable: S of this tile was issued after the previous P.V)
+                // O *= alpha on this half's 64 columns
                 if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) {
+                    for (int c = 0; c < 2; ++c) {
                         uint32_t v[32];
                         tmem_load32(o_addr + c * 32, v);
 #pragma unroll
@@ -900,13 +910,14 @@ __global__ void __launch_bounds__(kThreads2, 1)
                         tmem_store32(o_addr + c * 32, v);
                     }
                 }
-                // probabilities written back as packed bf16 over the columns of S
                 const float nm = m_used == -INFINITY ? 0.f : -m_used;
                 const float2 nm2 = make_float2(nm, nm);
                 float2 rs2 = make_float2(0.f, 0.f), rsb2 = make_float2(0.f, 0.f);
-                // pass 2: 32 keys at a time (re-read: keeps the registers of a pass low)
+                // half 0: S columns [0,32),[32,64) -> P columns [0,16),[16,32);
+                // half 1: S columns [96,128),[64,96) -> P columns [112,128),[96,112)
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
+                for (int cc = 0; cc < 2; ++cc) {
+                    const int c = hf ? 1 - cc : cc;
                     uint32_t v[32];
                     tmem_load32(s_addr + c * 32, v);
                     if (nvis < (c + 1) * 32) {
@@ -924,7 +935,7 @@ __global__ void __launch_bounds__(kThreads2, 1)
                         rs2 = __fadd2_rn(rs2, pp);
                         rsb2 = __fadd2_rn(rsb2, make_float2(bf16lo(pk[e / 2]), bf16hi(pk[e / 2])));
                     }
-                    tmem_store16(s_addr + c * 16, pk);
+                    tmem_store16(lane_addr + hf * 96 + c * 16, pk);
                 }
                 tmem_store_wait();
                 l = l * alpha + (rs2.x + rs2.y);
@@ -934,47 +945,62 @@ __global__ void __launch_bounds__(kThreads2, 1)
 #pragma unroll
                 for (int e = 0; e < 16; ++e) zero[e] = 0u;
 #pragma unroll
-                for (int c = 0; c < 4; ++c) tmem_store16(s_addr + c * 16, zero);
+                for (int c = 0; c < 2; ++c) tmem_store16(lane_addr + hf * 96 + c * 16, zero);
                 tmem_store_wait();
             }
-            // keys past the sequence's length inside its last page: zero their V
-            // rows so that 0 * whatever the pool holds there cannot give NaN
+            // keys past the sequence's length inside its last page: zero their V rows
             const int key0 = g.kb + j * kTileN;
             if (x == 0 && key0 + kTileN > g.kv_len && g.kv_len > key0) {
-                // tile A's warpgroup does it; tile B's P.V is issued after tile A's
                 const int vs = j % kVStages;
-                if (!wait_warp(&v_full[vs], (j / kVStages) & 1)) break;
-                const int first = g.kv_len - key0;
-                const int lastr = min(kTileN, (first + 31) / 32 * 32);
-                uint8_t* vt = smem + kV2Off + vs * kTileBytes;
-                for (int idx = r; idx < (lastr - first) * 16; idx += kTileM) {
-                    const int row = first + idx / 16, cc = idx % 16;
-                    *reinterpret_cast<uint4*>(vt + (cc >> 3) * kHalfBytes + sw128_offset(row, cc & 7)) =
-                        make_uint4(0u, 0u, 0u, 0u);
+                ok_t = __all_sync(0xffffffffu, wait(&v_full[vs], (j / kVStages) & 1));
+                if (ok_t) {
+                    const int first = g.kv_len - key0;
+                    const int lastr = min(kTileN, (first + 31) / 32 * 32);
+                    uint8_t* vt = smem + kV2Off + vs * kTileBytes;
+                    for (int idx = hf * kTileM + r; idx < (lastr - first) * 16; idx += 2 * kTileM) {
+                        const int row = first + idx / 16, c16 = idx % 16;
+                        *reinterpret_cast<uint4*>(vt + (c16 >> 3) * kHalfBytes + sw128_offset(row, c16 & 7)) =
+                            make_uint4(0u, 0u, 0u, 0u);
+                    }
+                    fence_proxy_async_smem();
                 }
-                fence_proxy_async_smem();
             }
             tc_fence_before();
             mbar_arrive(&p_full[x]);
         }
-        // ---- epilogue: O / l, 32 columns at a time
-        const bool ok = wait_warp(&o_full[x], 0);
+        // ---- epilogue: the two halves' sums, then O / l on this half's columns
+        const bool ok_o = __all_sync(0xffffffffu, ok && wait(&o_full[x], 0));
         tc_fence_after();
-        const bool any = l > 0.f && l_b > 0.f;
-        const float inv_l = any ? 1.0f / l_b : 0.f;
+        // every key-loop exchange has been read: o_full follows both halves' last P
+        float* xl = xch + x * 2 * kTileM + r;  // [tile][0: l, 1: l_b][row]
+        bar_sync_n(bar_id, 8 * 32);
+        if (hf == 1) {
+            xl[0] = l;
+            xl[kTileM] = l_b;
+        }
+        bar_sync_n(bar_id, 8 * 32);
+        float inv_l = 0.f;
+        if (hf == 0) {
+            const float lt = l + xl[0], lbt = l_b + xl[kTileM];
+            const bool any = lt > 0.f && lbt > 0.f;
+            inv_l = any ? 1.0f / lbt : 0.f;
+            if (ok_o && row_exists) store_row_lse(p, g, i, h, any ? (m_used + __log2f(lt)) * kLn2 : -INFINITY);
+            xl[0] = inv_l;
+        }
+        bar_sync_n(bar_id, 8 * 32);
+        if (hf == 1) inv_l = xl[0];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
+        for (int c = 0; c < 2; ++c) {
             uint32_t v[32];
             tmem_load32(o_addr + c * 32, v);
-            if (ok && row_exists) store_row_chunk(p, g, i, h, c, v, inv_l);
+            if (ok_o && row_exists) store_row_chunk(p, g, i, h, hf * 2 + c, v, inv_l);
         }
-        if (ok && row_exists) store_row_lse(p, g, i, h, any ? (m_used + __log2f(l)) * kLn2 : -INFINITY);
     }
 
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == 9) tmem_dealloc(tmem, kTmemCols);
+    if (warp == 17) tmem_dealloc(tmem, kTmemCols);
 }
 
 template <int G>
