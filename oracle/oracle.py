@@ -375,3 +375,134 @@ def copy_kv_slots(k_pools, v_pools, src_slots, dst_slots):
         k_out[:, d_ // P, d_ % P] = kr
         v_out[:, d_ // P, d_ % P] = vr
     return k_out, v_out
+
+
+# ----------------------------------------------------------------------------
+# exact-window layout of the frame-causal blocks (per-block rows with private
+# pages), computed at commit
+# ----------------------------------------------------------------------------
+
+def causal_blocks(num_staged: int, block_size: int):
+    """Causal blocks of a forward's staged tokens: consecutive runs of
+    ``block_size`` tokens, the last one shorter when ``num_staged`` is not a
+    multiple.  Returns ``[(first, count), ...]`` in staged-token indices.
+
+    [VG] Description, Attention and Cache ("Frame-causal attention needs no
+    mask" bullet: the staged tokens are cut into causal blocks that run as one
+    ragged batch; block sizes are declared with the geometry).
+    READING: one block size per forward, the last block partial.
+    """
+    out = []
+    t = 0
+    while t < num_staged:
+        n = min(block_size, num_staged - t)
+        out.append((t, n))
+        t += n
+    return out
+
+
+def exact_window_keys(pin: int, committed: int, window: int, num_staged: int, block_size: int,
+                      k: int):
+    """Logical key positions causal block ``k`` attends to.
+
+    The cache is one long sequence [fixed region | committed history | staged
+    tokens] ([VG] Description, Cache): the first ``pin`` tokens are the fixed
+    region, ``committed`` tokens of history follow, then this forward's
+    ``num_staged`` staged tokens.  Block ``k`` sees the whole fixed region,
+    the ``window`` tokens just before its own first token (history and the
+    earlier blocks of this forward), and its own tokens.
+    READING: the window slides with the block (each block's window starts
+    ``window`` tokens before the block; the pages count a per-block
+    window-start page among the partly visible pages) and never reaches into
+    the fixed region.
+    """
+    first, n = causal_blocks(num_staged, block_size)[k]
+    s = pin + committed + first
+    ws = max(pin, s - window)
+    return list(range(pin)) + list(range(ws, s + n))
+
+
+def causal_layout(table, pin: int, committed: int, window: int, num_staged: int,
+                  block_size: int, private_pages, page_size: int = 32):
+    """Per-block rows that read exactly each causal block's window, in one
+    ragged batch without a mask and without a duplicated key.
+
+    [VG] Description, Cache ("Exact window" bullet and the commit bullet:
+    a layout kernel reads the table and rewrites every per-block tensor at
+    commit; one pool-to-pool copy fills the private pages), and the review
+    notes on the private pages (committed_private: copies of committed tokens
+    made at commit; current_private: copies of earlier blocks' tokens of the
+    same forward, written every forward).
+
+    ``table[lp]`` is the physical page of logical page ``lp`` of the long
+    sequence (slot of logical position p = table[p // P] * P + p % P).
+    ``private_pages[k]`` lists the physical pages reserved for block ``k``'s
+    private region.
+
+    Row of block k, in key order:
+      1. every logical page that is fully visible to the block and ends at or
+         before the block's first token, by reference, in logical order;
+      2. its private pages, holding every other visible token in logical order:
+         the visible tokens of partly visible pages (fixed-region tail,
+         window-start page, the earlier tokens of the block's start page) and
+         then the block's own tokens, which therefore stay the row's last keys.
+    READING: the pages name the three kinds of partly visible page but not the
+    order inside the private region; logical order is taken.
+
+    The i-th private token of block k lives at slot
+    ``private_pages[k][i // P] * P + i % P`` and is filled by one of:
+      * committed (position < pin + committed): a slot-to-slot copy at commit,
+        ``(src slot, dst slot)``;
+      * current (an earlier block's staged token): a write from the staged
+        source row every forward, ``(staged index, dst slot)``;
+      * own: the staged token's second destination.
+    Every staged token's first destination is its own logical slot (it becomes
+    history at commit).
+
+    Returns a dict: ``rows`` (list of page lists), ``kv_lens``, ``q_indptr``,
+    ``staged_slots``, ``staged_slots2``, ``committed`` (list of (src, dst)),
+    ``current`` (list of (staged index, dst)).
+    """
+    P = page_size
+    base = pin + committed
+
+    def slot(p):
+        return int(table[p // P]) * P + p % P
+
+    blocks = causal_blocks(num_staged, block_size)
+    rows, kv_lens, q_indptr = [], [], [0]
+    staged_slots = [slot(base + t) for t in range(num_staged)]
+    staged_slots2 = [-1] * num_staged
+    committed_copies, current_copies = [], []
+    for k, (first, n) in enumerate(blocks):
+        s = base + first
+        vis = exact_window_keys(pin, committed, window, num_staged, block_size, k)
+        vis_set = set(vis)
+        end = s + n
+        direct = []
+        for lp in range((end + P - 1) // P):
+            a = lp * P
+            if a + P <= s and all(a + o in vis_set for o in range(P)):
+                direct.append(lp)
+        covered = set()
+        for lp in direct:
+            covered.update(range(lp * P, lp * P + P))
+        private_tokens = [p for p in vis if p not in covered]
+        private_tokens.sort()
+        need = (len(private_tokens) + P - 1) // P
+        if need > len(private_pages[k]):
+            raise ValueError(f"block {k} needs {need} private pages, has {len(private_pages[k])}")
+        row = [int(table[lp]) for lp in direct] + [int(private_pages[k][j]) for j in range(need)]
+        rows.append(row)
+        kv_lens.append(len(direct) * P + len(private_tokens))
+        q_indptr.append(q_indptr[-1] + n)
+        for i, p in enumerate(private_tokens):
+            dst = int(private_pages[k][i // P]) * P + i % P
+            if p < base:
+                committed_copies.append((slot(p), dst))
+            elif p < s:
+                current_copies.append((p - base, dst))
+            else:
+                staged_slots2[p - base] = dst
+    return dict(rows=rows, kv_lens=kv_lens, q_indptr=q_indptr, staged_slots=staged_slots,
+                staged_slots2=staged_slots2, committed=committed_copies, current=current_copies)
