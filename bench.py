@@ -50,7 +50,8 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="gqa_decode",
                     choices=["gqa_decode", "chunked_prefill", "block_causal_video",
-                             "shared_prefix", "tiny_decode", "multi_token_decode"])
+                             "shared_prefix", "tiny_decode", "multi_token_decode",
+                             "exact_window_video", "exact_window_denoise"])
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-sample-seqs", type=int, default=64)
@@ -367,10 +368,88 @@ class StepPlan:
         self.__dict__.update(kw)
 
 
+def build_exact_window_plan(name, rank, dev, stream):
+    """A forward over exact windows: the commit (device layout + the committed
+    private copies) runs once at set-up and is timed as an auxiliary call; a
+    step is the forward of one layer: the staged K/V to their two slots, the
+    earlier blocks' tokens to the later blocks' private pages, and one unmasked
+    attention over all causal blocks."""
+    import torch
+    from paged_kv_cache_189_gb300 import pkv, workloads as wl
+
+    case = wl.exact_window_video(seed=6 + rank, blocks_per_chunk=4 if name == "exact_window_video" else 1)
+    Hq, Hkv, D = case.num_q_heads, case.num_kv_heads, case.head_dim
+    t = dict(k_pool=case.k_pool.to(dev), v_pool=case.v_pool.to(dev), q=case.q.to(dev),
+             new_k=case.new_k.to(dev), new_v=case.new_v.to(dev), table=case.table.to(dev),
+             priv=case.private_pages.to(dev),
+             committed=torch.tensor([case.committed], dtype=torch.int64, device=dev))
+    bufs = pkv.causal_layout_buffers(case.staged, case.block, case.row_stride, dev)
+
+    def commit():
+        pkv.causal_layout(t["table"], t["committed"], case.pin, case.window, case.staged, case.block,
+                          t["priv"], bufs, stream=stream)
+        pkv.copy_kv_slots(t["k_pool"], t["v_pool"], bufs["committed_src"], bufs["committed_dst"],
+                          stream=stream)
+
+    with torch.cuda.stream(stream):
+        commit()
+    torch.cuda.synchronize()
+
+    def scatters():
+        pkv.kv_scatter_slots(t["new_k"], t["new_v"], bufs["staged_slots"], t["k_pool"], t["v_pool"],
+                             slots2=bufs["staged_slots2"], stream=stream)
+        pkv.kv_scatter_slots(t["new_k"], t["new_v"], bufs["current_dst"], t["k_pool"], t["v_pool"],
+                             src_idx=bufs["current_src_idx"], stream=stream)
+
+    # key counts per block, closed form of the window (also what the device wrote)
+    base = case.pin + case.committed
+    kv_lens, ns = [], []
+    for k in range(case.num_blocks):
+        first = k * case.block
+        n = min(case.block, case.staged - first)
+        kv_lens.append(case.pin + min(case.window, base + first - case.pin) + n)
+        ns.append(n)
+    assert kv_lens == bufs["kv_lens"].tolist()
+    pairs = sum(n * kl for n, kl in zip(ns, kv_lens))
+    flops = 4.0 * D * Hq * pairs
+    out = torch.empty(case.staged, Hq, D, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty(case.staged, Hq, dtype=torch.float32, device=dev)
+    ws_b = pkv.paged_attention_workspace_size(case.num_blocks, case.block, Hq, Hkv, D, case.max_kv_len)
+    ws = torch.empty(max(ws_b, 256), dtype=torch.uint8, device=dev)
+
+    def attention():
+        pkv.paged_attention(t["q"], t["k_pool"], t["v_pool"], bufs["rows"], bufs["kv_lens"],
+                            bufs["q_indptr"], out, lse=lse, max_q_rows=case.block,
+                            max_kv_len=case.max_kv_len, mask="none", workspace=ws, stream=stream)
+
+    tok = Hkv * D * 2 * 2
+    n_cur = int((bufs["current_dst"] >= 0).sum())
+    n_com = int((bufs["committed_dst"] >= 0).sum())
+    aux = {"scatter": (scatters, case.staged * tok * 3 + n_cur * tok * 2, "GB/s"),
+           "commit": (commit, n_com * tok * 2, "GB/s")}
+    peak_tc, tc_kind = measured_tensor_peak()
+    cfg = {"workload": name, "pin_tokens": case.pin, "history_tokens": case.committed,
+           "window_tokens": case.window, "staged_tokens": case.staged, "causal_block": case.block,
+           "blocks": case.num_blocks, "kv_len_per_block": kv_lens, "q_heads": Hq, "kv_heads": Hkv,
+           "head_dim": D, "page": 32, "mask": "none (exact-window rows)",
+           "visible_pairs_per_head": pairs, "flops_per_step": flops,
+           "l2": "K/V read per step larger than L2", "committed_private_copies": n_com,
+           "current_private_copies": n_cur}
+    return StepPlan(case=case, cfg=cfg, metric="prefill TFLOP/s", unit="TFLOP/s", work=flops, scale=1e12,
+                    queries=case.staged, pre=[scatters], dominant=attention, post=[], aux=aux,
+                    dom_label="paged_attention over the exact-window rows: tcgen05 tile kernel",
+                    dom_work=flops / 1e12, bound="tensor", peak=peak_tc, peak_unit="TFLOP/s",
+                    peak_src=f"{tc_kind} bf16_tflops_sustained",
+                    h2d=([case.q, case.new_k, case.new_v], [t["q"], t["new_k"], t["new_v"]]),
+                    d2h=[out, lse], launches=3, traffic_sources=ATTN_TC_SOURCES)
+
+
 def build_plan(name, rank, dev, stream):
     import torch
     from paged_kv_cache_189_gb300 import pkv, workloads as wl
 
+    if name in ("exact_window_video", "exact_window_denoise"):
+        return build_exact_window_plan(name, rank, dev, stream)
     case = {"gqa_decode": wl.gqa_decode, "chunked_prefill": wl.chunked_prefill,
             "block_causal_video": wl.block_causal_video, "shared_prefix": wl.shared_prefix,
             "tiny_decode": wl.tiny_decode, "multi_token_decode": wl.multi_token_decode}[name](

@@ -229,6 +229,77 @@ pkv_status copy_kv_slots(void* k_pool, void* v_pool, int num_layers, int64_t lay
                          int32_t* err, void* stream);
 
 /*
+ * causal_layout -- the per-block rows of a forward over exact windows,
+ * computed on the device (at commit: nothing is uploaded from the host).
+ *
+ * [VG] Description, Cache ("Exact window" bullet and the commit bullet: a
+ * layout kernel reads the table and rewrites every per-block tensor in place;
+ * a pool-to-pool copy fills the private pages) and the review notes on the
+ * private pages (committed_private: copies of committed tokens, made at
+ * commit; current_private: copies of earlier blocks' tokens of the same
+ * forward, written every forward).
+ *
+ * The cache is one long sequence [fixed region | committed history | staged
+ * tokens]: positions [0, pin_tokens) are the fixed region, *committed tokens
+ * of history follow (a device int64, advanced by the caller at commit), then
+ * the forward's num_staged staged tokens, cut into causal blocks of
+ * block_size (the last one shorter).  Block k attends to the fixed region,
+ * the window_tokens tokens just before its first token (never reaching into
+ * the fixed region) and its own tokens; the window slides with the block.
+ * table[lp] is the physical page of logical page lp (slot of logical
+ * position p = table[p / 32] * 32 + p % 32); private_pages[k * private_stride
+ * + i] are block k's reserved pages.
+ *
+ * Row k (rows[k * row_stride ...], -1 after its last page): every logical
+ * page fully visible to the block that ends at or before the block's first
+ * token, by reference and in logical order, then the block's private pages,
+ * which hold every other visible token in logical order (the visible tokens
+ * of the fixed-region tail, of the window-start page and of the block's
+ * start page, then the block's own tokens, which are the row's last keys).
+ * kv_lens[k] = the row's keys; q_indptr[k] = the block's first staged token,
+ * q_indptr[num_blocks] = num_staged.  Attention over the rows with
+ * PKV_MASK_NONE, q_indptr as the query ranges and all rows real then reads
+ * exactly each block's window, each key once.
+ *
+ * Writes that fill the private region:
+ *  - staged_slots[t] = the slot of staged token t's own logical position,
+ *    staged_slots2[t] = its slot in its block's private region: the two
+ *    destinations of kv_scatter_slots for the forward's K/V;
+ *  - committed_src/dst[k * PKV_LAYOUT_COMMITTED_PER_BLOCK + c]: slot-to-slot
+ *    copies of committed tokens into block k's private region, for
+ *    copy_kv_slots at commit (all layers);
+ *  - current_src_idx/dst[k * PKV_LAYOUT_CURRENT_PER_BLOCK + c]: earlier
+ *    blocks' staged tokens (index into the forward's staged K/V) into block
+ *    k's private region, for kv_scatter_slots with src_idx every forward.
+ * Unused list entries are -1 (both fields), which both consumers skip.
+ *
+ *  page_size          32
+ *  capacities         committed_capacity >= num_blocks *
+ *                     PKV_LAYOUT_COMMITTED_PER_BLOCK, current_capacity >=
+ *                     num_blocks * PKV_LAYOUT_CURRENT_PER_BLOCK (checked)
+ *  private_stride     block k needs ceil((private tokens) / 32) pages, at most
+ *                     ceil((3 * 31 + block_size) / 32): besides its own tokens a
+ *                     block copies the visible part of at most three partly
+ *                     visible pages
+ *  err                nullable device int32: a row longer than row_stride or a
+ *                     private region larger than private_stride pages ORs
+ *                     PKV_ERRBIT_LEN (the row is truncated, the overflowing
+ *                     private tokens skipped); a logical page at or past
+ *                     num_logical_pages ORs PKV_ERRBIT_PAGE (its entries -1).
+ */
+#define PKV_LAYOUT_COMMITTED_PER_BLOCK 93 /* 3 partly visible pages x 31 */
+#define PKV_LAYOUT_CURRENT_PER_BLOCK 62  /* 2 partly visible pages x 31 */
+
+pkv_status causal_layout(const int32_t* table, int64_t num_logical_pages, const int64_t* committed,
+                         int64_t pin_tokens, int64_t window_tokens, int num_staged, int block_size,
+                         const int32_t* private_pages, int private_stride, int page_size,
+                         int32_t* rows, int64_t row_stride, int32_t* kv_lens, int32_t* q_indptr,
+                         int64_t* staged_slots, int64_t* staged_slots2, int64_t* committed_src,
+                         int64_t* committed_dst, int64_t committed_capacity,
+                         int64_t* current_src_idx, int64_t* current_dst, int64_t current_capacity,
+                         int32_t* err, void* stream);
+
+/*
  * paged_attention_no_alloc -- paged_attention for callers that cannot allocate.
  *
  * The pages describe no such entry point; it exists for callers that have no

@@ -506,3 +506,44 @@ def causal_layout(table, pin: int, committed: int, window: int, num_staged: int,
                 staged_slots2[p - base] = dst
     return dict(rows=rows, kv_lens=kv_lens, q_indptr=q_indptr, staged_slots=staged_slots,
                 staged_slots2=staged_slots2, committed=committed_copies, current=current_copies)
+
+
+def exact_window_attention(q, k_seq, v_seq, pin: int, committed: int, window: int,
+                           num_staged: int, block_size: int, scale=None, rows=None):
+    """Attention of each staged query token over exactly its causal block's
+    window, read straight from the logical sequence (no pages, no layout).
+
+    [VG] Description, Cache ("Exact window" bullet: the fp32 exact-window
+    reference both backends are compared with) and the frame-causal bullet.
+    ``q``: ``[num_staged, Hq, D]`` bf16 bits; ``k_seq``/``v_seq``:
+    ``[pin + committed + num_staged, Hkv, D]`` bf16 bits of the long sequence
+    by logical position.  Visible set of block k: ``exact_window_keys``.
+    Returns ``(O [num_staged, Hq, D] f64, LSE [num_staged, Hq] f64)``;
+    ``rows`` restricts the computation to those staged indices (others 0 / -inf).
+    """
+    qf = bf16_to_f64(np.asarray(q))
+    Kf = bf16_to_f64(np.asarray(k_seq))
+    Vf = bf16_to_f64(np.asarray(v_seq))
+    T, Hq, D = qf.shape
+    Hkv = Kf.shape[1]
+    G = Hq // Hkv
+    sc = 1.0 / np.sqrt(D) if scale is None else scale
+    O = np.zeros((T, Hq, D))
+    L = np.full((T, Hq), -np.inf)
+    want = set(range(T)) if rows is None else set(int(r) for r in rows)
+    for k, (first, n) in enumerate(causal_blocks(num_staged, block_size)):
+        ts = [t for t in range(first, first + n) if t in want]
+        if not ts:
+            continue
+        vis = np.array(exact_window_keys(pin, committed, window, num_staged, block_size, k))
+        for kvh in range(Hkv):
+            Kb, Vb = Kf[vis, kvh], Vf[vis, kvh]
+            for g in range(G):
+                h = kvh * G + g
+                S = sc * (qf[ts, h] @ Kb.T)           # [rows, keys]
+                m = S.max(axis=1, keepdims=True)
+                W_ = np.exp(S - m)
+                l = W_.sum(axis=1)
+                O[ts, h] = (W_ @ Vb) / l[:, None]
+                L[ts, h] = m[:, 0] + np.log(l)
+    return O, L

@@ -109,16 +109,34 @@ Plan plan_attention(int batch, int max_q_rows, int Hq, int Hkv, int D, int max_k
     Plan pl;
     const int G = Hkv > 0 ? Hq / Hkv : 0;
     if (!(flags & PKV_FLAG_SIMT_ONLY) && max_q_rows > 1 && pkv::attn_tc_supported(D, G)) {
-        // tensor-core tiles; split the keys only when the tiles cannot half-fill the GPU
+        // tensor-core tiles, one CTA per tile (two tiles when a sequence has
+        // more rows than one holds).  With at most two waves of CTAs the last
+        // wave can leave most SMs idle (every CTA of an unmasked or long
+        // causal row runs about as long as the others), so the keys are split
+        // to the count that minimises waves / splits, plus ~2 % of a CTA per
+        // split for the partial states and their merge, when that saves at
+        // least 10 %; splits keep >= 512 keys.  More CTAs than that are
+        // balanced by the block scheduler.
         pl.kernel = Kernel::kTile;
-        const int64_t tiles = static_cast<int64_t>((max_q_rows + pkv::attn_tc_rows_per_tile(G) - 1) /
-                                                   pkv::attn_tc_rows_per_tile(G)) * Hkv * batch;
+        const int tq = pkv::attn_tc_rows_per_tile(G);
+        const int rows_per_cta = max_q_rows > tq ? 2 * tq : tq;
+        const int64_t ctas = static_cast<int64_t>((max_q_rows + rows_per_cta - 1) / rows_per_cta) * Hkv * batch;
         int s = 1;
         if (num_splits > 0) {
             s = num_splits;
-        } else if (tiles * 2 < kPlanSMs) {
-            s = static_cast<int>(std::min<int64_t>(8, (kPlanSMs + tiles - 1) / tiles));
-            s = std::max(1, std::min(s, (max_kv_len + 511) / 512));
+        } else if (ctas <= 2 * kPlanSMs) {
+            const int s_max = std::max(1, std::min(8, max_kv_len / 512));
+            const double unsplit = static_cast<double>((ctas + kPlanSMs - 1) / kPlanSMs);
+            double best = unsplit;
+            for (int c = 2; c <= s_max; ++c) {
+                const double waves = static_cast<double>((ctas * c + kPlanSMs - 1) / kPlanSMs);
+                const double cost = waves / c + 0.02 * c;
+                if (cost < best - 1e-9) {
+                    best = cost;
+                    s = c;
+                }
+            }
+            if (best > 0.9 * unsplit) s = 1;
         }
         const int per = (max_kv_len + s - 1) / std::max(s, 1);
         pl.split_keys = std::max(kTileKeys, (per + kTileKeys - 1) / kTileKeys * kTileKeys);
@@ -432,6 +450,42 @@ pkv_status copy_kv_slots(void* k_pool, void* v_pool, int num_layers, int64_t lay
                          num_kv_heads, head_dim, esz, src_slots, dst_slots, num_copies,
                          (flags & PKV_FLAG_CHECKED) != 0, err};
     return from_cuda(pkv::launch_copy_slots(a, static_cast<cudaStream_t>(stream)), "copy launch");
+}
+
+pkv_status causal_layout(const int32_t* table, int64_t num_logical_pages, const int64_t* committed,
+                         int64_t pin_tokens, int64_t window_tokens, int num_staged, int block_size,
+                         const int32_t* private_pages, int private_stride, int page_size,
+                         int32_t* rows, int64_t row_stride, int32_t* kv_lens, int32_t* q_indptr,
+                         int64_t* staged_slots, int64_t* staged_slots2, int64_t* committed_src,
+                         int64_t* committed_dst, int64_t committed_capacity,
+                         int64_t* current_src_idx, int64_t* current_dst, int64_t current_capacity,
+                         int32_t* err, void* stream) {
+    if (page_size != 32) return fail(PKV_ERR_UNSUPPORTED, "layout: page_size %d (32 only)", page_size);
+    if (num_staged < 0 || block_size <= 0 || pin_tokens < 0 || window_tokens < 0 ||
+        num_logical_pages < 0 || private_stride < 0 || row_stride < 0)
+        return fail(PKV_ERR_INVALID_ARG, "layout: negative size or block_size < 1");
+    if (num_staged == 0) return ok();
+    const int64_t num_blocks = (static_cast<int64_t>(num_staged) + block_size - 1) / block_size;
+    if (!table || !committed || !private_pages || !rows || !kv_lens || !q_indptr || !staged_slots ||
+        !staged_slots2 || !committed_src || !committed_dst || !current_src_idx || !current_dst)
+        return fail(PKV_ERR_INVALID_ARG, "layout: null pointer");
+    if (row_stride < 1 || private_stride < 1)
+        return fail(PKV_ERR_INVALID_ARG, "layout: row_stride and private_stride must be >= 1");
+    if (committed_capacity < num_blocks * PKV_LAYOUT_COMMITTED_PER_BLOCK ||
+        current_capacity < num_blocks * PKV_LAYOUT_CURRENT_PER_BLOCK)
+        return fail(PKV_ERR_INVALID_ARG,
+                    "layout: copy lists need %lld committed and %lld current entries for %lld blocks",
+                    static_cast<long long>(num_blocks * PKV_LAYOUT_COMMITTED_PER_BLOCK),
+                    static_cast<long long>(num_blocks * PKV_LAYOUT_CURRENT_PER_BLOCK),
+                    static_cast<long long>(num_blocks));
+    if (pin_tokens + window_tokens + block_size > 0x7fffffffLL)
+        return fail(PKV_ERR_UNSUPPORTED, "layout: a row of more than 2^31 keys");
+    if (num_blocks > 0x7fffffffLL) return fail(PKV_ERR_UNSUPPORTED, "layout: too many blocks");
+    pkv::LayoutArgs a{table, num_logical_pages, committed, pin_tokens, window_tokens, num_staged,
+                      block_size, static_cast<int>(num_blocks), private_pages, private_stride, rows,
+                      row_stride, kv_lens, q_indptr, staged_slots, staged_slots2, committed_src,
+                      committed_dst, current_src_idx, current_dst, err};
+    return from_cuda(pkv::launch_causal_layout(a, static_cast<cudaStream_t>(stream)), "layout launch");
 }
 
 pkv_status rotate_rows(void* x, int64_t rows, int64_t cols, int64_t row_stride, int elem_size_b,

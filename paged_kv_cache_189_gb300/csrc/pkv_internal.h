@@ -57,6 +57,28 @@ struct RopeArgs {
 cudaError_t launch_rope_write(const RopeArgs& a, cudaStream_t s);
 
 // ---------------------------- pool-to-pool slot copy --------------------------
+struct LayoutArgs {
+    const int32_t* table;
+    int64_t num_logical_pages;
+    const int64_t* committed;  // device scalar
+    int64_t pin, window;
+    int num_staged, block_size, num_blocks;
+    const int32_t* private_pages;
+    int private_stride;
+    int32_t* rows;
+    int64_t row_stride;
+    int32_t* kv_lens;
+    int32_t* q_indptr;
+    int64_t* staged_slots;
+    int64_t* staged_slots2;
+    int64_t* com_src;
+    int64_t* com_dst;
+    int64_t* cur_src;
+    int64_t* cur_dst;
+    int32_t* err;
+};
+cudaError_t launch_causal_layout(const LayoutArgs& a, cudaStream_t s);
+
 struct CopySlotsArgs {
     void* k_pool;
     void* v_pool;

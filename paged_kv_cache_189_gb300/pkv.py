@@ -26,7 +26,8 @@ PKV_ERRBIT_SLOT, PKV_ERRBIT_SRC, PKV_ERRBIT_PAGE, PKV_ERRBIT_LEN, PKV_ERRBIT_TIM
 # every symbol include/pkv.h declares
 EXPORTED = ("pkv_status_string", "pkv_last_error", "kv_scatter_slots",
             "paged_attention_workspace_size", "paged_attention", "merge_attn_states",
-            "rotate_rows", "paged_attention_no_alloc", "rope_write_kv_paged", "copy_kv_slots")
+            "rotate_rows", "paged_attention_no_alloc", "rope_write_kv_paged", "copy_kv_slots",
+            "causal_layout")
 NO_ALLOC_SCRATCH_BYTES = 32 << 20
 
 _vp, _i64, _i32, _u32, _f32, _sz = (ctypes.c_void_p, ctypes.c_int64, ctypes.c_int,
@@ -51,6 +52,8 @@ _SIGNATURES = {
                                    _vp]),
     "copy_kv_slots": (_i32, [_vp, _vp, _i32, _i64, _i64, _i32, _i64, _i32, _i32, _i32, _vp, _vp,
                              _i64, _u32, _vp, _vp]),
+    "causal_layout": (_i32, [_vp, _i64, _vp, _i64, _i64, _i32, _i32, _vp, _i32, _i32, _vp, _i64,
+                             _vp, _vp, _vp, _vp, _vp, _vp, _i64, _vp, _vp, _i64, _vp, _vp]),
 }
 
 _lib = None
@@ -240,3 +243,42 @@ def copy_kv_slots(k_pools, v_pools, src_slots, dst_slots, checked=False, err=Non
                              src_slots.numel(), PKV_FLAG_CHECKED if checked else 0, _ptr(err),
                              _stream(stream))
     _check("copy_kv_slots", st)
+
+
+LAYOUT_COMMITTED_PER_BLOCK = 93
+LAYOUT_CURRENT_PER_BLOCK = 62
+
+
+def causal_layout_buffers(num_staged, block_size, row_stride, device="cuda"):
+    """Output tensors of :func:`causal_layout` for a forward of ``num_staged``
+    tokens in blocks of ``block_size`` (allocated here, by the caller's side)."""
+    import torch
+    nb = (num_staged + block_size - 1) // block_size
+    i32 = dict(dtype=torch.int32, device=device)
+    i64 = dict(dtype=torch.int64, device=device)
+    return dict(rows=torch.full((nb, row_stride), -1, **i32), kv_lens=torch.zeros(nb, **i32),
+                q_indptr=torch.zeros(nb + 1, **i32), staged_slots=torch.full((num_staged,), -1, **i64),
+                staged_slots2=torch.full((num_staged,), -1, **i64),
+                committed_src=torch.full((nb * LAYOUT_COMMITTED_PER_BLOCK,), -1, **i64),
+                committed_dst=torch.full((nb * LAYOUT_COMMITTED_PER_BLOCK,), -1, **i64),
+                current_src_idx=torch.full((nb * LAYOUT_CURRENT_PER_BLOCK,), -1, **i64),
+                current_dst=torch.full((nb * LAYOUT_CURRENT_PER_BLOCK,), -1, **i64))
+
+
+def causal_layout(table, committed, pin_tokens, window_tokens, num_staged, block_size,
+                  private_pages, out, err=None, stream=None):
+    """Per-block rows over exact windows (see ``include/pkv.h``).  ``table``:
+    int32 logical page table; ``committed``: int64 device scalar (history
+    tokens); ``private_pages``: int32 ``[blocks, stride]``; ``out``: the dict of
+    :func:`causal_layout_buffers`, rewritten in place."""
+    assert private_pages.dim() == 2 and private_pages.is_contiguous()
+    rows = out["rows"]
+    st = lib().causal_layout(_ptr(table), table.numel(), _ptr(committed), pin_tokens, window_tokens,
+                             num_staged, block_size, _ptr(private_pages), private_pages.shape[1], 32,
+                             _ptr(rows), rows.shape[1], _ptr(out["kv_lens"]), _ptr(out["q_indptr"]),
+                             _ptr(out["staged_slots"]), _ptr(out["staged_slots2"]),
+                             _ptr(out["committed_src"]), _ptr(out["committed_dst"]),
+                             out["committed_src"].numel(), _ptr(out["current_src_idx"]),
+                             _ptr(out["current_dst"]), out["current_src_idx"].numel(), _ptr(err),
+                             _stream(stream))
+    _check("causal_layout", st)

@@ -314,6 +314,79 @@ def random_case(seed: int, batch: int, Hq: int, Hkv: int, D: int, kv_range=(1, 3
                            mask=mask, causal_block=causal_block, q_scale=q_scale)
 
 
+@dataclass
+class ExactWindowCase:
+    """One forward of the exact-window cache: a long sequence [fixed region |
+    committed history | staged tokens] in a paged pool, the forward's staged
+    K/V and queries, and each causal block's reserved private pages."""
+    name: str
+    pin: int                      # fixed-region tokens
+    committed: int                # committed history tokens
+    window: int                   # window tokens before each block
+    staged: int                   # the forward's tokens
+    block: int                    # causal block size
+    num_q_heads: int
+    num_kv_heads: int
+    head_dim: int
+    k_pool: torch.Tensor          # [pages, P, Hkv, D] bf16; committed tokens at their slots
+    v_pool: torch.Tensor
+    table: torch.Tensor           # [logical pages] int32, physical page of each logical page
+    private_pages: torch.Tensor   # [blocks, cap] int32
+    new_k: torch.Tensor           # [staged, Hkv, D] bf16
+    new_v: torch.Tensor
+    q: torch.Tensor               # [staged, Hq, D] bf16
+
+    @property
+    def num_blocks(self) -> int:
+        return -(-self.staged // self.block)
+
+    @property
+    def max_kv_len(self) -> int:
+        return self.pin + self.window + self.block
+
+    @property
+    def row_stride(self) -> int:
+        return -(-self.max_kv_len // PAGE_SIZE) + 4
+
+
+def exact_window(seed: int, pin: int, committed: int, window: int, staged: int, block: int,
+                 Hq: int = 32, Hkv: int = 8, D: int = 128, name: str = "exact_window") -> ExactWindowCase:
+    """Pages of the long sequence and the blocks' private pages are drawn from a
+    seeded permutation of the pool; every pool value (private pages included,
+    so a missing copy shows) is N(0, 1) bf16."""
+    P = PAGE_SIZE
+    rng = np.random.default_rng(seed)
+    gen = torch.Generator().manual_seed(seed)
+    total = pin + committed + staged
+    n_log = -(-total // P)
+    nb = -(-staged // block)
+    cap = -(-(3 * (P - 1) + block) // P)
+    num_pages = n_log + nb * cap + 8
+    perm = rng.permutation(num_pages).astype(np.int32)
+    table = perm[:n_log]
+    private = perm[n_log:n_log + nb * cap].reshape(nb, cap)
+    return ExactWindowCase(
+        name=name, pin=pin, committed=committed, window=window, staged=staged, block=block,
+        num_q_heads=Hq, num_kv_heads=Hkv, head_dim=D,
+        k_pool=randn_bf16((num_pages, P, Hkv, D), gen), v_pool=randn_bf16((num_pages, P, Hkv, D), gen),
+        table=torch.from_numpy(table.copy()), private_pages=torch.from_numpy(private.copy()),
+        new_k=randn_bf16((staged, Hkv, D), gen), new_v=randn_bf16((staged, Hkv, D), gen),
+        q=randn_bf16((staged, Hq, D), gen))
+
+
+def exact_window_video(seed: int = 6, blocks_per_chunk: int = 4) -> ExactWindowCase:
+    """The exact-window geometry of the cache's benchmark: a 512-token prompt,
+    96 finished frames of 394 tokens as history, a window of 95 frames, a chunk
+    of 4 frames (1576 tokens); 32 query / 8 K/V heads of 128.  The clean pass
+    cuts the chunk into 4 frame-causal blocks; a denoising forward is one
+    block (``blocks_per_chunk=1``)."""
+    frame = 394
+    chunk = 4 * frame
+    return exact_window(seed, pin=512, committed=96 * frame, window=95 * frame, staged=chunk,
+                        block=chunk // blocks_per_chunk,
+                        name="exact_window_video" if blocks_per_chunk > 1 else "exact_window_denoise")
+
+
 WORKLOADS = {
     "tiny_decode": tiny_decode,
     "gqa_decode": gqa_decode,

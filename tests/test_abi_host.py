@@ -125,3 +125,19 @@ def test_rotate_and_merge_host_validation(L):
         pkv.PKV_ERR_UNSUPPORTED
     assert L.merge_attn_states(FAKE, None, FAKE, FAKE, 0, 3, 4, 64, FAKE, 0, None, None) == \
         pkv.PKV_ERR_INVALID_ARG
+
+
+def test_causal_layout_host_validation(L):
+    def lay(page=32, staged=100, block=30, com_cap=4 * 93, cur_cap=4 * 62, table=FAKE, row_stride=64,
+            priv_stride=8, pin=0, window=0):
+        return L.causal_layout(table, 10, FAKE, pin, window, staged, block, FAKE, priv_stride, page, FAKE,
+                               row_stride, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, com_cap, FAKE, FAKE, cur_cap,
+                               None, None)
+    assert lay(page=16) == pkv.PKV_ERR_UNSUPPORTED
+    assert lay(block=0) == pkv.PKV_ERR_INVALID_ARG
+    assert lay(staged=0, table=None) == pkv.PKV_OK           # empty forward: nothing to do
+    assert lay(table=None) == pkv.PKV_ERR_INVALID_ARG
+    assert lay(com_cap=3 * 93) == pkv.PKV_ERR_INVALID_ARG    # 4 blocks need 4 x 93 entries
+    assert lay(cur_cap=4 * 62 - 1) == pkv.PKV_ERR_INVALID_ARG
+    assert lay(row_stride=0) == pkv.PKV_ERR_INVALID_ARG
+    assert lay(pin=2 ** 31, window=1) == pkv.PKV_ERR_UNSUPPORTED

@@ -244,3 +244,30 @@ def test_zero_query_one_hot_values_through_layout():
             for t in range(first, first + n):
                 np.testing.assert_allclose(O[t, 0], want, atol=1e-15)
                 assert abs(LSE[t, 0] - np.log(len(vis))) < 1e-12
+
+
+def test_exact_window_equals_block_causal_when_window_cuts_nothing():
+    """With a window reaching back to the fixed region for every block, the
+    exact window is the block-causal visible set over the whole sequence, so
+    the direct definition must equal the paged oracle with the block-causal
+    mask (itself pinned to torch SDPA)."""
+    rng = np.random.default_rng(5)
+    pin, committed, staged, block, H, Hq, D = 37, 90, 70, 24, 2, 4, 64
+    total = pin + committed + staged
+    window = committed + staged
+    K = _bits(rng.standard_normal((total, H, D)))
+    V = _bits(rng.standard_normal((total, H, D)))
+    q = _bits(rng.standard_normal((staged, Hq, D)))
+    O1, L1 = orc.exact_window_attention(q, K, V, pin, committed, window, staged, block)
+    P = 32
+    n_pages = (total + P - 1) // P
+    kp = np.zeros((n_pages, P, H, D), np.uint16)
+    vp = np.zeros_like(kp)
+    for p in range(total):
+        kp[p // P, p % P] = K[p]
+        vp[p // P, p % P] = V[p]
+    O2, L2 = orc.paged_attention(q, kp, vp, np.arange(n_pages)[None], np.array([total]),
+                                 np.array([0, staged]), q_real=np.array([staged]),
+                                 mask=orc.MASK_BLOCK_CAUSAL, causal_block=block)
+    np.testing.assert_allclose(O1, O2, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(L1, L2, rtol=1e-12, atol=1e-12)
