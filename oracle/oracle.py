@@ -547,3 +547,77 @@ def exact_window_attention(q, k_seq, v_seq, pin: int, committed: int, window: in
                 O[ts, h] = (W_ @ Vb) / l[:, None]
                 L[ts, h] = m[:, 0] + np.log(l)
     return O, L
+
+
+# ----------------------------------------------------------------------------
+# shared-prefix planner: groups of rows sharing their leading pages
+# ----------------------------------------------------------------------------
+
+def plan_shared_prefix(block_table, kv_lens, q_lens, page_size: int = 32):
+    """Group the rows of a decode / verification batch whose block tables
+    start with the same pages, and split every row into its group's shared run
+    and its private tail.
+
+    [SP] commit notes: rows whose K/V block tables start with identical pages
+    are grouped, each group's shared pages are read once and merged with every
+    row's private tail; once per step a device kernel builds each row's page
+    table from its group's shared run onward (batch order) and its K/V length
+    past the run; the planner's grouping is keyed on every block-table entry
+    it read (entries past a row's last page ignored).
+
+    READINGS: two rows belong together when their first pages are equal (the
+    pages' grouping key) and both have at least one whole page before their
+    first new token; a group's shared run is the longest run of leading pages
+    identical in every member, cut at the first page that holds a member's new
+    tokens (only whole, committed pages are shared); a row alone in its group
+    shares nothing (run 0).  Groups are ordered by their first row, members by
+    row index.
+
+    ``block_table`` ``[B, width]``; ``kv_lens`` ``[B]`` keys including this
+    step's ``q_lens`` ``[B]`` new tokens (the row's last keys).
+    Returns a dict: ``groups`` (list of member-row lists), ``run_pages`` (per
+    group), ``group_rows`` (per group: run pages then every member's tail pages
+    in member order), ``tail_start`` (per row: its tail's first page index in
+    its group's row), ``tail_lens`` (per row), ``group_of`` (per row), ``perm``
+    (rows in group order).
+    """
+    P = page_size
+    table = np.asarray(block_table)
+    kv = [int(x) for x in kv_lens]
+    ql = [int(x) for x in q_lens]
+    B = len(kv)
+    committed_pages = [(kv[r] - ql[r]) // P for r in range(B)]
+    leader = list(range(B))
+    for r in range(B):
+        if committed_pages[r] < 1:
+            continue
+        for r2 in range(r):
+            if committed_pages[r2] >= 1 and table[r2][0] == table[r][0]:
+                leader[r] = leader[r2]
+                break
+    order = []
+    for r in range(B):
+        if leader[r] == r:
+            order.append(r)
+    groups = [[r for r in range(B) if leader[r] == g] for g in order]
+    run_pages, group_rows = [], []
+    tail_start, tail_lens, group_of = [0] * B, [0] * B, [0] * B
+    for gi, members in enumerate(groups):
+        run = 0
+        if len(members) > 1:
+            cap = min(committed_pages[m] for m in members)
+            first = members[0]
+            while run < cap and all(table[m][run] == table[first][run] for m in members):
+                run += 1
+        row = [int(x) for x in table[members[0]][:run]]
+        for m in members:
+            group_of[m] = gi
+            tail_start[m] = len(row)
+            tl = kv[m] - run * P
+            tail_lens[m] = tl
+            row.extend(int(x) for x in table[m][run:run + (tl + P - 1) // P])
+        run_pages.append(run)
+        group_rows.append(row)
+    perm = [m for members in groups for m in members]
+    return dict(groups=groups, run_pages=run_pages, group_rows=group_rows, tail_start=tail_start,
+                tail_lens=tail_lens, group_of=group_of, perm=perm)
