@@ -300,6 +300,93 @@ pkv_status causal_layout(const int32_t* table, int64_t num_logical_pages, const 
                          int32_t* err, void* stream);
 
 /*
+ * plan_shared_prefix -- group the rows of a batch that share their leading
+ * pages, on the device, once per step.
+ *
+ * [SP] commit notes: rows whose K/V block tables start with identical pages
+ * are grouped, each group's shared pages read once and merged with every
+ * row's private tail; a device kernel builds each row's page table from its
+ * group's shared run onward and its K/V length past the run; the grouping
+ * depends on every block-table entry it reads.
+ *
+ * Row r has kv_lens[r] keys, the last q_indptr[r+1] - q_indptr[r] of them
+ * this step's tokens; its whole committed pages are (kv - q) / 32.  Rows with
+ * at least one committed page and the same first page form a group (ordered
+ * by their first row; members by row index).  A group's shared run is the
+ * longest run of leading pages identical in every member, at most the
+ * smallest member's committed pages; a row alone has run 0.
+ *
+ * Outputs (device, caller-allocated, all rewritten; groups g < *num_groups):
+ *  group_rows[g * group_row_stride ...]  the run's pages, then every member's
+ *                                        tail pages in member order, then -1
+ *  run_lens[g]          32 * run pages (0 for g >= *num_groups)
+ *  group_indptr[g]      members of group g are perm[group_indptr[g] ..
+ *                       group_indptr[g + 1]); batch from *num_groups on
+ *  perm[i], group_of[r] rows in group order; a row's group
+ *  tail_start[r], tail_lens[r]  first page of row r's tail in its group's row;
+ *                       keys of its tail (kv_lens[r] - run_lens[group])
+ *  num_groups           device int32
+ *
+ *  batch          <= 1024 (one CTA plans the whole batch)
+ *  max_pages      pages of block_table a row may use (<= block_table_stride)
+ *  group_row_stride  >= the longest group row: max_pages * (largest group)
+ *                 is always enough; a longer row ORs PKV_ERRBIT_LEN into *err
+ *                 (nullable) and is truncated
+ */
+pkv_status plan_shared_prefix(const int32_t* block_table, int64_t block_table_stride,
+                              const int32_t* kv_lens, const int32_t* q_indptr, int batch,
+                              int max_pages, int32_t* group_rows, int64_t group_row_stride,
+                              int32_t* run_lens, int32_t* group_indptr, int32_t* perm,
+                              int32_t* group_of, int32_t* tail_start, int32_t* tail_lens,
+                              int32_t* num_groups, int32_t* err, void* stream);
+
+/*
+ * shared_prefix_attention -- attention of a grouped batch (plan_shared_prefix)
+ * in one launch: every query token attends to its group's shared run and its
+ * own tail in a single online softmax, each group's shared pages read once
+ * per group (and K/V head) instead of once per row; no merge step.
+ *
+ * [SP] commit notes: n-sample rows grouped by identical leading pages, the
+ * shared pages read once and merged with every row's private tail; a fused
+ * kernel does prefix, tail and merge for up to 16 query tokens per row (so
+ * speculative verification steps of K draft tokens + 1 are served too).
+ * Here the merge is exact by construction: the run and the tail are two key
+ * ranges of one softmax.
+ *
+ * Row r's query tokens are q[q_indptr[r] .. q_indptr[r+1]) (the row's last
+ * keys); token i of ql attends to keys [0, run_lens[g]) of its group row g
+ * and to [32 * tail_start[r], 32 * tail_start[r] + tail_lens[r] - ql + i + 1)
+ * (causal inside the tail).  Outputs are written at the tokens' own
+ * positions: out [tokens][num_q_heads][head_dim], lse [tokens][num_q_heads]
+ * (natural log; nullable).
+ *
+ *  group_rows ... num_groups   as written by plan_shared_prefix (device)
+ *  batch            rows of the plan (= group slots)
+ *  max_q_len        >= every row's query tokens (<= 16 is what the pages serve)
+ *  max_group_tokens >= the query tokens of any group (sizes the grid)
+ *  max_group_keys   >= the longest group row in keys (sizes the key splits)
+ *  head_dim 128, num_q_heads / num_kv_heads in {1, 2, 4, 8, 16} (tensor-core
+ *  tiles); other shapes return PKV_ERR_UNSUPPORTED.
+ *  workspace        shared_prefix_attention_workspace_size bytes (256-aligned)
+ *                   for the key splits it chooses; may be 0 bytes
+ */
+size_t shared_prefix_attention_workspace_size(int batch, int max_q_len, int max_group_tokens,
+                                              int max_group_keys, int num_q_heads,
+                                              int num_kv_heads, int head_dim, int num_splits);
+pkv_status shared_prefix_attention(const void* q, int64_t q_token_stride, int64_t q_head_stride,
+                                   const void* k_pool, const void* v_pool, int64_t num_pages,
+                                   int page_size, int64_t page_stride, const int32_t* group_rows,
+                                   int64_t group_row_stride, const int32_t* run_lens,
+                                   const int32_t* group_indptr, const int32_t* perm,
+                                   const int32_t* tail_start, const int32_t* tail_lens,
+                                   const int32_t* num_groups, const int32_t* q_indptr, int batch,
+                                   int max_q_len, int max_group_tokens, int max_group_keys,
+                                   int num_q_heads, int num_kv_heads, int head_dim, float scale,
+                                   void* out, pkv_dtype out_dtype, float* lse, void* workspace,
+                                   size_t workspace_bytes, int num_splits, unsigned flags,
+                                   int32_t* err, void* stream);
+
+/*
  * paged_attention_no_alloc -- paged_attention for callers that cannot allocate.
  *
  * The pages describe no such entry point; it exists for callers that have no

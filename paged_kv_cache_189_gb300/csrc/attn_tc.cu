@@ -226,7 +226,62 @@ __device__ __forceinline__ void store_row_lse(const AttnParams& p, const TileGeo
     }
 }
 
-template <int G>
+// ---------------------------------------------------------------------------
+// Grouped mode: the rows of a tile are the query tokens of one shared-prefix
+// group (its members in order, each member's tokens in order) x the G heads.
+// ---------------------------------------------------------------------------
+struct GroupRow {
+    int tok;      // token index in q / out (-1: no such row)
+    int a, b, c;  // visible keys of the group row: [0, a) u [b, c)
+};
+
+// Token t of group slot `grp` (its members grp_perm[first .. first + count)).
+// Member m's tokens are its last keys: token i of ql sees the shared run and
+// its tail up to its own position (causal inside the tail).
+__device__ __forceinline__ GroupRow group_row(const AttnParams& p, int grp, int first, int count, int t) {
+    GroupRow gr{-1, 0, 0, 0};
+    int acc = 0;
+    for (int k = 0; k < count; ++k) {
+        const int m = p.grp_perm[first + k];
+        const int q0 = p.q_indptr[m], ql = p.q_indptr[m + 1] - q0;
+        if (t < acc + ql) {
+            const int i = t - acc;
+            gr.tok = q0 + i;
+            gr.a = p.grp_run_lens[grp];
+            gr.b = 32 * p.grp_tail_start[m];
+            gr.c = gr.b + p.grp_tail_lens[m] - ql + i + 1;
+            return gr;
+        }
+        acc += ql;
+    }
+    return gr;
+}
+
+// Group slot, split and token tile of this CTA; nrows = the group's tokens
+// (0 for a slot past the number of groups).
+__device__ __forceinline__ TileGeom group_geometry(const AttnParams& p, int TQ, int& first, int& count) {
+    TileGeom g;
+    g.b = blockIdx.z / p.num_splits;
+    g.split = blockIdx.z - g.b * p.num_splits;
+    g.kvh = blockIdx.y;
+    g.r0 = 0;
+    g.t0 = blockIdx.x * TQ;
+    g.kb = g.split * p.split_keys;
+    g.nrows = g.qreal = g.kv_len = g.key_hi = g.nt = 0;
+    first = count = 0;
+    if (g.b >= *p.grp_num_groups) return g;
+    first = p.grp_indptr[g.b];
+    count = p.grp_indptr[g.b + 1] - first;
+    int T = 0;
+    for (int k = 0; k < count; ++k) {
+        const int m = p.grp_perm[first + k];
+        T += p.q_indptr[m + 1] - p.q_indptr[m];
+    }
+    g.nrows = g.qreal = T;
+    return g;
+}
+
+template <int G, bool GRP>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                    const AttnParams p) {
@@ -235,15 +290,41 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
-    const TileGeom g = tile_geometry(p, TQ);
-    if (g.t0 >= g.nrows) return;  // tile past this sequence's rows (uniform)
+    TileGeom g;
+    int grp_first = 0, grp_count = 0;
+    if constexpr (!GRP) {
+        g = tile_geometry(p, TQ);
+        if (g.t0 >= g.nrows) return;  // tile past this sequence's rows (uniform)
+    } else {
+        g = group_geometry(p, TQ, grp_first, grp_count);
+        if (g.t0 >= g.nrows) return;  // empty group slot, or tile past the group's tokens
+        // the keys the tile's rows see end at the largest of their visible ends
+        // (reduced in the flag area of shared memory, initialised further down)
+        int* s_keyhi = reinterpret_cast<int*>(smem + kFlagOff + 8);
+        if (threadIdx.x == 0) *s_keyhi = 0;
+        __syncthreads();
+        if (threadIdx.x < kTileM) {
+            const GroupRow gr = group_row(p, g.b, grp_first, grp_count, g.t0 + threadIdx.x / G);
+            if (gr.tok >= 0) atomicMax(s_keyhi, max(gr.a, gr.c));
+        }
+        __syncthreads();
+        g.kv_len = *s_keyhi;
+        g.key_hi = min(g.kv_len, g.kb + p.split_keys);
+        g.nt = g.key_hi > g.kb ? (g.key_hi - g.kb + kTileN - 1) / kTileN : 0;
+    }
 
     if (g.nt == 0) {
         // no visible key in this split for any row of the tile: empty states
         if (threadIdx.x < kTileM) {
             const int r = threadIdx.x;
-            const int i = g.t0 + r / G;
-            if (i < g.nrows) {
+            int i = g.t0 + r / G;
+            bool exists = i < g.nrows;
+            if constexpr (GRP) {
+                const GroupRow gr = group_row(p, g.b, grp_first, grp_count, i);
+                i = gr.tok;
+                exists = gr.tok >= 0;
+            }
+            if (exists) {
                 uint32_t zero[32];
 #pragma unroll
                 for (int e = 0; e < 32; ++e) zero[e] = 0u;
@@ -402,11 +483,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ============================ softmax ===============================
         const int r = threadIdx.x;             // tile row = tensor-memory lane
         const int t = r / G, hg = r % G;
-        const int i = g.t0 + t;                // query row within the sequence
         const int h = g.kvh * G + hg;
-        const bool row_exists = i < g.nrows;
-        const int limit = row_exists ? visible_keys(i, g.qreal, g.kv_len, p.mask, max(p.causal_block, 1))
-                                     : 0;
+        int i = g.t0 + t;                      // query row within the sequence (grouped: token)
+        bool row_exists = i < g.nrows;
+        int limit = 0;
+        int vis_a = 0, vis_b = 0, vis_c = 0;   // grouped: visible keys [0, a) u [b, c)
+        if constexpr (GRP) {
+            const GroupRow gr = group_row(p, g.b, grp_first, grp_count, i);
+            i = gr.tok;
+            row_exists = gr.tok >= 0;
+            vis_a = gr.a;
+            vis_b = gr.b;
+            vis_c = gr.c;
+        } else {
+            limit = row_exists ? visible_keys(i, g.qreal, g.kv_len, p.mask, max(p.causal_block, 1)) : 0;
+        }
         // ---- Q tile -> swizzled shared memory (rows past the sequence: zeros)
         {
             const uint4* src = reinterpret_cast<const uint4*>(
@@ -432,22 +523,38 @@ __global__ void __launch_bounds__(kThreads, 1)
         };
         // a warp none of whose rows sees a key (rows past the sequence, padding
         // rows) writes zero probabilities and skips the softmax arithmetic
-        const bool warp_live = __any_sync(0xffffffffu, limit > 0);
+        const bool warp_live = GRP || __any_sync(0xffffffffu, limit > 0);
         for (int j = 0; j < g.nt; ++j) {
             if (!wait_warp(&s_full[j & 1], (j >> 1) & 1)) break;
             tc_fence_after();
             uint32_t pk[kTileN / 2];
             float alpha = 1.f;
-            if (warp_live) {
+            bool live = warp_live;
+            if constexpr (GRP) {
+                // grouped rows see the shared run and their own tail: per key tile
+                const int k0 = g.kb + j * kTileN;
+                live = __any_sync(0xffffffffu, row_exists && (k0 < vis_a || (k0 < vis_c && k0 + kTileN > vis_b)));
+            }
+            if (live) {
                 const int key0 = g.kb + j * kTileN;
                 uint32_t sv[kTileN];  // raw scores of this row (f32 bits)
                 tmem_load128(lane_addr + (j & 1) * 128, sv);
-                // keys at or past this row's visible limit are masked (diagonal tiles only)
-                const int nvis = limit - key0;
-                if (nvis < kTileN) {
+                if constexpr (GRP) {
+                    const int ta = vis_a - key0, tb = vis_b - key0, tc = vis_c - key0;
+                    if (!row_exists || !(ta >= kTileN || (tb <= 0 && tc >= kTileN))) {
 #pragma unroll
-                    for (int e = 0; e < kTileN; ++e)
-                        sv[e] = e < nvis ? sv[e] : __float_as_uint(-INFINITY);
+                        for (int e = 0; e < kTileN; ++e)
+                            sv[e] = row_exists && (e < ta || (e >= tb && e < tc)) ? sv[e]
+                                                                                  : __float_as_uint(-INFINITY);
+                    }
+                } else {
+                    // keys at or past this row's visible limit are masked (diagonal tiles only)
+                    const int nvis = limit - key0;
+                    if (nvis < kTileN) {
+#pragma unroll
+                        for (int e = 0; e < kTileN; ++e)
+                            sv[e] = e < nvis ? sv[e] : __float_as_uint(-INFINITY);
+                    }
                 }
                 // row maximum of the raw scores (the scale is positive)
                 float mx = __uint_as_float(sv[0]);
@@ -486,7 +593,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // P buffer and O are free once the previous P.V finished
             if (j > 0 && !wait_warp(p_free, (j - 1) & 1)) break;
             tc_fence_after();
-            if (warp_live && j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+            if (live && j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
                 // O *= alpha for this row (warp-collective tensor-memory access)
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
@@ -520,6 +627,32 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int row = first + idx / 16, c = idx % 16;
                     *reinterpret_cast<uint4*>(vt + (c >> 3) * kHalfBytes + sw128_offset(row, c & 7)) =
                         make_uint4(0u, 0u, 0u, 0u);
+                }
+            }
+            if constexpr (GRP) {
+                // the rest of each member's last tail page is seen by no row: zero
+                // those V rows too (same reason)
+                bool any_gap = false;
+                for (int k = 0; k < grp_count; ++k) {
+                    const int m = p.grp_perm[grp_first + k];
+                    const int g0 = 32 * p.grp_tail_start[m] + p.grp_tail_lens[m];
+                    const int g1 = (g0 + 31) / 32 * 32;
+                    any_gap |= g0 < g1 && g0 < key0 + kTileN && g1 > key0;
+                }
+                if (any_gap) {
+                    const int vs = j % kVStages;
+                    if (!wait_warp(&v_full[vs], (j / kVStages) & 1)) break;
+                    uint8_t* vt = smem + kVOff + vs * kTileBytes;
+                    for (int k = 0; k < grp_count; ++k) {
+                        const int m = p.grp_perm[grp_first + k];
+                        const int g0 = 32 * p.grp_tail_start[m] + p.grp_tail_lens[m];
+                        const int lo = max(g0, key0) - key0, hi = min((g0 + 31) / 32 * 32, key0 + kTileN) - key0;
+                        for (int idx = r; idx < (hi - lo) * 16; idx += kTileM) {
+                            const int row = lo + idx / 16, c = idx % 16;
+                            *reinterpret_cast<uint4*>(vt + (c >> 3) * kHalfBytes + sw128_offset(row, c & 7)) =
+                                make_uint4(0u, 0u, 0u, 0u);
+                        }
+                    }
                 }
             }
             fence_proxy_async_smem();
@@ -1016,8 +1149,20 @@ cudaError_t launch_g2(const AttnParams& p, const void* tk, const void* tv, cudaS
 }
 
 template <int G>
+cudaError_t launch_grp(const AttnParams& p, const void* tk, const void* tv, cudaStream_t s) {
+    auto kern = attn_tc_kernel<G, true>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e != cudaSuccess) return e;
+    const int TQ = kTileM / G;
+    dim3 grid((p.grp_max_tokens + TQ - 1) / TQ, p.num_kv_heads, p.batch * p.num_splits);
+    kern<<<grid, kThreads, kSmemBytes, s>>>(*static_cast<const CUtensorMap*>(tk),
+                                            *static_cast<const CUtensorMap*>(tv), p);
+    return cudaGetLastError();
+}
+
+template <int G>
 cudaError_t launch_g(const AttnParams& p, const void* tk, const void* tv, cudaStream_t s) {
-    auto kern = attn_tc_kernel<G>;
+    auto kern = attn_tc_kernel<G, false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return e;
     const int TQ = kTileM / G;
@@ -1034,6 +1179,17 @@ bool attn_tc_supported(int head_dim, int group) {
 }
 
 int attn_tc_rows_per_tile(int group) { return kTileM / group; }
+
+cudaError_t launch_attn_tc_grouped(const AttnParams& p, const void* tk, const void* tv, cudaStream_t s) {
+    switch (p.num_q_heads / p.num_kv_heads) {
+        case 1: return launch_grp<1>(p, tk, tv, s);
+        case 2: return launch_grp<2>(p, tk, tv, s);
+        case 4: return launch_grp<4>(p, tk, tv, s);
+        case 8: return launch_grp<8>(p, tk, tv, s);
+        case 16: return launch_grp<16>(p, tk, tv, s);
+    }
+    return cudaErrorInvalidValue;
+}
 
 cudaError_t launch_attn_tc(const AttnParams& p, const void*, const void* tk, const void* tv,
                            cudaStream_t s) {

@@ -79,11 +79,14 @@ __global__ void __launch_bounds__(256) split_reduce_kernel(AttnParams p) {
     if (row_in_seq >= nrows) return;
     const int row = r0 + row_in_seq;
     if (row >= static_cast<int64_t>(p.batch) * p.max_q_rows) return;  // workspace bound
-    const int qreal = p.q_real ? p.q_real[b] : nrows;
-    int kv_len = min(p.kv_lens[b], p.max_kv_len);
-    if (row_in_seq >= qreal) kv_len = 0;
-    // splits that hold keys of this row (the rows of one sequence share them)
-    const int nsplit = min(p.num_splits, (kv_len + p.split_keys - 1) / p.split_keys);
+    int nsplit = p.num_splits;  // grouped mode: every split wrote a state for every token
+    if (!p.grp_perm) {
+        const int qreal = p.q_real ? p.q_real[b] : nrows;
+        int kv_len = min(p.kv_lens[b], p.max_kv_len);
+        if (row_in_seq >= qreal) kv_len = 0;
+        // splits that hold keys of this row (the rows of one sequence share them)
+        nsplit = min(p.num_splits, (kv_len + p.split_keys - 1) / p.split_keys);
+    }
     const int64_t st = static_cast<int64_t>(row) * H + h;
     const float* lses = p.ws_lse + st * p.num_splits;
     float m = -INFINITY;

@@ -364,6 +364,153 @@ pkv_status paged_attention(const void* q, int64_t q_token_stride, int64_t q_head
     return from_cuda(pkv::launch_decode(p, &tk, &tv, s), "attention (decode)");
 }
 
+namespace {
+// Key splits of a grouped call: one CTA per (group, token tile, K/V head);
+// the groups' count is known only on the device, so the host bound (every
+// slot a group) sizes the choice, like plan_attention's tile rule.
+Plan plan_grouped(int batch, int max_q_len, int max_group_tokens, int max_group_keys, int Hq, int Hkv,
+                  int D, int num_splits) {
+    Plan pl;
+    pl.kernel = Kernel::kTile;
+    const int G = Hkv > 0 ? Hq / Hkv : 1;
+    const int tq = pkv::attn_tc_rows_per_tile(G);
+    const int64_t ctas = static_cast<int64_t>((max_group_tokens + tq - 1) / tq) * Hkv * batch;
+    int s = 1;
+    if (num_splits > 0) {
+        s = num_splits;
+    } else if (ctas <= 2 * kPlanSMs) {
+        const int s_max = std::max(1, std::min(8, max_group_keys / 512));
+        const double unsplit = static_cast<double>((ctas + kPlanSMs - 1) / kPlanSMs);
+        double best = unsplit;
+        for (int c = 2; c <= s_max; ++c) {
+            const double waves = static_cast<double>((ctas * c + kPlanSMs - 1) / kPlanSMs);
+            const double cost = waves / c + 0.02 * c;
+            if (cost < best - 1e-9) {
+                best = cost;
+                s = c;
+            }
+        }
+        if (best > 0.9 * unsplit) s = 1;
+    }
+    const int per = (max_group_keys + s - 1) / std::max(s, 1);
+    pl.split_keys = std::max(kTileKeys, (per + kTileKeys - 1) / kTileKeys * kTileKeys);
+    pl.splits = std::max(1, (max_group_keys + pl.split_keys - 1) / pl.split_keys);
+    if (pl.splits > 1) {
+        const size_t states = static_cast<size_t>(batch) * max_q_len * Hq * pl.splits;
+        pl.ws_bytes = round_up(states * D * sizeof(float), 256) + round_up(states * sizeof(float), 256);
+    }
+    return pl;
+}
+}  // namespace
+
+size_t shared_prefix_attention_workspace_size(int batch, int max_q_len, int max_group_tokens,
+                                              int max_group_keys, int num_q_heads, int num_kv_heads,
+                                              int head_dim, int num_splits) {
+    if (batch <= 0 || max_q_len <= 0 || max_group_tokens <= 0 || num_kv_heads <= 0) return 0;
+    return plan_grouped(batch, max_q_len, max_group_tokens, max_group_keys, num_q_heads, num_kv_heads,
+                        head_dim, num_splits)
+        .ws_bytes;
+}
+
+pkv_status shared_prefix_attention(const void* q, int64_t q_token_stride, int64_t q_head_stride,
+                                   const void* k_pool, const void* v_pool, int64_t num_pages,
+                                   int page_size, int64_t page_stride, const int32_t* group_rows,
+                                   int64_t group_row_stride, const int32_t* run_lens,
+                                   const int32_t* group_indptr, const int32_t* perm,
+                                   const int32_t* tail_start, const int32_t* tail_lens,
+                                   const int32_t* num_groups, const int32_t* q_indptr, int batch,
+                                   int max_q_len, int max_group_tokens, int max_group_keys,
+                                   int num_q_heads, int num_kv_heads, int head_dim, float scale,
+                                   void* out, pkv_dtype out_dtype, float* lse, void* workspace,
+                                   size_t workspace_bytes, int num_splits, unsigned flags,
+                                   int32_t* err, void* stream) {
+    if (batch < 0 || max_q_len < 0 || max_group_tokens < 0 || max_group_keys < 0 || num_q_heads < 0 ||
+        num_kv_heads < 0 || num_pages < 0 || num_splits < 0)
+        return fail(PKV_ERR_INVALID_ARG, "shared prefix: negative size");
+    if (batch == 0 || max_q_len == 0 || max_group_tokens == 0 || num_q_heads == 0) return ok();
+    if (num_kv_heads == 0 || num_q_heads % num_kv_heads != 0)
+        return fail(PKV_ERR_INVALID_ARG, "shared prefix: %d query heads is not a multiple of %d K/V heads",
+                    num_q_heads, num_kv_heads);
+    if (!q || !k_pool || !v_pool || !group_rows || !run_lens || !group_indptr || !perm || !tail_start ||
+        !tail_lens || !num_groups || !q_indptr || !out)
+        return fail(PKV_ERR_INVALID_ARG, "shared prefix: null pointer");
+    if (page_size != 32)
+        return fail(PKV_ERR_UNSUPPORTED, "shared prefix: page_size %d (only 32-token pages)", page_size);
+    if (!pkv::attn_tc_supported(head_dim, num_q_heads / num_kv_heads))
+        return fail(PKV_ERR_UNSUPPORTED, "shared prefix: head_dim 128 and 1-16 grouped heads only");
+    if (out_dtype != PKV_BF16 && out_dtype != PKV_F32)
+        return fail(PKV_ERR_UNSUPPORTED, "shared prefix: output dtype must be bf16 or f32");
+    if (batch > 65535 || num_kv_heads > 65535)
+        return fail(PKV_ERR_UNSUPPORTED, "shared prefix: batch or K/V heads above 65535");
+    if (page_stride < static_cast<int64_t>(page_size) * num_kv_heads * head_dim || page_stride % 8)
+        return fail(PKV_ERR_INVALID_ARG, "shared prefix: page_stride must cover a page, multiple of 8");
+    if (!aligned(q, 16) || !aligned(k_pool, 16) || !aligned(v_pool, 16) || q_token_stride % 8 ||
+        q_head_stride % 8 || q_token_stride < 0 || q_head_stride < 0)
+        return fail(PKV_ERR_INVALID_ARG, "shared prefix: q / pools 16-byte aligned, strides multiple of 8");
+    if (!aligned(out, 16) || (lse && !aligned(lse, 4)))
+        return fail(PKV_ERR_INVALID_ARG, "shared prefix: output must be 16-byte aligned");
+    if (group_row_stride < (static_cast<int64_t>(max_group_keys) + 31) / 32)
+        return fail(PKV_ERR_INVALID_ARG, "shared prefix: group_row_stride below max_group_keys / 32");
+    const Plan pl = plan_grouped(batch, max_q_len, max_group_tokens, max_group_keys, num_q_heads,
+                                 num_kv_heads, head_dim, num_splits);
+    if (pl.ws_bytes > 0 && (!workspace || workspace_bytes < pl.ws_bytes || !aligned(workspace, 256)))
+        return fail(PKV_ERR_WORKSPACE, "shared prefix: workspace needs %zu bytes, 256-byte aligned",
+                    pl.ws_bytes);
+    if (static_cast<int64_t>(batch) * pl.splits > 65535)
+        return fail(PKV_ERR_UNSUPPORTED, "shared prefix: batch x key splits above 65535");
+
+    pkv::AttnParams p{};
+    p.q = q;
+    p.q_token_stride = q_token_stride;
+    p.q_head_stride = q_head_stride;
+    p.k_pool = k_pool;
+    p.v_pool = v_pool;
+    p.num_pages = num_pages;
+    p.page_stride = page_stride;
+    p.block_table = group_rows;
+    p.block_table_stride = group_row_stride;
+    p.q_indptr = q_indptr;
+    p.batch = batch;
+    p.max_q_rows = max_q_len;
+    p.max_kv_len = max_group_keys;
+    p.num_q_heads = num_q_heads;
+    p.num_kv_heads = num_kv_heads;
+    p.head_dim = head_dim;
+    p.mask = PKV_MASK_NONE;
+    const float sc = scale > 0.f ? scale : 1.0f / std::sqrt(static_cast<float>(head_dim));
+    p.scale_log2 = sc * 1.4426950408889634f;
+    p.out = out;
+    p.out_f32 = out_dtype == PKV_F32;
+    p.lse = lse;
+    p.num_splits = pl.splits;
+    p.split_keys = pl.split_keys;
+    p.checked = (flags & PKV_FLAG_CHECKED) != 0;
+    p.err = err;
+    p.grp_run_lens = run_lens;
+    p.grp_indptr = group_indptr;
+    p.grp_perm = perm;
+    p.grp_tail_start = tail_start;
+    p.grp_tail_lens = tail_lens;
+    p.grp_num_groups = num_groups;
+    p.grp_max_tokens = max_group_tokens;
+    if (pl.splits > 1) {
+        const size_t states = static_cast<size_t>(batch) * max_q_len * num_q_heads * pl.splits;
+        p.ws_o = static_cast<float*>(workspace);
+        p.ws_lse = reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                            round_up(states * head_dim * sizeof(float), 256));
+    }
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    CUtensorMap tk, tv;
+    pkv_status st = make_pool_map(&tk, k_pool, head_dim, num_kv_heads, page_size, num_pages, page_stride);
+    if (st != PKV_OK) return st;
+    st = make_pool_map(&tv, v_pool, head_dim, num_kv_heads, page_size, num_pages, page_stride);
+    if (st != PKV_OK) return st;
+    cudaError_t e = pkv::launch_attn_tc_grouped(p, &tk, &tv, s);
+    if (e != cudaSuccess) return from_cuda(e, "shared prefix (grouped tiles)");
+    if (pl.splits > 1) return from_cuda(pkv::launch_split_reduce(p, s), "shared prefix (split reduce)");
+    return ok();
+}
+
 pkv_status merge_attn_states(const void* o_a, const float* lse_a, const void* o_b,
                              const float* lse_b, pkv_dtype in_dtype, int64_t rows, int num_heads,
                              int head_dim, void* o_out, pkv_dtype out_dtype, float* lse_out,
@@ -486,6 +633,29 @@ pkv_status causal_layout(const int32_t* table, int64_t num_logical_pages, const 
                       row_stride, kv_lens, q_indptr, staged_slots, staged_slots2, committed_src,
                       committed_dst, current_src_idx, current_dst, err};
     return from_cuda(pkv::launch_causal_layout(a, static_cast<cudaStream_t>(stream)), "layout launch");
+}
+
+pkv_status plan_shared_prefix(const int32_t* block_table, int64_t block_table_stride,
+                              const int32_t* kv_lens, const int32_t* q_indptr, int batch,
+                              int max_pages, int32_t* group_rows, int64_t group_row_stride,
+                              int32_t* run_lens, int32_t* group_indptr, int32_t* perm,
+                              int32_t* group_of, int32_t* tail_start, int32_t* tail_lens,
+                              int32_t* num_groups, int32_t* err, void* stream) {
+    if (batch < 0 || max_pages < 0 || group_row_stride < 0)
+        return fail(PKV_ERR_INVALID_ARG, "plan: negative size");
+    if (batch == 0) return ok();
+    if (batch > 1024) return fail(PKV_ERR_UNSUPPORTED, "plan: batch %d above 1024", batch);
+    if (!block_table || !kv_lens || !q_indptr || !group_rows || !run_lens || !group_indptr || !perm ||
+        !group_of || !tail_start || !tail_lens || !num_groups)
+        return fail(PKV_ERR_INVALID_ARG, "plan: null pointer");
+    if (block_table_stride < max_pages)
+        return fail(PKV_ERR_INVALID_ARG, "plan: block_table_stride %lld < max_pages %d",
+                    static_cast<long long>(block_table_stride), max_pages);
+    if (group_row_stride < 1) return fail(PKV_ERR_INVALID_ARG, "plan: group_row_stride must be >= 1");
+    pkv::PlanArgs a{block_table, block_table_stride, kv_lens, q_indptr, batch, max_pages, group_rows,
+                    group_row_stride, run_lens, group_indptr, perm, group_of, tail_start, tail_lens,
+                    num_groups, err};
+    return from_cuda(pkv::launch_plan(a, static_cast<cudaStream_t>(stream)), "plan launch");
 }
 
 pkv_status rotate_rows(void* x, int64_t rows, int64_t cols, int64_t row_stride, int elem_size_b,

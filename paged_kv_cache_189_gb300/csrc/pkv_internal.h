@@ -57,6 +57,25 @@ struct RopeArgs {
 cudaError_t launch_rope_write(const RopeArgs& a, cudaStream_t s);
 
 // ---------------------------- pool-to-pool slot copy --------------------------
+struct PlanArgs {
+    const int32_t* block_table;
+    int64_t block_table_stride;
+    const int32_t* kv_lens;
+    const int32_t* q_indptr;
+    int batch, max_pages;
+    int32_t* group_rows;
+    int64_t group_row_stride;
+    int32_t* run_lens;
+    int32_t* group_indptr;
+    int32_t* perm;
+    int32_t* group_of;
+    int32_t* tail_start;
+    int32_t* tail_lens;
+    int32_t* num_groups;
+    int32_t* err;
+};
+cudaError_t launch_plan(const PlanArgs& a, cudaStream_t s);
+
 struct LayoutArgs {
     const int32_t* table;
     int64_t num_logical_pages;
@@ -136,6 +155,16 @@ struct AttnParams {
     int* ws_counters;  // decode: [0] unit ticket, [1 + b*Hkv + h] finished splits
     bool checked;
     int32_t* err;
+    // shared-prefix groups (grouped tile mode, grp_perm != nullptr): block_table
+    // holds the group rows, batch is the number of group slots, q_indptr the
+    // original rows' query tokens; kv_lens and q_real are not used
+    const int32_t* grp_run_lens;    // [groups] keys of each group's shared run
+    const int32_t* grp_indptr;      // [groups + 1] members in grp_perm
+    const int32_t* grp_perm;        // rows in group order
+    const int32_t* grp_tail_start;  // [rows] first page of the row's tail in its group row
+    const int32_t* grp_tail_lens;   // [rows] keys of the row's tail
+    const int32_t* grp_num_groups;  // device scalar
+    int grp_max_tokens;             // host bound on the query tokens of one group
 };
 
 // Decode kernel (one query row per sequence), split-KV, SIMT; K/V pages
@@ -148,6 +177,12 @@ size_t decode_counter_bytes(int batch, int num_kv_heads);
 // Generic SIMT kernel: any rows, masks, group sizes; no splits.  A slow
 // cross-check of the fast kernels and the path for shapes they do not cover.
 cudaError_t launch_attn_simt(const AttnParams& p, cudaStream_t s);
+
+// Grouped mode of the one-tile tensor-core kernel: one CTA per (group, tile of
+// the group's query tokens, K/V head); each row attends to its group's shared
+// run and its own tail in one online softmax.
+cudaError_t launch_attn_tc_grouped(const AttnParams& p, const void* tmap_k, const void* tmap_v,
+                                   cudaStream_t s);
 
 // Tensor-core tile kernel (tcgen05 / TMEM, TMA-fed) for many query rows.
 cudaError_t launch_attn_tc(const AttnParams& p, const void* tmap_q, const void* tmap_k,

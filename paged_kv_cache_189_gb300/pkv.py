@@ -27,7 +27,8 @@ PKV_ERRBIT_SLOT, PKV_ERRBIT_SRC, PKV_ERRBIT_PAGE, PKV_ERRBIT_LEN, PKV_ERRBIT_TIM
 EXPORTED = ("pkv_status_string", "pkv_last_error", "kv_scatter_slots",
             "paged_attention_workspace_size", "paged_attention", "merge_attn_states",
             "rotate_rows", "paged_attention_no_alloc", "rope_write_kv_paged", "copy_kv_slots",
-            "causal_layout")
+            "causal_layout", "plan_shared_prefix", "shared_prefix_attention",
+            "shared_prefix_attention_workspace_size")
 NO_ALLOC_SCRATCH_BYTES = 32 << 20
 
 _vp, _i64, _i32, _u32, _f32, _sz = (ctypes.c_void_p, ctypes.c_int64, ctypes.c_int,
@@ -54,6 +55,12 @@ _SIGNATURES = {
                              _i64, _u32, _vp, _vp]),
     "causal_layout": (_i32, [_vp, _i64, _vp, _i64, _i64, _i32, _i32, _vp, _i32, _i32, _vp, _i64,
                              _vp, _vp, _vp, _vp, _vp, _vp, _i64, _vp, _vp, _i64, _vp, _vp]),
+    "plan_shared_prefix": (_i32, [_vp, _i64, _vp, _vp, _i32, _i32, _vp, _i64, _vp, _vp, _vp, _vp, _vp,
+                                  _vp, _vp, _vp, _vp]),
+    "shared_prefix_attention_workspace_size": (_sz, [_i32, _i32, _i32, _i32, _i32, _i32, _i32, _i32]),
+    "shared_prefix_attention": (_i32, [_vp, _i64, _i64, _vp, _vp, _i64, _i32, _i64, _vp, _i64, _vp, _vp,
+                                       _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32,
+                                       _i32, _f32, _vp, _i32, _vp, _vp, _sz, _i32, _u32, _vp, _vp]),
 }
 
 _lib = None
@@ -282,3 +289,56 @@ def causal_layout(table, committed, pin_tokens, window_tokens, num_staged, block
                              _ptr(out["current_dst"]), out["current_src_idx"].numel(), _ptr(err),
                              _stream(stream))
     _check("causal_layout", st)
+
+
+def plan_buffers(batch, group_row_stride, device="cuda"):
+    """Output tensors of :func:`plan_shared_prefix` for a batch of ``batch`` rows."""
+    import torch
+    i32 = dict(dtype=torch.int32, device=device)
+    return dict(group_rows=torch.full((batch, group_row_stride), -1, **i32),
+                run_lens=torch.zeros(batch, **i32), group_indptr=torch.zeros(batch + 1, **i32),
+                perm=torch.zeros(batch, **i32), group_of=torch.zeros(batch, **i32),
+                tail_start=torch.zeros(batch, **i32), tail_lens=torch.zeros(batch, **i32),
+                num_groups=torch.zeros(1, **i32))
+
+
+def plan_shared_prefix(block_table, kv_lens, q_indptr, out, max_pages=None, err=None, stream=None):
+    """Shared-prefix grouping of the batch's rows (see ``include/pkv.h``);
+    ``out``: the dict of :func:`plan_buffers`, rewritten in place."""
+    B = kv_lens.numel()
+    mp = block_table.shape[1] if max_pages is None else max_pages
+    gr = out["group_rows"]
+    st = lib().plan_shared_prefix(_ptr(block_table), block_table.stride(0), _ptr(kv_lens), _ptr(q_indptr), B,
+                                  mp, _ptr(gr), gr.shape[1], _ptr(out["run_lens"]), _ptr(out["group_indptr"]),
+                                  _ptr(out["perm"]), _ptr(out["group_of"]), _ptr(out["tail_start"]),
+                                  _ptr(out["tail_lens"]), _ptr(out["num_groups"]), _ptr(err),
+                                  _stream(stream))
+    _check("plan_shared_prefix", st)
+
+
+def shared_prefix_attention_workspace_size(batch, max_q_len, max_group_tokens, max_group_keys,
+                                           num_q_heads, num_kv_heads, head_dim, num_splits=0) -> int:
+    return int(lib().shared_prefix_attention_workspace_size(batch, max_q_len, max_group_tokens,
+                                                            max_group_keys, num_q_heads, num_kv_heads,
+                                                            head_dim, num_splits))
+
+
+def shared_prefix_attention(q, k_pool, v_pool, plan, q_indptr, out, *, max_q_len, max_group_tokens,
+                            max_group_keys, lse=None, scale=0.0, workspace=None, num_splits=0, flags=0,
+                            err=None, stream=None):
+    """One-launch attention of a planned batch (``plan``: the dict of
+    :func:`plan_buffers` after :func:`plan_shared_prefix`); outputs at the
+    tokens' own positions in ``out [tokens, Hq, D]`` / ``lse [tokens, Hq]``."""
+    n, P, H, D, page_stride = _pool_geometry(k_pool)
+    assert v_pool.shape == k_pool.shape and v_pool.stride() == k_pool.stride()
+    assert q.stride(2) == 1 and out.is_contiguous()
+    B = q_indptr.numel() - 1
+    gr = plan["group_rows"]
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = lib().shared_prefix_attention(
+        _ptr(q), q.stride(0), q.stride(1), _ptr(k_pool), _ptr(v_pool), n, P, page_stride, _ptr(gr),
+        gr.stride(0), _ptr(plan["run_lens"]), _ptr(plan["group_indptr"]), _ptr(plan["perm"]),
+        _ptr(plan["tail_start"]), _ptr(plan["tail_lens"]), _ptr(plan["num_groups"]), _ptr(q_indptr), B,
+        max_q_len, max_group_tokens, max_group_keys, q.shape[1], H, D, scale, _ptr(out), _dtype(out),
+        _ptr(lse), _ptr(workspace), ws_bytes, num_splits, flags, _ptr(err), _stream(stream))
+    _check("shared_prefix_attention", st)

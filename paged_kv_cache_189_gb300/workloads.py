@@ -217,11 +217,12 @@ def chunked_prefill(seed: int = 2, batch: int = 8, chunk: int = 512, lo: int = 2
 
 def shared_prefix(seed: int = 3, groups: int = 16, samples: int = 8, prefix: int = 4096,
                   tail_lo: int = 1, tail_hi: int = 1024, Hq: int = 32, Hkv: int = 8,
-                  D: int = 128) -> PagedCase:
+                  D: int = 128, q_len: int = 1) -> PagedCase:
     """16 prompt groups x 8 samples; each group's 4096-token prefix (128 whole
     pages) is referenced once, by the group's prefix table; each sample owns a
-    private tail of U[1, 1024] tokens (the last one is this step's token,
-    scattered first) in its own pages. One query row per sample.
+    private tail of U[1, 1024] tokens (the last ``q_len`` are this step's
+    tokens, scattered first) in its own pages. ``q_len`` query rows per sample
+    (1: decode; more: speculative verification of draft tokens).
 
     Returned case: ``block_table`` / ``kv_lens`` describe the full rows
     (prefix ++ tail) for the oracle; ``extra`` holds the split the method uses:
@@ -232,7 +233,7 @@ def shared_prefix(seed: int = 3, groups: int = 16, samples: int = 8, prefix: int
     rng = np.random.default_rng(seed)
     gen = torch.Generator().manual_seed(seed)
     n_rows = groups * samples
-    tails = rng.integers(tail_lo, tail_hi, size=n_rows, endpoint=True)
+    tails = np.maximum(rng.integers(tail_lo, tail_hi, size=n_rows, endpoint=True), q_len)
     prefix_pages = prefix // P
     tail_pages = [int(-(-int(t) // P)) for t in tails]
     used = groups * prefix_pages + sum(tail_pages)
@@ -255,26 +256,26 @@ def shared_prefix(seed: int = 3, groups: int = 16, samples: int = 8, prefix: int
 
     k_pool = randn_bf16((num_pages, P, Hkv, D), gen)
     v_pool = randn_bf16((num_pages, P, Hkv, D), gen)
-    q = randn_bf16((n_rows, Hq, D), gen)
-    new_k = randn_bf16((n_rows, Hkv, D), gen)
-    new_v = randn_bf16((n_rows, Hkv, D), gen)
-    slots = np.array([slot_of(tail_table[r], int(tails[r]) - 1) for r in range(n_rows)],
-                     dtype=np.int64)
-    ones = np.ones(n_rows, dtype=np.int32)
+    q = randn_bf16((n_rows * q_len, Hq, D), gen)
+    new_k = randn_bf16((n_rows * q_len, Hkv, D), gen)
+    new_v = randn_bf16((n_rows * q_len, Hkv, D), gen)
+    slots = np.array([slot_of(tail_table[r], int(tails[r]) - q_len + i) for r in range(n_rows)
+                      for i in range(q_len)], dtype=np.int64)
+    ones = np.full(n_rows, q_len, dtype=np.int32)
     case = PagedCase(
         name="shared_prefix", num_q_heads=Hq, num_kv_heads=Hkv, head_dim=D, page_size=P,
         k_pool=k_pool, v_pool=v_pool, block_table=torch.from_numpy(full_table),
         kv_lens=torch.from_numpy((prefix + tails).astype(np.int32)), q=q,
-        q_indptr=torch.from_numpy(np.arange(n_rows + 1, dtype=np.int32)),
+        q_indptr=torch.from_numpy(np.arange(n_rows + 1, dtype=np.int32) * q_len),
         q_real=torch.from_numpy(ones), new_k=new_k, new_v=new_v,
         slots=torch.from_numpy(slots), mask="causal")
     case.extra.update(
         groups=groups, samples=samples,
         prefix_table=torch.from_numpy(prefix_table),
         prefix_lens=torch.full((groups,), prefix, dtype=torch.int32),
-        # the group's sample rows packed as one query "sequence" of n rows
-        prefix_q_indptr=torch.from_numpy(np.arange(groups + 1, dtype=np.int32) * samples),
-        prefix_q_real=torch.full((groups,), samples, dtype=torch.int32),
+        # the group's sample rows packed as one query "sequence" of n x q_len rows
+        prefix_q_indptr=torch.from_numpy(np.arange(groups + 1, dtype=np.int32) * samples * q_len),
+        prefix_q_real=torch.full((groups,), samples * q_len, dtype=torch.int32), q_len=q_len,
         tail_table=torch.from_numpy(tail_table),
         tail_lens=torch.from_numpy(tails.astype(np.int32)))
     return case
@@ -312,6 +313,55 @@ def random_case(seed: int, batch: int, Hq: int, Hkv: int, D: int, kv_range=(1, 3
     kv = np.maximum(kv, q_real)
     return build_pool_case(f"random_{seed}", seed, kv, q_real + pad, q_real, Hq, Hkv, D,
                            mask=mask, causal_block=causal_block, q_scale=q_scale)
+
+
+def nsample_tables(rng, n_groups: int = 5, loners: int = 4, width: int = 40, page: int = PAGE_SIZE):
+    """Block tables of an n-sample batch for the shared-prefix planner: groups
+    of 2-6 rows sharing 1-8 leading pages (distinct first pages per group),
+    every other group's members also sharing the page that holds their new
+    tokens (a plan must stop its shared run before it), private tails, and
+    rows that share nothing; rows of different groups interleaved.  Returns
+    ``(table [B, width] int32, kv_lens, q_lens, truth)`` with ``truth`` the
+    built groups as ``(sorted member rows, shared pages)``."""
+    P = page
+    next_page = [1000]
+
+    def fresh(n):
+        out = list(range(next_page[0], next_page[0] + n))
+        next_page[0] += n
+        return out
+
+    rows, truth = [], []
+    for gi in range(n_groups):
+        shared = fresh(int(rng.integers(1, 9)))
+        common_last = fresh(1) if gi % 2 else None
+        members = []
+        for _ in range(int(rng.integers(2, 7))):
+            q = int(rng.integers(1, 5))
+            if common_last is not None:
+                tail = common_last
+                kv = len(shared) * P + int(rng.integers(q, P + 1))
+            else:
+                tail_pages = int(rng.integers(1, 6))
+                tail = fresh(tail_pages)
+                kv = (len(shared) + tail_pages - 1) * P + int(rng.integers(1, P + 1))
+                kv = max(kv, len(shared) * P + q)
+            members.append(len(rows))
+            rows.append((shared + tail, kv, q))
+        truth.append((members, len(shared)))
+    for _ in range(loners):
+        pages = fresh(int(rng.integers(1, 6)))
+        rows.append((pages, (len(pages) - 1) * P + int(rng.integers(1, P + 1)), 1))
+    order = rng.permutation(len(rows))
+    rows = [rows[i] for i in order]
+    inv = {int(o): i for i, o in enumerate(order)}
+    truth = [(sorted(inv[m] for m in members), run) for members, run in truth]
+    table = np.full((len(rows), width), -1, np.int32)
+    for r, (pages, _, _) in enumerate(rows):
+        table[r, :len(pages)] = pages
+    kv = np.array([x[1] for x in rows])
+    ql = np.array([x[2] for x in rows])
+    return table, kv, ql, truth
 
 
 @dataclass

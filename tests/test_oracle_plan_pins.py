@@ -16,6 +16,7 @@ import pytest
 import torch
 
 from oracle import oracle as orc
+from paged_kv_cache_189_gb300.workloads import nsample_tables as nsample_batch
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "shared_prefix_plan_small.txt")
 P = 32
@@ -51,51 +52,6 @@ def test_plan_golden():
     assert plan["group_rows"] == [g["group_row"][i] for i in range(len(g["groups"]))]
     for k in ("tail_start", "tail_lens", "group_of", "perm"):
         assert plan[k] == g[k], k
-
-
-def nsample_batch(rng, n_groups=5, loners=4, width=40):
-    """Groups of 2-6 rows sharing 1-8 leading pages (distinct first pages),
-    each row with a private tail; plus rows sharing nothing."""
-    next_page = [1000]
-
-    def fresh(n):
-        out = list(range(next_page[0], next_page[0] + n))
-        next_page[0] += n
-        return out
-
-    rows, truth = [], []
-    for gi in range(n_groups):
-        shared = fresh(int(rng.integers(1, 9)))
-        # every other group's members also share the page that holds their new
-        # tokens: the run must stop before it
-        common_last = fresh(1) if gi % 2 else None
-        members = []
-        for _ in range(int(rng.integers(2, 7))):
-            q = int(rng.integers(1, 5))
-            if common_last is not None:
-                tail = common_last
-                kv = len(shared) * P + int(rng.integers(q, P + 1))
-            else:
-                tail_pages = int(rng.integers(1, 6))
-                tail = fresh(tail_pages)
-                kv = (len(shared) + tail_pages - 1) * P + int(rng.integers(1, P + 1))
-                kv = max(kv, len(shared) * P + q)    # new tokens never inside the shared pages
-            members.append(len(rows))
-            rows.append((shared + tail, kv, q))
-        truth.append((members, len(shared)))
-    for _ in range(loners):
-        pages = fresh(int(rng.integers(1, 6)))
-        rows.append((pages, (len(pages) - 1) * P + int(rng.integers(1, P + 1)), 1))
-    order = rng.permutation(len(rows))          # interleave the groups in the batch
-    rows = [rows[i] for i in order]
-    inv = {int(o): i for i, o in enumerate(order)}
-    truth = [(sorted(inv[m] for m in members), run) for members, run in truth]
-    table = np.full((len(rows), width), -1, np.int32)
-    for r, (pages, _, _) in enumerate(rows):
-        table[r, :len(pages)] = pages
-    kv = np.array([x[1] for x in rows])
-    ql = np.array([x[2] for x in rows])
-    return table, kv, ql, truth
 
 
 @pytest.mark.parametrize("seed", range(8))
