@@ -50,8 +50,9 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="gqa_decode",
                     choices=["gqa_decode", "chunked_prefill", "block_causal_video",
-                             "shared_prefix", "tiny_decode", "multi_token_decode",
-                             "exact_window_video", "exact_window_denoise"])
+                             "shared_prefix", "shared_prefix_fused", "shared_prefix_verify",
+                             "tiny_decode", "multi_token_decode", "exact_window_video",
+                             "exact_window_denoise"])
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-sample-seqs", type=int, default=64)
@@ -452,8 +453,11 @@ def build_plan(name, rank, dev, stream):
         return build_exact_window_plan(name, rank, dev, stream)
     case = {"gqa_decode": wl.gqa_decode, "chunked_prefill": wl.chunked_prefill,
             "block_causal_video": wl.block_causal_video, "shared_prefix": wl.shared_prefix,
+            "shared_prefix_fused": wl.shared_prefix,
+            "shared_prefix_verify": lambda seed: wl.shared_prefix(seed, q_len=4),
             "tiny_decode": wl.tiny_decode, "multi_token_decode": wl.multi_token_decode}[name](
         seed={"gqa_decode": 1, "chunked_prefill": 2, "shared_prefix": 3, "block_causal_video": 4,
+              "shared_prefix_fused": 3, "shared_prefix_verify": 3,
               "tiny_decode": 0, "multi_token_decode": 5}[name] + rank)
     Hq, Hkv, D = case.num_q_heads, case.num_kv_heads, case.head_dim
     rows = case.q.shape[0]
@@ -579,6 +583,43 @@ def build_plan(name, rank, dev, stream):
                         dom_work=prefix_bytes, bound="hbm", peak=peak_hbm, peak_unit="GB/s",
                         peak_src=f"{hbm_kind} hbm_gbs", h2d=(h2d_src, h2d_dst), d2h=d2h_src,
                         launches=6, traffic_sources=ATTN_TC_SOURCES)
+    if name in ("shared_prefix_fused", "shared_prefix_verify"):
+        # the step plans the grouping on the device (plan_shared_prefix) and runs
+        # every row's shared run + tail in one launch (shared_prefix_attention)
+        e = case.extra
+        Gn, n_s, q_len = e["groups"], e["samples"], e["q_len"]
+        B = case.batch
+        width = case.block_table.shape[1]
+        stride = width * n_s                       # a group row: at most n_s full rows
+        max_keys = stride * 32
+        plan_out = pkv.plan_buffers(B, stride, dev)
+        mgt = n_s * q_len                          # tokens of one group
+        ws_b = pkv.shared_prefix_attention_workspace_size(B, q_len, mgt, max_keys, Hq, Hkv, D)
+        ws = torch.empty(max(ws_b, 256), dtype=torch.uint8, device=dev)
+        plan_call = lambda: pkv.plan_shared_prefix(t["bt"], t["kl"], t["qi"], plan_out, stream=stream)
+        dom = lambda: pkv.shared_prefix_attention(t["q"], t["k_pool"], t["v_pool"], plan_out, t["qi"], out,
+                                                  lse=lse, max_q_len=q_len, max_group_tokens=mgt,
+                                                  max_group_keys=max_keys, workspace=ws, stream=stream)
+        prefix = int(e["prefix_lens"][0])
+        prefix_bytes = Gn * prefix * kv_tok_bytes
+        tail_bytes = int(e["tail_lens"].sum()) * kv_tok_bytes
+        io_bytes = rows * Hq * (D * 2 * 2 + 4)
+        aux["plan"] = (plan_call, B * width * 4 * 2, "GB/s")
+        cfg.update(groups=Gn, samples=n_s, q_len=q_len, prefix=prefix, tail="U[1,1024]",
+                   kv_bytes_per_step=prefix_bytes + tail_bytes,
+                   kv_bytes_without_sharing=B * prefix * kv_tok_bytes + tail_bytes,
+                   l2="prefix pages 16.8 MB per group; 537 MB of K/V per step",
+                   grouping="planned on the device every step")
+        h2d_src = [case.q, case.new_k, case.new_v, case.slots, case.kv_lens, case.block_table]
+        h2d_dst = [t["q"], t["new_k"], t["new_v"], t["slots"], t["kl"], t["bt"]]
+        return StepPlan(case=case, cfg=cfg, metric="shared-prefix KV GB/s", unit="GB/s",
+                        work=prefix_bytes + tail_bytes, scale=1e9, queries=rows, pre=[scatter, plan_call],
+                        dominant=dom, post=[], aux=aux,
+                        dom_label="shared_prefix_attention: one grouped tcgen05 tile launch (run + "
+                                  "tails of a group per CTA), HBM-bound",
+                        dom_work=prefix_bytes + tail_bytes + io_bytes, bound="hbm", peak=peak_hbm,
+                        peak_unit="GB/s", peak_src=f"{hbm_kind} hbm_gbs", h2d=(h2d_src, h2d_dst),
+                        d2h=d2h_src, launches=3, traffic_sources=ATTN_TC_SOURCES)
     raise ValueError(name)
 
 

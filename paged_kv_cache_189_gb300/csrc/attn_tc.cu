@@ -54,7 +54,8 @@ constexpr int kBarOff = kPOff + kTileBytes;
 constexpr int kNumBars = 1 + 2 * kKStages + 2 * kVStages + 2 + 2;
 constexpr int kTmemSlotOff = kBarOff + kNumBars * 8;
 constexpr int kFlagOff = kTmemSlotOff + 8;
-constexpr int kSmemBytes = kFlagOff + 16;
+constexpr int kXchOff = kFlagOff + 16;            // replicated rows: [2][4][32] maxima, [2][4][32] sums
+constexpr int kSmemBytes = kXchOff + 2 * 2 * 4 * 32 * 4;
 static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
 constexpr uint32_t kTmemCols = 512;     // S0 [0,128), S1 [128,256), O [256,384)
 constexpr float kLazyRescale = 8.0f;    // move the running max only past 2^8 growth
@@ -140,6 +141,21 @@ __device__ __forceinline__ void tmem_store32(uint32_t taddr, const uint32_t (&v)
         ::"r"(taddr), PKV_W8(0), PKV_W8(8), PKV_W8(16), PKV_W8(24) : "memory");
 }
 #undef PKV_W8
+
+// named barrier `id` over `count` threads that also returns the AND of `pred`
+__device__ __forceinline__ bool bar_and(int id, int count, bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 q, %1, 0;\n\t"
+        "bar.red.and.pred p, %2, %3, q;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(r) : "r"(static_cast<uint32_t>(pred)), "r"(id), "r"(count) : "memory");
+    return r != 0;
+}
+__device__ __forceinline__ void bar_sync_n(int id, int count) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
 
 // Shared-memory matrix descriptor: 128-byte swizzle, start address, leading
 // and stride byte offsets (all in 16-byte units), descriptor version 1.
@@ -281,11 +297,12 @@ __device__ __forceinline__ TileGeom group_geometry(const AttnParams& p, int TQ, 
     return g;
 }
 
-template <int G, bool GRP>
+template <int G, bool GRP, int REP>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                    const AttnParams p) {
-    constexpr int TQ = kTileM / G;
+    constexpr int ND = kTileM / REP;  // distinct rows of the tile (each held REP times)
+    constexpr int TQ = ND / G;
     extern __shared__ __align__(1024) uint8_t smem[];
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -303,7 +320,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         int* s_keyhi = reinterpret_cast<int*>(smem + kFlagOff + 8);
         if (threadIdx.x == 0) *s_keyhi = 0;
         __syncthreads();
-        if (threadIdx.x < kTileM) {
+        if (threadIdx.x < ND) {
             const GroupRow gr = group_row(p, g.b, grp_first, grp_count, g.t0 + threadIdx.x / G);
             if (gr.tok >= 0) atomicMax(s_keyhi, max(gr.a, gr.c));
         }
@@ -315,7 +332,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (g.nt == 0) {
         // no visible key in this split for any row of the tile: empty states
-        if (threadIdx.x < kTileM) {
+        if (threadIdx.x < ND) {
             const int r = threadIdx.x;
             int i = g.t0 + r / G;
             bool exists = i < g.nrows;
@@ -481,196 +498,496 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else {
         // ============================ softmax ===============================
-        const int r = threadIdx.x;             // tile row = tensor-memory lane
-        const int t = r / G, hg = r % G;
-        const int h = g.kvh * G + hg;
-        int i = g.t0 + t;                      // query row within the sequence (grouped: token)
-        bool row_exists = i < g.nrows;
-        int limit = 0;
-        int vis_a = 0, vis_b = 0, vis_c = 0;   // grouped: visible keys [0, a) u [b, c)
-        if constexpr (GRP) {
-            const GroupRow gr = group_row(p, g.b, grp_first, grp_count, i);
-            i = gr.tok;
-            row_exists = gr.tok >= 0;
-            vis_a = gr.a;
-            vis_b = gr.b;
-            vis_c = gr.c;
-        } else {
-            limit = row_exists ? visible_keys(i, g.qreal, g.kv_len, p.mask, max(p.causal_block, 1)) : 0;
-        }
-        // ---- Q tile -> swizzled shared memory (rows past the sequence: zeros)
-        {
-            const uint4* src = reinterpret_cast<const uint4*>(
-                static_cast<const __nv_bfloat16*>(p.q) + static_cast<int64_t>(g.r0 + i) * p.q_token_stride +
-                static_cast<int64_t>(h) * p.q_head_stride);
-#pragma unroll
-            for (int c = 0; c < 16; ++c) {
-                const uint4 v = row_exists ? src[c] : make_uint4(0u, 0u, 0u, 0u);
-                *reinterpret_cast<uint4*>(smem + kQOff + (c >> 3) * kHalfBytes +
-                                          sw128_offset(r, c & 7)) = v;
-            }
-            fence_proxy_async_smem();
-            mbar_arrive(q_ready);
-        }
-        const uint32_t lane_addr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
-        float m_used = -INFINITY;   // base-2 running maximum used for the exponentials
-        float l = 0.f, l_b = 0.f;
-        uint8_t* prow = smem + kPOff;
-        // warp-collective tensor-memory accesses follow every wait, so a wait
-        // counts as passed only if it passed in every lane of the warp
-        auto wait_warp = [&](uint64_t* bar, uint32_t parity) -> bool {
-            return __all_sync(0xffffffffu, wait(bar, parity));
-        };
-        // a warp none of whose rows sees a key (rows past the sequence, padding
-        // rows) writes zero probabilities and skips the softmax arithmetic
-        const bool warp_live = GRP || __any_sync(0xffffffffu, limit > 0);
-        for (int j = 0; j < g.nt; ++j) {
-            if (!wait_warp(&s_full[j & 1], (j >> 1) & 1)) break;
-            tc_fence_after();
-            uint32_t pk[kTileN / 2];
-            float alpha = 1.f;
-            bool live = warp_live;
+        if constexpr (REP == 1) {
+            const int r = threadIdx.x;             // tile row = tensor-memory lane
+            const int t = r / G, hg = r % G;
+            const int h = g.kvh * G + hg;
+            int i = g.t0 + t;                      // query row within the sequence (grouped: token)
+            bool row_exists = i < g.nrows;
+            int limit = 0;
+            int vis_a = 0, vis_b = 0, vis_c = 0;   // grouped: visible keys [0, a) u [b, c)
             if constexpr (GRP) {
-                // grouped rows see the shared run and their own tail: per key tile
-                const int k0 = g.kb + j * kTileN;
-                live = __any_sync(0xffffffffu, row_exists && (k0 < vis_a || (k0 < vis_c && k0 + kTileN > vis_b)));
-            }
-            if (live) {
-                const int key0 = g.kb + j * kTileN;
-                uint32_t sv[kTileN];  // raw scores of this row (f32 bits)
-                tmem_load128(lane_addr + (j & 1) * 128, sv);
-                if constexpr (GRP) {
-                    const int ta = vis_a - key0, tb = vis_b - key0, tc = vis_c - key0;
-                    if (!row_exists || !(ta >= kTileN || (tb <= 0 && tc >= kTileN))) {
-#pragma unroll
-                        for (int e = 0; e < kTileN; ++e)
-                            sv[e] = row_exists && (e < ta || (e >= tb && e < tc)) ? sv[e]
-                                                                                  : __float_as_uint(-INFINITY);
-                    }
-                } else {
-                    // keys at or past this row's visible limit are masked (diagonal tiles only)
-                    const int nvis = limit - key0;
-                    if (nvis < kTileN) {
-#pragma unroll
-                        for (int e = 0; e < kTileN; ++e)
-                            sv[e] = e < nvis ? sv[e] : __float_as_uint(-INFINITY);
-                    }
-                }
-                // row maximum of the raw scores (the scale is positive)
-                float mx = __uint_as_float(sv[0]);
-#pragma unroll
-                for (int e = 1; e + 1 < kTileN; e += 2)
-                    mx = fmaxf(mx, fmaxf(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])));
-                mx = fmaxf(mx, __uint_as_float(sv[kTileN - 1]));
-                mx *= p.scale_log2;
-                if (mx > m_used + kLazyRescale) {   // also true the first time a key is visible
-                    alpha = fast_exp2(m_used - mx);  // 0 when m_used was -inf
-                    m_used = mx;
-                }
-                const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
-                const float nm = m_used == -INFINITY ? 0.f : -m_used;
-                const float2 nm2 = make_float2(nm, nm);
-                float2 rs2 = make_float2(0.f, 0.f), rsb2 = make_float2(0.f, 0.f);
-#pragma unroll
-                for (int e = 0; e < kTileN; e += 2) {
-                    // exponent argument s * scale - m for two keys in one packed FMA
-                    const float2 xx = __ffma2_rn(make_float2(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])),
-                                                 sc2, nm2);
-                    const float2 pp = make_float2(fast_exp2(xx.x), fast_exp2(xx.y));
-                    pk[e / 2] = pack_bf16x2(pp.x, pp.y);
-                    rs2 = __fadd2_rn(rs2, pp);
-                    rsb2 = __fadd2_rn(rsb2, make_float2(bf16lo(pk[e / 2]), bf16hi(pk[e / 2])));
-                }
-                // O is normalised by the sum of the bf16 probabilities the P.V product
-                // used (numerator and denominator carry the same rounding); the LSE
-                // uses the sum of the unrounded ones
-                l = l * alpha + (rs2.x + rs2.y);
-                l_b = l_b * alpha + (rsb2.x + rsb2.y);
+                const GroupRow gr = group_row(p, g.b, grp_first, grp_count, i);
+                i = gr.tok;
+                row_exists = gr.tok >= 0;
+                vis_a = gr.a;
+                vis_b = gr.b;
+                vis_c = gr.c;
             } else {
-#pragma unroll
-                for (int e = 0; e < kTileN / 2; ++e) pk[e] = 0u;
+                limit = row_exists ? visible_keys(i, g.qreal, g.kv_len, p.mask, max(p.causal_block, 1)) : 0;
             }
-            // P buffer and O are free once the previous P.V finished
-            if (j > 0 && !wait_warp(p_free, (j - 1) & 1)) break;
-            tc_fence_after();
-            if (live && j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-                // O *= alpha for this row (warp-collective tensor-memory access)
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    uint32_t v[32];
-                    tmem_load32(lane_addr + 256 + c * 32, v);
-#pragma unroll
-                    for (int e = 0; e < 32; e += 2) {
-                        const float2 o2 = __fmul2_rn(make_float2(__uint_as_float(v[e]), __uint_as_float(v[e + 1])),
-                                                     make_float2(alpha, alpha));
-                        v[e] = __float_as_uint(o2.x);
-                        v[e + 1] = __float_as_uint(o2.y);
+            // ---- Q tile -> swizzled shared memory (rows past the sequence: zeros)
+            {
+                const uint4* src = reinterpret_cast<const uint4*>(
+                    static_cast<const __nv_bfloat16*>(p.q) + static_cast<int64_t>(g.r0 + i) * p.q_token_stride +
+                    static_cast<int64_t>(h) * p.q_head_stride);
+    #pragma unroll
+                for (int c = 0; c < 16; ++c) {
+                    const uint4 v = row_exists ? src[c] : make_uint4(0u, 0u, 0u, 0u);
+                    *reinterpret_cast<uint4*>(smem + kQOff + (c >> 3) * kHalfBytes +
+                                              sw128_offset(r, c & 7)) = v;
+                }
+                fence_proxy_async_smem();
+                mbar_arrive(q_ready);
+            }
+            const uint32_t lane_addr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+            float m_used = -INFINITY;   // base-2 running maximum used for the exponentials
+            float l = 0.f, l_b = 0.f;
+            uint8_t* prow = smem + kPOff;
+            // warp-collective tensor-memory accesses follow every wait, so a wait
+            // counts as passed only if it passed in every lane of the warp
+            auto wait_warp = [&](uint64_t* bar, uint32_t parity) -> bool {
+                return __all_sync(0xffffffffu, wait(bar, parity));
+            };
+            // a warp none of whose rows sees a key (rows past the sequence, padding
+            // rows) writes zero probabilities and skips the softmax arithmetic
+            const bool warp_live = GRP || __any_sync(0xffffffffu, limit > 0);
+            for (int j = 0; j < g.nt; ++j) {
+                if (!wait_warp(&s_full[j & 1], (j >> 1) & 1)) break;
+                tc_fence_after();
+                uint32_t pk[kTileN / 2];
+                float alpha = 1.f;
+                bool live = warp_live;
+                if constexpr (GRP) {
+                    // grouped rows see the shared run and their own tail: per key tile
+                    const int k0 = g.kb + j * kTileN;
+                    live = __any_sync(0xffffffffu, row_exists && (k0 < vis_a || (k0 < vis_c && k0 + kTileN > vis_b)));
+                }
+                if (live) {
+                    const int key0 = g.kb + j * kTileN;
+                    uint32_t sv[kTileN];  // raw scores of this row (f32 bits)
+                    tmem_load128(lane_addr + (j & 1) * 128, sv);
+                    if constexpr (GRP) {
+                        const int ta = vis_a - key0, tb = vis_b - key0, tc = vis_c - key0;
+                        if (!row_exists || !(ta >= kTileN || (tb <= 0 && tc >= kTileN))) {
+    #pragma unroll
+                            for (int e = 0; e < kTileN; ++e)
+                                sv[e] = row_exists && (e < ta || (e >= tb && e < tc)) ? sv[e]
+                                                                                      : __float_as_uint(-INFINITY);
+                        }
+                    } else {
+                        // keys at or past this row's visible limit are masked (diagonal tiles only)
+                        const int nvis = limit - key0;
+                        if (nvis < kTileN) {
+    #pragma unroll
+                            for (int e = 0; e < kTileN; ++e)
+                                sv[e] = e < nvis ? sv[e] : __float_as_uint(-INFINITY);
+                        }
                     }
-                    tmem_store32(lane_addr + 256 + c * 32, v);
+                    // row maximum of the raw scores (the scale is positive)
+                    float mx = __uint_as_float(sv[0]);
+    #pragma unroll
+                    for (int e = 1; e + 1 < kTileN; e += 2)
+                        mx = fmaxf(mx, fmaxf(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])));
+                    mx = fmaxf(mx, __uint_as_float(sv[kTileN - 1]));
+                    mx *= p.scale_log2;
+                    if (mx > m_used + kLazyRescale) {   // also true the first time a key is visible
+                        alpha = fast_exp2(m_used - mx);  // 0 when m_used was -inf
+                        m_used = mx;
+                    }
+                    const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
+                    const float nm = m_used == -INFINITY ? 0.f : -m_used;
+                    const float2 nm2 = make_float2(nm, nm);
+                    float2 rs2 = make_float2(0.f, 0.f), rsb2 = make_float2(0.f, 0.f);
+    #pragma unroll
+                    for (int e = 0; e < kTileN; e += 2) {
+                        // exponent argument s * scale - m for two keys in one packed FMA
+                        const float2 xx = __ffma2_rn(make_float2(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])),
+                                                     sc2, nm2);
+                        const float2 pp = make_float2(fast_exp2(xx.x), fast_exp2(xx.y));
+                        pk[e / 2] = pack_bf16x2(pp.x, pp.y);
+                        rs2 = __fadd2_rn(rs2, pp);
+                        rsb2 = __fadd2_rn(rsb2, make_float2(bf16lo(pk[e / 2]), bf16hi(pk[e / 2])));
+                    }
+                    // O is normalised by the sum of the bf16 probabilities the P.V product
+                    // used (numerator and denominator carry the same rounding); the LSE
+                    // uses the sum of the unrounded ones
+                    l = l * alpha + (rs2.x + rs2.y);
+                    l_b = l_b * alpha + (rsb2.x + rsb2.y);
+                } else {
+    #pragma unroll
+                    for (int e = 0; e < kTileN / 2; ++e) pk[e] = 0u;
                 }
-            }
-            const int key0 = g.kb + j * kTileN;
-            // P row -> shared memory, K-major 128-byte swizzle, two 64-key halves
-#pragma unroll
-            for (int c = 0; c < 16; ++c)
-                *reinterpret_cast<uint4*>(prow + (c >> 3) * kHalfBytes + sw128_offset(r, c & 7)) =
-                    make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-            // V rows of keys past the sequence's length inside its last page hold
-            // whatever the pool holds there; zero them so 0 * garbage cannot make NaN
-            if (key0 + kTileN > g.kv_len && g.kv_len > key0) {
-                const int vs = j % kVStages;
-                if (!wait_warp(&v_full[vs], (j / kVStages) & 1)) break;
-                const int first = g.kv_len - key0;
-                const int last = min(kTileN, (first + 31) / 32 * 32);
-                uint8_t* vt = smem + kVOff + vs * kTileBytes;
-                for (int idx = r; idx < (last - first) * 16; idx += kTileM) {
-                    const int row = first + idx / 16, c = idx % 16;
-                    *reinterpret_cast<uint4*>(vt + (c >> 3) * kHalfBytes + sw128_offset(row, c & 7)) =
-                        make_uint4(0u, 0u, 0u, 0u);
+                // P buffer and O are free once the previous P.V finished
+                if (j > 0 && !wait_warp(p_free, (j - 1) & 1)) break;
+                tc_fence_after();
+                if (live && j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+                    // O *= alpha for this row (warp-collective tensor-memory access)
+    #pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        uint32_t v[32];
+                        tmem_load32(lane_addr + 256 + c * 32, v);
+    #pragma unroll
+                        for (int e = 0; e < 32; e += 2) {
+                            const float2 o2 = __fmul2_rn(make_float2(__uint_as_float(v[e]), __uint_as_float(v[e + 1])),
+                                                         make_float2(alpha, alpha));
+                            v[e] = __float_as_uint(o2.x);
+                            v[e + 1] = __float_as_uint(o2.y);
+                        }
+                        tmem_store32(lane_addr + 256 + c * 32, v);
+                    }
                 }
-            }
-            if constexpr (GRP) {
-                // the rest of each member's last tail page is seen by no row: zero
-                // those V rows too (same reason)
-                bool any_gap = false;
-                for (int k = 0; k < grp_count; ++k) {
-                    const int m = p.grp_perm[grp_first + k];
-                    const int g0 = 32 * p.grp_tail_start[m] + p.grp_tail_lens[m];
-                    const int g1 = (g0 + 31) / 32 * 32;
-                    any_gap |= g0 < g1 && g0 < key0 + kTileN && g1 > key0;
-                }
-                if (any_gap) {
+                const int key0 = g.kb + j * kTileN;
+                // P row -> shared memory, K-major 128-byte swizzle, two 64-key halves
+    #pragma unroll
+                for (int c = 0; c < 16; ++c)
+                    *reinterpret_cast<uint4*>(prow + (c >> 3) * kHalfBytes + sw128_offset(r, c & 7)) =
+                        make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+                // V rows of keys past the sequence's length inside its last page hold
+                // whatever the pool holds there; zero them so 0 * garbage cannot make NaN
+                if (key0 + kTileN > g.kv_len && g.kv_len > key0) {
                     const int vs = j % kVStages;
                     if (!wait_warp(&v_full[vs], (j / kVStages) & 1)) break;
+                    const int first = g.kv_len - key0;
+                    const int last = min(kTileN, (first + 31) / 32 * 32);
                     uint8_t* vt = smem + kVOff + vs * kTileBytes;
+                    for (int idx = r; idx < (last - first) * 16; idx += kTileM) {
+                        const int row = first + idx / 16, c = idx % 16;
+                        *reinterpret_cast<uint4*>(vt + (c >> 3) * kHalfBytes + sw128_offset(row, c & 7)) =
+                            make_uint4(0u, 0u, 0u, 0u);
+                    }
+                }
+                if constexpr (GRP) {
+                    // the rest of each member's last tail page is seen by no row: zero
+                    // those V rows too (same reason)
+                    bool any_gap = false;
                     for (int k = 0; k < grp_count; ++k) {
                         const int m = p.grp_perm[grp_first + k];
                         const int g0 = 32 * p.grp_tail_start[m] + p.grp_tail_lens[m];
-                        const int lo = max(g0, key0) - key0, hi = min((g0 + 31) / 32 * 32, key0 + kTileN) - key0;
-                        for (int idx = r; idx < (hi - lo) * 16; idx += kTileM) {
-                            const int row = lo + idx / 16, c = idx % 16;
-                            *reinterpret_cast<uint4*>(vt + (c >> 3) * kHalfBytes + sw128_offset(row, c & 7)) =
-                                make_uint4(0u, 0u, 0u, 0u);
+                        const int g1 = (g0 + 31) / 32 * 32;
+                        any_gap |= g0 < g1 && g0 < key0 + kTileN && g1 > key0;
+                    }
+                    if (any_gap) {
+                        const int vs = j % kVStages;
+                        if (!wait_warp(&v_full[vs], (j / kVStages) & 1)) break;
+                        uint8_t* vt = smem + kVOff + vs * kTileBytes;
+                        for (int k = 0; k < grp_count; ++k) {
+                            const int m = p.grp_perm[grp_first + k];
+                            const int g0 = 32 * p.grp_tail_start[m] + p.grp_tail_lens[m];
+                            const int lo = max(g0, key0) - key0, hi = min((g0 + 31) / 32 * 32, key0 + kTileN) - key0;
+                            for (int idx = r; idx < (hi - lo) * 16; idx += kTileM) {
+                                const int row = lo + idx / 16, c = idx % 16;
+                                *reinterpret_cast<uint4*>(vt + (c >> 3) * kHalfBytes + sw128_offset(row, c & 7)) =
+                                    make_uint4(0u, 0u, 0u, 0u);
+                            }
                         }
                     }
                 }
+                fence_proxy_async_smem();
+                tc_fence_before();
+                mbar_arrive(p_full);
             }
-            fence_proxy_async_smem();
-            tc_fence_before();
-            mbar_arrive(p_full);
+            // ---- epilogue: O / l, 32 columns at a time
+            const bool ok = wait_warp(p_free, (g.nt - 1) & 1);
+            tc_fence_after();
+            const bool any = l > 0.f && l_b > 0.f;
+            const float inv_l = any ? 1.0f / l_b : 0.f;
+    #pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                uint32_t v[32];
+                tmem_load32(lane_addr + 256 + c * 32, v);
+                if (ok && row_exists) store_row_chunk(p, g, i, h, c, v, inv_l);
+            }
+            if (ok && row_exists) store_row_lse(p, g, i, h, any ? (m_used + __log2f(l)) * kLn2 : -INFINITY);
+        } else {
+            // The tile's ND distinct rows are held REP times: lane r holds distinct row
+            // dr = r % ND and, of every 128-key tile, the CW = 128 / REP key columns
+            // [part * CW, part * CW + CW), part = r / ND.  Its P row is zero outside
+            // them, so the REP copies of a row accumulate disjoint partial sums of O
+            // (all with the same running maximum, exchanged every key tile) that the
+            // epilogue adds.  REP = 1 is the plain one-row-per-lane tile.
+            constexpr int CW = kTileN / REP;
+            const int r = threadIdx.x;             // tensor-memory lane
+            const int dr = r % ND, part = r / ND;
+            const int t = dr / G, hg = dr % G;
+            const int h = g.kvh * G + hg;
+            int i = g.t0 + t;                      // query row within the sequence (grouped: token)
+            bool row_exists = i < g.nrows;
+            int limit = 0;
+            int vis_a = 0, vis_b = 0, vis_c = 0;   // grouped: visible keys [0, a) u [b, c)
+            if constexpr (GRP) {
+                const GroupRow gr = group_row(p, g.b, grp_first, grp_count, i);
+                i = gr.tok;
+                row_exists = gr.tok >= 0;
+                vis_a = gr.a;
+                vis_b = gr.b;
+                vis_c = gr.c;
+            } else {
+                limit = row_exists ? visible_keys(i, g.qreal, g.kv_len, p.mask, max(p.causal_block, 1)) : 0;
+            }
+            // ---- Q tile -> swizzled shared memory (rows past the sequence: zeros)
+            {
+                const uint4* src = reinterpret_cast<const uint4*>(
+                    static_cast<const __nv_bfloat16*>(p.q) + static_cast<int64_t>(g.r0 + i) * p.q_token_stride +
+                    static_cast<int64_t>(h) * p.q_head_stride);
+    #pragma unroll
+                for (int c = 0; c < 16; ++c) {
+                    const uint4 v = row_exists ? src[c] : make_uint4(0u, 0u, 0u, 0u);
+                    *reinterpret_cast<uint4*>(smem + kQOff + (c >> 3) * kHalfBytes +
+                                              sw128_offset(r, c & 7)) = v;
+                }
+                fence_proxy_async_smem();
+                mbar_arrive(q_ready);
+            }
+            const uint32_t lane_addr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+            float m_used = -INFINITY;   // base-2 running maximum used for the exponentials
+            float l = 0.f, l_b = 0.f;
+            uint8_t* prow = smem + kPOff;
+            float* xmax = reinterpret_cast<float*>(smem + kXchOff);  // [key tile parity][part][dr]
+            float* xsum = xmax + 2 * 4 * 32;                          // [l, l_b][part][dr]
+            // warp-collective tensor-memory accesses follow every wait, so a wait
+            // counts as passed only if it passed in every lane of the warp
+            auto wait_warp = [&](uint64_t* bar, uint32_t parity) -> bool {
+                return __all_sync(0xffffffffu, wait(bar, parity));
+            };
+            // a warp none of whose rows sees a key (rows past the sequence, padding
+            // rows) writes zero probabilities and skips the softmax arithmetic
+            const bool warp_live = GRP || __any_sync(0xffffffffu, limit > 0);
+            // with copies, the four warps exchange maxima every key tile; a failed
+            // wait is carried to the next exchange, where all of them leave together
+            bool ok_run = true;
+            for (int j = 0; j < g.nt; ++j) {
+                ok_run = ok_run && wait_warp(&s_full[j & 1], (j >> 1) & 1);
+                if (REP == 1 && !ok_run) break;
+                tc_fence_after();
+                const int key0 = g.kb + j * kTileN;
+                const int col0 = key0 + part * CW;  // first key of this lane's columns
+                bool live = warp_live;
+                if constexpr (GRP) {
+                    // grouped rows see the shared run and their own tail: per key tile
+                    live = __any_sync(0xffffffffu, row_exists && (key0 < vis_a || (key0 < vis_c && key0 + kTileN > vis_b)));
+                }
+                uint32_t pk[CW / 2];
+                float alpha = 1.f;
+                uint32_t sv[CW];  // raw scores of this row's columns (f32 bits)
+                float mx = -INFINITY;
+                if (ok_run && live) {
+                    if constexpr (CW == kTileN) {
+                        tmem_load128(lane_addr + (j & 1) * 128, sv);
+                    } else {
+    #pragma unroll
+                        for (int c = 0; c < CW / 32; ++c) {
+                            uint32_t v32[32];
+                            tmem_load32(lane_addr + (j & 1) * 128 + part * CW + c * 32, v32);
+    #pragma unroll
+                            for (int e = 0; e < 32; ++e) sv[c * 32 + e] = v32[e];
+                        }
+                    }
+                    if constexpr (GRP) {
+                        const int ta = vis_a - col0, tb = vis_b - col0, tc = vis_c - col0;
+                        if (!row_exists || !(ta >= CW || (tb <= 0 && tc >= CW))) {
+    #pragma unroll
+                            for (int e = 0; e < CW; ++e)
+                                sv[e] = row_exists && (e < ta || (e >= tb && e < tc)) ? sv[e]
+                                                                                      : __float_as_uint(-INFINITY);
+                        }
+                    } else {
+                        // keys at or past this row's visible limit are masked (diagonal tiles only)
+                        const int nvis = limit - col0;
+                        if (nvis < CW) {
+    #pragma unroll
+                            for (int e = 0; e < CW; ++e)
+                                sv[e] = e < nvis ? sv[e] : __float_as_uint(-INFINITY);
+                        }
+                    }
+                    // row maximum of the raw scores (the scale is positive)
+                    mx = __uint_as_float(sv[0]);
+    #pragma unroll
+                    for (int e = 1; e + 1 < CW; e += 2)
+                        mx = fmaxf(mx, fmaxf(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])));
+                    mx = fmaxf(mx, __uint_as_float(sv[CW - 1]));
+                }
+                if constexpr (REP > 1) {
+                    xmax[((j & 1) * REP + part) * ND + dr] = mx;
+                    if (!bar_and(1, kTileM, ok_run)) break;
+                    mx = -INFINITY;
+    #pragma unroll
+                    for (int q = 0; q < REP; ++q) mx = fmaxf(mx, xmax[((j & 1) * REP + q) * ND + dr]);
+                }
+                if (ok_run && live) {
+                    mx *= p.scale_log2;
+                    if (mx > m_used + kLazyRescale) {   // also true the first time a key is visible
+                        alpha = fast_exp2(m_used - mx);  // 0 when m_used was -inf
+                        m_used = mx;
+                    }
+                    const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
+                    const float nm = m_used == -INFINITY ? 0.f : -m_used;
+                    const float2 nm2 = make_float2(nm, nm);
+                    float2 rs2 = make_float2(0.f, 0.f), rsb2 = make_float2(0.f, 0.f);
+    #pragma unroll
+                    for (int e = 0; e < CW; e += 2) {
+                        // exponent argument s * scale - m for two keys in one packed FMA
+                        const float2 xx = __ffma2_rn(make_float2(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])),
+                                                     sc2, nm2);
+                        const float2 pp = make_float2(fast_exp2(xx.x), fast_exp2(xx.y));
+                        pk[e / 2] = pack_bf16x2(pp.x, pp.y);
+                        rs2 = __fadd2_rn(rs2, pp);
+                        rsb2 = __fadd2_rn(rsb2, make_float2(bf16lo(pk[e / 2]), bf16hi(pk[e / 2])));
+                    }
+                    // O is normalised by the sum of the bf16 probabilities the P.V product
+                    // used (numerator and denominator carry the same rounding); the LSE
+                    // uses the sum of the unrounded ones
+                    l = l * alpha + (rs2.x + rs2.y);
+                    l_b = l_b * alpha + (rsb2.x + rsb2.y);
+                } else {
+    #pragma unroll
+                    for (int e = 0; e < CW / 2; ++e) pk[e] = 0u;
+                }
+                // P buffer and O are free once the previous P.V finished
+                if (j > 0) ok_run = ok_run && wait_warp(p_free, (j - 1) & 1);
+                if (REP == 1 && !ok_run) break;
+                tc_fence_after();
+                if (ok_run) {
+                    if (live && j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+                        // O *= alpha for this row (warp-collective tensor-memory access)
+    #pragma unroll
+                        for (int c = 0; c < 4; ++c) {
+                            uint32_t v[32];
+                            tmem_load32(lane_addr + 256 + c * 32, v);
+    #pragma unroll
+                            for (int e = 0; e < 32; e += 2) {
+                                const float2 o2 = __fmul2_rn(make_float2(__uint_as_float(v[e]), __uint_as_float(v[e + 1])),
+                                                             make_float2(alpha, alpha));
+                                v[e] = __float_as_uint(o2.x);
+                                v[e + 1] = __float_as_uint(o2.y);
+                            }
+                            tmem_store32(lane_addr + 256 + c * 32, v);
+                        }
+                    }
+                    // P row -> shared memory, K-major 128-byte swizzle, two 64-key halves;
+                    // 16-byte chunk c holds keys [8c, 8c + 8): this lane's chunks from pk,
+                    // the others zero
+    #pragma unroll
+                    for (int cc = 0; cc < CW / 8; ++cc) {
+                        const int c = part * (CW / 8) + cc;
+                        *reinterpret_cast<uint4*>(prow + (c >> 3) * kHalfBytes + sw128_offset(r, c & 7)) =
+                            make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
+                    }
+                    if constexpr (REP > 1) {
+    #pragma unroll
+                        for (int c = 0; c < 16; ++c)
+                            if (c / (CW / 8) != part)
+                                *reinterpret_cast<uint4*>(prow + (c >> 3) * kHalfBytes + sw128_offset(r, c & 7)) =
+                                    make_uint4(0u, 0u, 0u, 0u);
+                    }
+                    // V rows of keys past the sequence's length inside its last page hold
+                    // whatever the pool holds there; zero them so 0 * garbage cannot make NaN
+                    if (key0 + kTileN > g.kv_len && g.kv_len > key0) {
+                        const int vs = j % kVStages;
+                        ok_run = ok_run && wait_warp(&v_full[vs], (j / kVStages) & 1);
+                        if (REP == 1 && !ok_run) break;
+                        if (ok_run) {
+                            const int first = g.kv_len - key0;
+                            const int last = min(kTileN, (first + 31) / 32 * 32);
+                            uint8_t* vt = smem + kVOff + vs * kTileBytes;
+                            for (int idx = r; idx < (last - first) * 16; idx += kTileM) {
+                                const int row = first + idx / 16, c = idx % 16;
+                                *reinterpret_cast<uint4*>(vt + (c >> 3) * kHalfBytes + sw128_offset(row, c & 7)) =
+                                    make_uint4(0u, 0u, 0u, 0u);
+                            }
+                        }
+                    }
+                    if constexpr (GRP) {
+                        // the rest of each member's last tail page is seen by no row: zero
+                        // those V rows too (same reason)
+                        bool any_gap = false;
+                        for (int k = 0; k < grp_count; ++k) {
+                            const int m = p.grp_perm[grp_first + k];
+                            const int g0 = 32 * p.grp_tail_start[m] + p.grp_tail_lens[m];
+                            const int g1 = (g0 + 31) / 32 * 32;
+                            any_gap |= g0 < g1 && g0 < key0 + kTileN && g1 > key0;
+                        }
+                        if (any_gap) {
+                            const int vs = j % kVStages;
+                            ok_run = ok_run && wait_warp(&v_full[vs], (j / kVStages) & 1);
+                            if (REP == 1 && !ok_run) break;
+                            uint8_t* vt = smem + kVOff + vs * kTileBytes;
+                            for (int k = 0; ok_run && k < grp_count; ++k) {
+                                const int m = p.grp_perm[grp_first + k];
+                                const int g0 = 32 * p.grp_tail_start[m] + p.grp_tail_lens[m];
+                                const int lo = max(g0, key0) - key0, hi = min((g0 + 31) / 32 * 32, key0 + kTileN) - key0;
+                                for (int idx = r; idx < (hi - lo) * 16; idx += kTileM) {
+                                    const int row = lo + idx / 16, c = idx % 16;
+                                    *reinterpret_cast<uint4*>(vt + (c >> 3) * kHalfBytes + sw128_offset(row, c & 7)) =
+                                        make_uint4(0u, 0u, 0u, 0u);
+                                }
+                            }
+                        }
+                    }
+                    fence_proxy_async_smem();
+                    tc_fence_before();
+                    mbar_arrive(p_full);
+                }
+            }
+            // ---- epilogue: O / l, 32 columns at a time
+            const bool ok = ok_run && wait_warp(p_free, (g.nt - 1) & 1);
+            tc_fence_after();
+            if constexpr (REP == 1) {
+                const bool any = l > 0.f && l_b > 0.f;
+                const float inv_l = any ? 1.0f / l_b : 0.f;
+    #pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t v[32];
+                    tmem_load32(lane_addr + 256 + c * 32, v);
+                    if (ok && row_exists) store_row_chunk(p, g, i, h, c, v, inv_l);
+                }
+                if (ok && row_exists) store_row_lse(p, g, i, h, any ? (m_used + __log2f(l)) * kLn2 : -INFINITY);
+            } else {
+                // the copies' partial sums: l and l_b through the exchange area, O rows
+                // through the K ring (drained: every K tile was consumed by an S that
+                // finished before the last P.V); float4 q of a row sits at slot
+                // (q + dr) mod 32 so that a warp's stores spread over the banks
+                float4* obuf = reinterpret_cast<float4*>(smem + kKOff);
+                xsum[(0 * REP + part) * ND + dr] = l;
+                xsum[(1 * REP + part) * ND + dr] = l_b;
+    #pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t v[32];
+                    tmem_load32(lane_addr + 256 + c * 32, v);
+    #pragma unroll
+                    for (int k = 0; k < 8; ++k) {
+                        const int q = c * 8 + k;
+                        obuf[(part * ND + dr) * 32 + ((q + dr) & 31)] =
+                            make_float4(__uint_as_float(v[4 * k]), __uint_as_float(v[4 * k + 1]),
+                                        __uint_as_float(v[4 * k + 2]), __uint_as_float(v[4 * k + 3]));
+                    }
+                }
+                bar_sync_n(1, kTileM);
+                float lt = 0.f, lbt = 0.f;
+    #pragma unroll
+                for (int q = 0; q < REP; ++q) {
+                    lt += xsum[(0 * REP + q) * ND + dr];
+                    lbt += xsum[(1 * REP + q) * ND + dr];
+                }
+                const bool any = lt > 0.f && lbt > 0.f;
+                const float inv_l = any ? 1.0f / lbt : 0.f;
+                // this lane adds up the copies' columns [part * CW, part * CW + CW) of its row
+    #pragma unroll
+                for (int cc = 0; cc < CW / 32; ++cc) {
+                    uint32_t v[32];
+    #pragma unroll
+                    for (int k = 0; k < 8; ++k) {
+                        const int q = (part * CW / 32 + cc) * 8 + k;
+                        float4 a4 = make_float4(0.f, 0.f, 0.f, 0.f);
+    #pragma unroll
+                        for (int c2 = 0; c2 < REP; ++c2) {
+                            const float4 b4 = obuf[(c2 * ND + dr) * 32 + ((q + dr) & 31)];
+                            a4.x += b4.x;
+                            a4.y += b4.y;
+                            a4.z += b4.z;
+                            a4.w += b4.w;
+                        }
+                        v[4 * k] = __float_as_uint(a4.x);
+                        v[4 * k + 1] = __float_as_uint(a4.y);
+                        v[4 * k + 2] = __float_as_uint(a4.z);
+                        v[4 * k + 3] = __float_as_uint(a4.w);
+                    }
+                    if (ok && row_exists) store_row_chunk(p, g, i, h, part * (CW / 32) + cc, v, inv_l);
+                }
+                if (ok && row_exists && part == 0)
+                    store_row_lse(p, g, i, h, any ? (m_used + __log2f(lt)) * kLn2 : -INFINITY);
+            }
         }
-        // ---- epilogue: O / l, 32 columns at a time
-        const bool ok = wait_warp(p_free, (g.nt - 1) & 1);
-        tc_fence_after();
-        const bool any = l > 0.f && l_b > 0.f;
-        const float inv_l = any ? 1.0f / l_b : 0.f;
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            uint32_t v[32];
-            tmem_load32(lane_addr + 256 + c * 32, v);
-            if (ok && row_exists) store_row_chunk(p, g, i, h, c, v, inv_l);
-        }
-        if (ok && row_exists) store_row_lse(p, g, i, h, any ? (m_used + __log2f(l)) * kLn2 : -INFINITY);
     }
 
     tc_fence_before();
@@ -737,20 +1054,6 @@ constexpr int kFlag2Off = kTmemSlot2Off + 8;
 constexpr int kSmemBytes2 = kFlag2Off + 16;
 static_assert(kSmemBytes2 <= 227 * 1024, "shared memory per CTA");
 
-// named barrier `id` over `count` threads that also returns the AND of `pred`
-__device__ __forceinline__ bool bar_and(int id, int count, bool pred) {
-    uint32_t r;
-    asm volatile(
-        "{\n\t.reg .pred p, q;\n\t"
-        "setp.ne.u32 q, %1, 0;\n\t"
-        "bar.red.and.pred p, %2, %3, q;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(r) : "r"(static_cast<uint32_t>(pred)), "r"(id), "r"(count) : "memory");
-    return r != 0;
-}
-__device__ __forceinline__ void bar_sync_n(int id, int count) {
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
-}
 
 template <int G>
 __global__ void __maxnreg__(96)
@@ -1148,28 +1451,35 @@ cudaError_t launch_g2(const AttnParams& p, const void* tk, const void* tv, cudaS
     return cudaGetLastError();
 }
 
-template <int G>
-cudaError_t launch_grp(const AttnParams& p, const void* tk, const void* tv, cudaStream_t s) {
-    auto kern = attn_tc_kernel<G, true>;
+// One-tile launches: when a tile's rows (query rows x grouped heads) fit in
+// one 32-lane quadrant, they are held four times and each warp takes a
+// quarter of every key tile's columns.
+template <int G, bool GRP, int REP>
+cudaError_t launch_one(const AttnParams& p, int rows, const void* tk, const void* tv, cudaStream_t s) {
+    auto kern = attn_tc_kernel<G, GRP, REP>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return e;
-    const int TQ = kTileM / G;
-    dim3 grid((p.grp_max_tokens + TQ - 1) / TQ, p.num_kv_heads, p.batch * p.num_splits);
+    const int TQ = kTileM / (G * REP);
+    dim3 grid((rows + TQ - 1) / TQ, p.num_kv_heads, p.batch * p.num_splits);
     kern<<<grid, kThreads, kSmemBytes, s>>>(*static_cast<const CUtensorMap*>(tk),
                                             *static_cast<const CUtensorMap*>(tv), p);
     return cudaGetLastError();
 }
 
+template <int G, bool GRP>
+cudaError_t launch_one_rep(const AttnParams& p, int rows, const void* tk, const void* tv, cudaStream_t s) {
+    if (rows * G <= kTileM / 4) return launch_one<G, GRP, 4>(p, rows, tk, tv, s);
+    return launch_one<G, GRP, 1>(p, rows, tk, tv, s);
+}
+
+template <int G>
+cudaError_t launch_grp(const AttnParams& p, const void* tk, const void* tv, cudaStream_t s) {
+    return launch_one_rep<G, true>(p, p.grp_max_tokens, tk, tv, s);
+}
+
 template <int G>
 cudaError_t launch_g(const AttnParams& p, const void* tk, const void* tv, cudaStream_t s) {
-    auto kern = attn_tc_kernel<G, false>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-    if (e != cudaSuccess) return e;
-    const int TQ = kTileM / G;
-    dim3 grid((p.max_q_rows + TQ - 1) / TQ, p.num_kv_heads, p.batch * p.num_splits);
-    kern<<<grid, kThreads, kSmemBytes, s>>>(*static_cast<const CUtensorMap*>(tk),
-                                            *static_cast<const CUtensorMap*>(tv), p);
-    return cudaGetLastError();
+    return launch_one_rep<G, false>(p, p.max_q_rows, tk, tv, s);
 }
 
 }  // namespace

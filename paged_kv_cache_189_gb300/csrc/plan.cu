@@ -20,8 +20,10 @@
 //    alone;
 //  * group row = the run, then each member's tail pages in member order; a
 //    row's tail = its keys past the run.
-// Single CTA (B <= 1024): the batch-wide rank and offset computations are
-// block scans in shared memory; the pairwise passes are O(B^2 / threads).
+// One CTA (B <= 1024) computes the grouping: the batch-wide ranks and offsets
+// are block scans in shared memory, the leader search O(B^2 / threads) in
+// shared memory, the common-prefix scan one thread per (member, page) pair.
+// A second kernel writes the group rows, one CTA per group slot.
 #include "pkv_common.cuh"
 #include "pkv_internal.h"
 
@@ -31,20 +33,31 @@ namespace {
 constexpr int kPP = 32;
 constexpr int kMaxRows = 1024;
 
-// exclusive prefix sum of v over the first n threads' values (n <= blockDim)
+// exclusive prefix sum of every thread's v in thread order: shuffle scans
+// inside each warp, then over the warps' totals (buf: 32 ints)
 __device__ int block_exclusive_scan(int v, int* buf) {
-    const int t = threadIdx.x;
-    buf[t] = v;
-    __syncthreads();
-    for (int off = 1; off < blockDim.x; off <<= 1) {
-        const int add = t >= off ? buf[t - off] : 0;
-        __syncthreads();
-        buf[t] += add;
-        __syncthreads();
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
     }
-    const int incl = buf[t];
+    if (lane == 31) buf[warp] = x;
     __syncthreads();
-    return incl - v;
+    if (warp == 0) {
+        int w = lane < (blockDim.x >> 5) ? buf[lane] : 0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, w, o);
+            if (lane >= o) w += y;
+        }
+        buf[lane] = w;
+    }
+    __syncthreads();
+    const int res = (warp > 0 ? buf[warp - 1] : 0) + x - v;
+    __syncthreads();  // buf is reused by the next scan
+    return res;
 }
 
 __global__ void __launch_bounds__(kMaxRows) plan_kernel(PlanArgs a) {
@@ -74,30 +87,71 @@ __global__ void __launch_bounds__(kMaxRows) plan_kernel(PlanArgs a) {
         s_size[r] = 0;
     }
     __syncthreads();
-    // leaders
-    int leader = r;
-    if (row && cp >= 1) {
-        const int f = s_first[r];
-        for (int r2 = 0; r2 < r; ++r2) {
-            if (s_cp[r2] >= 1 && s_first[r2] == f) {
-                leader = r2;
-                break;
+    // leaders: one warp per row, its lanes test 32 earlier rows per step (ballot)
+    const int warp = r >> 5, lane = r & 31, nwarps = blockDim.x >> 5;
+    for (int rr = warp; rr < B; rr += nwarps) {
+        int ld = rr;
+        if (s_cp[rr] >= 1) {
+            const int f = s_first[rr];
+            for (int b0 = 0; b0 < rr; b0 += 32) {
+                const int r2 = b0 + lane;
+                const unsigned bal = __ballot_sync(0xffffffffu, r2 < rr && s_cp[r2] >= 1 && s_first[r2] == f);
+                if (bal) {
+                    ld = b0 + __ffs(bal) - 1;
+                    break;
+                }
             }
         }
-    }
-    if (row) {
-        s_leader[r] = leader;
-        atomicAdd(&s_size[leader], 1);
-        if (leader == r) s_run[r] = cp;
+        if (lane == 0) {
+            s_leader[rr] = ld;
+            atomicAdd(&s_size[ld], 1);
+            if (ld == rr) s_run[rr] = s_cp[rr];
+        }
     }
     __syncthreads();
-    // shared run: every member lowers its leader's run to their common prefix
-    if (row && leader != r) {
-        const int32_t* lrow = a.block_table + static_cast<int64_t>(leader) * a.block_table_stride;
-        const int lim = min(cp, s_cp[leader]);
-        int p = 0;
-        while (p < lim && trow[p] == lrow[p]) ++p;
-        atomicMin(&s_run[leader], p);
+    const int leader = row ? s_leader[r] : r;
+    // shared run: every member lowers its leader's run to the first page where
+    // they differ; one thread per (member, page) pair over the batch (offsets of
+    // each row's pairs by a block scan), every load independent
+    {
+        int npairs = 0;
+        if (row && leader != r) {
+            npairs = min(cp, s_cp[leader]);
+            atomicMin(&s_run[leader], cp);  // never past a member's new tokens
+        }
+        const int off = block_exclusive_scan(npairs, s_scan);
+        s_tp[r] = row ? off : 0;            // scratch: first pair of row r
+        __shared__ int s_total_pairs;
+        if (r == blockDim.x - 1) s_total_pairs = off + npairs;
+        __syncthreads();
+        const int total = s_total_pairs;
+        // 8 pairs per thread per round: all 16 loads issued before any compare
+        for (int f0 = r; f0 < total; f0 += 8 * blockDim.x) {
+            int32_t va[8], vb[8];
+            int pg[8], ld[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const int f = f0 + k * blockDim.x;
+                va[k] = vb[k] = 0;
+                pg[k] = -1;
+                ld[k] = 0;
+                if (f < total) {
+                    // the row whose pairs hold f: last row with start <= f (binary search)
+                    int lo = 0, hi = B - 1;
+                    while (lo < hi) {
+                        const int mid = (lo + hi + 1) >> 1;
+                        if (s_tp[mid] <= f) lo = mid; else hi = mid - 1;
+                    }
+                    pg[k] = f - s_tp[lo];
+                    ld[k] = s_leader[lo];
+                    va[k] = a.block_table[static_cast<int64_t>(lo) * a.block_table_stride + pg[k]];
+                    vb[k] = a.block_table[static_cast<int64_t>(ld[k]) * a.block_table_stride + pg[k]];
+                }
+            }
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+                if (pg[k] >= 0 && va[k] != vb[k]) atomicMin(&s_run[ld[k]], pg[k]);
+        }
     }
     __syncthreads();
     if (row && leader == r && s_size[r] < 2) s_run[r] = 0;
@@ -115,14 +169,31 @@ __global__ void __launch_bounds__(kMaxRows) plan_kernel(PlanArgs a) {
         s_tp[r] = tail_pages;
     }
     __syncthreads();
+    // position among the group's members and tail start: one warp per row sums
+    // the earlier members' tail pages 32 rows per step
+    __shared__ int s_pos[kMaxRows], s_tstart[kMaxRows];
+    for (int rr = warp; rr < B; rr += nwarps) {
+        const int ld = s_leader[rr];
+        int cnt = 0, pages = 0;
+        for (int b0 = 0; b0 < rr; b0 += 32) {
+            const int r2 = b0 + lane;
+            const bool same = r2 < rr && s_leader[r2] == ld;
+            cnt += __popc(__ballot_sync(0xffffffffu, same));
+            int v = same ? s_tp[r2] : 0;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+            pages += v;
+        }
+        if (lane == 0) {
+            s_pos[rr] = cnt;
+            s_tstart[rr] = s_run[ld] + pages;
+        }
+    }
+    __syncthreads();
     int tail_start = run;
     if (row) {
-        for (int r2 = 0; r2 < r; ++r2) {
-            if (s_leader[r2] == leader) {
-                ++pos;
-                tail_start += s_tp[r2];
-            }
-        }
+        pos = s_pos[r];
+        tail_start = s_tstart[r];
     }
     // group index and offsets (scans over leader flags / sizes in row order)
     const bool is_leader = row && leader == r;
@@ -149,38 +220,73 @@ __global__ void __launch_bounds__(kMaxRows) plan_kernel(PlanArgs a) {
         a.perm[s_goff[leader] + pos] = r;
         a.tail_start[r] = tail_start;
         a.tail_lens[r] = tail_len;
-        int32_t* grow = a.group_rows + static_cast<int64_t>(g) * a.group_row_stride;
         if (is_leader) {
             a.run_lens[g] = run * kPP;
             a.group_indptr[g] = s_goff[r];
-            for (int p = 0; p < run && p < a.group_row_stride; ++p) grow[p] = trow[p];
         }
         if (tail_start + tail_pages > a.group_row_stride) set_err(a.err, PKV_ERRBIT_LEN);
-        for (int i = 0; i < tail_pages && tail_start + i < a.group_row_stride; ++i)
-            grow[tail_start + i] = trow[run + i];
     }
     // unused group slots; group_indptr[g] = B from the group count on
     for (int g = ngroups + r; g <= B; g += blockDim.x) {
         if (g < B) a.run_lens[g] = 0;
         a.group_indptr[g] = B;
     }
-    // the last member of each group knows where its group's pages end
-    if (row) {
-        bool last = true;
-        for (int r2 = r + 1; r2 < B; ++r2) {
-            if (s_leader[r2] == leader) {
-                last = false;
-                break;
-            }
-        }
-        if (last) {
-            int32_t* grow = a.group_rows + static_cast<int64_t>(s_gidx[leader]) * a.group_row_stride;
-            for (int64_t p = tail_start + tail_pages; p < a.group_row_stride; ++p) grow[p] = -1;
+}
+
+// One CTA per group slot: the slot's row (the run from its first member, every
+// member's tail pages at its tail start, -1 after), written from the plan's
+// outputs; a slot past the number of groups gets -1 throughout.
+__global__ void __launch_bounds__(256) plan_rows_kernel(PlanArgs a) {
+    const int g = blockIdx.x;
+    const int64_t stride = a.group_row_stride;
+    int32_t* grow = a.group_rows + static_cast<int64_t>(g) * stride;
+    const int ngroups = *a.num_groups;
+    // the group's members (row, tail start) in shared memory; then every entry of
+    // the row is one independent load: the run from the first member, a tail
+    // page from the member whose tail covers it, or -1
+    __shared__ int s_m[kMaxRows], s_ts[kMaxRows];
+    __shared__ int s_n, s_run, s_end;
+    if (threadIdx.x == 0) {
+        s_n = 0;
+        s_run = 0;
+        s_end = 0;
+        if (g < ngroups) {
+            const int first = a.group_indptr[g], last = a.group_indptr[g + 1];
+            s_n = min(last - first, kMaxRows);
+            s_run = a.run_lens[g] / kPP;
         }
     }
-    for (int64_t i = static_cast<int64_t>(ngroups) * a.group_row_stride + r;
-         i < static_cast<int64_t>(B) * a.group_row_stride; i += blockDim.x)
-        a.group_rows[i] = -1;
+    __syncthreads();
+    const int n = s_n, run = s_run;
+    if (g < ngroups) {
+        const int first = a.group_indptr[g];
+        for (int k = threadIdx.x; k < n; k += blockDim.x) {
+            const int m = a.perm[first + k];
+            s_m[k] = m;
+            s_ts[k] = a.tail_start[m];
+            if (k == n - 1) {
+                const int tp = min((a.tail_lens[m] + kPP - 1) / kPP, max(a.max_pages - run, 0));
+                s_end = a.tail_start[m] + tp;
+            }
+        }
+    }
+    __syncthreads();
+    const int64_t end = s_end < stride ? s_end : stride;
+    const int32_t* lrow = n > 0 ? a.block_table + static_cast<int64_t>(s_m[0]) * a.block_table_stride : nullptr;
+    for (int64_t p = threadIdx.x; p < stride; p += blockDim.x) {
+        int32_t v = -1;
+        if (p < run) {
+            v = lrow[p];
+        } else if (p < end) {
+            int lo = 0, hi = n - 1;  // last member whose tail starts at or before p
+            while (lo < hi) {
+                const int mid = (lo + hi + 1) >> 1;
+                if (s_ts[mid] <= p) lo = mid; else hi = mid - 1;
+            }
+            v = a.block_table[static_cast<int64_t>(s_m[lo]) * a.block_table_stride + run + (p - s_ts[lo])];
+        }
+        grow[p] = v;
+    }
 }
 
 }  // namespace
@@ -188,6 +294,9 @@ __global__ void __launch_bounds__(kMaxRows) plan_kernel(PlanArgs a) {
 cudaError_t launch_plan(const PlanArgs& a, cudaStream_t s) {
     if (a.batch == 0) return cudaSuccess;
     plan_kernel<<<1, kMaxRows, 0, s>>>(a);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    plan_rows_kernel<<<a.batch, 256, 0, s>>>(a);
     return cudaGetLastError();
 }
 

@@ -141,3 +141,25 @@ def test_causal_layout_host_validation(L):
     assert lay(cur_cap=4 * 62 - 1) == pkv.PKV_ERR_INVALID_ARG
     assert lay(row_stride=0) == pkv.PKV_ERR_INVALID_ARG
     assert lay(pin=2 ** 31, window=1) == pkv.PKV_ERR_UNSUPPORTED
+
+
+def test_plan_and_shared_prefix_host_validation(L):
+    def plan(batch=8, max_pages=4, stride_bt=4, stride_out=16, table=FAKE):
+        return L.plan_shared_prefix(table, stride_bt, FAKE, FAKE, batch, max_pages, FAKE, stride_out, FAKE,
+                                    FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, None)
+    assert plan(batch=0, table=None) == pkv.PKV_OK
+    assert plan(batch=1025) == pkv.PKV_ERR_UNSUPPORTED
+    assert plan(table=None) == pkv.PKV_ERR_INVALID_ARG
+    assert plan(stride_bt=3) == pkv.PKV_ERR_INVALID_ARG      # table narrower than max_pages
+    assert plan(stride_out=0) == pkv.PKV_ERR_INVALID_ARG
+
+    def spa(D=128, Hq=32, Hkv=8, page=32, out=FAKE, row_stride=64, max_keys=2048, ws=None, ws_bytes=0):
+        return L.shared_prefix_attention(FAKE, 4096, 128, FAKE, FAKE, 100, page, 32 * Hkv * 128, FAKE, row_stride,
+                                         FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 16, 1, 8, max_keys, Hq, Hkv, D,
+                                         0.0, out, pkv.PKV_BF16, None, ws, ws_bytes, 0, 0, None, None)
+    assert spa(D=64) == pkv.PKV_ERR_UNSUPPORTED              # tensor-core tiles: head_dim 128
+    assert spa(Hq=24) == pkv.PKV_ERR_UNSUPPORTED             # group of 3
+    assert spa(page=16) == pkv.PKV_ERR_UNSUPPORTED
+    assert spa(out=None) == pkv.PKV_ERR_INVALID_ARG
+    assert spa(row_stride=63) == pkv.PKV_ERR_INVALID_ARG     # row narrower than max_group_keys
+    assert pkv.shared_prefix_attention_workspace_size(16, 1, 8, 2048, 32, 8, 128) >= 0
