@@ -20,8 +20,10 @@
 //    mask, online softmax in base 2 with a lazily moved maximum, write P as
 //    bf16 into shared memory in the MMA's K-major swizzled layout, rescale O
 //    in tensor memory when the maximum moved; finally normalise O and store it.
-//  * warp 4 lane 0 (producer): TMA loads of K pages (3-stage ring) and V
-//    pages (2-stage ring), 4 pages x 2 column halves per 128-key tile, through
+//  * warp 4 lane 0 (producer): TMA loads of K pages (2-stage ring) and V
+//    pages (3-stage ring: V of tile j + 3 can only start once P.V of tile j
+//    finished, so the deeper ring goes to V), 4 pages x 2 column halves per
+//    128-key tile, through
 //    the block table; pages past the sequence are read out of bounds, which
 //    TMA fills with zeros.
 //  * warp 5 (MMA): allocates 512 tensor-memory columns (two S buffers and O),
@@ -40,8 +42,8 @@ namespace {
 constexpr int kD = 128;                 // head dim handled here
 constexpr int kTileM = 128;             // query rows per tile (tensor-memory lanes)
 constexpr int kTileN = 128;             // keys per tile
-constexpr int kKStages = 3;
-constexpr int kVStages = 2;
+constexpr int kKStages = 2;
+constexpr int kVStages = 3;
 constexpr int kThreads = 192;
 constexpr int kHalfBytes = kTileM * 128;           // 128 rows x 64 bf16 = 16 KiB
 constexpr int kTileBytes = 2 * kHalfBytes;         // 128 x 128 bf16 = 32 KiB
@@ -50,7 +52,7 @@ constexpr int kKOff = kQOff + kTileBytes;
 constexpr int kVOff = kKOff + kKStages * kTileBytes;
 constexpr int kPOff = kVOff + kVStages * kTileBytes;
 constexpr int kBarOff = kPOff + kTileBytes;
-// barriers: q_ready, k_full[3], k_empty[3], v_full[2], v_empty[2], s_full[2], p_full, p_free
+// barriers: q_ready, k_full[2], k_empty[2], v_full[3], v_empty[3], s_full[2], p_full, p_free
 constexpr int kNumBars = 1 + 2 * kKStages + 2 * kVStages + 2 + 2;
 constexpr int kTmemSlotOff = kBarOff + kNumBars * 8;
 constexpr int kFlagOff = kTmemSlotOff + 8;
@@ -1000,7 +1002,7 @@ constexpr int kQ2Off = 0;                                   // Q_A, Q_B
 constexpr int kK2Off = kQ2Off + 2 * kTileBytes;
 constexpr int kV2Off = kK2Off + kKStages * kTileBytes;
 constexpr int kBar2Off = kV2Off + kVStages * kTileBytes;
-// barriers: q_ready, k_full[3], k_empty[3], v_full[2], v_empty[2], s_full[2], p_full[2], o_full[2]
+// barriers: q_ready, k_full[2], k_empty[2], v_full[3], v_empty[3], s_full[2], p_full[2], o_full[2]
 constexpr int kNumBars2 = 1 + 2 * kKStages + 2 * kVStages + 6;
 
 #define PKV_W4(i) "r"(v[i + 0]), "r"(v[i + 1]), "r"(v[i + 2]), "r"(v[i + 3])
