@@ -477,12 +477,13 @@ def build_plan(name, rank, dev, stream):
     peak_hbm, hbm_kind = measured_peaks()
     peak_tc, tc_kind = measured_tensor_peak()
 
-    def attention_call(q, bt, kl, qi, qr, o, l, max_q_rows, max_kv_len, mask, cb=0):
+    def attention_call(q, bt, kl, qi, qr, o, l, max_q_rows, max_kv_len, mask, cb=0, on=None):
         ws_b = pkv.paged_attention_workspace_size(int(kl.numel()), max_q_rows, Hq, Hkv, D, max_kv_len)
         ws = torch.empty(max(ws_b, 256), dtype=torch.uint8, device=dev)
+        st = stream if on is None else on
         return lambda: pkv.paged_attention(q, t["k_pool"], t["v_pool"], bt, kl, qi, o, q_real=qr,
                                            lse=l, max_q_rows=max_q_rows, max_kv_len=max_kv_len,
-                                           mask=mask, causal_block=cb, workspace=ws, stream=stream)
+                                           mask=mask, causal_block=cb, workspace=ws, stream=st)
 
     h2d_src = [case.q, case.new_k, case.new_v, case.slots, case.kv_lens, case.block_table]
     h2d_dst = [t["q"], t["new_k"], t["new_v"], t["slots"], t["kl"], t["bt"]]
@@ -565,6 +566,22 @@ def build_plan(name, rank, dev, stream):
         tail = attention_call(t["q"], pt["tt"], pt["tl"], t["qi"], t["qr"], o_t, l_t, 1, mt,
                               "causal")
         merge = lambda: pkv.merge_attn_states(o_p, l_p, o_t, l_t, out, lse, stream=stream)
+        # the prefix and tail calls are independent: the tail call runs on a
+        # second stream, forked after the scatter and joined before the merge
+        side = torch.cuda.Stream(device=dev)
+        ev_fork, ev_join = torch.cuda.Event(), torch.cuda.Event()
+        tail_side = attention_call(t["q"], pt["tt"], pt["tl"], t["qi"], t["qr"], o_t, l_t, 1, mt, "causal",
+                                   on=side)
+
+        def fork_tail():
+            ev_fork.record(stream)
+            side.wait_event(ev_fork)
+            tail_side()
+            ev_join.record(side)
+
+        def join_merge():
+            stream.wait_event(ev_join)
+            merge()
         prefix_bytes = Gn * prefix * kv_tok_bytes
         tail_bytes = int(e["tail_lens"].sum()) * kv_tok_bytes
         aux["tail_attention"] = (tail, tail_bytes, "GB/s")
@@ -576,10 +593,11 @@ def build_plan(name, rank, dev, stream):
         h2d_src = [case.q, case.new_k, case.new_v, case.slots, e["tail_lens"], e["tail_table"]]
         h2d_dst = [t["q"], t["new_k"], t["new_v"], t["slots"], pt["tl"], pt["tt"]]
         return StepPlan(case=case, cfg=cfg, metric="shared-prefix KV GB/s", unit="GB/s",
-                        work=prefix_bytes + tail_bytes, scale=1e9, queries=rows, pre=[scatter],
-                        dominant=dom, post=[tail, merge], aux=aux,
+                        work=prefix_bytes + tail_bytes, scale=1e9, queries=rows, pre=[scatter, fork_tail],
+                        dominant=dom, post=[join_merge], aux=aux,
                         dom_label="paged_attention, prefix call: tcgen05 tile kernel, 8 samples x 4 "
-                                  "heads = 32 of 128 tile rows, HBM-bound",
+                                  "heads = 32 rows held 4 times, HBM-bound (the tail call runs "
+                                  "concurrently on a second stream)",
                         dom_work=prefix_bytes, bound="hbm", peak=peak_hbm, peak_unit="GB/s",
                         peak_src=f"{hbm_kind} hbm_gbs", h2d=(h2d_src, h2d_dst), d2h=d2h_src,
                         launches=6, traffic_sources=ATTN_TC_SOURCES)
