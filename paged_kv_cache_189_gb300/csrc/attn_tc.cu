@@ -144,6 +144,20 @@ __device__ __forceinline__ void tmem_store32(uint32_t taddr, const uint32_t (&v)
 }
 #undef PKV_W8
 
+// max of three values in one instruction
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+// acc += the two bf16 values of a packed pair, each widened exactly to f32
+__device__ __forceinline__ void add_bf16x2(float2& acc, uint32_t pk) {
+    asm("{\n\t.reg .b16 lo, hi;\n\t"
+        "mov.b32 {lo, hi}, %2;\n\t"
+        "add.rn.f32.bf16 %0, lo, %0;\n\t"
+        "add.rn.f32.bf16 %1, hi, %1;\n\t}"
+        : "+f"(acc.x), "+f"(acc.y) : "r"(pk));
+}
 // named barrier `id` over `count` threads that also returns the AND of `pred`
 __device__ __forceinline__ bool bar_and(int id, int count, bool pred) {
     uint32_t r;
@@ -580,7 +594,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     float mx = __uint_as_float(sv[0]);
     #pragma unroll
                     for (int e = 1; e + 1 < kTileN; e += 2)
-                        mx = fmaxf(mx, fmaxf(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])));
+                        mx = fmax3(mx, __uint_as_float(sv[e]), __uint_as_float(sv[e + 1]));
                     mx = fmaxf(mx, __uint_as_float(sv[kTileN - 1]));
                     mx *= p.scale_log2;
                     if (mx > m_used + kLazyRescale) {   // also true the first time a key is visible
@@ -599,7 +613,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const float2 pp = make_float2(fast_exp2(xx.x), fast_exp2(xx.y));
                         pk[e / 2] = pack_bf16x2(pp.x, pp.y);
                         rs2 = __fadd2_rn(rs2, pp);
-                        rsb2 = __fadd2_rn(rsb2, make_float2(bf16lo(pk[e / 2]), bf16hi(pk[e / 2])));
+                        add_bf16x2(rsb2, pk[e / 2]);
                     }
                     // O is normalised by the sum of the bf16 probabilities the P.V product
                     // used (numerator and denominator carry the same rounding); the LSE
@@ -796,7 +810,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mx = __uint_as_float(sv[0]);
     #pragma unroll
                     for (int e = 1; e + 1 < CW; e += 2)
-                        mx = fmaxf(mx, fmaxf(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])));
+                        mx = fmax3(mx, __uint_as_float(sv[e]), __uint_as_float(sv[e + 1]));
                     mx = fmaxf(mx, __uint_as_float(sv[CW - 1]));
                 }
                 if constexpr (REP > 1) {
@@ -824,7 +838,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const float2 pp = make_float2(fast_exp2(xx.x), fast_exp2(xx.y));
                         pk[e / 2] = pack_bf16x2(pp.x, pp.y);
                         rs2 = __fadd2_rn(rs2, pp);
-                        rsb2 = __fadd2_rn(rsb2, make_float2(bf16lo(pk[e / 2]), bf16hi(pk[e / 2])));
+                        add_bf16x2(rsb2, pk[e / 2]);
                     }
                     // O is normalised by the sum of the bf16 probabilities the P.V product
                     // used (numerator and denominator carry the same rounding); the LSE
@@ -1312,11 +1326,12 @@ __global__ void __maxnreg__(96)
 #pragma unroll
                     for (int q = 0; q < 4; ++q) a[q] = __uint_as_float(sv[q]);
 #pragma unroll
-                    for (int e = 4; e < 32; e += 4) {
+                    for (int e = 4; e < 32; e += 8) {
 #pragma unroll
-                        for (int q = 0; q < 4; ++q) a[q] = fmaxf(a[q], __uint_as_float(sv[e + q]));
+                        for (int q = 0; q < 4; ++q)
+                            a[q] = fmax3(a[q], __uint_as_float(sv[e + q]), __uint_as_float(sv[e + 4 + q]));
                     }
-                    mpart = fmaxf(mpart, fmaxf(fmaxf(a[0], a[1]), fmaxf(a[2], a[3])));
+                    mpart = fmax3(mpart, fmax3(a[0], a[1], a[2]), a[3]);
                 }
             }
             // exchange the two halves' maxima; also agree on whether every wait succeeded
@@ -1371,7 +1386,7 @@ __global__ void __maxnreg__(96)
                         const float2 pp = make_float2(fast_exp2(xx.x), fast_exp2(xx.y));
                         pk[e / 2] = pack_bf16x2(pp.x, pp.y);
                         rs2 = __fadd2_rn(rs2, pp);
-                        rsb2 = __fadd2_rn(rsb2, make_float2(bf16lo(pk[e / 2]), bf16hi(pk[e / 2])));
+                        add_bf16x2(rsb2, pk[e / 2]);
                     }
                     tmem_store16(lane_addr + hf * 96 + c * 16, pk);
                 }
