@@ -1100,6 +1100,9 @@ __global__ void __maxnreg__(96)
         g.nt = g.key_hi > g.kb ? (g.key_hi - g.kb + kTileN - 1) / kTileN : 0;
     }
     if (g.t0 >= g.nrows) return;  // uniform
+    // tile B holds rows (false in the last CTA of a sequence whose rows end in
+    // tile A): otherwise its MMAs and its softmax warps' key loop are skipped
+    const bool two = g.t0 + TQ < g.nrows;
 
     if (g.nt == 0) {
         if (threadIdx.x < 2 * kTileM) {
@@ -1244,7 +1247,7 @@ __global__ void __maxnreg__(96)
             if (ok) {
                 tc_fence_after();
                 issue_s(0, 0);
-                issue_s(1, 0);
+                if (two) issue_s(1, 0);
                 umma_commit(&k_empty[0]);
             }
             for (int j = 0; ok && j < g.nt; ++j) {
@@ -1259,14 +1262,16 @@ __global__ void __maxnreg__(96)
                 } else {
                     umma_commit(&o_full[0]);
                 }
-                if (!wait(&p_full[1], j & 1)) break;
-                tc_fence_after();
-                issue_pv(1, j);
+                if (two) {
+                    if (!wait(&p_full[1], j & 1)) break;
+                    tc_fence_after();
+                    issue_pv(1, j);
+                }
                 umma_commit(&v_empty[j % kVStages]);
                 if (more) {
-                    issue_s(1, j + 1);
+                    if (two) issue_s(1, j + 1);
                     umma_commit(&k_empty[(j + 1) % kKStages]);
-                } else {
+                } else if (two) {
                     umma_commit(&o_full[1]);
                 }
             }
@@ -1307,7 +1312,8 @@ __global__ void __maxnreg__(96)
         const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
         const bool warp_live = __any_sync(0xffffffffu, limit > 0);
         bool ok = true;
-        for (int j = 0; j < g.nt; ++j) {
+        const int nt_mine = (x == 1 && !two) ? 0 : g.nt;  // no rows in tile B: nothing to do
+        for (int j = 0; j < nt_mine; ++j) {
             bool ok_t = __all_sync(0xffffffffu, wait(&s_full[x], j & 1));
             tc_fence_after();
             const int nvis = limit - (g.kb + j * kTileN) - hf * 64;  // visible columns of this half
@@ -1422,7 +1428,7 @@ __global__ void __maxnreg__(96)
             mbar_arrive(&p_full[x]);
         }
         // ---- epilogue: the two halves' sums, then O / l on this half's columns
-        const bool ok_o = __all_sync(0xffffffffu, ok && wait(&o_full[x], 0));
+        const bool ok_o = __all_sync(0xffffffffu, ok && nt_mine > 0 && wait(&o_full[x], 0));
         tc_fence_after();
         // every key-loop exchange has been read: o_full follows both halves' last P
         float* xl = xch + x * 2 * kTileM + r;  // [tile][0: l, 1: l_b][row]
