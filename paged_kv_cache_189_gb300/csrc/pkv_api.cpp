@@ -156,15 +156,21 @@ Plan plan_attention(int batch, int max_q_rows, int Hq, int Hkv, int D, int max_k
     // persistent CTAs (3 per SM); each unit ends with a merge of its warps'
     // states, so units should be long, but numerous enough to balance ragged
     // lengths: aim for ~6 units per resident CTA at the host's length bound,
-    // never below the pages' minimum split of 512 keys.
+    // never below the pages' minimum split of 512 keys, and at least 1024 keys
+    // while that still leaves one unit per resident CTA (short rows, e.g. the
+    // private tails of shared-prefix rows, pay the per-unit cost otherwise).
     int keys = kDecodeSplitKeys;
     if (num_splits > 0) {
         const int per = (max_kv_len + num_splits - 1) / num_splits;
         keys = std::max(32, (per + 31) / 32 * 32);
     } else {
-        const int64_t target_units = 6 * 3 * kPlanSMs;
-        const int64_t per = (static_cast<int64_t>(max_kv_len) * batch * Hkv + target_units - 1) / target_units;
-        keys = static_cast<int>(std::max<int64_t>(kDecodeSplitKeys, (per + 31) / 32 * 32));
+        const int64_t resident = 3 * kPlanSMs;
+        const int64_t pairs = static_cast<int64_t>(batch) * Hkv;
+        const int64_t target_units = 6 * resident;
+        const int64_t per = (static_cast<int64_t>(max_kv_len) * pairs + target_units - 1) / target_units;
+        const int64_t fill = (static_cast<int64_t>(max_kv_len) * pairs + resident - 1) / resident;
+        const int64_t lo = std::max<int64_t>(kDecodeSplitKeys, std::min<int64_t>(1024, fill));
+        keys = static_cast<int>((std::max<int64_t>(lo, per) + 31) / 32 * 32);
     }
     pl.split_keys = keys;
     pl.splits = std::max(1, (max_kv_len + keys - 1) / keys);
