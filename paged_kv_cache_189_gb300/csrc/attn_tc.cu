@@ -1465,7 +1465,15 @@ __global__ void __maxnreg__(96)
 template <int G>
 cudaError_t launch_g2(const AttnParams& p, const void* tk, const void* tv, cudaStream_t s) {
     auto kern = attn_tc2_kernel<G>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes2);
+    // shared-memory opt-in: once per device
+    static DeviceOnce opted;
+    int dev = 0, done = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    e = opted.get(dev, &done, [&](int, int* v) {
+        *v = 1;
+        return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes2);
+    });
     if (e != cudaSuccess) return e;
     const int TQ = kTileM / G;
     dim3 grid((p.max_q_rows + 2 * TQ - 1) / (2 * TQ), p.num_kv_heads, p.batch * p.num_splits);
@@ -1480,7 +1488,15 @@ cudaError_t launch_g2(const AttnParams& p, const void* tk, const void* tv, cudaS
 template <int G, bool GRP, int REP>
 cudaError_t launch_one(const AttnParams& p, int rows, const void* tk, const void* tv, cudaStream_t s) {
     auto kern = attn_tc_kernel<G, GRP, REP>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    // shared-memory opt-in: once per device
+    static DeviceOnce opted;
+    int dev = 0, done = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    e = opted.get(dev, &done, [&](int, int* v) {
+        *v = 1;
+        return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    });
     if (e != cudaSuccess) return e;
     const int TQ = kTileM / (G * REP);
     dim3 grid((rows + TQ - 1) / TQ, p.num_kv_heads, p.batch * p.num_splits);

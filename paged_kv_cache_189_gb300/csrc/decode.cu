@@ -554,13 +554,20 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks)
 }
 
 template <int D, int G>
-cudaError_t launch_dg(const AttnParams& p, const void* tk, const void* tv, int sms, cudaStream_t s) {
+cudaError_t launch_dg(const AttnParams& p, const void* tk, const void* tv, int dev, int sms, cudaStream_t s) {
     using S = DecodeSmem<D, G>;
     auto kern = decode_kernel<D, G>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kBytes);
-    if (e != cudaSuccess) return e;
+    // shared-memory opt-in and occupancy: once per device
+    static DeviceOnce occupancy;
     int per_sm = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, S::kBytes);
+    cudaError_t e = occupancy.get(dev, &per_sm, [&](int, int* v) {
+        cudaError_t r = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kBytes);
+        if (r != cudaSuccess) return r;
+        int n = 0;
+        r = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, kThreads, S::kBytes);
+        *v = n > 0 ? n : 1;
+        return r;
+    });
     if (e != cudaSuccess) return e;
     const int64_t units = static_cast<int64_t>(p.batch) * p.num_kv_heads * p.num_splits;
     const int64_t grid = std::min<int64_t>(units, static_cast<int64_t>(std::max(per_sm, 1)) * sms);
@@ -583,14 +590,17 @@ cudaError_t launch_decode(const AttnParams& p, const void* tk, const void* tv, c
     int dev = 0, sms = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    static DeviceOnce sm_count;
+    e = sm_count.get(dev, &sms, [](int d, int* v) {
+        return cudaDeviceGetAttribute(v, cudaDevAttrMultiProcessorCount, d);
+    });
     if (e != cudaSuccess) return e;
     // the unit tickets and the per-(sequence, head) split counts start at zero
     e = cudaMemsetAsync(p.ws_counters, 0, decode_counter_bytes(p.batch, p.num_kv_heads), s);
     if (e != cudaSuccess) return e;
     const int G = p.num_q_heads / p.num_kv_heads;
 #define PKV_DEC(D_, G_) \
-    if (p.head_dim == D_ && G == G_) return launch_dg<D_, G_>(p, tk, tv, sms, s);
+    if (p.head_dim == D_ && G == G_) return launch_dg<D_, G_>(p, tk, tv, dev, sms, s);
     PKV_DEC(128, 4) PKV_DEC(128, 2) PKV_DEC(128, 1)
     PKV_DEC(64, 4) PKV_DEC(64, 2) PKV_DEC(64, 1)
 #undef PKV_DEC

@@ -5,6 +5,7 @@
 
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
+#include <atomic>
 #include <stdint.h>
 
 #include "pkv.h"
@@ -57,6 +58,33 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
     return t;
 }
+
+// ---------------------------------------------------------------------------
+// Host side: per-device values of a launch configuration, computed once
+// (a kernel's shared-memory opt-in, its occupancy, the SM count) so a call
+// does not repeat those runtime queries.
+// ---------------------------------------------------------------------------
+struct DeviceOnce {
+    static constexpr int kMaxDevices = 64;
+    std::atomic<int> value[kMaxDevices];
+    // f(dev, &v) computes the value; 0 is never a valid cached value
+    template <typename F>
+    cudaError_t get(int dev, int* out, F f) {
+        if (dev >= 0 && dev < kMaxDevices) {
+            const int v = value[dev].load(std::memory_order_relaxed);
+            if (v != 0) {
+                *out = v;
+                return cudaSuccess;
+            }
+        }
+        int v = 0;
+        cudaError_t e = f(dev, &v);
+        if (e != cudaSuccess) return e;
+        if (dev >= 0 && dev < kMaxDevices) value[dev].store(v, std::memory_order_relaxed);
+        *out = v;
+        return cudaSuccess;
+    }
+};
 
 // ---------------------------------------------------------------------------
 // mbarrier (shared::cta)
