@@ -1060,8 +1060,9 @@ __device__ __forceinline__ void umma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, u
 // overwrites S values the other has not read yet.
 // Roles (576 threads): warps 0-7 softmax A, warps 8-15 softmax B (quadrant
 // warp & 3, key half (warp >> 2) & 1), warp 16 TMA producer, warp 17 MMA.
-// Every wait gives up after ~2 s; the per-tile exchange barrier also ANDs the
-// waits' results, so the 256 threads of a tile leave the key loop together.
+// Every wait gives up after ~2 s; the exchange barrier of a lane quadrant's two
+// warps (a named barrier per quadrant and tile) also ANDs the waits' results,
+// so the two leave the key loop together.
 // ===========================================================================
 constexpr int kThreads2 = 576;
 constexpr int kXch2Off = kBar2Off + kNumBars2 * 8;            // float [2 tiles][2 halves][128 rows]
@@ -1149,7 +1150,7 @@ __global__ void __maxnreg__(96)
         }
         for (int x = 0; x < 2; ++x) {
             mbar_init(&s_full[x], 1);
-            mbar_init(&p_full[x], 2 * kTileM);
+            mbar_init(&p_full[x], 8);  // one elected arrive per softmax warp
             mbar_init(&o_full[x], 1);
         }
         *abort_flag = 0;
@@ -1284,7 +1285,7 @@ __global__ void __maxnreg__(96)
         const int t = r / G, hg = r % G;
         const int i = g.t0 + x * TQ + t;
         const int h = g.kvh * G + hg;
-        const int bar_id = 1 + x;
+        const int bar_id = 1 + x * 4 + (warp & 3);  // the two warps of this lane quadrant
         const bool row_exists = i < g.nrows;
         const int limit = row_exists ? visible_keys(i, g.qreal, g.kv_len, p.mask, max(p.causal_block, 1))
                                      : 0;
@@ -1342,7 +1343,7 @@ __global__ void __maxnreg__(96)
             }
             // exchange the two halves' maxima; also agree on whether every wait succeeded
             *xmine = mpart;
-            if (!bar_and(bar_id, 8 * 32, ok_t)) {
+            if (!bar_and(bar_id, 2 * 32, ok_t)) {
                 ok = false;
                 break;
             }
@@ -1425,19 +1426,20 @@ __global__ void __maxnreg__(96)
                 }
             }
             tc_fence_before();
-            mbar_arrive(&p_full[x]);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&p_full[x]);
         }
         // ---- epilogue: the two halves' sums, then O / l on this half's columns
         const bool ok_o = __all_sync(0xffffffffu, ok && nt_mine > 0 && wait(&o_full[x], 0));
         tc_fence_after();
         // every key-loop exchange has been read: o_full follows both halves' last P
         float* xl = xch + x * 2 * kTileM + r;  // [tile][0: l, 1: l_b][row]
-        bar_sync_n(bar_id, 8 * 32);
+        bar_sync_n(bar_id, 2 * 32);
         if (hf == 1) {
             xl[0] = l;
             xl[kTileM] = l_b;
         }
-        bar_sync_n(bar_id, 8 * 32);
+        bar_sync_n(bar_id, 2 * 32);
         float inv_l = 0.f;
         if (hf == 0) {
             const float lt = l + xl[0], lbt = l_b + xl[kTileM];
@@ -1446,7 +1448,7 @@ __global__ void __maxnreg__(96)
             if (ok_o && row_exists) store_row_lse(p, g, i, h, any ? (m_used + __log2f(lt)) * kLn2 : -INFINITY);
             xl[0] = inv_l;
         }
-        bar_sync_n(bar_id, 8 * 32);
+        bar_sync_n(bar_id, 2 * 32);
         if (hf == 1) inv_l = xl[0];
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
