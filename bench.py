@@ -730,21 +730,28 @@ def run_ours(args):
     #      The host runs one step ahead, as a serving loop does: it enqueues
     #      step i (inputs copied in, the step, the result copied into one of
     #      two pinned buffers) and then waits for step i - 1's result.
+    #      A step's inputs travel as one copy: one pinned host buffer holds them
+    #      all (each at a 256-byte aligned offset) and the step's device input
+    #      tensors are rebound to views of one device buffer of the same
+    #      layout; the results (output and LSE) likewise come back as one copy.
     srcs, dsts = plan.h2d
-    h_in = [x.pin_memory() for x in srcs]
-    h_out = [[torch.empty(x.shape, dtype=x.dtype).pin_memory() for x in plan.d2h] for _ in range(2)]
-    h2d = sum(x.numel() * x.element_size() for x in h_in)
-    d2h = sum(x.numel() * x.element_size() for x in h_out[0])
+    d_in, in_offs = packed_device(dsts, dev)
+    h_in = torch.empty(d_in.numel(), dtype=torch.uint8).pin_memory()
+    for x, o in zip(srcs, in_offs):
+        n = x.numel() * x.element_size()
+        h_in[o:o + n].copy_(x.contiguous().view(-1).view(torch.uint8))
+    d_out, _ = packed_device(plan.d2h, dev)
+    h_out = [torch.empty(d_out.numel(), dtype=torch.uint8).pin_memory() for _ in range(2)]
+    h2d = h_in.numel()
+    d2h = d_out.numel()
     done = [torch.cuda.Event(), torch.cuda.Event()]
 
     def e2e_steps(n):
         for i in range(n):
             with torch.cuda.stream(stream):
-                for hs, dd in zip(h_in, dsts):
-                    dd.copy_(hs, non_blocking=True)
+                d_in.copy_(h_in, non_blocking=True)
                 step()
-                for hd, ds in zip(h_out[i % 2], plan.d2h):
-                    hd.copy_(ds, non_blocking=True)
+                h_out[i % 2].copy_(d_out, non_blocking=True)
                 done[i % 2].record(stream)
             if i >= 1:
                 done[(i - 1) % 2].synchronize()  # step i - 1's result is on the host
@@ -790,6 +797,23 @@ def run_ours(args):
         print(json.dumps(line), flush=True)
     barrier(dist)
     return 0
+
+
+def packed_device(tensors, dev):
+    """One device byte buffer holding every tensor of ``tensors`` at a 256-byte
+    aligned offset; each tensor is rebound in place to its view of the buffer
+    (the step's callables keep working on the same tensor objects).  Returns
+    ``(buffer, offsets)``.  The tensors' contents are not carried over."""
+    import torch
+    offs, total = [], 0
+    for x in tensors:
+        assert x.is_contiguous()
+        offs.append(total)
+        total += -(-x.numel() * x.element_size() // 256) * 256
+    buf = torch.empty(max(total, 256), dtype=torch.uint8, device=dev)
+    for x, o in zip(tensors, offs):
+        x.set_(buf.untyped_storage(), o // x.element_size(), x.shape, x.stride())
+    return buf, offs
 
 
 def cpu_baseline_for(plan, args):
