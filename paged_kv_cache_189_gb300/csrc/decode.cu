@@ -9,12 +9,16 @@
 //
 // Decode is bound by HBM: every K/V byte is read once and used for the
 // G = Hq/Hkv query heads that share it.  The GB300 design:
-//  * work unit = (split of 512 keys = 16 pages, K/V head, sequence).  Units are
-//    numbered split-major and handed out by an atomic ticket, so the kernel is
-//    persistent (a few CTAs per SM) and balances ragged lengths dynamically;
-//    the grid never depends on device lengths, so a call is graph-capturable.
-//  * one producer lane per CTA fetches tickets, skips units past a sequence's
-//    length, copies the unit's G query rows into shared memory with bulk
+//  * work unit = (split of split_keys keys, K/V head, sequence), handed out by
+//    an atomic ticket, so the kernel is persistent (a few CTAs per SM) and
+//    balances ragged lengths dynamically; the grid never depends on device
+//    lengths, so a call is graph-capturable.  A one-CTA planning launch before
+//    it orders the units: every full split first (split-major, sequences with
+//    more full splits first), then each sequence's partial last split, longest
+//    first, then the rows without keys -- so the launch ends on the shortest
+//    units instead of leaving SMs idle behind full-length ones.
+//  * one producer lane per CTA fetches tickets, reads each ticket's unit from
+//    the planned list, copies the unit's G query rows into shared memory with bulk
 //    copies, and streams the unit's pages of one K/V head (32 x D of K and of
 //    V, 64-column TMA boxes, 128-byte swizzle) into a 4-stage ring.  It runs
 //    ahead across unit boundaries, so the ring stays full while the consumers
@@ -87,6 +91,166 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
     asm volatile(
         "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
         ::"r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar)) : "memory");
+}
+
+// ---------------------------------------------------------------------------
+// Scheduling region of the workspace: [0] unit ticket and [1 + b*Hkv + h]
+// finished splits; the unit count; the sequences in full-split order; the unit
+// list (split, b*Hkv + h) in ticket order.
+// ---------------------------------------------------------------------------
+constexpr int kPlanThreads = 1024;
+constexpr int kPlanMaxFull = 2047;  // full splits per sequence the planner orders
+constexpr int kPlanBuckets = 1024;  // length buckets of the partial splits
+
+__host__ __device__ constexpr size_t align256(size_t n) { return (n + 255) / 256 * 256; }
+
+struct Sched {
+    int* counters;
+    int* total;
+    int* seq_at_pos;
+    int2* list;
+    __host__ __device__ static size_t counters_bytes(int B, int Hkv) {
+        return align256((static_cast<size_t>(B) * Hkv + 1) * sizeof(int));
+    }
+    __host__ __device__ static size_t bytes(int B, int Hkv, int S) {
+        return counters_bytes(B, Hkv) + 256 + align256(static_cast<size_t>(B) * sizeof(int)) +
+               align256(static_cast<size_t>(B) * Hkv * (S > 0 ? S : 1) * sizeof(int2));
+    }
+    __host__ __device__ Sched(void* base, int B, int Hkv) {
+        char* w = static_cast<char*>(base);
+        counters = reinterpret_cast<int*>(w);
+        w += counters_bytes(B, Hkv);
+        total = reinterpret_cast<int*>(w);
+        w += 256;
+        seq_at_pos = reinterpret_cast<int*>(w);
+        w += align256(static_cast<size_t>(B) * sizeof(int));
+        list = reinterpret_cast<int2*>(w);
+    }
+};
+
+// whether the planner orders the units of this call (else: split-major order)
+__host__ __device__ inline bool plan_listed(const AttnParams& p) {
+    return p.max_kv_len / p.split_keys <= kPlanMaxFull;
+}
+
+// The keys a decode row attends (0 for a padding row), or -1 for a sequence
+// without rows; the same reading of the inputs as the producer's.
+__device__ __forceinline__ int row_keys(const AttnParams& p, int b) {
+    const int nrows = p.q_indptr[b + 1] - p.q_indptr[b];
+    if (nrows <= 0) return -1;
+    const int qreal = p.q_real ? p.q_real[b] : nrows;
+    const int kv = min(max(p.kv_lens[b], 0), p.max_kv_len);
+    return qreal <= 0 ? 0 : kv;
+}
+
+// In-place exclusive prefix sum of a[0, n), n <= 2 * kPlanThreads; returns the
+// total.  All threads of the block call it.
+__device__ int block_scan_exclusive(int* a, int n, int* warp_tot) {
+    const int t = threadIdx.x, lane = t & 31, w = t >> 5;
+    const int i0 = 2 * t, i1 = 2 * t + 1;
+    const int x0 = i0 < n ? a[i0] : 0, x1 = i1 < n ? a[i1] : 0;
+    int v = x0 + x1;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v += y;
+    }
+    if (lane == 31) warp_tot[w] = v;
+    __syncthreads();
+    if (w == 0) {
+        int u = warp_tot[lane];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, u, o);
+            if (lane >= o) u += y;
+        }
+        warp_tot[lane] = u;  // inclusive over warps
+    }
+    __syncthreads();
+    const int before = (w > 0 ? warp_tot[w - 1] : 0) + v - (x0 + x1);
+    const int total = warp_tot[31];
+    __syncthreads();
+    if (i0 < n) a[i0] = before;
+    if (i1 < n) a[i1] = before + x0;
+    __syncthreads();
+    return total;
+}
+
+__global__ void __launch_bounds__(kPlanThreads) decode_plan_kernel(const AttnParams p) {
+    __shared__ int cnt_f[kPlanMaxFull + 2];   // sequences per full-split count, then cursors
+    __shared__ int gt_f[kPlanMaxFull + 2];    // sequences with more than s full splits
+    __shared__ int cnt_r[kPlanBuckets];       // partial splits per length bucket, then cursors
+    __shared__ int warp_tot[32];
+    __shared__ int n_empty, e_cur;
+    const int B = p.batch, Hkv = p.num_kv_heads, SK = p.split_keys;
+    const int nF = p.max_kv_len / SK + 1;     // full-split counts 0 .. nF - 1
+    Sched sc(p.ws_counters, B, Hkv);
+    const int tid = threadIdx.x;
+    for (int i = tid; i <= B * Hkv; i += kPlanThreads) sc.counters[i] = 0;
+    for (int i = tid; i < nF + 1; i += kPlanThreads) cnt_f[i] = 0;
+    for (int i = tid; i < kPlanBuckets; i += kPlanThreads) cnt_r[i] = 0;
+    if (tid == 0) n_empty = e_cur = 0;
+    __syncthreads();
+    auto bucket_of = [&](int r) {  // longer partial splits in higher buckets
+        return static_cast<int>((static_cast<int64_t>(r) * kPlanBuckets) / SK);
+    };
+    for (int b = tid; b < B; b += kPlanThreads) {
+        const int kv = row_keys(p, b);
+        if (kv < 0) continue;
+        const int f = kv / SK, r = kv - f * SK;
+        atomicAdd(&cnt_f[f], 1);
+        if (r > 0) atomicAdd(&cnt_r[bucket_of(r)], 1);
+        if (kv == 0) atomicAdd(&n_empty, 1);
+    }
+    __syncthreads();
+    // sequences with more than s full splits: gt_f[s] = (all with f >= 1) - #{1 <= f <= s}
+    cnt_f[0] = 0;  // sequences without a full split take no position
+    __syncthreads();
+    for (int i = tid; i < nF; i += kPlanThreads) gt_f[i] = cnt_f[i];
+    __syncthreads();
+    const int with_full = block_scan_exclusive(gt_f, nF, warp_tot);  // gt_f[s] = #{f < s}
+    for (int i = tid; i < nF; i += kPlanThreads) {
+        const int le = gt_f[i] + cnt_f[i];       // #{1 <= f <= s}
+        gt_f[i] = with_full - le;                // #{f > s}
+        cnt_f[i] = with_full - le;               // cursor: positions of f == s start here
+    }
+    __syncthreads();
+    // unit index of the first full unit of split s: Hkv * sum_{t < s} gt_f[t]
+    const int full_seq_splits = block_scan_exclusive(gt_f, nF, warp_tot);
+    const int full_units = full_seq_splits * Hkv;
+    // partial splits, longest bucket first: start of bucket k = #{buckets > k}
+    const int partials = block_scan_exclusive(cnt_r, kPlanBuckets, warp_tot);  // #{< k}
+    __syncthreads();
+    for (int b = tid; b < B; b += kPlanThreads) {
+        const int kv = row_keys(p, b);
+        if (kv < 0) continue;
+        const int f = kv / SK, r = kv - f * SK;
+        if (f > 0) sc.seq_at_pos[atomicAdd(&cnt_f[f], 1)] = b;
+        int at = -1, split = 0;
+        if (r > 0) {
+            // descending: the first slot of bucket k is partials - #{<= k}
+            const int k = bucket_of(r);
+            const int below = atomicAdd(&cnt_r[k], 1);  // #{< k} + rank in bucket
+            at = full_units + (partials - 1 - below) * Hkv;
+            split = f;
+        } else if (kv == 0) {
+            at = full_units + (partials + atomicAdd(&e_cur, 1)) * Hkv;
+        }
+        if (at >= 0)
+            for (int h = 0; h < Hkv; ++h) sc.list[at + h] = make_int2(split, b * Hkv + h);
+    }
+    __syncthreads();
+    // full units, split-major; split s holds the gt_f-count sequences of most full splits
+    for (int u = tid; u < full_units; u += kPlanThreads) {
+        int lo = 0, hi = nF - 1;  // last s with Hkv * gt_f[s] <= u (gt_f now holds the prefix)
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (gt_f[mid] * Hkv <= u) lo = mid; else hi = mid - 1;
+        }
+        const int idx = u - gt_f[lo] * Hkv;
+        sc.list[u] = make_int2(lo, sc.seq_at_pos[idx / Hkv] * Hkv + idx % Hkv);
+    }
+    if (tid == 0) *sc.total = full_units + (partials + n_empty) * Hkv;
 }
 
 __device__ __forceinline__ void consumer_sync() {
@@ -302,9 +466,11 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks)
         if (lane != 0) return;
         prefetch_tmap(&tm_k);
         prefetch_tmap(&tm_v);
-        int* ticket = p.ws_counters;
+        const Sched sc(p.ws_counters, p.batch, Hkv);
+        int* ticket = sc.counters;
         const int BH = p.batch * Hkv;
-        const int units = BH * S_;
+        const bool listed = plan_listed(p);
+        const int units = listed ? __ldcg(sc.total) : BH * S_;
         int i = 0;  // pages issued so far (ring position)
         bool alive = true;
         for (int k = 0; alive; ++k) {
@@ -313,8 +479,15 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks)
             for (;;) {
                 const int u = atomicAdd(ticket, 1);
                 if (u >= units) break;
-                const int split = u / BH;
-                const int bh = u - split * BH;
+                int split, bh;
+                if (listed) {
+                    const int2 e = __ldcg(&sc.list[u]);
+                    split = e.x;
+                    bh = e.y;
+                } else {
+                    split = u / BH;
+                    bh = u - split * BH;
+                }
                 const int b = bh / Hkv;
                 const int r0 = p.q_indptr[b];
                 const int nrows = p.q_indptr[b + 1] - r0;
@@ -531,14 +704,33 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks)
                     const int g = e / D, dd = e - (e / D) * D;
                     const int64_t st = static_cast<int64_t>(d.r0) * Hq + d.kvh * G + g;
                     const float* lses = p.ws_lse + st * S_;
-                    float M = -INFINITY;
-                    for (int sp = 0; sp < d.nsplit; ++sp) M = fmaxf(M, __ldcg(lses + sp));
-                    float L = 0.f, O = 0.f;
-                    if (M != -INFINITY) {
-                        for (int sp = 0; sp < d.nsplit; ++sp) {
-                            const float w = __expf(__ldcg(lses + sp) - M);
-                            L += w;
-                            O = fmaf(w, __ldcg(p.ws_o + (st * S_ + sp) * D + dd), O);
+                    const float* os = p.ws_o + st * S_ * D + dd;
+                    // the splits' states eight at a time, all loads in flight
+                    // together, merged online (one chunk: max first, then sums)
+                    float M = -INFINITY, L = 0.f, O = 0.f;
+                    for (int sp0 = 0; sp0 < d.nsplit; sp0 += 8) {
+                        float lv[8], ov[8];
+#pragma unroll
+                        for (int u = 0; u < 8; ++u) {
+                            const bool in = sp0 + u < d.nsplit;
+                            lv[u] = in ? __ldcg(lses + sp0 + u) : -INFINITY;
+                            ov[u] = in ? __ldcg(os + static_cast<int64_t>(sp0 + u) * D) : 0.f;
+                        }
+                        float mc = lv[0];
+#pragma unroll
+                        for (int u = 1; u < 8; ++u) mc = fmaxf(mc, lv[u]);
+                        const float Mn = fmaxf(M, mc);
+                        if (Mn != -INFINITY) {
+                            const float c = __expf(M - Mn);  // 0 while nothing was merged
+                            L *= c;
+                            O *= c;
+#pragma unroll
+                            for (int u = 0; u < 8; ++u) {
+                                const float w = __expf(lv[u] - Mn);
+                                L += w;
+                                O = fmaf(w, ov[u], O);
+                            }
+                            M = Mn;
                         }
                     }
                     O *= L > 0.f ? 1.0f / L : 0.f;
@@ -582,8 +774,8 @@ bool decode_supported(int head_dim, int group) {
     return (head_dim == 64 || head_dim == 128) && (group == 1 || group == 2 || group == 4);
 }
 
-size_t decode_counter_bytes(int batch, int num_kv_heads) {
-    return (static_cast<size_t>(batch) * num_kv_heads + 1) * sizeof(int);
+size_t decode_sched_bytes(int batch, int num_kv_heads, int splits) {
+    return Sched::bytes(batch, num_kv_heads, splits);
 }
 
 cudaError_t launch_decode(const AttnParams& p, const void* tk, const void* tv, cudaStream_t s) {
@@ -595,8 +787,14 @@ cudaError_t launch_decode(const AttnParams& p, const void* tk, const void* tv, c
         return cudaDeviceGetAttribute(v, cudaDevAttrMultiProcessorCount, d);
     });
     if (e != cudaSuccess) return e;
-    // the unit tickets and the per-(sequence, head) split counts start at zero
-    e = cudaMemsetAsync(p.ws_counters, 0, decode_counter_bytes(p.batch, p.num_kv_heads), s);
+    // the unit tickets and the per-(sequence, head) split counts start at zero;
+    // the planner also writes the unit order
+    if (plan_listed(p)) {
+        decode_plan_kernel<<<1, kPlanThreads, 0, s>>>(p);
+        e = cudaGetLastError();
+    } else {
+        e = cudaMemsetAsync(p.ws_counters, 0, Sched::counters_bytes(p.batch, p.num_kv_heads), s);
+    }
     if (e != cudaSuccess) return e;
     const int G = p.num_q_heads / p.num_kv_heads;
 #define PKV_DEC(D_, G_) \

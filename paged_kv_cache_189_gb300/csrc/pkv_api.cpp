@@ -174,8 +174,8 @@ Plan plan_attention(int batch, int max_q_rows, int Hq, int Hkv, int D, int max_k
     }
     pl.split_keys = keys;
     pl.splits = std::max(1, (max_kv_len + keys - 1) / keys);
-    // [scheduling counters][partial outputs][partial LSEs]
-    pl.ws_bytes = round_up(pkv::decode_counter_bytes(batch, Hkv), 256);
+    // [scheduling: counters, unit order][partial outputs][partial LSEs]
+    pl.ws_bytes = round_up(pkv::decode_sched_bytes(batch, Hkv, pl.splits), 256);
     if (pl.splits > 1) {
         const size_t states = static_cast<size_t>(batch) * max_q_rows * Hq * pl.splits;
         pl.ws_bytes += round_up(states * D * sizeof(float), 256) + round_up(states * sizeof(float), 256);
@@ -345,7 +345,7 @@ pkv_status paged_attention(const void* q, int64_t q_token_stride, int64_t q_head
     if (pl.kernel == Kernel::kDecode) {
         char* w = static_cast<char*>(workspace);
         p.ws_counters = reinterpret_cast<int*>(w);
-        w += round_up(pkv::decode_counter_bytes(batch, num_kv_heads), 256);
+        w += round_up(pkv::decode_sched_bytes(batch, num_kv_heads, pl.splits), 256);
         if (pl.splits > 1) {
             const size_t states = static_cast<size_t>(batch) * max_q_rows * num_q_heads * pl.splits;
             p.ws_o = reinterpret_cast<float*>(w);

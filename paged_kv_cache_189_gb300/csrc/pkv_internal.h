@@ -172,7 +172,7 @@ struct AttnParams {
 cudaError_t launch_decode(const AttnParams& p, const void* tmap_k, const void* tmap_v,
                           cudaStream_t s);
 bool decode_supported(int head_dim, int group);
-size_t decode_counter_bytes(int batch, int num_kv_heads);
+size_t decode_sched_bytes(int batch, int num_kv_heads, int splits);  // scheduling region of the workspace
 
 // Generic SIMT kernel: any rows, masks, group sizes; no splits.  A slow
 // cross-check of the fast kernels and the path for shapes they do not cover.
