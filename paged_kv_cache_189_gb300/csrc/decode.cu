@@ -101,6 +101,7 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
 constexpr int kPlanThreads = 1024;
 constexpr int kPlanMaxFull = 2047;  // full splits per sequence the planner orders
 constexpr int kPlanBuckets = 1024;  // length buckets of the partial splits
+constexpr int kPlanSmemSeqs = 4096; // sequences whose full-split order stays in shared memory
 
 __host__ __device__ constexpr size_t align256(size_t n) { return (n + 255) / 256 * 256; }
 
@@ -182,10 +183,16 @@ __global__ void __launch_bounds__(kPlanThreads) decode_plan_kernel(const AttnPar
     __shared__ int cnt_r[kPlanBuckets];       // partial splits per length bucket, then cursors
     __shared__ int warp_tot[32];
     __shared__ int n_empty, e_cur;
+    __shared__ int seq_smem[kPlanSmemSeqs];   // sequences in full-split order (small batches)
+    // the decode launch behind this one may start its prologue now; it waits
+    // for this grid's writes before reading any of them
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int B = p.batch, Hkv = p.num_kv_heads, SK = p.split_keys;
     const int nF = p.max_kv_len / SK + 1;     // full-split counts 0 .. nF - 1
     Sched sc(p.ws_counters, B, Hkv);
+    int* seq_at_pos = B <= kPlanSmemSeqs ? seq_smem : sc.seq_at_pos;
     const int tid = threadIdx.x;
+    int keys0 = -1;                           // row_keys of b = tid (the first pass's)
     for (int i = tid; i <= B * Hkv; i += kPlanThreads) sc.counters[i] = 0;
     for (int i = tid; i < nF + 1; i += kPlanThreads) cnt_f[i] = 0;
     for (int i = tid; i < kPlanBuckets; i += kPlanThreads) cnt_r[i] = 0;
@@ -194,8 +201,9 @@ __global__ void __launch_bounds__(kPlanThreads) decode_plan_kernel(const AttnPar
     auto bucket_of = [&](int r) {  // longer partial splits in higher buckets
         return static_cast<int>((static_cast<int64_t>(r) * kPlanBuckets) / SK);
     };
-    for (int b = tid; b < B; b += kPlanThreads) {
+    for (int b = tid, j = 0; b < B; b += kPlanThreads, ++j) {
         const int kv = row_keys(p, b);
+        if (j == 0) keys0 = kv;
         if (kv < 0) continue;
         const int f = kv / SK, r = kv - f * SK;
         atomicAdd(&cnt_f[f], 1);
@@ -221,11 +229,11 @@ __global__ void __launch_bounds__(kPlanThreads) decode_plan_kernel(const AttnPar
     // partial splits, longest bucket first: start of bucket k = #{buckets > k}
     const int partials = block_scan_exclusive(cnt_r, kPlanBuckets, warp_tot);  // #{< k}
     __syncthreads();
-    for (int b = tid; b < B; b += kPlanThreads) {
-        const int kv = row_keys(p, b);
+    for (int b = tid, j = 0; b < B; b += kPlanThreads, ++j) {
+        const int kv = j == 0 ? keys0 : row_keys(p, b);
         if (kv < 0) continue;
         const int f = kv / SK, r = kv - f * SK;
-        if (f > 0) sc.seq_at_pos[atomicAdd(&cnt_f[f], 1)] = b;
+        if (f > 0) seq_at_pos[atomicAdd(&cnt_f[f], 1)] = b;
         int at = -1, split = 0;
         if (r > 0) {
             // descending: the first slot of bucket k is partials - #{<= k}
@@ -248,7 +256,7 @@ __global__ void __launch_bounds__(kPlanThreads) decode_plan_kernel(const AttnPar
             if (gt_f[mid] * Hkv <= u) lo = mid; else hi = mid - 1;
         }
         const int idx = u - gt_f[lo] * Hkv;
-        sc.list[u] = make_int2(lo, sc.seq_at_pos[idx / Hkv] * Hkv + idx % Hkv);
+        sc.list[u] = make_int2(lo, seq_at_pos[idx / Hkv] * Hkv + idx % Hkv);
     }
     if (tid == 0) *sc.total = full_units + (partials + n_empty) * Hkv;
 }
@@ -459,6 +467,9 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks)
         flags[1] = 0;  // set when a consumer wait gives up
         fence_mbar_init();
     }
+    // launched behind the planner with programmatic serialisation: its unit
+    // order and zeroed counters are visible after this wait
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     __syncthreads();
 
     if (warp == kWarps) {
@@ -746,7 +757,8 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks)
 }
 
 template <int D, int G>
-cudaError_t launch_dg(const AttnParams& p, const void* tk, const void* tv, int dev, int sms, cudaStream_t s) {
+cudaError_t launch_dg(const AttnParams& p, const void* tk, const void* tv, int dev, int sms, bool after_plan,
+                      cudaStream_t s) {
     using S = DecodeSmem<D, G>;
     auto kern = decode_kernel<D, G>;
     // shared-memory opt-in and occupancy: once per device
@@ -763,9 +775,20 @@ cudaError_t launch_dg(const AttnParams& p, const void* tk, const void* tv, int d
     if (e != cudaSuccess) return e;
     const int64_t units = static_cast<int64_t>(p.batch) * p.num_kv_heads * p.num_splits;
     const int64_t grid = std::min<int64_t>(units, static_cast<int64_t>(std::max(per_sm, 1)) * sms);
-    kern<<<static_cast<unsigned>(grid), kThreads, S::kBytes, s>>>(
-        *static_cast<const CUtensorMap*>(tk), *static_cast<const CUtensorMap*>(tv), p);
-    return cudaGetLastError();
+    // behind the planner: programmatic serialisation lets the launch and the
+    // CTAs' prologue overlap the planner (the kernel waits for its writes)
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = S::kBytes;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = after_plan ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kern, *static_cast<const CUtensorMap*>(tk),
+                              *static_cast<const CUtensorMap*>(tv), p);
 }
 
 }  // namespace
@@ -789,7 +812,8 @@ cudaError_t launch_decode(const AttnParams& p, const void* tk, const void* tv, c
     if (e != cudaSuccess) return e;
     // the unit tickets and the per-(sequence, head) split counts start at zero;
     // the planner also writes the unit order
-    if (plan_listed(p)) {
+    const bool planned = plan_listed(p);
+    if (planned) {
         decode_plan_kernel<<<1, kPlanThreads, 0, s>>>(p);
         e = cudaGetLastError();
     } else {
@@ -798,7 +822,7 @@ cudaError_t launch_decode(const AttnParams& p, const void* tk, const void* tv, c
     if (e != cudaSuccess) return e;
     const int G = p.num_q_heads / p.num_kv_heads;
 #define PKV_DEC(D_, G_) \
-    if (p.head_dim == D_ && G == G_) return launch_dg<D_, G_>(p, tk, tv, dev, sms, s);
+    if (p.head_dim == D_ && G == G_) return launch_dg<D_, G_>(p, tk, tv, dev, sms, planned, s);
     PKV_DEC(128, 4) PKV_DEC(128, 2) PKV_DEC(128, 1)
     PKV_DEC(64, 4) PKV_DEC(64, 2) PKV_DEC(64, 1)
 #undef PKV_DEC
