@@ -61,6 +61,7 @@ constexpr int kSmemBytes = kXchOff + 2 * 2 * 4 * 32 * 4;
 static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
 constexpr uint32_t kTmemCols = 512;     // S0 [0,128), S1 [128,256), O [256,384)
 constexpr float kLazyRescale = 8.0f;    // move the running max only past 2^8 growth
+constexpr int kOrderMaxBatch = 128;     // longest-first dispatch up to this batch (B^2 ranking)
 
 // ---------------------------------------------------------------------------
 // tcgen05 wrappers
@@ -200,10 +201,34 @@ struct TileGeom {
     int b, kvh, split, r0, nrows, qreal, kv_len, t0, kb, key_hi, nt;
 };
 
-__device__ __forceinline__ TileGeom tile_geometry(const AttnParams& p, int TQ) {
+// The sequence at position `pos` when the batch is ordered by key count,
+// longest first (ties by index; any count order gives a permutation).  Every
+// thread of the block calls it; `scratch` holds 2 * batch + 1 ints of shared
+// memory that nothing else uses yet.
+__device__ int longest_first(const AttnParams& p, int pos, int* scratch) {
+    const int B = p.batch;
+    int* rank = scratch;
+    int* keys = scratch + B + 1;
+    for (int i = threadIdx.x; i < B; i += blockDim.x) {
+        rank[i] = 0;
+        keys[i] = p.kv_lens[i];
+    }
+    __syncthreads();
+    for (int pi = threadIdx.x; pi < B * B; pi += blockDim.x) {
+        const int b = pi / B, o = pi - b * B;
+        if (keys[o] > keys[b] || (keys[o] == keys[b] && o < b)) atomicAdd(&rank[b], 1);
+    }
+    __syncthreads();
+    for (int b = threadIdx.x; b < B; b += blockDim.x)
+        if (rank[b] == pos) rank[B] = b;
+    __syncthreads();
+    return rank[B];
+}
+
+__device__ __forceinline__ TileGeom tile_geometry(const AttnParams& p, int TQ, int b) {
     TileGeom g;
-    g.b = blockIdx.z / p.num_splits;
-    g.split = blockIdx.z - g.b * p.num_splits;
+    g.b = b;
+    g.split = blockIdx.z - (blockIdx.z / p.num_splits) * p.num_splits;
     g.kvh = blockIdx.y;
     g.r0 = p.q_indptr[g.b];
     g.nrows = min(p.q_indptr[g.b + 1] - g.r0, p.max_q_rows);
@@ -326,7 +351,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     TileGeom g;
     int grp_first = 0, grp_count = 0;
     if constexpr (!GRP) {
-        g = tile_geometry(p, TQ);
+        int b = blockIdx.z / p.num_splits;
+        if (p.order_by_keys) b = longest_first(p, b, reinterpret_cast<int*>(smem + kKOff));
+        g = tile_geometry(p, TQ, b);
         if (g.t0 >= g.nrows) return;  // tile past this sequence's rows (uniform)
     } else {
         g = group_geometry(p, TQ, grp_first, grp_count);
@@ -1502,8 +1529,19 @@ cudaError_t launch_one(const AttnParams& p, int rows, const void* tk, const void
     if (e != cudaSuccess) return e;
     const int TQ = kTileM / (G * REP);
     dim3 grid((rows + TQ - 1) / TQ, p.num_kv_heads, p.batch * p.num_splits);
+    // more than one wave of CTAs (one per SM) over a small batch: dispatch the
+    // longest sequences first, so the last wave holds the shortest ones
+    static DeviceOnce sm_count;
+    int sms = 0;
+    e = sm_count.get(dev, &sms, [](int d, int* v) {
+        return cudaDeviceGetAttribute(v, cudaDevAttrMultiProcessorCount, d);
+    });
+    if (e != cudaSuccess) return e;
+    AttnParams q = p;
+    q.order_by_keys = !GRP && p.batch >= 2 && p.batch <= kOrderMaxBatch &&
+                      static_cast<int64_t>(grid.x) * grid.y * grid.z > sms;
     kern<<<grid, kThreads, kSmemBytes, s>>>(*static_cast<const CUtensorMap*>(tk),
-                                            *static_cast<const CUtensorMap*>(tv), p);
+                                            *static_cast<const CUtensorMap*>(tv), q);
     return cudaGetLastError();
 }
 

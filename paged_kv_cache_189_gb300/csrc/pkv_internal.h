@@ -155,6 +155,9 @@ struct AttnParams {
     int* ws_counters;  // decode: [0] unit ticket, [1 + b*Hkv + h] finished splits
     bool checked;
     int32_t* err;
+    // one-tile kernel: block z takes the (z / num_splits)-th sequence by key
+    // count, longest first, so that a grid of several waves starts with them
+    bool order_by_keys;
     // shared-prefix groups (grouped tile mode, grp_perm != nullptr): block_table
     // holds the group rows, batch is the number of group slots, q_indptr the
     // original rows' query tokens; kv_lens and q_real are not used
