@@ -12,11 +12,12 @@
 //  * work unit = (split of split_keys keys, K/V head, sequence), handed out by
 //    an atomic ticket, so the kernel is persistent (a few CTAs per SM) and
 //    balances ragged lengths dynamically; the grid never depends on device
-//    lengths, so a call is graph-capturable.  A one-CTA planning launch before
-//    it orders the units: every full split first (split-major, sequences with
-//    more full splits first), then each sequence's partial last split, longest
-//    first, then the rows without keys -- so the launch ends on the shortest
-//    units instead of leaving SMs idle behind full-length ones.
+//    lengths, so a call is graph-capturable.  When the units outnumber the
+//    CTAs, a one-CTA planning launch before it orders them: every full split
+//    first (split-major, sequences with more full splits first), then each
+//    sequence's partial last split, longest first, then the rows without keys
+//    -- so the launch ends on the shortest units instead of leaving SMs idle
+//    behind full-length ones.
 //  * one producer lane per CTA fetches tickets, reads each ticket's unit from
 //    the planned list, copies the unit's G query rows into shared memory with bulk
 //    copies, and streams the unit's pages of one K/V head (32 x D of K and of
@@ -129,10 +130,8 @@ struct Sched {
     }
 };
 
-// whether the planner orders the units of this call (else: split-major order)
-__host__ __device__ inline bool plan_listed(const AttnParams& p) {
-    return p.max_kv_len / p.split_keys <= kPlanMaxFull;
-}
+// whether the planner can order the units of this call (else: split-major)
+inline bool plan_fits(const AttnParams& p) { return p.max_kv_len / p.split_keys <= kPlanMaxFull; }
 
 // The keys a decode row attends (0 for a padding row), or -1 for a sequence
 // without rows; the same reading of the inputs as the producer's.
@@ -480,7 +479,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks)
         const Sched sc(p.ws_counters, p.batch, Hkv);
         int* ticket = sc.counters;
         const int BH = p.batch * Hkv;
-        const bool listed = plan_listed(p);
+        const bool listed = p.planned;
         const int units = listed ? __ldcg(sc.total) : BH * S_;
         int i = 0;  // pages issued so far (ring position)
         bool alive = true;
@@ -757,7 +756,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks)
 }
 
 template <int D, int G>
-cudaError_t launch_dg(const AttnParams& p, const void* tk, const void* tv, int dev, int sms, bool after_plan,
+cudaError_t launch_dg(const AttnParams& p_in, const void* tk, const void* tv, int dev, int sms,
                       cudaStream_t s) {
     using S = DecodeSmem<D, G>;
     auto kern = decode_kernel<D, G>;
@@ -773,8 +772,21 @@ cudaError_t launch_dg(const AttnParams& p, const void* tk, const void* tv, int d
         return r;
     });
     if (e != cudaSuccess) return e;
-    const int64_t units = static_cast<int64_t>(p.batch) * p.num_kv_heads * p.num_splits;
+    const int64_t units = static_cast<int64_t>(p_in.batch) * p_in.num_kv_heads * p_in.num_splits;
     const int64_t grid = std::min<int64_t>(units, static_cast<int64_t>(std::max(per_sm, 1)) * sms);
+    // the unit tickets and the per-(sequence, head) split counts start at zero.
+    // With more units than CTAs the planner also orders the units (the tail
+    // then runs on the shortest); otherwise every unit starts at once and a
+    // plain reset is the shorter path
+    AttnParams p = p_in;
+    p.planned = units > grid && plan_fits(p);
+    if (p.planned) {
+        decode_plan_kernel<<<1, kPlanThreads, 0, s>>>(p);
+        e = cudaGetLastError();
+    } else {
+        e = cudaMemsetAsync(p.ws_counters, 0, Sched::counters_bytes(p.batch, p.num_kv_heads), s);
+    }
+    if (e != cudaSuccess) return e;
     // behind the planner: programmatic serialisation lets the launch and the
     // CTAs' prologue overlap the planner (the kernel waits for its writes)
     cudaLaunchConfig_t cfg = {};
@@ -786,7 +798,7 @@ cudaError_t launch_dg(const AttnParams& p, const void* tk, const void* tv, int d
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = after_plan ? 1 : 0;
+    cfg.numAttrs = p.planned ? 1 : 0;
     return cudaLaunchKernelEx(&cfg, kern, *static_cast<const CUtensorMap*>(tk),
                               *static_cast<const CUtensorMap*>(tv), p);
 }
@@ -810,19 +822,9 @@ cudaError_t launch_decode(const AttnParams& p, const void* tk, const void* tv, c
         return cudaDeviceGetAttribute(v, cudaDevAttrMultiProcessorCount, d);
     });
     if (e != cudaSuccess) return e;
-    // the unit tickets and the per-(sequence, head) split counts start at zero;
-    // the planner also writes the unit order
-    const bool planned = plan_listed(p);
-    if (planned) {
-        decode_plan_kernel<<<1, kPlanThreads, 0, s>>>(p);
-        e = cudaGetLastError();
-    } else {
-        e = cudaMemsetAsync(p.ws_counters, 0, Sched::counters_bytes(p.batch, p.num_kv_heads), s);
-    }
-    if (e != cudaSuccess) return e;
     const int G = p.num_q_heads / p.num_kv_heads;
 #define PKV_DEC(D_, G_) \
-    if (p.head_dim == D_ && G == G_) return launch_dg<D_, G_>(p, tk, tv, dev, sms, planned, s);
+    if (p.head_dim == D_ && G == G_) return launch_dg<D_, G_>(p, tk, tv, dev, sms, s);
     PKV_DEC(128, 4) PKV_DEC(128, 2) PKV_DEC(128, 1)
     PKV_DEC(64, 4) PKV_DEC(64, 2) PKV_DEC(64, 1)
 #undef PKV_DEC

@@ -153,6 +153,7 @@ struct AttnParams {
     float* ws_o;       // [rows_bound][Hq][splits][D] partial outputs (splits > 1)
     float* ws_lse;     // [rows_bound][Hq][splits]
     int* ws_counters;  // decode: [0] unit ticket, [1 + b*Hkv + h] finished splits
+    bool planned;      // decode: units taken from the planned order (else split-major)
     bool checked;
     int32_t* err;
     // one-tile kernel: block z takes the (z / num_splits)-th sequence by key
