@@ -500,7 +500,7 @@ def build_plan(name, rank, dev, stream):
         return StepPlan(case=case, cfg=cfg, metric=METRIC, unit=UNIT, work=kv_bytes, scale=1e9,
                         queries=rows, pre=[scatter], dominant=dom, post=[], aux=aux,
                         dom_label="paged_attention: persistent split-KV decode kernel with the split "
-                                  "merge fused in (plus a 2 KB counter memset)",
+                                  "merge fused in, behind a one-CTA launch that orders its work units",
                         dom_work=attn_bytes, bound="hbm", peak=peak_hbm, peak_unit="GB/s",
                         peak_src=f"{hbm_kind} hbm_gbs", h2d=(h2d_src, h2d_dst), d2h=d2h_src,
                         launches=3, traffic_sources=DECODE_SOURCES)
