@@ -101,6 +101,34 @@ def test_decode_zero_length_and_empty_sequences():
     assert_attention_close(out, lse, O, L, c)
 
 
+def test_decode_planned_order_edge_cases():
+    """A batch whose decode units outnumber the persistent CTAs, so they are
+    taken in the planned order (full splits first, partial splits longest
+    first), with the planner's edge cases: rows that attend nothing (padding),
+    sequences without rows, lengths ending exactly on a split boundary, a
+    one-key row."""
+    rng = np.random.default_rng(31)
+    B, Hq, Hkv, D = 96, 32, 8, 128
+    kv = rng.integers(1, 6000, size=B, endpoint=True)
+    # the automatic split size for this batch: ~6 units per resident CTA (3 per
+    # SM on 152 SMs), at least 512 keys and min(1024, one unit per CTA)
+    pairs, mk = B * Hkv, int(kv.max())
+    per = -(-mk * pairs // (6 * 456))
+    lo = max(512, min(1024, -(-mk * pairs // 456)))
+    sk = -(-max(lo, per) // 32) * 32
+    kv[0:4] = [sk, 2 * sk, 3 * sk, 1]
+    q_rows = np.ones(B, dtype=np.int64)
+    q_real = np.ones(B, dtype=np.int64)
+    q_rows[[10, 11]] = 0
+    q_real[[10, 11]] = 0          # sequences without rows
+    q_real[[20, 21, 22]] = 0      # padding rows: attend nothing, come back zero
+    c = wl.build_pool_case("planned_edges", 31, kv, q_rows, q_real, Hq, Hkv, D, mask="causal")
+    out, lse, *_, err = gpu_step(c)
+    O, L, *_ = oracle_step(c)
+    assert err == 0
+    assert_attention_close(out, lse, O, L, c)
+
+
 def test_decode_checked_mode_bad_page_flags_error():
     c = wl.random_case(14, batch=3, Hq=8, Hkv=2, D=128, kv_range=(40, 90))
     c.block_table[1, 0] = c.num_pages + 5

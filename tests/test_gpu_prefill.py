@@ -48,6 +48,26 @@ def test_few_rows_per_sequence(q_len):
     assert_attention_close(out, lse, O, L, c)
 
 
+def test_longest_first_dispatch_edge_cases():
+    """Several rows per sequence over a batch whose CTAs span more than one
+    wave, so each CTA takes its sequence in longest-first order: sequences
+    without rows, padding rows, equal lengths (ties broken by index)."""
+    rng = np.random.default_rng(41)
+    B, q_len = 40, 4
+    kv = rng.integers(q_len, 3000, size=B, endpoint=True)
+    kv[5:9] = 1234                 # ties
+    q_rows = np.full(B, q_len, dtype=np.int64)
+    q_real = np.full(B, q_len, dtype=np.int64)
+    q_rows[[3, 17]] = 0
+    q_real[[3, 17]] = 0            # sequences without rows
+    q_real[[7, 30]] = 2            # two real rows and two padding rows
+    c = wl.build_pool_case("longest_first", 41, kv, q_rows, q_real, 32, 8, 128, mask="causal")
+    out, lse, *_, err = gpu_step(c)
+    O, L, *_ = oracle_step(c)
+    assert err == 0
+    assert_attention_close(out, lse, O, L, c)
+
+
 @pytest.mark.parametrize("num_splits", [2, 5])
 def test_tile_kernel_key_splits(num_splits):
     c = wl.random_case(401, batch=2, Hq=32, Hkv=8, D=128, kv_range=(600, 1500), q_range=(20, 64),
