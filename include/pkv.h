@@ -151,7 +151,11 @@ pkv_status kv_scatter_slots(const void* k_src, const void* v_src, int64_t num_to
  *  out          device [total_rows][num_q_heads][head_dim], bf16 or f32 (dense)
  *  lse          device f32 [total_rows][num_q_heads] or NULL
  *  workspace    device scratch of paged_attention_workspace_size(...) bytes
- *               (256-byte aligned); may be NULL when that size is 0
+ *               (256-byte aligned); may be NULL when that size is 0.  It holds
+ *               the decode kernel's scheduling state (counters, the planned
+ *               order of its work units) and the split partial states; each
+ *               call initialises what it uses, so it needs no clearing, but one
+ *               workspace must not serve two calls in flight at once
  *  num_splits   key splits per sequence (split-KV); 0 = chosen from the bounds
  */
 size_t paged_attention_workspace_size(int batch, int max_q_rows, int num_q_heads,
