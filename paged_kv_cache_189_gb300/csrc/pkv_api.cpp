@@ -108,7 +108,12 @@ Plan plan_attention(int batch, int max_q_rows, int Hq, int Hkv, int D, int max_k
                     int num_splits, unsigned flags) {
     Plan pl;
     const int G = Hkv > 0 ? Hq / Hkv : 0;
-    if (!(flags & PKV_FLAG_SIMT_ONLY) && max_q_rows > 1 && pkv::attn_tc_supported(D, G)) {
+    // tensor-core tiles for several rows per sequence, and for single-row
+    // decode with a head group the decode kernel does not take (8 or 16 query
+    // heads per K/V head: one token x G heads fills a tile held four times)
+    const bool decode_kernel_takes = max_q_rows == 1 && pkv::decode_supported(D, G);
+    if (!(flags & PKV_FLAG_SIMT_ONLY) && max_q_rows >= 1 && !decode_kernel_takes &&
+        pkv::attn_tc_supported(D, G)) {
         // tensor-core tiles, one CTA per tile (two tiles when a sequence has
         // more rows than one holds).  With at most two waves of CTAs the last
         // wave can leave most SMs idle (every CTA of an unmasked or long

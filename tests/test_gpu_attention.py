@@ -40,7 +40,9 @@ def test_tiny_decode_scatter_into_free_slots():
 
 
 @pytest.mark.parametrize("Hq,Hkv,D", [(32, 8, 128), (8, 4, 128), (8, 8, 128), (4, 2, 64),
-                                      (16, 4, 64), (6, 6, 64)])
+                                      (16, 4, 64), (6, 6, 64),
+                                      # head groups of 8 and 16: the tile kernel
+                                      (64, 8, 128), (32, 2, 128)])
 @pytest.mark.parametrize("num_splits", [0, 1, 3])
 def test_decode_random(Hq, Hkv, D, num_splits):
     c = wl.random_case(100 + Hq + D + num_splits, batch=7, Hq=Hq, Hkv=Hkv, D=D,
@@ -98,6 +100,17 @@ def test_decode_zero_length_and_empty_sequences():
     c.slots[2] = -1
     out, lse, *_ = gpu_step(c)
     O, L, *_ = oracle_step(c)
+    assert_attention_close(out, lse, O, L, c)
+
+
+def test_decode_group_8_full_size():
+    """Single-row decode with 64 query / 8 K/V heads (head group 8) over the
+    GQA decode lengths, through the tensor-core tile kernel, every row against
+    the oracle."""
+    c = wl.gqa_decode(Hq=64, Hkv=8)
+    out, lse, kg, vg, err = gpu_step(c)
+    O, L, *_ = oracle_step(c)
+    assert err == 0
     assert_attention_close(out, lse, O, L, c)
 
 
