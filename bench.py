@@ -503,7 +503,10 @@ def build_plan(name, rank, dev, stream):
                                   "merge fused in, behind a one-CTA launch that orders its work units",
                         dom_work=attn_bytes, bound="hbm", peak=peak_hbm, peak_unit="GB/s",
                         peak_src=f"{hbm_kind} hbm_gbs", h2d=(h2d_src, h2d_dst), d2h=d2h_src,
-                        launches=3, traffic_sources=DECODE_SOURCES)
+                        # scatter, the unit-order planner (only when the units outnumber
+                        # the persistent CTAs; the tiny batch resets its counters with a
+                        # memset node instead) and the decode kernel
+                        launches=3 if name == "gqa_decode" else 2, traffic_sources=DECODE_SOURCES)
     if name == "multi_token_decode":
         attn_bytes, kv_bytes = decode_bytes(case)
         dom = attention_call(t["q"], t["bt"], t["kl"], t["qi"], t["qr"], out, lse, case.max_q_rows,
