@@ -444,7 +444,9 @@ def build_exact_window_plan(name, rank, dev, stream):
                     dom_work=flops / 1e12, bound="tensor", peak=peak_tc, peak_unit="TFLOP/s",
                     peak_src=f"{tc_kind} bf16_tflops (burst)",
                     h2d=([case.q, case.new_k, case.new_v], [t["q"], t["new_k"], t["new_v"]]),
-                    d2h=[out, lse], launches=3, traffic_sources=ATTN_TC_SOURCES)
+                    # two scatters, the tile kernel, the split reduce (both
+                    # exact-window workloads split their keys)
+                    d2h=[out, lse], launches=4, traffic_sources=ATTN_TC_SOURCES)
 
 
 def build_plan(name, rank, dev, stream):
@@ -605,7 +607,8 @@ def build_plan(name, rank, dev, stream):
                                   "concurrently on a second stream)",
                         dom_work=prefix_bytes, bound="hbm", peak=peak_hbm, peak_unit="GB/s",
                         peak_src=f"{hbm_kind} hbm_gbs", h2d=(h2d_src, h2d_dst), d2h=d2h_src,
-                        launches=6, traffic_sources=ATTN_TC_SOURCES)
+                        # scatter, the planner's two kernels, the grouped tile kernel
+                        launches=4, traffic_sources=ATTN_TC_SOURCES)
     if name in ("shared_prefix_fused", "shared_prefix_verify"):
         # the step plans the grouping on the device (plan_shared_prefix) and runs
         # every row's shared run + tail in one launch (shared_prefix_attention)
@@ -642,7 +645,9 @@ def build_plan(name, rank, dev, stream):
                                   "tails of a group per CTA), HBM-bound",
                         dom_work=prefix_bytes + tail_bytes + io_bytes, bound="hbm", peak=peak_hbm,
                         peak_unit="GB/s", peak_src=f"{hbm_kind} hbm_gbs", h2d=(h2d_src, h2d_dst),
-                        d2h=d2h_src, launches=3, traffic_sources=ATTN_TC_SOURCES)
+                        # scatter, prefix tile, the tail call (unit-order planner +
+                        # decode kernel), merge
+                        d2h=d2h_src, launches=5, traffic_sources=ATTN_TC_SOURCES)
     raise ValueError(name)
 
 
