@@ -93,6 +93,12 @@ def test_workspace_size(L):
     assert pkv.paged_attention_workspace_size(4, 16, 32, 8, 128, 8193,
                                               flags=pkv.PKV_FLAG_SIMT_ONLY) == 0
     assert pkv.paged_attention_workspace_size(0, 1, 32, 8, 128, 8193) == 0
+    # one row per sequence with a head group of 8 or 16 (head_dim 128) takes the
+    # tensor-core tile path: no decode scheduling region, and no split partials
+    # for a grid of more than two waves (64 sequences x 8 heads = 512 CTAs)
+    assert pkv.paged_attention_workspace_size(64, 1, 64, 8, 128, 8193) == 0
+    assert pkv.paged_attention_workspace_size(64, 1, 128, 8, 128, 8193) == 0
+    assert pkv.paged_attention_workspace_size(64, 1, 32, 8, 128, 8193) > 0   # group 4: decode kernel
 
 
 def test_scatter_host_validation(L):
