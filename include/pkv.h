@@ -157,10 +157,38 @@ pkv_status kv_scatter_slots(const void* k_src, const void* v_src, int64_t num_to
  *               call initialises what it uses, so it needs no clearing, but one
  *               workspace must not serve two calls in flight at once
  *  num_splits   key splits per sequence (split-KV); 0 = chosen from the bounds
+ *               and the current device's SM count ([SP] commit notes on
+ *               generation split-KV: split only when the grid under-fills the
+ *               SMs, chunks of at least 512 tokens)
+ *
+ * The split choice, and with it the workspace size, depends on the SM count
+ * of the device current at the call (152 when no device can be queried), so
+ * size the workspace with the device current that the call will use.
  */
 size_t paged_attention_workspace_size(int batch, int max_q_rows, int num_q_heads,
                                       int num_kv_heads, int head_dim, int max_kv_len,
                                       int num_splits, unsigned flags);
+
+/*
+ * pkv_plan_attention -- the launch plan paged_attention makes for these host
+ * bounds on a GPU with num_sms SMs (<= 0: the current device's count): which
+ * kernel runs (*kernel: a pkv_kernel value), the key splits per sequence and
+ * keys per split, and the workspace bytes (what paged_attention_workspace_size
+ * returns when num_sms is the current device's).  Host only: reads no device
+ * memory and launches nothing.  PKV_ERR_INVALID_ARG for non-positive sizes,
+ * head counts that do not divide, or a null output pointer.
+ */
+typedef enum {
+    PKV_KERNEL_NONE = 0,
+    PKV_KERNEL_DECODE = 1, /* persistent split-KV decode kernel (SIMT, TMA-fed)   */
+    PKV_KERNEL_TILE = 2,   /* tcgen05 / TMEM tile kernel (+ split reduce)         */
+    PKV_KERNEL_SIMT = 3    /* generic kernel (PKV_FLAG_SIMT_ONLY, other shapes)   */
+} pkv_kernel;
+
+pkv_status pkv_plan_attention(int batch, int max_q_rows, int num_q_heads, int num_kv_heads,
+                              int head_dim, int max_kv_len, int num_splits, unsigned flags,
+                              int num_sms, int* kernel, int* splits, int* split_keys,
+                              size_t* workspace_bytes);
 
 pkv_status paged_attention(const void* q, int64_t q_token_stride, int64_t q_head_stride,
                            const void* k_pool, const void* v_pool, int64_t num_pages,
@@ -407,7 +435,10 @@ pkv_status shared_prefix_attention(const void* q, int64_t q_token_stride, int64_
  *    paged_attention_workspace_size reports for the same arguments) returns
  *    PKV_ERR_WORKSPACE with a message, before anything is enqueued.
  *  - The first call with a given device current looks up the array's address
- *    on that device; make that first call before any stream capture.
+ *    on that device; make that first call before any stream capture.  The
+ *    address is looked up again when that device's context has changed since
+ *    (a cudaDeviceReset in between), so such a call must also come before
+ *    any capture.
  *  - Every call on a device uses the same array and leaves its contents
  *    behind (what must start at zero is cleared by each call), so calls that
  *    can overlap on the GPU (unordered streams) race and must be serialised.

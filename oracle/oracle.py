@@ -316,14 +316,23 @@ def rope_write_kv_paged(q, k_src, v_src, positions, cos_sin, slots, k_pool, v_po
     result), rotate its K heads the same way and write them, with its V heads
     unrotated, into pool slot ``slots[t]`` (negative: no write).
 
+    [SP] commit notes: rope_write_kv_paged rotates Q in place and writes the
+    rotated K and the V straight to the pool, at the absolute positions.
+
     ``q``: ``[T, Hq, D]`` bf16 bits; ``k_src``/``v_src``: ``[T, Hkv, D]`` bf16
     bits; ``cos_sin``: ``[max_pos, D]`` float (cos of the D/2 pairs, then their
     sin); pools ``[pages, P, Hkv, D]`` bf16 bits.
 
-    Returns ``(q_rot float64 [T, Hq, D], k_rot float64 [T, Hkv, D],
-    k_pool_out, v_pool_out)``: the rotated values exactly (the device rounds
-    them to bf16), and the pools with V copied bit for bit and the K slots
-    marked by the rows of ``k_rot`` (compare K through ``k_rot``).
+    Returns ``(q_rot, k_rot, k_pool_out, v_pool_out, k_written)``:
+
+    * ``q_rot`` float64 ``[T, Hq, D]`` and ``k_rot`` float64 ``[T, Hkv, D]``:
+      the rotated values exactly (the device rounds them to bf16);
+    * ``k_pool_out`` float64 ``[pages, P, Hkv, D]``: the K pool after the
+      write, every slot ``slots[t] >= 0`` holding the exact ``k_rot[t]`` and
+      every other slot the exact value of its unchanged bf16 entry;
+    * ``v_pool_out``: the V pool's bf16 bits after the write (V is copied bit
+      for bit);
+    * ``k_written`` bool ``[pages, P]``: the slots the call wrote.
     """
     qf = bf16_to_f64(bf16_bits(q))
     kf = bf16_to_f64(bf16_bits(k_src))
@@ -334,16 +343,19 @@ def rope_write_kv_paged(q, k_src, v_src, positions, cos_sin, slots, k_pool, v_po
     sin = cs[pos, h:][:, None, :]
     q_rot = rope_rotate(qf, cos, sin)
     k_rot = rope_rotate(kf, cos, sin)
-    k_out = np.array(bf16_bits(k_pool), copy=True)
+    k_out = bf16_to_f64(bf16_bits(k_pool))
     v_out = np.array(bf16_bits(v_pool), copy=True)
     vb = bf16_bits(v_src)
     P = k_out.shape[1]
+    written = np.zeros(k_out.shape[:2], dtype=bool)
     for t, s_ in enumerate(np.asarray(slots)):
         s_ = int(s_)
         if s_ < 0:
             continue
+        k_out[s_ // P, s_ % P] = k_rot[t]
         v_out[s_ // P, s_ % P] = vb[t]
-    return q_rot, k_rot, k_out, v_out
+        written[s_ // P, s_ % P] = True
+    return q_rot, k_rot, k_out, v_out, written
 
 
 # ----------------------------------------------------------------------------

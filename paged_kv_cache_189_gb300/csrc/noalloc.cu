@@ -12,12 +12,15 @@
 //
 // The array is PKV_NO_ALLOC_SCRATCH_BYTES large and lives on every GPU that
 // loads the library until the process exits.  Its device address is looked up
-// once per device, on the first call made with that device current; that
-// first call should therefore happen before any stream capture.  All calls on
-// a device share the array, so calls that may run at the same time on the GPU
-// (different streams without ordering) race on it.  The counters that must
-// start at zero are cleared by every call (as paged_attention does); the
-// partial outputs are fully rewritten before they are read.
+// on the first call made with a device current, and again whenever that
+// device's context has changed since (after cudaDeviceReset the module is
+// loaded anew and the array may move); that first call should therefore
+// happen before any stream capture.  All calls on a device share the array,
+// so calls that may run at the same time on the GPU (different streams
+// without ordering) race on it.  The counters that must start at zero are
+// cleared by every call (as paged_attention does); the partial outputs are
+// fully rewritten before they are read.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <cstdio>
@@ -33,6 +36,24 @@ static __device__ __align__(256) unsigned char g_scratch[PKV_NO_ALLOC_SCRATCH_BY
 constexpr int kMaxDevices = 128;
 std::mutex g_mu;
 void* g_scratch_addr[kMaxDevices] = {};
+CUcontext g_scratch_ctx[kMaxDevices] = {};
+
+// cuCtxGetCurrent through the runtime's driver entry point (no link-time
+// dependency on libcuda); null if the driver does not offer it.
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+CtxGetCurrentFn ctx_get_current_fn() {
+    static CtxGetCurrentFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<CtxGetCurrentFn>(p);
+    });
+    return fn;
+}
 
 // Device address of the scratch array on the current device (host code may
 // not use the symbol itself as a pointer).
@@ -43,8 +64,18 @@ pkv_status scratch_on_current_device(void** out) {
         return pkv::report(PKV_ERR_CUDA, "paged_attention_no_alloc: cudaGetDevice failed");
     if (dev < 0 || dev >= kMaxDevices)
         return pkv::report(PKV_ERR_UNSUPPORTED, "paged_attention_no_alloc: device index too large");
+    // the context current on this thread (null before the runtime has made
+    // one current; the lookup below does that)
+    auto current_ctx = [] {
+        CUcontext c = nullptr;
+        if (auto fn = ctx_get_current_fn()) {
+            if (fn(&c) != CUDA_SUCCESS) c = nullptr;
+        }
+        return c;
+    };
+    const CUcontext ctx = current_ctx();
     std::lock_guard<std::mutex> lock(g_mu);
-    if (!g_scratch_addr[dev]) {
+    if (!g_scratch_addr[dev] || !ctx || g_scratch_ctx[dev] != ctx) {
         void* p = nullptr;
         e = cudaGetSymbolAddress(&p, g_scratch);
         if (e != cudaSuccess || !p) {
@@ -54,6 +85,7 @@ pkv_status scratch_on_current_device(void** out) {
             return pkv::report(PKV_ERR_CUDA, msg);
         }
         g_scratch_addr[dev] = p;
+        g_scratch_ctx[dev] = current_ctx();
     }
     *out = g_scratch_addr[dev];
     return PKV_OK;

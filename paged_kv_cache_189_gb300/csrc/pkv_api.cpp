@@ -10,6 +10,7 @@
 #include <cstdio>
 #include <cstring>
 #include <algorithm>
+#include <atomic>
 #include <mutex>
 #include <string>
 
@@ -98,14 +99,65 @@ struct Plan {
 };
 
 constexpr int kDecodeSplitKeys = 512;  // 16 pages: the pages' minimum split of 512 tokens
-constexpr int kPlanSMs = 152;          // GB300; only shapes the split choice
+constexpr int kDefaultSMs = 152;       // GB300: planned for when no device can be queried
 constexpr int kTileKeys = 128;         // key tile of the tensor-core kernel
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// SM count of the current device, cached per device; kDefaultSMs when no
+// device can be queried (a host without a GPU sizing workspaces).  The split
+// choice and the workspace size depend on it, so a workspace sized with one
+// device current fits the calls made with that device current.
+int current_device_sms() {
+    constexpr int kMaxDev = 64;
+    static std::atomic<int> cache[kMaxDev];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return kDefaultSMs;
+    }
+    if (dev >= 0 && dev < kMaxDev) {
+        const int v = cache[dev].load(std::memory_order_relaxed);
+        if (v > 0) return v;
+    }
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) {
+        cudaGetLastError();
+        return kDefaultSMs;
+    }
+    if (dev >= 0 && dev < kMaxDev) cache[dev].store(sms, std::memory_order_relaxed);
+    return sms;
+}
+
+// Key splits of the tile kernels: with at most two waves of CTAs the last
+// wave can leave most SMs idle (every CTA of an unmasked or long causal row
+// runs about as long as the others), so the keys are split to the count that
+// minimises waves / splits, plus ~2 % of a CTA per split for the partial
+// states and their merge, when that saves at least 10 %; splits keep >= 512
+// keys.  More CTAs than that are balanced by the block scheduler.
+int tile_splits(int64_t ctas, int max_keys, int num_splits, int sms) {
+    if (num_splits > 0) return num_splits;
+    int s = 1;
+    if (ctas <= 2 * static_cast<int64_t>(sms)) {
+        const int s_max = std::max(1, std::min(8, max_keys / 512));
+        const double unsplit = static_cast<double>((ctas + sms - 1) / sms);
+        double best = unsplit;
+        for (int c = 2; c <= s_max; ++c) {
+            const double waves = static_cast<double>((ctas * c + sms - 1) / sms);
+            const double cost = waves / c + 0.02 * c;
+            if (cost < best - 1e-9) {
+                best = cost;
+                s = c;
+            }
+        }
+        if (best > 0.9 * unsplit) s = 1;
+    }
+    return s;
+}
+
 
 Plan plan_attention(int batch, int max_q_rows, int Hq, int Hkv, int D, int max_kv_len,
-                    int num_splits, unsigned flags) {
+                    int num_splits, unsigned flags, int sms) {
     Plan pl;
     const int G = Hkv > 0 ? Hq / Hkv : 0;
     // tensor-core tiles for several rows per sequence, and for single-row
@@ -115,34 +167,12 @@ Plan plan_attention(int batch, int max_q_rows, int Hq, int Hkv, int D, int max_k
     if (!(flags & PKV_FLAG_SIMT_ONLY) && max_q_rows >= 1 && !decode_kernel_takes &&
         pkv::attn_tc_supported(D, G)) {
         // tensor-core tiles, one CTA per tile (two tiles when a sequence has
-        // more rows than one holds).  With at most two waves of CTAs the last
-        // wave can leave most SMs idle (every CTA of an unmasked or long
-        // causal row runs about as long as the others), so the keys are split
-        // to the count that minimises waves / splits, plus ~2 % of a CTA per
-        // split for the partial states and their merge, when that saves at
-        // least 10 %; splits keep >= 512 keys.  More CTAs than that are
-        // balanced by the block scheduler.
+        // more rows than one holds), keys split as tile_splits chooses.
         pl.kernel = Kernel::kTile;
         const int tq = pkv::attn_tc_rows_per_tile(G);
         const int rows_per_cta = max_q_rows > tq ? 2 * tq : tq;
         const int64_t ctas = static_cast<int64_t>((max_q_rows + rows_per_cta - 1) / rows_per_cta) * Hkv * batch;
-        int s = 1;
-        if (num_splits > 0) {
-            s = num_splits;
-        } else if (ctas <= 2 * kPlanSMs) {
-            const int s_max = std::max(1, std::min(8, max_kv_len / 512));
-            const double unsplit = static_cast<double>((ctas + kPlanSMs - 1) / kPlanSMs);
-            double best = unsplit;
-            for (int c = 2; c <= s_max; ++c) {
-                const double waves = static_cast<double>((ctas * c + kPlanSMs - 1) / kPlanSMs);
-                const double cost = waves / c + 0.02 * c;
-                if (cost < best - 1e-9) {
-                    best = cost;
-                    s = c;
-                }
-            }
-            if (best > 0.9 * unsplit) s = 1;
-        }
+        const int s = tile_splits(ctas, max_kv_len, num_splits, sms);
         const int per = (max_kv_len + s - 1) / std::max(s, 1);
         pl.split_keys = std::max(kTileKeys, (per + kTileKeys - 1) / kTileKeys * kTileKeys);
         pl.splits = std::max(1, (max_kv_len + pl.split_keys - 1) / pl.split_keys);
@@ -169,7 +199,7 @@ Plan plan_attention(int batch, int max_q_rows, int Hq, int Hkv, int D, int max_k
         const int per = (max_kv_len + num_splits - 1) / num_splits;
         keys = std::max(32, (per + 31) / 32 * 32);
     } else {
-        const int64_t resident = 3 * kPlanSMs;
+        const int64_t resident = 3 * static_cast<int64_t>(sms);
         const int64_t pairs = static_cast<int64_t>(batch) * Hkv;
         const int64_t target_units = 6 * resident;
         const int64_t per = (static_cast<int64_t>(max_kv_len) * pairs + target_units - 1) / target_units;
@@ -249,8 +279,29 @@ size_t paged_attention_workspace_size(int batch, int max_q_rows, int num_q_heads
     if (batch <= 0 || max_q_rows <= 0 || num_q_heads <= 0 || num_kv_heads <= 0 || max_kv_len < 0)
         return 0;
     return plan_attention(batch, max_q_rows, num_q_heads, num_kv_heads, head_dim, max_kv_len,
-                          num_splits, flags)
+                          num_splits, flags, current_device_sms())
         .ws_bytes;
+}
+
+pkv_status pkv_plan_attention(int batch, int max_q_rows, int num_q_heads, int num_kv_heads,
+                              int head_dim, int max_kv_len, int num_splits, unsigned flags,
+                              int num_sms, int* kernel, int* splits, int* split_keys,
+                              size_t* workspace_bytes) {
+    if (batch <= 0 || max_q_rows <= 0 || num_q_heads <= 0 || num_kv_heads <= 0 || max_kv_len < 0 ||
+        num_splits < 0 || num_q_heads % num_kv_heads != 0)
+        return fail(PKV_ERR_INVALID_ARG, "plan: sizes must be positive, heads a multiple of K/V heads");
+    if (!kernel || !splits || !split_keys || !workspace_bytes)
+        return fail(PKV_ERR_INVALID_ARG, "plan: null output pointer");
+    const Plan pl = plan_attention(batch, max_q_rows, num_q_heads, num_kv_heads, head_dim, max_kv_len,
+                                   num_splits, flags, num_sms > 0 ? num_sms : current_device_sms());
+    *kernel = pl.kernel == Kernel::kDecode ? static_cast<int>(PKV_KERNEL_DECODE)
+            : pl.kernel == Kernel::kTile   ? static_cast<int>(PKV_KERNEL_TILE)
+            : pl.kernel == Kernel::kSimt   ? static_cast<int>(PKV_KERNEL_SIMT)
+                                           : static_cast<int>(PKV_KERNEL_NONE);
+    *splits = pl.splits;
+    *split_keys = pl.split_keys;
+    *workspace_bytes = pl.ws_bytes;
+    return ok();
 }
 
 pkv_status paged_attention(const void* q, int64_t q_token_stride, int64_t q_head_stride,
@@ -302,7 +353,7 @@ pkv_status paged_attention(const void* q, int64_t q_token_stride, int64_t q_head
         return fail(PKV_ERR_INVALID_ARG, "attention: checked mode needs an error flag");
 
     const Plan pl = plan_attention(batch, max_q_rows, num_q_heads, num_kv_heads, head_dim,
-                                   max_kv_len, num_splits, flags);
+                                   max_kv_len, num_splits, flags, current_device_sms());
     if (pl.ws_bytes > 0) {
         if (!workspace || workspace_bytes < pl.ws_bytes || !aligned(workspace, 256))
             return fail(PKV_ERR_WORKSPACE, "attention: workspace needs %zu bytes, 256-byte aligned",
@@ -380,29 +431,13 @@ namespace {
 // the groups' count is known only on the device, so the host bound (every
 // slot a group) sizes the choice, like plan_attention's tile rule.
 Plan plan_grouped(int batch, int max_q_len, int max_group_tokens, int max_group_keys, int Hq, int Hkv,
-                  int D, int num_splits) {
+                  int D, int num_splits, int sms) {
     Plan pl;
     pl.kernel = Kernel::kTile;
     const int G = Hkv > 0 ? Hq / Hkv : 1;
     const int tq = pkv::attn_tc_rows_per_tile(G);
     const int64_t ctas = static_cast<int64_t>((max_group_tokens + tq - 1) / tq) * Hkv * batch;
-    int s = 1;
-    if (num_splits > 0) {
-        s = num_splits;
-    } else if (ctas <= 2 * kPlanSMs) {
-        const int s_max = std::max(1, std::min(8, max_group_keys / 512));
-        const double unsplit = static_cast<double>((ctas + kPlanSMs - 1) / kPlanSMs);
-        double best = unsplit;
-        for (int c = 2; c <= s_max; ++c) {
-            const double waves = static_cast<double>((ctas * c + kPlanSMs - 1) / kPlanSMs);
-            const double cost = waves / c + 0.02 * c;
-            if (cost < best - 1e-9) {
-                best = cost;
-                s = c;
-            }
-        }
-        if (best > 0.9 * unsplit) s = 1;
-    }
+    const int s = tile_splits(ctas, max_group_keys, num_splits, sms);
     const int per = (max_group_keys + s - 1) / std::max(s, 1);
     pl.split_keys = std::max(kTileKeys, (per + kTileKeys - 1) / kTileKeys * kTileKeys);
     pl.splits = std::max(1, (max_group_keys + pl.split_keys - 1) / pl.split_keys);
@@ -419,7 +454,7 @@ size_t shared_prefix_attention_workspace_size(int batch, int max_q_len, int max_
                                               int head_dim, int num_splits) {
     if (batch <= 0 || max_q_len <= 0 || max_group_tokens <= 0 || num_kv_heads <= 0) return 0;
     return plan_grouped(batch, max_q_len, max_group_tokens, max_group_keys, num_q_heads, num_kv_heads,
-                        head_dim, num_splits)
+                        head_dim, num_splits, current_device_sms())
         .ws_bytes;
 }
 
@@ -463,7 +498,7 @@ pkv_status shared_prefix_attention(const void* q, int64_t q_token_stride, int64_
     if (group_row_stride < (static_cast<int64_t>(max_group_keys) + 31) / 32)
         return fail(PKV_ERR_INVALID_ARG, "shared prefix: group_row_stride below max_group_keys / 32");
     const Plan pl = plan_grouped(batch, max_q_len, max_group_tokens, max_group_keys, num_q_heads,
-                                 num_kv_heads, head_dim, num_splits);
+                                 num_kv_heads, head_dim, num_splits, current_device_sms());
     if (pl.ws_bytes > 0 && (!workspace || workspace_bytes < pl.ws_bytes || !aligned(workspace, 256)))
         return fail(PKV_ERR_WORKSPACE, "shared prefix: workspace needs %zu bytes, 256-byte aligned",
                     pl.ws_bytes);

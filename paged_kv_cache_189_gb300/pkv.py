@@ -28,7 +28,7 @@ EXPORTED = ("pkv_status_string", "pkv_last_error", "kv_scatter_slots",
             "paged_attention_workspace_size", "paged_attention", "merge_attn_states",
             "rotate_rows", "paged_attention_no_alloc", "rope_write_kv_paged", "copy_kv_slots",
             "causal_layout", "plan_shared_prefix", "shared_prefix_attention",
-            "shared_prefix_attention_workspace_size")
+            "shared_prefix_attention_workspace_size", "pkv_plan_attention")
 NO_ALLOC_SCRATCH_BYTES = 32 << 20
 
 _vp, _i64, _i32, _u32, _f32, _sz = (ctypes.c_void_p, ctypes.c_int64, ctypes.c_int,
@@ -39,6 +39,8 @@ _SIGNATURES = {
     "kv_scatter_slots": (_i32, [_vp, _vp, _i64, _i64, _i32, _i32, _i64, _i64, _vp, _vp, _vp,
                                 _vp, _vp, _i64, _i32, _i64, _i32, _u32, _vp, _vp]),
     "paged_attention_workspace_size": (_sz, [_i32, _i32, _i32, _i32, _i32, _i32, _i32, _u32]),
+    "pkv_plan_attention": (_i32, [_i32, _i32, _i32, _i32, _i32, _i32, _i32, _u32, _i32, _vp, _vp, _vp,
+                                  _vp]),
     "paged_attention": (_i32, [_vp, _i64, _i64, _vp, _vp, _i64, _i32, _i64, _vp, _i64, _vp, _vp,
                                _vp, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _f32, _vp,
                                _i32, _vp, _vp, _sz, _i32, _u32, _vp, _vp]),
@@ -150,6 +152,22 @@ def paged_attention_workspace_size(batch, max_q_rows, num_q_heads, num_kv_heads,
                                    max_kv_len, num_splits=0, flags=0) -> int:
     return int(lib().paged_attention_workspace_size(batch, max_q_rows, num_q_heads, num_kv_heads,
                                                     head_dim, max_kv_len, num_splits, flags))
+
+
+PKV_KERNEL_NONE, PKV_KERNEL_DECODE, PKV_KERNEL_TILE, PKV_KERNEL_SIMT = range(4)
+
+
+def plan_attention(batch, max_q_rows, num_q_heads, num_kv_heads, head_dim, max_kv_len,
+                   num_splits=0, flags=0, num_sms=0) -> dict:
+    """The launch plan of ``paged_attention`` for these host bounds on a GPU
+    with ``num_sms`` SMs (0: the current device's): kernel, splits, keys per
+    split and workspace bytes."""
+    k, s, sk, ws = ctypes.c_int(), ctypes.c_int(), ctypes.c_int(), ctypes.c_size_t()
+    st = lib().pkv_plan_attention(batch, max_q_rows, num_q_heads, num_kv_heads, head_dim, max_kv_len,
+                                  num_splits, flags, num_sms, ctypes.byref(k), ctypes.byref(s),
+                                  ctypes.byref(sk), ctypes.byref(ws))
+    _check("pkv_plan_attention", st)
+    return {"kernel": k.value, "splits": s.value, "split_keys": sk.value, "workspace_bytes": ws.value}
 
 
 def paged_attention(q, k_pool, v_pool, block_table, kv_lens, q_indptr, out, *, q_real=None,

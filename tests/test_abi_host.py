@@ -170,3 +170,34 @@ def test_plan_and_shared_prefix_host_validation(L):
     assert spa(out=None) == pkv.PKV_ERR_INVALID_ARG
     assert spa(row_stride=63) == pkv.PKV_ERR_INVALID_ARG     # row narrower than max_group_keys
     assert pkv.shared_prefix_attention_workspace_size(16, 1, 8, 2048, 32, 8, 128) >= 0
+
+
+def test_plan_follows_the_sm_count(L):
+    """The split planner sizes its choice by the GPU's SM count, so the same
+    bounds plan differently on GPUs of different sizes; with no device to query
+    (this host) the workspace size is the 152-SM plan's."""
+    # exact-window denoising forward: 25 CTAs of two 32-token tiles x 8 K/V
+    # heads = 200 CTAs.  On 152 SMs two waves, so 3 key splits (4 waves of
+    # thirds, 1.39 against 2 unsplit); on 200 SMs one wave, no split; on 100
+    # SMs exactly two waves that no split count shortens by 10 %
+    p152 = pkv.plan_attention(1, 1576, 32, 8, 128, 39518, num_sms=152)
+    p200 = pkv.plan_attention(1, 1576, 32, 8, 128, 39518, num_sms=200)
+    p100 = pkv.plan_attention(1, 1576, 32, 8, 128, 39518, num_sms=100)
+    assert p152["kernel"] == p200["kernel"] == pkv.PKV_KERNEL_TILE
+    assert (p152["splits"], p200["splits"], p100["splits"]) == (3, 1, 1)
+    assert p152["workspace_bytes"] > 0 and p200["workspace_bytes"] == 0
+    # decode: ~6 work units per resident CTA (3 per SM): 8193 keys x 512
+    # (sequence, head) pairs / (6 x 456) -> 1536 keys per split on 152 SMs,
+    # 3072 on 76
+    d152 = pkv.plan_attention(64, 1, 32, 8, 128, 8193, num_sms=152)
+    d76 = pkv.plan_attention(64, 1, 32, 8, 128, 8193, num_sms=76)
+    assert d152["kernel"] == d76["kernel"] == pkv.PKV_KERNEL_DECODE
+    assert (d152["split_keys"], d152["splits"]) == (1536, 6)
+    assert (d76["split_keys"], d76["splits"]) == (3072, 3)
+    assert d76["workspace_bytes"] < d152["workspace_bytes"]
+    # workspace_size plans for the current device (here: none -> 152 SMs)
+    assert pkv.paged_attention_workspace_size(64, 1, 32, 8, 128, 8193) == d152["workspace_bytes"]
+    assert pkv.paged_attention_workspace_size(1, 1576, 32, 8, 128, 39518) == p152["workspace_bytes"]
+    # bad arguments are refused on the host
+    with pytest.raises(pkv.PkvError):
+        pkv.plan_attention(4, 1, 30, 8, 128, 100)

@@ -123,12 +123,10 @@ def test_decode_planned_order_edge_cases():
     rng = np.random.default_rng(31)
     B, Hq, Hkv, D = 96, 32, 8, 128
     kv = rng.integers(1, 6000, size=B, endpoint=True)
-    # the automatic split size for this batch: ~6 units per resident CTA (3 per
-    # SM on 152 SMs), at least 512 keys and min(1024, one unit per CTA)
-    pairs, mk = B * Hkv, int(kv.max())
-    per = -(-mk * pairs // (6 * 456))
-    lo = max(512, min(1024, -(-mk * pairs // 456)))
-    sk = -(-max(lo, per) // 32) * 32
+    # the automatic split size for this batch on this device's SM count (~6
+    # units per resident CTA, at least 512 keys)
+    sk = pkv.plan_attention(B, 1, Hq, Hkv, D, int(kv.max()))["split_keys"]
+    assert 3 * sk <= int(kv.max())
     kv[0:4] = [sk, 2 * sk, 3 * sk, 1]
     q_rows = np.ones(B, dtype=np.int64)
     q_real = np.ones(B, dtype=np.int64)

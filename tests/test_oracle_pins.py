@@ -441,10 +441,10 @@ def test_rope_write_kv_paged_writes_v_exactly_and_skips_sentinels():
     v = wl.randn_bf16((T, Hkv, D), gen)
     kp = wl.randn_bf16((pages, 32, Hkv, D), gen)
     vp = wl.randn_bf16((pages, 32, Hkv, D), gen)
-    table, _ = _cos_sin_table(64, D)
+    table, ang = _cos_sin_table(64, D)
     pos = np.array([3, 0, 63, 10, 11, 12])
     slots = np.array([5, 40, -1, 70, 2, 33], dtype=np.int64)
-    q_rot, k_rot, k_out, v_out = orc.rope_write_kv_paged(q, k, v, pos, table, slots, kp, vp)
+    q_rot, k_rot, k_out, v_out, written = orc.rope_write_kv_paged(q, k, v, pos, table, slots, kp, vp)
     ref_v = bits(vp).reshape(-1, Hkv, D).copy()
     ok = slots >= 0
     ref_v[slots[ok]] = bits(v)[ok]
@@ -452,6 +452,38 @@ def test_rope_write_kv_paged_writes_v_exactly_and_skips_sentinels():
     # token 1 sits at position 0: unrotated
     np.testing.assert_array_equal(q_rot[1], f64(q)[1])
     np.testing.assert_array_equal(k_rot[1], f64(k)[1])
+    # the K pool: numpy fancy-index assignment of the rotated rows, each rotated
+    # as complex numbers (a different formulation), every other slot unchanged
+    z = (f64(k)[..., :D // 2] + 1j * f64(k)[..., D // 2:]) * np.exp(1j * ang[pos])[:, None, :]
+    ref_k = f64(kp).reshape(-1, Hkv, D).copy()
+    ref_k[slots[ok]] = np.concatenate([z.real, z.imag], axis=-1)[ok]
+    np.testing.assert_allclose(k_out.reshape(-1, Hkv, D), ref_k, rtol=1e-13, atol=1e-13)
+    ref_w = np.zeros(pages * 32, dtype=bool)
+    ref_w[slots[ok]] = True
+    np.testing.assert_array_equal(written.reshape(-1), ref_w)
+    np.testing.assert_array_equal(k_out.reshape(-1, Hkv, D)[~ref_w], f64(kp).reshape(-1, Hkv, D)[~ref_w])
+
+
+def test_rope_write_kv_paged_slot_placement_is_pinned():
+    """Planted placement mistakes (the K row written at the previous slot, or
+    the sentinel token written at slot 0) change the oracle's K pool: a
+    distinct random row lands in every written slot, so the pool alone names
+    where each rotated row went."""
+    gen = torch.Generator().manual_seed(4)
+    T, Hkv, D, pages = 5, 1, 8, 1
+    k = wl.randn_bf16((T, Hkv, D), gen)
+    kp = wl.randn_bf16((pages, 32, Hkv, D), gen)
+    table, _ = _cos_sin_table(8, D)
+    pos = np.zeros(T, dtype=np.int64)          # identity rotation: K rows copied exactly
+    slots = np.array([7, -1, 3, 30, 12], dtype=np.int64)
+    _, _, k_out, _, written = orc.rope_write_kv_paged(k.repeat(1, 2, 1), k, k, pos, table, slots, kp, kp)
+    flat = k_out.reshape(-1, Hkv, D)
+    for t, s_ in enumerate(slots):
+        if s_ >= 0:
+            np.testing.assert_array_equal(flat[s_], f64(k)[t])
+            assert not np.array_equal(flat[s_ - 1], f64(k)[t])
+    assert written.sum() == 4 and not written.reshape(-1)[0]
+    np.testing.assert_array_equal(flat[0], f64(kp).reshape(-1, Hkv, D)[0])
 
 
 def test_copy_kv_slots_matches_fancy_indexing_across_layers():
