@@ -2,17 +2,24 @@
 
 One step = one pass of the hot path over one batch of synthetic input:
 ``kv_scatter_slots`` of this step's new K/V rows, then ``paged_attention``
-(split-KV decode kernel + split reduction).  The default workload is the GQA
-decode batch (64 sequences, 32 query / 8 K/V heads, head_dim 128, 32-token
-pages, cached lengths U[512, 8192], one new token each); the metric is the
-K/V bytes the attention reads per second (paged decode KV GB/s), with
-queries/s and the fraction of the measured HBM peak alongside.
+(and, per workload, the merge or the rotation of the rolling buffer).  The
+headline workload is the GQA decode batch (64 sequences, 32 query / 8 K/V
+heads, head_dim 128, 32-token pages, cached lengths U[512, 8192], one new
+token each); the metric is the K/V bytes the attention reads per second
+(paged decode KV GB/s), with queries/s and the fraction of the measured HBM
+peak alongside.  The same JSON line carries, under ``workloads``, every other
+workload measured the same way (chunked causal prefill and the block-causal
+video step in prefill TFLOP/s; the shared-prefix step, its one-launch form and
+the plain-decode ablation, multi-token decode and tiny decode in KV GB/s; the
+exact-window denoising forward in prefill TFLOP/s), each with its roofline,
+clocks, end-to-end figure and the fp64 oracle's time on the host cores.
 
-Usage: ``python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]``.
-Under torchrun every rank runs its own replica of the workload (seed + rank:
-the sequences shard across GPUs with no collective on the data path; weak
-scaling); rank 0 prints one JSON line.  ``--impl reference`` times the fp64
-CPU oracle on a bounded sample of the same workload instead.
+Usage: ``python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+[--workload NAME] [--only]``.  ``--only`` measures just ``--workload``.
+Under torchrun every rank runs its own independent replica of each workload
+(seed + rank: weak scaling with no collective on the data path); rank 0 prints
+one JSON line.  ``--impl reference`` times the fp64 CPU oracle on a bounded
+sample of the same workload instead.
 """
 from __future__ import annotations
 
@@ -51,12 +58,20 @@ def parse():
     ap.add_argument("--workload", default="gqa_decode",
                     choices=["gqa_decode", "chunked_prefill", "block_causal_video",
                              "shared_prefix", "shared_prefix_fused", "shared_prefix_verify",
+                             "shared_prefix_plain_decode",
                              "tiny_decode", "multi_token_decode", "exact_window_video",
                              "exact_window_denoise"])
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-sample-seqs", type=int, default=64)
+    ap.add_argument("--only", action="store_true",
+                    help="measure only --workload (no 'workloads' object)")
     return ap.parse_args()
+
+
+# the workloads measured besides the headline one, in the order they run
+EXTRA_WORKLOADS = ("tiny_decode", "chunked_prefill", "shared_prefix", "shared_prefix_fused",
+                   "shared_prefix_plain_decode", "block_causal_video", "multi_token_decode",
+                   "exact_window_denoise")
 
 
 # ----------------------------------------------------------------------------
@@ -192,41 +207,86 @@ def _oracle_init(shm_names, shapes, meta):
     _W.update(meta)
 
 
-def _oracle_seq(b):
+def _local_pool(table_row, kv_len, scatter):
+    """The pages of one row (logical order) as a small pool, with this step's
+    scattered rows ``scatter`` ({slot: (k row, v row)}) applied to copies of
+    the touched pages; the shared pools stay read-only."""
+    kb, vb = _W["k"], _W["v"]
+    P = kb.shape[1]
+    used = [int(x) for x in table_row[: -(-int(kv_len) // P)]]
+    kp = np.stack([kb[p] for p in used])
+    vp = np.stack([vb[p] for p in used])
+    where = {p: i for i, p in enumerate(used)}
+    for s_, (kr, vr) in scatter.items():
+        i = where.get(s_ // P)
+        if i is not None:
+            kp[i, s_ % P] = kr
+            vp[i, s_ % P] = vr
+    return kp, vp, np.arange(len(used), dtype=np.int32)[None, :]
+
+
+def _scatter_rows(r0, r1):
+    slots = _W["slots"][r0:r1]
+    return {int(s_): (_W["new_k"][r0 + i], _W["new_v"][r0 + i]) for i, s_ in enumerate(slots) if s_ >= 0}
+
+
+def _oracle_task(task):
+    """One unit of the oracle's work on the step; returns a checksum so the
+    work is not optimised away.
+
+    ("seq", b, rows): sequence b's rows (absolute row indices; None = all),
+      after the step's scatter of its new rows;
+    ("group", g): a shared-prefix group: the prefix call over its samples'
+      rows (mask none), each sample's tail call (causal), and the merge;
+    ("window", rows): exact-window attention of the staged rows ``rows``
+      over the long sequence (history from the pool, staged tokens new)."""
     sys.path.insert(0, ROOT)
     from oracle import oracle as orc
-    qi = _W["q_indptr"]
-    kb, vb = _W["k"], _W["v"]
-    # the step's scatter of this sequence's new rows (into a private copy of
-    # the touched rows is not needed: attention reads the slot through the table)
-    r0, r1 = int(qi[b]), int(qi[b + 1])
-    slots = _W["slots"][r0:r1]
-    P = kb.shape[1]
-    k_local = {int(s): _W["new_k"][r0 + i] for i, s in enumerate(slots) if s >= 0}
-    v_local = {int(s): _W["new_v"][r0 + i] for i, s in enumerate(slots) if s >= 0}
-    table = _W["block_table"][b:b + 1]
-    # materialise the touched pages with the scattered rows (oracle scatter on a
-    # copy of just this sequence's pages keeps the shared pool read-only)
-    pages = sorted({int(s) // P for s in k_local})
-    kcopy = {p: kb[p].copy() for p in pages}
-    vcopy = {p: vb[p].copy() for p in pages}
-    for s, row in k_local.items():
-        kcopy[s // P][s % P] = row
-    for s, row in v_local.items():
-        vcopy[s // P][s % P] = row
-    # a small pool holding this sequence's pages, table remapped onto it
-    used = [int(x) for x in table[0] if x >= 0][: -(-int(_W["kv_lens"][b]) // P)]
-    kp = np.stack([kcopy.get(p, kb[p]) for p in used])
-    vp = np.stack([vcopy.get(p, vb[p]) for p in used])
-    t = np.arange(len(used), dtype=np.int32)[None, :]
-    O, L = orc.paged_attention(_W["q"][r0:r1], kp, vp, t, _W["kv_lens"][b:b + 1],
-                               np.array([0, r1 - r0]), _W["q_real"][b:b + 1], mask=_W["mask"],
-                               causal_block=_W["causal_block"])
-    return float(np.nansum(O))
+    kind = task[0]
+    if kind == "seq":
+        _, b, rows = task
+        qi = _W["q_indptr"]
+        r0, r1 = int(qi[b]), int(qi[b + 1])
+        kp, vp, t = _local_pool(_W["block_table"][b], _W["kv_lens"][b], _scatter_rows(r0, r1))
+        local = None if rows is None else [r - r0 for r in rows]
+        O, _ = orc.paged_attention(_W["q"][r0:r1], kp, vp, t, _W["kv_lens"][b:b + 1],
+                                   np.array([0, r1 - r0]), _W["q_real"][b:b + 1], mask=_W["mask"],
+                                   causal_block=_W["causal_block"], rows=local)
+        return float(np.nansum(O))
+    if kind == "group":
+        g = task[1]
+        n, ql = _W["samples"], _W["q_len"]
+        r0, r1 = g * n * ql, (g + 1) * n * ql
+        kp, vp, t = _local_pool(_W["prefix_table"][g], _W["prefix_lens"][g], {})
+        O_p, L_p = orc.paged_attention(_W["q"][r0:r1], kp, vp, t, _W["prefix_lens"][g:g + 1],
+                                       np.array([0, r1 - r0]), None, mask="none")
+        total = 0.0
+        for r in range(g * n, (g + 1) * n):
+            a0, a1 = r * ql, (r + 1) * ql
+            kp, vp, t = _local_pool(_W["tail_table"][r], _W["tail_lens"][r], _scatter_rows(a0, a1))
+            O_t, L_t = orc.paged_attention(_W["q"][a0:a1], kp, vp, t, _W["tail_lens"][r:r + 1],
+                                           np.array([0, ql]), None, mask="causal")
+            O, _ = orc.merge_attn_states(O_p[a0 - r0:a1 - r0], L_p[a0 - r0:a1 - r0], O_t, L_t)
+            total += float(np.nansum(O))
+        return total
+    if kind == "window":
+        rows = task[1]
+        kb, vb = _W["k"], _W["v"]
+        P = kb.shape[1]
+        base = _W["pin"] + _W["committed"]
+        pos = np.arange(base)
+        pages = _W["table"][pos // P]
+        k_seq = np.concatenate([kb[pages, pos % P], _W["new_k"]])
+        v_seq = np.concatenate([vb[pages, pos % P], _W["new_v"]])
+        O, _ = orc.exact_window_attention(_W["q"], k_seq, v_seq, _W["pin"], _W["committed"],
+                                          _W["window"], _W["staged"], _W["block"], rows=rows)
+        return float(np.nansum(O))
+    raise ValueError(kind)
 
 
 class OraclePool:
-    """Oracle over sequences of a case, one single-threaded worker per core."""
+    """The oracle over tasks of one workload's step, one single-threaded
+    worker process per core (spawned, so it is safe after CUDA is up)."""
 
     def __init__(self, case, workers):
         import multiprocessing as mp
@@ -241,27 +301,41 @@ class OraclePool:
             self.shms.append(shm)
             names[key], shapes[key] = shm.name, arr.shape
         meta = dict(q=orc.bf16_bits(case.q), new_k=orc.bf16_bits(case.new_k),
-                    new_v=orc.bf16_bits(case.new_v), slots=case.slots.numpy(),
-                    block_table=case.block_table.numpy(), kv_lens=case.kv_lens.numpy(),
-                    q_indptr=case.q_indptr.numpy(), q_real=case.q_real.numpy(),
-                    mask=case.mask, causal_block=case.causal_block)
+                    new_v=orc.bf16_bits(case.new_v))
+        if hasattr(case, "block_table"):
+            meta.update(slots=case.slots.numpy(), block_table=case.block_table.numpy(),
+                        kv_lens=case.kv_lens.numpy(), q_indptr=case.q_indptr.numpy(),
+                        q_real=case.q_real.numpy(), mask=case.mask, causal_block=case.causal_block)
+            e = case.extra
+            if "prefix_table" in e:
+                meta.update(samples=e["samples"], q_len=e["q_len"],
+                            prefix_table=e["prefix_table"].numpy(), prefix_lens=e["prefix_lens"].numpy(),
+                            tail_table=e["tail_table"].numpy(), tail_lens=e["tail_lens"].numpy())
+        else:   # an exact-window forward
+            meta.update(table=case.table.numpy(), pin=case.pin, committed=case.committed,
+                        window=case.window, staged=case.staged, block=case.block)
         for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
             os.environ[var] = "1"
         ctx = mp.get_context("spawn")
         self.workers = workers
         self.pool = ctx.Pool(workers, initializer=_oracle_init, initargs=(names, shapes, meta))
-        self.pool.map(_oracle_seq, [0] * workers)  # warm the workers
+        self.pool.map(abs, range(workers))  # wait for every worker to start
 
-    def run(self, seqs):
+    def run(self, tasks):
         t0 = time.perf_counter()
-        self.pool.map(_oracle_seq, list(seqs), chunksize=1)
+        self.pool.map(_oracle_task, list(tasks), chunksize=1)
         return time.perf_counter() - t0
 
     def close(self):
         self.pool.terminate()
-        for s in self.shms:
-            s.close()
-            s.unlink()
+        self.pool.join()
+        for s_ in self.shms:
+            s_.close()
+            s_.unlink()
+
+
+def host_cores():
+    return os.cpu_count() or 1
 
 
 def measured_peaks():
@@ -307,42 +381,209 @@ def committed_traffic(workload, kernel_sources):
 
 
 # ----------------------------------------------------------------------------
+# the oracle's bounded sample of each workload's step
+# ----------------------------------------------------------------------------
+def _oracle_warm(_):
+    sys.path.insert(0, ROOT)
+    from oracle import oracle  # noqa: F401  (import cost kept out of the timed run)
+    return 0
+
+
+def _chunks(seq, n):
+    n = max(1, min(n, len(seq)))
+    return [seq[i::n] for i in range(n)]
+
+
+def oracle_sample(name, case, workers):
+    """Tasks of the oracle's sample of one step of workload ``name``, the work
+    they stand for in the workload metric's base unit (bytes or flops), and a
+    one-line description."""
+    if name == "exact_window_denoise" or name == "exact_window_video":
+        Hq, D = case.num_q_heads, case.head_dim
+        rows = list(range(0, case.staged, 8))
+        from oracle import oracle as orc
+        pairs = sum(len(orc.exact_window_keys(case.pin, case.committed, case.window, case.staged,
+                                              case.block, r // case.block)) for r in rows)
+        return ([("window", c) for c in _chunks(rows, workers)], 4.0 * D * Hq * pairs,
+                f"{len(rows)} of {case.staged} query rows (every 8th), exact-window attention "
+                "over the long sequence, fp64")
+    Hq, Hkv, D = case.num_q_heads, case.num_kv_heads, case.head_dim
+    tok = Hkv * D * 2 * 2
+    kvl = case.kv_lens.numpy().astype(np.int64)
+    qi = case.q_indptr.numpy()
+    if name in ("gqa_decode", "multi_token_decode", "shared_prefix_plain_decode"):
+        tasks = [("seq", b, None) for b in range(case.batch)]
+        return (tasks, float(kvl.sum() * tok),
+                f"all {case.batch} sequences of the step (scatter + attention over each "
+                "sequence's whole row, fp64)")
+    if name == "tiny_decode":
+        reps = 500
+        tasks = [("seq", b, None) for b in range(case.batch)] * reps
+        return (tasks, float(kvl.sum() * tok * reps),
+                f"the whole step (both sequences: scatter + decode attention, fp64) {reps} times")
+    if name in ("shared_prefix", "shared_prefix_fused"):
+        e = case.extra
+        prefix = int(e["prefix_lens"][0])
+        work = e["groups"] * prefix * tok + int(e["tail_lens"].sum()) * tok
+        return ([("group", g) for g in range(e["groups"])], float(work),
+                f"all {e['groups']} groups of the step: prefix call over each group's "
+                f"{e['samples']} rows, every sample's tail call and the merge, fp64")
+    if name in ("chunked_prefill", "block_causal_video"):
+        from oracle import oracle as orc
+        qr = case.q_real.numpy()
+        stride = 8 if name == "chunked_prefill" else 4
+        tasks, pairs, nrows = [], 0, 0
+        for b in range(case.batch):
+            rows = list(range(int(qi[b]), int(qi[b]) + int(qr[b]), stride))
+            nrows += len(rows)
+            pairs += sum(orc.visible_keys(r - int(qi[b]), int(qr[b]), int(kvl[b]), case.mask,
+                                          case.causal_block) for r in rows)
+            per_seq = max(1, workers // case.batch)
+            tasks += [("seq", b, c) for c in _chunks(rows, per_seq)]
+        return (tasks, 4.0 * D * Hq * pairs,
+                f"{nrows} of {int(qr.sum())} real query rows (every {stride}th row of each "
+                "sequence, after the step's scatter), fp64; the rotation is not included"
+                if name == "block_causal_video" else
+                f"{nrows} of {int(qr.sum())} real query rows (every {stride}th row of each "
+                "sequence, after the step's scatter), fp64")
+    return None
+
+
+def time_oracle(name, case, workers, scale, unit, tasks=None):
+    """Run the oracle's sample of one step on ``workers`` processes; returns
+    (value in the metric's unit, seconds, description)."""
+    sample = oracle_sample(name, case, workers)
+    if sample is None:
+        return None
+    tk, work, desc = sample
+    if tasks is not None:
+        tk, work = tasks
+    pool = OraclePool(case, workers)
+    try:
+        pool.pool.map(_oracle_warm, range(workers))
+        dt = pool.run(tk)
+    finally:
+        pool.close()
+    return work / dt / scale, dt, desc
+
+
+def cpu_baseline_for(name, case, unit, scale):
+    """The fp64 oracle, as it stands, on a bounded sample of the same step, on
+    every host core (one single-threaded worker each); for the two decode
+    workloads also on one core."""
+    cores = host_cores()
+    r = time_oracle(name, case, cores, scale, unit)
+    if r is None:
+        return None
+    value, dt, desc = r
+    out = {"value": value, "unit": unit, "cores": cores, "host_cores": cores, "kind": "oracle",
+           "sample": f"{desc}; {dt:.2f} s on {cores} worker processes"}
+    if name in ("gqa_decode", "tiny_decode"):
+        Hkv, D = case.num_kv_heads, case.head_dim
+        kvl = case.kv_lens.numpy().astype(np.int64)
+        if name == "gqa_decode":
+            seqs = list(range(16))
+            tasks = ([("seq", b, None) for b in seqs], float(kvl[seqs].sum() * Hkv * D * 4))
+            what = "16 of the 64 sequences of the step"
+        else:
+            tasks = ([("seq", b, None) for b in range(case.batch)] * 200, float(kvl.sum() * Hkv * D * 4 * 200))
+            what = "the whole step 200 times"
+        v1, dt1, _ = time_oracle(name, case, 1, scale, unit, tasks=tasks)
+        out["one_thread"] = {"value": v1, "unit": unit, "cores": 1,
+                             "sample": f"{what} (scatter + decode attention, fp64); {dt1:.2f} s on "
+                                       "one worker process"}
+    return out
+
+
+# ----------------------------------------------------------------------------
 def run_reference(args):
+    """The reference arm: the fp64 oracle, as it stands, on the host cores, on
+    a bounded sample of each step of the workload (rank 0 only)."""
     rank, world, _ = dist_env()
     if rank != 0:
         return 0
     from paged_kv_cache_189_gb300 import workloads as wl
-    case = wl.gqa_decode(seed=1)
-    _, kv_bytes_all = decode_bytes(case)
-    workers = min(16, os.cpu_count() or 1)
-    pool = OraclePool(case, workers)
-    per_step = min(args.cpu_sample_seqs, 16)
-    seqs_all = list(range(case.batch))
-    kvl = case.kv_lens.numpy().astype(np.int64)
-    times, bytes_done = [], []
+    name = args.workload
+    case = make_case(name, 0)
+    meta = WORKLOAD_META[name]
+    cores = host_cores()
+    sample = oracle_sample(name, case, cores)
+    if sample is None:
+        print(json.dumps({"impl": "reference", "unavailable": f"no oracle sample for {name}"}))
+        return 0
+    tasks, work, desc = sample
+    pool = OraclePool(case, cores)
+    pool.pool.map(_oracle_warm, range(cores))
+    times = []
     for i in range(args.warmup + args.steps):
-        seqs = [seqs_all[(i * per_step + j) % case.batch] for j in range(per_step)]
-        dt = pool.run(seqs)
+        dt = pool.run(tasks)
         if i >= args.warmup:
             times.append(dt)
-            bytes_done.append(int(kvl[seqs].sum()) * case.num_kv_heads * case.head_dim * 4)
     pool.close()
     total_t = sum(times)
-    value = sum(bytes_done) / total_t / 1e9
-    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
-            "steps": args.steps, "warmup": args.warmup,
+    value = work * len(times) / total_t / meta["scale"]
+    line = {"impl": "reference", "metric": meta["metric"], "value": value, "unit": meta["unit"],
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": 1e3 * total_t / max(1, len(times)), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": "gqa_decode", "batch": case.batch, "q_heads": 32,
-                       "kv_heads": 8, "head_dim": 128, "page": 32,
-                       "kv_len": "U[512,8192]+1", "sample_seqs_per_step": per_step},
-            "cpu_baseline": {"value": value, "unit": UNIT, "cores": workers, "kind": "oracle",
-                             "sample": f"{per_step} of the 64 sequences per step (rotating), "
-                                       "decode attention incl. the step's scatter"},
-            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+            "config": {"workload": name, **meta["config"], "oracle_sample": desc},
+            "cpu_baseline": {"value": value, "unit": meta["unit"], "cores": cores, "host_cores": cores,
+                             "kind": "oracle", "sample": f"{desc}, each step"},
+            "e2e": {"value": value, "unit": meta["unit"], "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     return 0
+
+
+# metric, unit and fixed configuration keys of each workload (as the bench
+# line of our arm states them)
+WORKLOAD_META = {
+    "gqa_decode": dict(metric=METRIC, unit="GB/s", scale=1e9,
+                       config=dict(batch=64, q_heads=32, kv_heads=8, head_dim=128, page=32,
+                                   kv_len="U[512,8192]+1")),
+    "tiny_decode": dict(metric=METRIC, unit="GB/s", scale=1e9,
+                        config=dict(batch=2, q_heads=4, kv_heads=2, head_dim=64, page=32,
+                                    kv_len="{37,100}")),
+    "multi_token_decode": dict(metric="multi-token decode KV GB/s", unit="GB/s", scale=1e9,
+                               config=dict(batch=64, q_heads=32, kv_heads=8, head_dim=128, page=32,
+                                           q_len=4, kv_len="U[512,8192]+4")),
+    "chunked_prefill": dict(metric="prefill TFLOP/s", unit="TFLOP/s", scale=1e12,
+                            config=dict(batch=8, q_heads=32, kv_heads=8, head_dim=128, page=32,
+                                        ctx="U[2048,16384]", chunk=512, mask="causal")),
+    "block_causal_video": dict(metric="prefill TFLOP/s", unit="TFLOP/s", scale=1e12,
+                               config=dict(batch=1, q_heads=40, kv_heads=40, head_dim=128, page=32,
+                                           kv_len=7800, q_rows=1568, q_real=1560, causal_block=1560,
+                                           mask="block_causal")),
+    "shared_prefix": dict(metric="shared-prefix KV GB/s", unit="GB/s", scale=1e9,
+                          config=dict(groups=16, samples=8, prefix=4096, tail="U[1,1024]", q_heads=32,
+                                      kv_heads=8, head_dim=128, page=32)),
+    "shared_prefix_fused": dict(metric="shared-prefix KV GB/s", unit="GB/s", scale=1e9,
+                                config=dict(groups=16, samples=8, prefix=4096, tail="U[1,1024]",
+                                            q_heads=32, kv_heads=8, head_dim=128, page=32)),
+    "shared_prefix_plain_decode": dict(metric="shared-prefix KV GB/s", unit="GB/s", scale=1e9,
+                                       config=dict(groups=16, samples=8, prefix=4096, tail="U[1,1024]",
+                                                   q_heads=32, kv_heads=8, head_dim=128, page=32)),
+    "exact_window_denoise": dict(metric="prefill TFLOP/s", unit="TFLOP/s", scale=1e12,
+                                 config=dict(q_heads=32, kv_heads=8, head_dim=128, page=32,
+                                             staged_tokens=1576, causal_block=1576)),
+}
+WORKLOAD_SEED = {"gqa_decode": 1, "chunked_prefill": 2, "shared_prefix": 3, "block_causal_video": 4,
+                 "shared_prefix_fused": 3, "shared_prefix_verify": 3, "shared_prefix_plain_decode": 3,
+                 "tiny_decode": 0, "multi_token_decode": 5, "exact_window_video": 6,
+                 "exact_window_denoise": 6}
+
+
+def make_case(name, rank):
+    """The seeded synthetic input of one workload for rank ``rank``."""
+    from paged_kv_cache_189_gb300 import workloads as wl
+    seed = WORKLOAD_SEED[name] + rank
+    if name in ("exact_window_video", "exact_window_denoise"):
+        return wl.exact_window_video(seed=seed, blocks_per_chunk=4 if name == "exact_window_video" else 1)
+    return {"gqa_decode": wl.gqa_decode, "chunked_prefill": wl.chunked_prefill,
+            "block_causal_video": wl.block_causal_video, "shared_prefix": wl.shared_prefix,
+            "shared_prefix_fused": wl.shared_prefix, "shared_prefix_plain_decode": wl.shared_prefix,
+            "shared_prefix_verify": lambda seed: wl.shared_prefix(seed, q_len=4),
+            "tiny_decode": wl.tiny_decode, "multi_token_decode": wl.multi_token_decode}[name](seed=seed)
 
 
 def visible_pairs(case):
@@ -380,7 +621,7 @@ def build_exact_window_plan(name, rank, dev, stream):
     import torch
     from paged_kv_cache_189_gb300 import pkv, workloads as wl
 
-    case = wl.exact_window_video(seed=6 + rank, blocks_per_chunk=4 if name == "exact_window_video" else 1)
+    case = make_case(name, rank)
     Hq, Hkv, D = case.num_q_heads, case.num_kv_heads, case.head_dim
     t = dict(k_pool=case.k_pool.to(dev), v_pool=case.v_pool.to(dev), q=case.q.to(dev),
              new_k=case.new_k.to(dev), new_v=case.new_v.to(dev), table=case.table.to(dev),
@@ -455,14 +696,7 @@ def build_plan(name, rank, dev, stream):
 
     if name in ("exact_window_video", "exact_window_denoise"):
         return build_exact_window_plan(name, rank, dev, stream)
-    case = {"gqa_decode": wl.gqa_decode, "chunked_prefill": wl.chunked_prefill,
-            "block_causal_video": wl.block_causal_video, "shared_prefix": wl.shared_prefix,
-            "shared_prefix_fused": wl.shared_prefix,
-            "shared_prefix_verify": lambda seed: wl.shared_prefix(seed, q_len=4),
-            "tiny_decode": wl.tiny_decode, "multi_token_decode": wl.multi_token_decode}[name](
-        seed={"gqa_decode": 1, "chunked_prefill": 2, "shared_prefix": 3, "block_causal_video": 4,
-              "shared_prefix_fused": 3, "shared_prefix_verify": 3,
-              "tiny_decode": 0, "multi_token_decode": 5}[name] + rank)
+    case = make_case(name, rank)
     Hq, Hkv, D = case.num_q_heads, case.num_kv_heads, case.head_dim
     rows = case.q.shape[0]
     t = dict(k_pool=case.k_pool.to(dev), v_pool=case.v_pool.to(dev), q=case.q.to(dev),
@@ -607,8 +841,9 @@ def build_plan(name, rank, dev, stream):
                                   "concurrently on a second stream)",
                         dom_work=prefix_bytes, bound="hbm", peak=peak_hbm, peak_unit="GB/s",
                         peak_src=f"{hbm_kind} hbm_gbs", h2d=(h2d_src, h2d_dst), d2h=d2h_src,
-                        # scatter, the planner's two kernels, the grouped tile kernel
-                        launches=4, traffic_sources=ATTN_TC_SOURCES)
+                        # scatter, prefix tile, the tail call (unit-order planner +
+                        # decode kernel), merge
+                        launches=5, traffic_sources=ATTN_TC_SOURCES)
     if name in ("shared_prefix_fused", "shared_prefix_verify"):
         # the step plans the grouping on the device (plan_shared_prefix) and runs
         # every row's shared run + tail in one launch (shared_prefix_attention)
@@ -645,26 +880,45 @@ def build_plan(name, rank, dev, stream):
                                   "tails of a group per CTA), HBM-bound",
                         dom_work=prefix_bytes + tail_bytes + io_bytes, bound="hbm", peak=peak_hbm,
                         peak_unit="GB/s", peak_src=f"{hbm_kind} hbm_gbs", h2d=(h2d_src, h2d_dst),
-                        # scatter, prefix tile, the tail call (unit-order planner +
-                        # decode kernel), merge
-                        d2h=d2h_src, launches=5, traffic_sources=ATTN_TC_SOURCES)
+                        # scatter, the planner's two kernels, the grouped tile kernel
+                        d2h=d2h_src, launches=4, traffic_sources=ATTN_TC_SOURCES)
+    if name == "shared_prefix_plain_decode":
+        # the ablation: every sample's whole row (prefix ++ tail) through plain
+        # decode, the prefix pages read once per sample instead of once per group
+        e = case.extra
+        Gn, n_s = e["groups"], e["samples"]
+        prefix = int(e["prefix_lens"][0])
+        prefix_bytes = Gn * prefix * kv_tok_bytes
+        tail_bytes = int(e["tail_lens"].sum()) * kv_tok_bytes
+        attn_bytes, kv_read = decode_bytes(case)
+        dom = attention_call(t["q"], t["bt"], t["kl"], t["qi"], t["qr"], out, lse, 1, case.max_kv_len,
+                             "causal")
+        cfg.update(groups=Gn, samples=n_s, prefix=prefix, tail="U[1,1024]",
+                   kv_bytes_per_step=prefix_bytes + tail_bytes, kv_bytes_read_per_step=kv_read,
+                   l2="prefix pages 16.8 MB per group; 2.4 GB of K/V read per step",
+                   note="value counts the shared prefix once per group, as the shared-prefix "
+                        "entries do, so the three values compare step times; roofline counts "
+                        "the bytes this path reads")
+        return StepPlan(case=case, cfg=cfg, metric="shared-prefix KV GB/s", unit="GB/s",
+                        work=prefix_bytes + tail_bytes, scale=1e9, queries=rows, pre=[scatter],
+                        dominant=dom, post=[], aux=aux,
+                        dom_label="paged_attention over each sample's whole row: persistent "
+                                  "split-KV decode kernel behind its unit-order planner",
+                        dom_work=attn_bytes, bound="hbm", peak=peak_hbm, peak_unit="GB/s",
+                        peak_src=f"{hbm_kind} hbm_gbs", h2d=(h2d_src, h2d_dst), d2h=d2h_src,
+                        # scatter, the unit-order planner, the decode kernel
+                        launches=3, traffic_sources=DECODE_SOURCES)
     raise ValueError(name)
 
 
-def run_ours(args):
+def measure(plan, name, args, rank, world, local, dev, stream, dist):
+    """Time one workload: warm-up, then exactly ``args.steps`` steps between
+    barriers and synchronisations (CUDA events on the launching stream, the
+    dominant call bracketed by its own events every step), the auxiliary
+    launches as CUDA-graph replays, then the end-to-end loop through the
+    public API from pinned host memory.  Returns the JSON entry (every rank
+    returns its copy; values aggregate over ranks)."""
     import torch
-    from paged_kv_cache_189_gb300 import build as pkv_build
-    rank, world, local = dist_env()
-    if not torch.cuda.is_available():
-        raise SystemExit("bench.py needs a CUDA GPU")
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    dist = init_dist(world, "nccl")
-    if rank == 0:
-        pkv_build.build()
-    barrier(dist)
-    stream = torch.cuda.Stream(device=dev)
-    plan = build_plan(args.workload, rank, dev, stream)
 
     def step():
         for f in plan.pre:
@@ -733,8 +987,7 @@ def run_ours(args):
         del graph
 
     # ---- end to end through the public API: pinned host inputs -> device,
-    #      the whole step, result read back to the host, every step
-    e2e_value = None
+    #      the whole step, result read back to the host, every step.
     #      The host runs one step ahead, as a serving loop does: it enqueues
     #      step i (inputs copied in, the step, the result copied into one of
     #      two pinned buffers) and then waits for step i - 1's result.
@@ -742,6 +995,7 @@ def run_ours(args):
     #      all (each at a 256-byte aligned offset) and the step's device input
     #      tensors are rebound to views of one device buffer of the same
     #      layout; the results (output and LSE) likewise come back as one copy.
+    e2e_value = None
     srcs, dsts = plan.h2d
     d_in, in_offs = packed_device(dsts, dev)
     h_in = torch.empty(d_in.numel(), dtype=torch.uint8).pin_memory()
@@ -776,32 +1030,71 @@ def run_ours(args):
         e2e_ms = max_over_ranks(dist, e0.elapsed_time(e1), dev)
         e2e_value = sum_over_ranks(dist, plan.work * args.e2e_steps, dev) / (e2e_ms * 1e-3) / plan.scale
 
+    dom_avg = statistics.mean(dom_ms)
+    achieved = plan.dom_work / (dom_avg * 1e-3) / (1e9 if plan.bound == "hbm" else 1.0)
+    traffic = committed_traffic(name, plan.traffic_sources)
+    entry = {
+        "metric": plan.metric, "value": value, "unit": plan.unit, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_total_max / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": dict(plan.cfg, parallelism=f"independent replicas x{world} (seed + rank), "
+                                             "no collective"),
+        "queries_per_s": queries_total / (ms_total_max * 1e-3),
+        "roofline": {"bound": plan.bound, "achieved": achieved, "peak": plan.peak,
+                     "unit": plan.peak_unit, "frac": achieved / plan.peak, "traffic": traffic,
+                     "kernel": plan.dom_label + "; CUDA events around the call each timed step",
+                     "work_per_launch": plan.dom_work, "avg_launch_ms": dom_avg,
+                     "peak_source": plan.peak_src},
+        "clocks": clk,
+        "e2e": {"value": e2e_value, "unit": plan.unit, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "steps": args.e2e_steps},
+        "gpu_launches": plan.launches * args.steps,
+        "aux": aux_out,
+    }
+    if plan.unit == "GB/s":
+        entry["hbm_frac"] = value / plan.peak if plan.bound == "hbm" else None
+    return entry
+
+
+def run_ours(args):
+    import gc
+    import torch
+    from paged_kv_cache_189_gb300 import build as pkv_build
+    rank, world, local = dist_env()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist = init_dist(world, "nccl")
     if rank == 0:
-        dom_avg = statistics.mean(dom_ms)
-        achieved = plan.dom_work / (dom_avg * 1e-3) / (1e9 if plan.bound == "hbm" else 1.0)
-        traffic = committed_traffic(args.workload, plan.traffic_sources)
-        line = {
-            "metric": plan.metric, "value": value, "unit": plan.unit, "n_gpus": world,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_total_max / args.steps,
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-            "data": "synthetic",
-            "config": dict(plan.cfg, parallelism=f"replicas x{world} (sequences sharded by rank)"),
-            "queries_per_s": queries_total / (ms_total_max * 1e-3),
-            "roofline": {"bound": plan.bound, "achieved": achieved, "peak": plan.peak,
-                         "unit": plan.peak_unit, "frac": achieved / plan.peak, "traffic": traffic,
-                         "kernel": plan.dom_label + "; CUDA events around the call each timed step",
-                         "work_per_launch": plan.dom_work, "avg_launch_ms": dom_avg,
-                         "peak_source": plan.peak_src},
-            "clocks": clk,
-            "e2e": {"value": e2e_value, "unit": plan.unit, "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": d2h, "steps": args.e2e_steps},
-            "gpu_launches": plan.launches * args.steps,
-            "aux": aux_out,
-        }
-        if plan.unit == "GB/s":
-            line["hbm_frac"] = value / plan.peak if plan.bound == "hbm" else None
-        if world == 1 and not args.no_cpu_baseline:
-            line["cpu_baseline"] = cpu_baseline_for(plan, args)
+        pkv_build.build()
+    barrier(dist)
+    stream = torch.cuda.Stream(device=dev)
+    names = [args.workload]
+    if not args.only and args.workload == "gqa_decode":
+        names += list(EXTRA_WORKLOADS)
+    line, extra = None, {}
+    for name in names:
+        plan = build_plan(name, rank, dev, stream)
+        entry = measure(plan, name, args, rank, world, local, dev, stream, dist)
+        case = plan.case
+        del plan
+        gc.collect()
+        torch.cuda.empty_cache()
+        if rank == 0 and world == 1 and not args.no_cpu_baseline:
+            entry["cpu_baseline"] = cpu_baseline_for(name, case, entry["unit"], 1e9 if entry["unit"] == "GB/s"
+                                                     else 1e12)
+        del case
+        if line is None:
+            line = entry
+        else:
+            extra[name] = {k: v for k, v in entry.items()
+                           if k not in ("n_gpus", "higher_is_better", "scaling", "vs_baseline", "data",
+                                        "dtype", "warmup")}
+    if rank == 0:
+        if extra:
+            line["workloads"] = extra
         print(json.dumps(line), flush=True)
     barrier(dist)
     return 0
@@ -822,25 +1115,6 @@ def packed_device(tensors, dev):
     for x, o in zip(tensors, offs):
         x.set_(buf.untyped_storage(), o // x.element_size(), x.shape, x.stride())
     return buf, offs
-
-
-def cpu_baseline_for(plan, args):
-    """The fp64 oracle on a bounded sample of the same step (whole sequences of
-    the decode batch; for the other workloads, a few sequences), in the metric's
-    unit, with the worker count as the cores used."""
-    case = plan.case
-    workers = min(16, os.cpu_count() or 1)
-    if args.workload not in ("gqa_decode", "tiny_decode"):
-        return None
-    pool = OraclePool(case, workers)
-    seqs = list(range(min(args.cpu_sample_seqs, case.batch)))
-    dt = pool.run(seqs)
-    pool.close()
-    kvl = case.kv_lens.numpy().astype(np.int64)
-    b = int(kvl[seqs].sum()) * case.num_kv_heads * case.head_dim * 4
-    return {"value": b / dt / 1e9, "unit": UNIT, "cores": workers, "kind": "oracle",
-            "sample": f"{len(seqs)} of {case.batch} sequences of the same step "
-                      f"(scatter + decode attention, fp64), {dt:.2f} s"}
 
 
 def main():

@@ -17,7 +17,7 @@ import torch
 
 from paged_kv_cache_189_gb300 import pkv, workloads as wl
 
-from pkv_testutil import assert_attention_close, oracle_step
+from pkv_testutil import assert_attention_close, oracle_step, real_row_mask
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -55,7 +55,10 @@ def _check_pair(case, num_splits=0):
     assert np.isfinite(g).all()
     diff = np.abs(g - r)
     assert diff.max() <= 1e-2 and diff.mean() <= 1e-3
-    assert np.abs(got_l.double().cpu().numpy() - ref_l.double().cpu().numpy()).max() <= 1e-3
+    real = real_row_mask(case)
+    gl, rl = got_l.double().cpu().numpy(), ref_l.double().cpu().numpy()
+    assert np.abs(gl[real] - rl[real]).max() <= 1e-3
+    assert np.isneginf(gl[~real]).all() and np.isneginf(rl[~real]).all()   # padding rows
     O, L, _, _ = oracle_step(case)
     assert_attention_close(got_o, got_l, O, L, case)
 
