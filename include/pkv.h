@@ -70,12 +70,22 @@ typedef enum {
 #define PKV_FLAG_CHECKED 0x1u     /* range-check device indices, report in *err */
 #define PKV_FLAG_SIMT_ONLY 0x2u   /* paged_attention: use the generic SIMT kernel
                                      (a slow cross-check of the fast kernels)   */
+/* paged_attention, test of the failure path: the decode kernel's consumer warps
+ * wait on a barrier that nothing completes, give up after ~20 us, set
+ * PKV_ERRBIT_TIMEOUT in *err (required) and wind down as after a real timeout
+ * (the producer's ring waits are ~20 us too; every copy already issued is
+ * waited for before a CTA exits).  The outputs are unspecified.  Only calls
+ * that run the decode kernel accept it (else PKV_ERR_UNSUPPORTED). */
+#define PKV_FLAG_TEST_WAIT_TIMEOUT 0x4u
 
 /* bits OR-ed into *err in checked mode */
 #define PKV_ERRBIT_SLOT 0x1       /* scatter slot >= num_pages * page_size      */
 #define PKV_ERRBIT_SRC 0x2        /* scatter source index out of range          */
 #define PKV_ERRBIT_PAGE 0x4       /* block-table entry outside [0, num_pages)   */
 #define PKV_ERRBIT_LEN 0x8        /* kv_len / q rows beyond the host bounds      */
+/* set in any mode: a device wait gave up (about 2 s; see PKV_FLAG_TEST_WAIT_TIMEOUT)
+   and the kernel wound down; the call's results are invalid */
+#define PKV_ERRBIT_TIMEOUT 0x10
 
 /* Human-readable name of a status, and the last validation message of this thread. */
 const char* pkv_status_string(pkv_status status);

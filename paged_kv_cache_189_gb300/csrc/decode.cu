@@ -59,6 +59,9 @@ constexpr int kWarps = 4;                      // consumer warps
 constexpr int kStages = PKV_DECODE_STAGES;     // pages in flight per CTA
 constexpr int kMinBlocks = PKV_DECODE_MIN_BLOCKS;  // CTAs per SM the sizes are chosen for
 constexpr int kThreads = (kWarps + 1) * 32;
+// PKV_FLAG_TEST_WAIT_TIMEOUT: the limit of the waits that are meant to run
+// out (consumers on a barrier nothing completes; the producer's ring waits)
+constexpr uint64_t kTestWaitNs = 20000;
 
 struct UnitDesc {
     int b, kvh, split, key_begin, key_end, r0, nsplit, pad;
@@ -83,7 +86,8 @@ struct DecodeSmem {
     static constexpr int kDescOff = kRedMLOff + kRedMLBytes;   // 2 UnitDesc + flags
     static constexpr int kDescBytes = 2 * sizeof(UnitDesc) + 16;
     static constexpr int kBarOff = (kDescOff + kDescBytes + 7) & ~7;
-    static constexpr int kBytes = kBarOff + (2 * kStages + 4) * 8;
+    // full[kStages], empty[kStages], dfull[2], dempty[2], never (test hook)
+    static constexpr int kBytes = kBarOff + (2 * kStages + 5) * 8;
     // 228 KiB of shared memory per SM, 1 KiB of it reserved per CTA
     static_assert(kBytes <= (228 / kMinBlocks - 1) * 1024, "CTAs per SM must fit in shared memory");
 };
@@ -435,6 +439,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks)
     uint64_t* empty = full + kStages;
     uint64_t* dfull = empty + kStages;   // [2] unit descriptor + its query rows landed
     uint64_t* dempty = dfull + 2;        // [2] consumers done with the descriptor slot
+    uint64_t* never = dempty + 2;        // test hook: a barrier nothing completes
     UnitDesc* desc = reinterpret_cast<UnitDesc*>(smem + S::kDescOff);
     int* flags = reinterpret_cast<int*>(smem + S::kDescOff + 2 * sizeof(UnitDesc));
     float* red_o = reinterpret_cast<float*>(smem + S::kRedOOff);
@@ -462,6 +467,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks)
             mbar_init(&dfull[s], 1);
             mbar_init(&dempty[s], kWarps);
         }
+        mbar_init(never, 1);
         flags[0] = 0;  // "this CTA merges the splits of its unit"
         flags[1] = 0;  // set when a consumer wait gives up
         fence_mbar_init();
@@ -481,7 +487,9 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks)
         const int BH = p.batch * Hkv;
         const bool listed = p.planned;
         const int units = listed ? __ldcg(sc.total) : BH * S_;
+        const uint64_t ring_limit = p.test_wait_timeout ? kTestWaitNs : 2000000000ull;
         int i = 0;  // pages issued so far (ring position)
+        int published = 0;  // unit descriptors published (dfull phases armed)
         bool alive = true;
         for (int k = 0; alive; ++k) {
             UnitDesc d;
@@ -523,7 +531,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks)
                 }
             }
             const int slot = k & 1;
-            if (k >= 2 && !mbar_wait(&dempty[slot], ((k >> 1) - 1) & 1)) {
+            if (k >= 2 && !mbar_wait(&dempty[slot], ((k >> 1) - 1) & 1, ring_limit)) {
                 set_err(p.err, PKV_ERRBIT_TIMEOUT);
                 d.b = -1;  // tell the consumers to stop (they may time out too)
             }
@@ -540,13 +548,14 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks)
             } else {
                 mbar_arrive(&dfull[slot]);
             }
+            published = k + 1;
             if (d.b < 0) break;
             const int npages = (d.key_end - d.key_begin + kPage - 1) / kPage;
             const int32_t* bt =
                 p.block_table + static_cast<int64_t>(d.b) * p.block_table_stride + d.key_begin / kPage;
             for (int pi = 0; pi < npages; ++pi, ++i) {
                 const int st = i % kStages;
-                if (i >= kStages && !mbar_wait(&empty[st], ((i / kStages) - 1) & 1)) {
+                if (i >= kStages && !mbar_wait(&empty[st], ((i / kStages) - 1) & 1, ring_limit)) {
                     set_err(p.err, PKV_ERRBIT_TIMEOUT);
                     alive = false;
                     break;
@@ -566,8 +575,11 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks)
                 }
             }
         }
-        // do not leave while copies into this CTA's shared memory are in flight
+        // do not leave while copies into this CTA's shared memory are in flight:
+        // the last pages of the ring, and the query rows of the last two
+        // descriptors (consumers that gave up never waited for them)
         for (int j = max(0, i - kStages); j < i; ++j) mbar_wait(&full[j % kStages], (j / kStages) & 1);
+        for (int k = max(0, published - 2); k < published; ++k) mbar_wait(&dfull[k & 1], (k >> 1) & 1);
         return;
     }
 
@@ -624,8 +636,15 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks)
 #pragma unroll
             for (int j = 0; j < kDPL / 2; ++j) ws.o2[g][j] = make_float2(0.f, 0.f);
 
-        const int npages = (d.key_end - d.key_begin + kPage - 1) / kPage;
+        int npages = (d.key_end - d.key_begin + kPage - 1) / kPage;
         bool failed = false;
+        if (p.test_wait_timeout && npages > 0 && !mbar_wait(never, 0, kTestWaitNs)) {
+            // the test hook: a page wait that runs out, before the unit's first
+            // page is consumed; the unit is abandoned as after a real timeout
+            if (lane == 0) set_err(p.err, PKV_ERRBIT_TIMEOUT);
+            failed = true;
+            npages = 0;
+        }
         for (int pi = 0; pi < npages; ++pi, ++i) {
             const int st = i % kStages;
             if (!mbar_wait(&full[st], (i / kStages) & 1)) {

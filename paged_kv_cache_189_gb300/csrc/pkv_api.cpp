@@ -349,8 +349,8 @@ pkv_status paged_attention(const void* q, int64_t q_token_stride, int64_t q_head
     if (block_table_stride < pages_needed)
         return fail(PKV_ERR_INVALID_ARG, "attention: block_table_stride %lld < %lld pages for max_kv_len",
                     (long long)block_table_stride, (long long)pages_needed);
-    if ((flags & PKV_FLAG_CHECKED) && !err)
-        return fail(PKV_ERR_INVALID_ARG, "attention: checked mode needs an error flag");
+    if ((flags & (PKV_FLAG_CHECKED | PKV_FLAG_TEST_WAIT_TIMEOUT)) && !err)
+        return fail(PKV_ERR_INVALID_ARG, "attention: checked mode and the wait test need an error flag");
 
     const Plan pl = plan_attention(batch, max_q_rows, num_q_heads, num_kv_heads, head_dim,
                                    max_kv_len, num_splits, flags, current_device_sms());
@@ -359,6 +359,8 @@ pkv_status paged_attention(const void* q, int64_t q_token_stride, int64_t q_head
             return fail(PKV_ERR_WORKSPACE, "attention: workspace needs %zu bytes, 256-byte aligned",
                         pl.ws_bytes);
     }
+    if ((flags & PKV_FLAG_TEST_WAIT_TIMEOUT) && pl.kernel != Kernel::kDecode)
+        return fail(PKV_ERR_UNSUPPORTED, "attention: the wait test runs on the decode kernel only");
 
     pkv::AttnParams p{};
     p.q = q;
@@ -390,6 +392,7 @@ pkv_status paged_attention(const void* q, int64_t q_token_stride, int64_t q_head
     p.split_keys = pl.split_keys;
     p.checked = (flags & PKV_FLAG_CHECKED) != 0;
     p.err = err;
+    p.test_wait_timeout = (flags & PKV_FLAG_TEST_WAIT_TIMEOUT) != 0;
     if (pl.kernel == Kernel::kTile && static_cast<int64_t>(batch) * pl.splits > 65535)
         return fail(PKV_ERR_UNSUPPORTED, "attention: batch x key splits above 65535");
     if (pl.kernel == Kernel::kTile && pl.splits > 1) {

@@ -10,11 +10,6 @@
 
 #include "pkv.h"
 
-#ifndef PKV_ERRBIT_TIMEOUT
-// A bounded wait inside a kernel gave up (set by the TMA / tensor-core kernels).
-#define PKV_ERRBIT_TIMEOUT 0x10
-#endif
-
 namespace pkv {
 
 constexpr float kLog2e = 1.4426950408889634f;

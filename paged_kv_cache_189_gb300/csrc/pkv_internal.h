@@ -156,6 +156,9 @@ struct AttnParams {
     bool planned;      // decode: units taken from the planned order (else split-major)
     bool checked;
     int32_t* err;
+    // decode kernel, PKV_FLAG_TEST_WAIT_TIMEOUT: consumers wait on a barrier
+    // nothing completes (short limit) and the producer's ring waits are short
+    bool test_wait_timeout;
     // one-tile kernel: block z takes the (z / num_splits)-th sequence by key
     // count, longest first, so that a grid of several waves starts with them
     bool order_by_keys;

@@ -20,6 +20,7 @@ PKV_BF16, PKV_F16, PKV_F32 = range(3)
 MASKS = {"none": 0, "causal": 1, "block_causal": 2}
 PKV_FLAG_CHECKED = 0x1
 PKV_FLAG_SIMT_ONLY = 0x2
+PKV_FLAG_TEST_WAIT_TIMEOUT = 0x4
 PKV_ERRBIT_SLOT, PKV_ERRBIT_SRC, PKV_ERRBIT_PAGE, PKV_ERRBIT_LEN, PKV_ERRBIT_TIMEOUT = (
     0x1, 0x2, 0x4, 0x8, 0x10)
 
