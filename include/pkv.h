@@ -77,6 +77,20 @@ typedef enum {
  * waited for before a CTA exits).  The outputs are unspecified.  Only calls
  * that run the decode kernel accept it (else PKV_ERR_UNSUPPORTED). */
 #define PKV_FLAG_TEST_WAIT_TIMEOUT 0x4u
+/* paged_attention: run the tensor-core tiles as one CTA per tile pair (keys
+ * split as planned); the default, and what PKV_FLAG_STREAM_K is measured
+ * against */
+#define PKV_FLAG_TILE_GRID 0x8u
+/* paged_attention: when the two-tile kernel runs with the automatic split
+ * count, schedule it stream-K style instead: one persistent CTA per SM runs
+ * one whole tile pair of the first wave and then a contiguous share of the
+ * remaining pairs' 128-key tiles; pairs split between CTAs leave partial
+ * states that a reduce merges (a planner, the persistent launch and the
+ * reduce: three launches).  Results agree with the grid within the attention
+ * tolerances.  Slower than the grid on the workloads measured here (identical
+ * tile pairs run at SM-dependent speeds that static shares cannot absorb), so
+ * not the default; a tuning aid for other GPUs and shapes */
+#define PKV_FLAG_STREAM_K 0x10u
 
 /* bits OR-ed into *err in checked mode */
 #define PKV_ERRBIT_SLOT 0x1       /* scatter slot >= num_pages * page_size      */
@@ -192,7 +206,10 @@ typedef enum {
     PKV_KERNEL_NONE = 0,
     PKV_KERNEL_DECODE = 1, /* persistent split-KV decode kernel (SIMT, TMA-fed)   */
     PKV_KERNEL_TILE = 2,   /* tcgen05 / TMEM tile kernel (+ split reduce)         */
-    PKV_KERNEL_SIMT = 3    /* generic kernel (PKV_FLAG_SIMT_ONLY, other shapes)   */
+    PKV_KERNEL_SIMT = 3,   /* generic kernel (PKV_FLAG_SIMT_ONLY, other shapes)   */
+    PKV_KERNEL_TILE_STREAM_K = 4 /* tile kernel on the stream-K schedule
+                                    (PKV_FLAG_STREAM_K): planner, persistent
+                                    CTAs, merge of split tile pairs */
 } pkv_kernel;
 
 pkv_status pkv_plan_attention(int batch, int max_q_rows, int num_q_heads, int num_kv_heads,

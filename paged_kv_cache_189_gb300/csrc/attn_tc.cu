@@ -1099,7 +1099,153 @@ constexpr int kSmemBytes2 = kFlag2Off + 16;
 static_assert(kSmemBytes2 <= 227 * 1024, "shared memory per CTA");
 
 
+// ---------------------------------------------------------------------------
+// Work of the two-tile kernel.  A unit is one tile pair (2 x TQ tokens) of one
+// sequence and K/V head, over the keys of one split; a segment is a range
+// [j0, j1) of a unit's 128-key tiles.  With the one-CTA-per-tile grid every
+// CTA runs one segment: its unit's whole key range.  The stream-K schedule
+// (tile pairs of at most two waves) keeps one CTA per SM: while the units fill
+// a whole wave, CTA c first runs unit c whole (the first wave, in grid order:
+// the units that read the same K/V run together and share it in L2); the
+// remaining units are shared out stream-K style, each CTA taking a contiguous
+// range of their key tiles, sized so that every CTA's whole-unit work plus its
+// share is the same.  Work is counted in key tiles: a unit whose rows fill
+// only one tile costs about as much per key tile as a pair (its softmax chain,
+// not the tensor pipe, sets the period; measured 0.96 of a pair's).
+// ---------------------------------------------------------------------------
+constexpr int kSkWeightPair = 1;
+constexpr int kSkWeightOne = 1;
+constexpr int kSkFragRows = 2 * kTileM;
+
+struct Seg {
+    TileGeom g;
+    int u, j0, j1;
+    bool two;
+    bool shared;  // from the stream-K share (else a whole unit of the first wave)
+};
+
+// Geometry of the tile pair x of sequence b, K/V head kvh, key split `split`.
+__device__ __forceinline__ TileGeom pair_geometry(const AttnParams& p, int TQ, int b, int kvh, int x,
+                                                  int split) {
+    TileGeom g;
+    g.b = b;
+    g.kvh = kvh;
+    g.split = split;
+    g.r0 = p.q_indptr[b];
+    g.nrows = min(p.q_indptr[b + 1] - g.r0, p.max_q_rows);
+    g.t0 = x * 2 * TQ;
+    g.qreal = min(p.q_real ? p.q_real[b] : g.nrows, g.nrows);
+    g.kv_len = min(max(p.kv_lens[b], 0), p.max_kv_len);
+    g.kb = split * p.split_keys;
+    const int ke = min(g.kv_len, g.kb + p.split_keys);
+    // visibility is non-decreasing in the row, so the pair's last real row bounds it
+    const int last = min(g.t0 + 2 * TQ, g.nrows) - 1;
+    int lim = 0;
+    if (g.t0 < g.qreal)
+        lim = visible_keys(min(last, g.qreal - 1), g.qreal, g.kv_len, p.mask, max(p.causal_block, 1));
+    g.key_hi = min(ke, lim);
+    g.nt = g.key_hi > g.kb ? (g.key_hi - g.kb + kTileN - 1) / kTileN : 0;
+    return g;
+}
+
+// Stream-K unit u: tile pairs fastest, then K/V heads, then sequences, so the
+// units that read the same K/V run on neighbouring CTAs at about the same time.
+__device__ __forceinline__ TileGeom sk_unit(const AttnParams& p, int TQ, int u) {
+    const int x = u % p.sk_tiles_x;
+    const int bh = u / p.sk_tiles_x;
+    return pair_geometry(p, TQ, bh / p.num_kv_heads, bh % p.num_kv_heads, x, 0);
+}
+
+__device__ __forceinline__ int sk_weight(const TileGeom& g, int TQ) {
+    return g.t0 + TQ < g.nrows ? kSkWeightPair : kSkWeightOne;
+}
+
+// The segments of one CTA, in order.  Every role of the CTA walks them itself.
+template <bool SK>
+struct SegIter {
+    int u = 0, end_u = 0;  // stream-K: next shared unit (index among the shared ones)
+    int a = 0, a1 = 0;     // this CTA's share [a, a1) of the shared units' weighted key tiles
+    bool dp = false;       // the first-wave unit is still to come
+    bool done = false;
+
+    __device__ __forceinline__ void init(const AttnParams& p) {
+        if constexpr (SK) {
+            dp = p.sk_dp > 0;
+            a = p.sk_cta_off[blockIdx.x];
+            a1 = p.sk_cta_off[blockIdx.x + 1];
+            end_u = p.sk_units - p.sk_dp;
+            // the last shared unit that starts at or before a
+            int lo = 0, hi = max(end_u - 1, 0);
+            while (lo < hi) {
+                const int mid = (lo + hi + 1) >> 1;
+                if (p.sk_unit_off[mid] <= a) lo = mid;
+                else hi = mid - 1;
+            }
+            u = lo;
+        }
+    }
+    __device__ __forceinline__ bool next(const AttnParams& p, int TQ, Seg& s) {
+        if constexpr (!SK) {
+            if (done) return false;
+            done = true;
+            s.g = pair_geometry(p, TQ, blockIdx.z / p.num_splits, blockIdx.y, blockIdx.x,
+                                blockIdx.z % p.num_splits);
+            s.u = -1;
+            s.j0 = 0;
+            s.j1 = s.g.nt;
+            s.two = s.g.t0 + TQ < s.g.nrows;
+            s.shared = false;
+            return s.g.t0 < s.g.nrows && s.g.nt > 0;
+        } else {
+            if (dp) {
+                dp = false;
+                s.g = sk_unit(p, TQ, blockIdx.x);
+                s.u = blockIdx.x;
+                s.j0 = 0;
+                s.j1 = s.g.nt;
+                s.two = s.g.t0 + TQ < s.g.nrows;
+                s.shared = false;
+                if (s.g.t0 < s.g.nrows && s.g.nt > 0) return true;
+            }
+            while (!done && a < a1 && u < end_u) {
+                const int off = p.sk_unit_off[u];
+                if (off >= a1) break;
+                const int off1 = p.sk_unit_off[u + 1];
+                const int cur = p.sk_dp + u++;
+                if (off1 == off) continue;  // no key tile
+                s.g = sk_unit(p, TQ, cur);
+                const int w = sk_weight(s.g, TQ);
+                s.u = cur;
+                s.j0 = a > off ? (a - off + w - 1) / w : 0;
+                s.j1 = min(s.g.nt, (a1 - off + w - 1) / w);
+                s.two = s.g.t0 + TQ < s.g.nrows;
+                s.shared = true;
+                if (s.j1 > s.j0) return true;
+            }
+            done = true;
+            return false;
+        }
+    }
+};
+
+// Zero output and LSE = -inf for the existing rows of a pair whose rows see no
+// key.  Threads 0 .. 2 * kTileM - 1 each take one row.
 template <int G>
+__device__ __forceinline__ void zero_pair_rows(const AttnParams& p, const TileGeom& g) {
+    constexpr int TQ = kTileM / G;
+    if (threadIdx.x >= 2 * kTileM) return;
+    const int x = threadIdx.x / kTileM, r = threadIdx.x % kTileM;
+    const int i = g.t0 + x * TQ + r / G;
+    if (i >= g.nrows) return;
+    uint32_t zero[32];
+#pragma unroll
+    for (int e = 0; e < 32; ++e) zero[e] = 0u;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) store_row_chunk(p, g, i, g.kvh * G + r % G, c, zero, 0.f);
+    store_row_lse(p, g, i, g.kvh * G + r % G, -INFINITY);
+}
+
+template <int G, bool SK>
 __global__ void __maxnreg__(96)
     attn_tc2_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                     const AttnParams p) {
@@ -1108,44 +1254,33 @@ __global__ void __maxnreg__(96)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
-    TileGeom g;
-    g.b = blockIdx.z / p.num_splits;
-    g.split = blockIdx.z - g.b * p.num_splits;
-    g.kvh = blockIdx.y;
-    g.r0 = p.q_indptr[g.b];
-    g.nrows = min(p.q_indptr[g.b + 1] - g.r0, p.max_q_rows);
-    g.t0 = blockIdx.x * 2 * TQ;
-    g.qreal = min(p.q_real ? p.q_real[g.b] : g.nrows, g.nrows);
-    g.kv_len = min(max(p.kv_lens[g.b], 0), p.max_kv_len);
-    g.kb = g.split * p.split_keys;
-    {
-        const int ke = min(g.kv_len, g.kb + p.split_keys);
-        const int last = min(g.t0 + 2 * TQ, g.nrows) - 1;
-        int lim = 0;
-        if (g.t0 < g.qreal)
-            lim = visible_keys(min(last, g.qreal - 1), g.qreal, g.kv_len, p.mask, max(p.causal_block, 1));
-        g.key_hi = min(ke, lim);
-        g.nt = g.key_hi > g.kb ? (g.key_hi - g.kb + kTileN - 1) / kTileN : 0;
-    }
-    if (g.t0 >= g.nrows) return;  // uniform
-    // tile B holds rows (false in the last CTA of a sequence whose rows end in
-    // tile A): otherwise its MMAs and its softmax warps' key loop are skipped
-    const bool two = g.t0 + TQ < g.nrows;
-
-    if (g.nt == 0) {
-        if (threadIdx.x < 2 * kTileM) {
-            const int x = threadIdx.x / kTileM, r = threadIdx.x % kTileM;
-            const int i = g.t0 + x * TQ + r / G;
-            if (i < g.nrows) {
-                uint32_t zero[32];
-#pragma unroll
-                for (int e = 0; e < 32; ++e) zero[e] = 0u;
-#pragma unroll
-                for (int c = 0; c < 4; ++c) store_row_chunk(p, g, i, g.kvh * G + r % G, c, zero, 0.f);
-                store_row_lse(p, g, i, g.kvh * G + r % G, -INFINITY);
-            }
+    SegIter<SK> it0;
+    if constexpr (SK) {
+        // launched behind the planner with programmatic serialisation: its unit
+        // offsets are visible after this wait
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+        // this CTA's fragment slots hold nothing until a partial segment says so
+        if (threadIdx.x < 2) p.sk_dir[blockIdx.x * 2 + threadIdx.x] = make_int4(-1, 0, 0, 0);
+        // pairs with rows but no visible key: zero rows (units u = CTA mod grid)
+        for (int u = blockIdx.x; u < p.sk_units; u += p.sk_ctas) {
+            const TileGeom g = sk_unit(p, TQ, u);
+            if (g.t0 < g.nrows && g.nt == 0) zero_pair_rows<G>(p, g);
         }
-        return;
+        it0.init(p);
+    } else {
+        const TileGeom g = pair_geometry(p, TQ, blockIdx.z / p.num_splits, blockIdx.y, blockIdx.x,
+                                         blockIdx.z % p.num_splits);
+        if (g.t0 >= g.nrows) return;  // uniform
+        if (g.nt == 0) {
+            zero_pair_rows<G>(p, g);
+            return;
+        }
+    }
+    {
+        // a CTA without a segment leaves before any set-up (uniform)
+        SegIter<SK> probe = it0;
+        Seg s;
+        if (!probe.next(p, TQ, s)) return;
     }
     if ((smem_u32(smem) & 1023u) != 0) {
         if (threadIdx.x == 0) set_err(p.err, PKV_ERRBIT_TIMEOUT);
@@ -1203,44 +1338,55 @@ __global__ void __maxnreg__(96)
 
     if (warp == 16) {
         // ============================ producer ==============================
+        // K and V tiles of every segment in order, through rings that run
+        // across segment boundaries (gt counts the tiles of all segments)
         if (lane == 0) {
             prefetch_tmap(&tm_k);
             prefetch_tmap(&tm_v);
-            const int32_t* bt = p.block_table + static_cast<int64_t>(g.b) * p.block_table_stride;
-            const int last_page = (g.kv_len + 31) / 32;
-            auto load_tile = [&](const CUtensorMap* tm, uint8_t* dst, uint64_t* bar, int j) {
-                mbar_arrive_expect_tx(bar, kTileBytes);
+            SegIter<SK> it = it0;
+            Seg sg;
+            int kn = 0, vn = 0;  // K and V tiles issued
+            bool alive = true;
+            while (alive && it.next(p, TQ, sg)) {
+                const TileGeom& g = sg.g;
+                const int32_t* bt = p.block_table + static_cast<int64_t>(g.b) * p.block_table_stride;
+                const int last_page = (g.kv_len + 31) / 32;
+                auto load_tile = [&](const CUtensorMap* tm, uint8_t* dst, uint64_t* bar, int j) {
+                    mbar_arrive_expect_tx(bar, kTileBytes);
 #pragma unroll
-                for (int pg = 0; pg < 4; ++pg) {
-                    const int lp = (g.kb + j * kTileN) / 32 + pg;
-                    int phys = lp < last_page ? bt[lp] : static_cast<int>(p.num_pages);
-                    if (p.checked && lp < last_page && (phys < 0 || phys >= p.num_pages)) {
-                        set_err(p.err, PKV_ERRBIT_PAGE);
-                        phys = static_cast<int>(p.num_pages);
+                    for (int pg = 0; pg < 4; ++pg) {
+                        const int lp = (g.kb + j * kTileN) / 32 + pg;
+                        int phys = lp < last_page ? bt[lp] : static_cast<int>(p.num_pages);
+                        if (p.checked && lp < last_page && (phys < 0 || phys >= p.num_pages)) {
+                            set_err(p.err, PKV_ERRBIT_PAGE);
+                            phys = static_cast<int>(p.num_pages);
+                        }
+#pragma unroll
+                        for (int h = 0; h < 2; ++h)
+                            tma_load_4d(dst + h * kHalfBytes + pg * 4096, tm, bar, h * 64, g.kvh, 0, phys);
                     }
-#pragma unroll
-                    for (int h = 0; h < 2; ++h)
-                        tma_load_4d(dst + h * kHalfBytes + pg * 4096, tm, bar, h * 64, g.kvh, 0, phys);
-                }
-            };
-            int k_issued = 0, v_issued = 0;
-            while (k_issued < g.nt || v_issued < g.nt) {
-                if (k_issued < g.nt) {
-                    const int s = k_issued % kKStages;
-                    if (k_issued >= kKStages && !wait(&k_empty[s], ((k_issued / kKStages) - 1) & 1)) break;
-                    load_tile(&tm_k, smem + kK2Off + s * kTileBytes, &k_full[s], k_issued);
-                    ++k_issued;
-                }
-                if (v_issued < k_issued) {
-                    const int s = v_issued % kVStages;
-                    if (v_issued >= kVStages && !wait(&v_empty[s], ((v_issued / kVStages) - 1) & 1)) break;
-                    load_tile(&tm_v, smem + kV2Off + s * kTileBytes, &v_full[s], v_issued);
-                    ++v_issued;
+                };
+                for (int j = sg.j0; j < sg.j1; ++j) {
+                    const int sk = kn % kKStages;
+                    if (kn >= kKStages && !wait(&k_empty[sk], ((kn / kKStages) - 1) & 1)) {
+                        alive = false;
+                        break;
+                    }
+                    load_tile(&tm_k, smem + kK2Off + sk * kTileBytes, &k_full[sk], j);
+                    ++kn;
+                    const int sv = vn % kVStages;
+                    if (vn >= kVStages && !wait(&v_empty[sv], ((vn / kVStages) - 1) & 1)) {
+                        alive = false;
+                        break;
+                    }
+                    load_tile(&tm_v, smem + kV2Off + sv * kTileBytes, &v_full[sv], j);
+                    ++vn;
                 }
             }
-            for (int j = max(0, k_issued - kKStages); j < k_issued; ++j)
+            // do not leave with copies into this CTA's shared memory in flight
+            for (int j = max(0, kn - kKStages); j < kn; ++j)
                 mbar_wait(&k_full[j % kKStages], (j / kKStages) & 1);
-            for (int j = max(0, v_issued - kVStages); j < v_issued; ++j)
+            for (int j = max(0, vn - kVStages); j < vn; ++j)
                 mbar_wait(&v_full[j % kVStages], (j / kVStages) & 1);
         }
     } else if (warp == 17) {
@@ -1248,9 +1394,9 @@ __global__ void __maxnreg__(96)
         if (lane == 0) {
             constexpr uint32_t kIdescS = idesc_bf16(kTileM, kTileN, false);
             constexpr uint32_t kIdescO = idesc_bf16(kTileM, kD, true);
-            auto issue_s = [&](int x, int j) {
+            auto issue_s = [&](int x, int gt) {
                 const uint32_t qa = sbase + kQ2Off + x * kTileBytes;
-                const uint32_t kbse = sbase + kK2Off + (j % kKStages) * kTileBytes;
+                const uint32_t kbse = sbase + kK2Off + (gt % kKStages) * kTileBytes;
 #pragma unroll
                 for (int kk = 0; kk < kD / 16; ++kk) {
                     const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
@@ -1259,8 +1405,8 @@ __global__ void __maxnreg__(96)
                 }
                 umma_commit(&s_full[x]);
             };
-            auto issue_pv = [&](int x, int j) {
-                const uint32_t vb = sbase + kV2Off + (j % kVStages) * kTileBytes;
+            auto issue_pv = [&](int x, int gt, bool acc) {
+                const uint32_t vb = sbase + kV2Off + (gt % kVStages) * kTileBytes;
 #pragma unroll
                 for (int kk = 0; kk < kTileN / 16; ++kk) {
                     // A = P in tensor memory: keys [0,64) packed in columns [0,32),
@@ -1268,39 +1414,61 @@ __global__ void __maxnreg__(96)
                     const uint32_t pcol = kk < 4 ? kk * 8 : 64 + kk * 8;
                     const uint64_t bdesc = sdesc_sw128(vb + kk * 16 * 128, kHalfBytes, 1024);
                     umma_bf16_ts(tmem + x * 256 + 128, tmem + x * 256 + pcol, bdesc, kIdescO,
-                                 (j > 0 || kk > 0) ? 1u : 0u);
+                                 (acc || kk > 0) ? 1u : 0u);
                 }
             };
-            bool ok = wait(q_ready, 0) && wait(&k_full[0], 0);
-            if (ok) {
+            SegIter<SK> it = it0;
+            Seg sg;
+            int gt = 0;          // K/V tiles consumed (ring position)
+            int na = 0, nb = 0;  // P tiles of tile A / tile B consumed
+            int qn = 0;          // segments (Q tiles loaded)
+            bool ok = true;
+            while (ok && it.next(p, TQ, sg)) {
+                const bool two = sg.two;
+                // the segment's Q tiles are in shared memory; its first S MMAs
+                // follow every MMA of the previous segment in the pipe
+                ok = wait(q_ready, qn & 1) && wait(&k_full[gt % kKStages], (gt / kKStages) & 1);
+                ++qn;
+                if (!ok) break;
                 tc_fence_after();
-                issue_s(0, 0);
-                if (two) issue_s(1, 0);
-                umma_commit(&k_empty[0]);
-            }
-            for (int j = 0; ok && j < g.nt; ++j) {
-                const bool more = j + 1 < g.nt;
-                if (!wait(&p_full[0], j & 1) || !wait(&v_full[j % kVStages], (j / kVStages) & 1)) break;
-                tc_fence_after();
-                issue_pv(0, j);
-                if (more) {
-                    if (!wait(&k_full[(j + 1) % kKStages], ((j + 1) / kKStages) & 1)) break;
+                issue_s(0, gt);
+                if (two) issue_s(1, gt);
+                umma_commit(&k_empty[gt % kKStages]);
+                for (int j = sg.j0; j < sg.j1; ++j, ++gt) {
+                    const bool more = j + 1 < sg.j1;
+                    if (!wait(&p_full[0], na & 1) || !wait(&v_full[gt % kVStages], (gt / kVStages) & 1)) {
+                        ok = false;
+                        break;
+                    }
+                    ++na;
                     tc_fence_after();
-                    issue_s(0, j + 1);
-                } else {
-                    umma_commit(&o_full[0]);
-                }
-                if (two) {
-                    if (!wait(&p_full[1], j & 1)) break;
-                    tc_fence_after();
-                    issue_pv(1, j);
-                }
-                umma_commit(&v_empty[j % kVStages]);
-                if (more) {
-                    if (two) issue_s(1, j + 1);
-                    umma_commit(&k_empty[(j + 1) % kKStages]);
-                } else if (two) {
-                    umma_commit(&o_full[1]);
+                    issue_pv(0, gt, j > sg.j0);
+                    if (more) {
+                        if (!wait(&k_full[(gt + 1) % kKStages], ((gt + 1) / kKStages) & 1)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        issue_s(0, gt + 1);
+                    } else {
+                        umma_commit(&o_full[0]);
+                    }
+                    if (two) {
+                        if (!wait(&p_full[1], nb & 1)) {
+                            ok = false;
+                            break;
+                        }
+                        ++nb;
+                        tc_fence_after();
+                        issue_pv(1, gt, j > sg.j0);
+                    }
+                    umma_commit(&v_empty[gt % kVStages]);
+                    if (more) {
+                        if (two) issue_s(1, gt + 1);
+                        umma_commit(&k_empty[(gt + 1) % kKStages]);
+                    } else if (two) {
+                        umma_commit(&o_full[1]);
+                    }
                 }
             }
         }
@@ -1310,178 +1478,232 @@ __global__ void __maxnreg__(96)
         const int hf = (warp >> 2) & 1;        // key half of each tile (and O column half)
         const int r = (warp & 3) * 32 + lane;  // row in the tile = tensor-memory lane
         const int t = r / G, hg = r % G;
-        const int i = g.t0 + x * TQ + t;
-        const int h = g.kvh * G + hg;
         const int bar_id = 1 + x * 4 + (warp & 3);  // the two warps of this lane quadrant
-        const bool row_exists = i < g.nrows;
-        const int limit = row_exists ? visible_keys(i, g.qreal, g.kv_len, p.mask, max(p.causal_block, 1))
-                                     : 0;
-        {
-            // this thread's half of the row's 16-byte chunks
-            const uint4* src = reinterpret_cast<const uint4*>(
-                static_cast<const __nv_bfloat16*>(p.q) + static_cast<int64_t>(g.r0 + i) * p.q_token_stride +
-                static_cast<int64_t>(h) * p.q_head_stride) + hf * 8;
-            uint8_t* qt = smem + kQ2Off + x * kTileBytes + hf * kHalfBytes;
-#pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                const uint4 v = row_exists ? src[c] : make_uint4(0u, 0u, 0u, 0u);
-                *reinterpret_cast<uint4*>(qt + sw128_offset(r, c)) = v;
-            }
-            fence_proxy_async_smem();
-            mbar_arrive(q_ready);
-        }
         const uint32_t lane_addr = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16) + x * 256;
-        const uint32_t s_addr = lane_addr + hf * 64;     // this half's S columns
+        const uint32_t s_addr = lane_addr + hf * 64;        // this half's S columns
         const uint32_t o_addr = lane_addr + 128 + hf * 64;  // this half's O columns
         float* xmine = xch + (x * 2 + hf) * kTileM + r;
         const float* xother = xch + (x * 2 + (hf ^ 1)) * kTileM + r;
-        float m_used = -INFINITY;
-        float l = 0.f, l_b = 0.f;
+        float* xl = xch + x * 2 * kTileM + r;  // [tile][0: l, 1: l_b][row]
         const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
-        const bool warp_live = __any_sync(0xffffffffu, limit > 0);
+        SegIter<SK> it = it0;
+        Seg sg;
+        int gt = 0;     // K/V ring position of the segment's first tile
+        int nit = 0;    // key tiles of this tile's rows processed (S / P phases)
+        int nseg = 0;   // segments in which this tile had rows (O phases)
+        int qn = 0;     // segments (Q phases)
+        int slot = 0;   // shared segments of this CTA (fragment slot of a partial one)
         bool ok = true;
-        const int nt_mine = (x == 1 && !two) ? 0 : g.nt;  // no rows in tile B: nothing to do
-        for (int j = 0; j < nt_mine; ++j) {
-            bool ok_t = __all_sync(0xffffffffu, wait(&s_full[x], j & 1));
-            tc_fence_after();
-            const int nvis = limit - (g.kb + j * kTileN) - hf * 64;  // visible columns of this half
-            float mpart = -INFINITY;
-            if (ok_t && warp_live) {
-                uint32_t sv[32];
+        while (ok && it.next(p, TQ, sg)) {
+            const TileGeom& g = sg.g;
+            const int i = g.t0 + x * TQ + t;
+            const int h = g.kvh * G + hg;
+            const bool row_exists = i < g.nrows;
+            const int limit = row_exists ? visible_keys(i, g.qreal, g.kv_len, p.mask, max(p.causal_block, 1))
+                                         : 0;
+            {
+                // this thread's half of the row's 16-byte chunks.  The previous
+                // segment's S MMAs have finished reading this Q tile (their S was
+                // consumed), and its O was read before this arrive, ahead of the
+                // segment's first P.V
+                const uint4* src = reinterpret_cast<const uint4*>(
+                    static_cast<const __nv_bfloat16*>(p.q) + static_cast<int64_t>(g.r0 + i) * p.q_token_stride +
+                    static_cast<int64_t>(h) * p.q_head_stride) + hf * 8;
+                uint8_t* qt = smem + kQ2Off + x * kTileBytes + hf * kHalfBytes;
 #pragma unroll
-                for (int c = 0; c < 2; ++c) {
-                    tmem_load32(s_addr + c * 32, sv);
-                    if (nvis < (c + 1) * 32) {
-#pragma unroll
-                        for (int e = 0; e < 32; ++e)
-                            sv[e] = c * 32 + e < nvis ? sv[e] : __float_as_uint(-INFINITY);
-                    }
-                    float a[4];
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) a[q] = __uint_as_float(sv[q]);
-#pragma unroll
-                    for (int e = 4; e < 32; e += 8) {
-#pragma unroll
-                        for (int q = 0; q < 4; ++q)
-                            a[q] = fmax3(a[q], __uint_as_float(sv[e + q]), __uint_as_float(sv[e + 4 + q]));
-                    }
-                    mpart = fmax3(mpart, fmax3(a[0], a[1], a[2]), a[3]);
+                for (int c = 0; c < 8; ++c) {
+                    const uint4 v = row_exists ? src[c] : make_uint4(0u, 0u, 0u, 0u);
+                    *reinterpret_cast<uint4*>(qt + sw128_offset(r, c)) = v;
                 }
+                fence_proxy_async_smem();
+                tc_fence_before();
+                mbar_arrive(q_ready);
             }
-            // exchange the two halves' maxima; also agree on whether every wait succeeded
-            *xmine = mpart;
-            if (!bar_and(bar_id, 2 * 32, ok_t)) {
-                ok = false;
-                break;
+            const bool active = x == 0 || sg.two;  // no rows in tile B: nothing to do
+            const int n_seg_tiles = sg.j1 - sg.j0;
+            if (!active) {
+                // one arrive per segment and thread: wait for this segment's
+                // Q phase before arriving for the next one
+                ok = wait(q_ready, qn & 1);
+                ++qn;
+                gt += n_seg_tiles;
+                slot += sg.shared ? 1 : 0;
+                continue;
             }
-            if (warp_live) {
-                const float mx = fmaxf(mpart, *xother) * p.scale_log2;
-                float alpha = 1.f;
-                if (mx > m_used + kLazyRescale) {
-                    alpha = fast_exp2(m_used - mx);
-                    m_used = mx;
-                }
-                // O *= alpha on this half's 64 columns
-                if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+            ++qn;
+            float m_used = -INFINITY;
+            float l = 0.f, l_b = 0.f;
+            const bool warp_live = __any_sync(0xffffffffu, limit > 0);
+            for (int j = sg.j0; j < sg.j1; ++j, ++nit) {
+                bool ok_t = __all_sync(0xffffffffu, wait(&s_full[x], nit & 1));
+                tc_fence_after();
+                const int nvis = limit - (g.kb + j * kTileN) - hf * 64;  // visible columns of this half
+                float mpart = -INFINITY;
+                if (ok_t && warp_live) {
+                    uint32_t sv[32];
 #pragma unroll
                     for (int c = 0; c < 2; ++c) {
+                        tmem_load32(s_addr + c * 32, sv);
+                        if (nvis < (c + 1) * 32) {
+#pragma unroll
+                            for (int e = 0; e < 32; ++e)
+                                sv[e] = c * 32 + e < nvis ? sv[e] : __float_as_uint(-INFINITY);
+                        }
+                        float a[4];
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) a[q] = __uint_as_float(sv[q]);
+#pragma unroll
+                        for (int e = 4; e < 32; e += 8) {
+#pragma unroll
+                            for (int q = 0; q < 4; ++q)
+                                a[q] = fmax3(a[q], __uint_as_float(sv[e + q]), __uint_as_float(sv[e + 4 + q]));
+                        }
+                        mpart = fmax3(mpart, fmax3(a[0], a[1], a[2]), a[3]);
+                    }
+                }
+                // exchange the two halves' maxima; also agree on whether every wait succeeded
+                *xmine = mpart;
+                if (!bar_and(bar_id, 2 * 32, ok_t)) {
+                    ok = false;
+                    break;
+                }
+                if (warp_live) {
+                    const float mx = fmaxf(mpart, *xother) * p.scale_log2;
+                    float alpha = 1.f;
+                    if (mx > m_used + kLazyRescale) {
+                        alpha = fast_exp2(m_used - mx);
+                        m_used = mx;
+                    }
+                    // O *= alpha on this half's 64 columns
+                    if (j > sg.j0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll
+                        for (int c = 0; c < 2; ++c) {
+                            uint32_t v[32];
+                            tmem_load32(o_addr + c * 32, v);
+#pragma unroll
+                            for (int e = 0; e < 32; e += 2) {
+                                const float2 o2 = __fmul2_rn(make_float2(__uint_as_float(v[e]), __uint_as_float(v[e + 1])),
+                                                             make_float2(alpha, alpha));
+                                v[e] = __float_as_uint(o2.x);
+                                v[e + 1] = __float_as_uint(o2.y);
+                            }
+                            tmem_store32(o_addr + c * 32, v);
+                        }
+                    }
+                    const float nm = m_used == -INFINITY ? 0.f : -m_used;
+                    const float2 nm2 = make_float2(nm, nm);
+                    float2 rs2 = make_float2(0.f, 0.f), rsb2 = make_float2(0.f, 0.f);
+                    // half 0: S columns [0,32),[32,64) -> P columns [0,16),[16,32);
+                    // half 1: S columns [96,128),[64,96) -> P columns [112,128),[96,112)
+#pragma unroll
+                    for (int cc = 0; cc < 2; ++cc) {
+                        const int c = hf ? 1 - cc : cc;
                         uint32_t v[32];
-                        tmem_load32(o_addr + c * 32, v);
+                        tmem_load32(s_addr + c * 32, v);
+                        if (nvis < (c + 1) * 32) {
+#pragma unroll
+                            for (int e = 0; e < 32; ++e)
+                                v[e] = c * 32 + e < nvis ? v[e] : __float_as_uint(-INFINITY);
+                        }
+                        uint32_t pk[16];
 #pragma unroll
                         for (int e = 0; e < 32; e += 2) {
-                            const float2 o2 = __fmul2_rn(make_float2(__uint_as_float(v[e]), __uint_as_float(v[e + 1])),
-                                                         make_float2(alpha, alpha));
-                            v[e] = __float_as_uint(o2.x);
-                            v[e + 1] = __float_as_uint(o2.y);
+                            const float2 xx = __ffma2_rn(make_float2(__uint_as_float(v[e]), __uint_as_float(v[e + 1])),
+                                                         sc2, nm2);
+                            const float2 pp = make_float2(fast_exp2(xx.x), fast_exp2(xx.y));
+                            pk[e / 2] = pack_bf16x2(pp.x, pp.y);
+                            rs2 = __fadd2_rn(rs2, pp);
+                            add_bf16x2(rsb2, pk[e / 2]);
                         }
-                        tmem_store32(o_addr + c * 32, v);
+                        tmem_store16(lane_addr + hf * 96 + c * 16, pk);
+                    }
+                    tmem_store_wait();
+                    l = l * alpha + (rs2.x + rs2.y);
+                    l_b = l_b * alpha + (rsb2.x + rsb2.y);
+                } else {
+                    uint32_t zero[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) zero[e] = 0u;
+#pragma unroll
+                    for (int c = 0; c < 2; ++c) tmem_store16(lane_addr + hf * 96 + c * 16, zero);
+                    tmem_store_wait();
+                }
+                // keys past the sequence's length inside its last page: zero their V rows
+                const int key0 = g.kb + j * kTileN;
+                if (x == 0 && key0 + kTileN > g.kv_len && g.kv_len > key0) {
+                    const int gj = gt + (j - sg.j0);
+                    const int vs = gj % kVStages;
+                    ok_t = __all_sync(0xffffffffu, wait(&v_full[vs], (gj / kVStages) & 1));
+                    if (ok_t) {
+                        const int first = g.kv_len - key0;
+                        const int lastr = min(kTileN, (first + 31) / 32 * 32);
+                        uint8_t* vt = smem + kV2Off + vs * kTileBytes;
+                        for (int idx = hf * kTileM + r; idx < (lastr - first) * 16; idx += 2 * kTileM) {
+                            const int row = first + idx / 16, c16 = idx % 16;
+                            *reinterpret_cast<uint4*>(vt + (c16 >> 3) * kHalfBytes + sw128_offset(row, c16 & 7)) =
+                                make_uint4(0u, 0u, 0u, 0u);
+                        }
+                        fence_proxy_async_smem();
                     }
                 }
-                const float nm = m_used == -INFINITY ? 0.f : -m_used;
-                const float2 nm2 = make_float2(nm, nm);
-                float2 rs2 = make_float2(0.f, 0.f), rsb2 = make_float2(0.f, 0.f);
-                // half 0: S columns [0,32),[32,64) -> P columns [0,16),[16,32);
-                // half 1: S columns [96,128),[64,96) -> P columns [112,128),[96,112)
-#pragma unroll
-                for (int cc = 0; cc < 2; ++cc) {
-                    const int c = hf ? 1 - cc : cc;
-                    uint32_t v[32];
-                    tmem_load32(s_addr + c * 32, v);
-                    if (nvis < (c + 1) * 32) {
-#pragma unroll
-                        for (int e = 0; e < 32; ++e)
-                            v[e] = c * 32 + e < nvis ? v[e] : __float_as_uint(-INFINITY);
-                    }
-                    uint32_t pk[16];
-#pragma unroll
-                    for (int e = 0; e < 32; e += 2) {
-                        const float2 xx = __ffma2_rn(make_float2(__uint_as_float(v[e]), __uint_as_float(v[e + 1])),
-                                                     sc2, nm2);
-                        const float2 pp = make_float2(fast_exp2(xx.x), fast_exp2(xx.y));
-                        pk[e / 2] = pack_bf16x2(pp.x, pp.y);
-                        rs2 = __fadd2_rn(rs2, pp);
-                        add_bf16x2(rsb2, pk[e / 2]);
-                    }
-                    tmem_store16(lane_addr + hf * 96 + c * 16, pk);
-                }
-                tmem_store_wait();
-                l = l * alpha + (rs2.x + rs2.y);
-                l_b = l_b * alpha + (rsb2.x + rsb2.y);
-            } else {
-                uint32_t zero[16];
-#pragma unroll
-                for (int e = 0; e < 16; ++e) zero[e] = 0u;
-#pragma unroll
-                for (int c = 0; c < 2; ++c) tmem_store16(lane_addr + hf * 96 + c * 16, zero);
-                tmem_store_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&p_full[x]);
             }
-            // keys past the sequence's length inside its last page: zero their V rows
-            const int key0 = g.kb + j * kTileN;
-            if (x == 0 && key0 + kTileN > g.kv_len && g.kv_len > key0) {
-                const int vs = j % kVStages;
-                ok_t = __all_sync(0xffffffffu, wait(&v_full[vs], (j / kVStages) & 1));
-                if (ok_t) {
-                    const int first = g.kv_len - key0;
-                    const int lastr = min(kTileN, (first + 31) / 32 * 32);
-                    uint8_t* vt = smem + kV2Off + vs * kTileBytes;
-                    for (int idx = hf * kTileM + r; idx < (lastr - first) * 16; idx += 2 * kTileM) {
-                        const int row = first + idx / 16, c16 = idx % 16;
-                        *reinterpret_cast<uint4*>(vt + (c16 >> 3) * kHalfBytes + sw128_offset(row, c16 & 7)) =
-                            make_uint4(0u, 0u, 0u, 0u);
+            // ---- epilogue: the two halves' sums, then O / l on this half's columns
+            const bool ok_o = __all_sync(0xffffffffu, ok && wait(&o_full[x], nseg & 1));
+            ++nseg;
+            tc_fence_after();
+            // every key-loop exchange has been read: o_full follows both halves' last P
+            bar_sync_n(bar_id, 2 * 32);
+            if (hf == 1) {
+                xl[0] = l;
+                xl[kTileM] = l_b;
+            }
+            bar_sync_n(bar_id, 2 * 32);
+            // a segment that is not its unit's whole key range leaves a partial
+            // state in this CTA's fragment slot (the first or the last segment)
+            const bool whole = sg.j0 == 0 && sg.j1 == g.nt;
+            const int fslot = blockIdx.x * 2 + (slot == 0 ? 0 : 1);
+            float inv_l = 0.f;
+            if (hf == 0) {
+                const float lt = l + xl[0], lbt = l_b + xl[kTileM];
+                const bool any = lt > 0.f && lbt > 0.f;
+                inv_l = any ? 1.0f / lbt : 0.f;
+                const float lse = any ? (m_used + __log2f(lt)) * kLn2 : -INFINITY;
+                if (ok_o && row_exists) {
+                    if (whole) store_row_lse(p, g, i, h, lse);
+                    else p.sk_frag_lse[static_cast<int64_t>(fslot) * kSkFragRows + x * kTileM + r] = lse;
+                }
+                xl[0] = inv_l;
+            }
+            bar_sync_n(bar_id, 2 * 32);
+            if (hf == 1) inv_l = xl[0];
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                uint32_t v[32];
+                tmem_load32(o_addr + c * 32, v);
+                if (ok_o && row_exists) {
+                    if (whole) {
+                        store_row_chunk(p, g, i, h, hf * 2 + c, v, inv_l);
+                    } else {
+                        float4* dst = reinterpret_cast<float4*>(
+                            p.sk_frag_o + (static_cast<int64_t>(fslot) * kSkFragRows + x * kTileM + r) * kD +
+                            (hf * 2 + c) * 32);
+#pragma unroll
+                        for (int q = 0; q < 8; ++q)
+                            dst[q] = make_float4(__uint_as_float(v[4 * q]) * inv_l, __uint_as_float(v[4 * q + 1]) * inv_l,
+                                                 __uint_as_float(v[4 * q + 2]) * inv_l,
+                                                 __uint_as_float(v[4 * q + 3]) * inv_l);
                     }
-                    fence_proxy_async_smem();
                 }
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&p_full[x]);
-        }
-        // ---- epilogue: the two halves' sums, then O / l on this half's columns
-        const bool ok_o = __all_sync(0xffffffffu, ok && nt_mine > 0 && wait(&o_full[x], 0));
-        tc_fence_after();
-        // every key-loop exchange has been read: o_full follows both halves' last P
-        float* xl = xch + x * 2 * kTileM + r;  // [tile][0: l, 1: l_b][row]
-        bar_sync_n(bar_id, 2 * 32);
-        if (hf == 1) {
-            xl[0] = l;
-            xl[kTileM] = l_b;
-        }
-        bar_sync_n(bar_id, 2 * 32);
-        float inv_l = 0.f;
-        if (hf == 0) {
-            const float lt = l + xl[0], lbt = l_b + xl[kTileM];
-            const bool any = lt > 0.f && lbt > 0.f;
-            inv_l = any ? 1.0f / lbt : 0.f;
-            if (ok_o && row_exists) store_row_lse(p, g, i, h, any ? (m_used + __log2f(lt)) * kLn2 : -INFINITY);
-            xl[0] = inv_l;
-        }
-        bar_sync_n(bar_id, 2 * 32);
-        if (hf == 1) inv_l = xl[0];
-#pragma unroll
-        for (int c = 0; c < 2; ++c) {
-            uint32_t v[32];
-            tmem_load32(o_addr + c * 32, v);
-            if (ok_o && row_exists) store_row_chunk(p, g, i, h, hf * 2 + c, v, inv_l);
+            if constexpr (SK) {
+                if (!whole && ok_o && threadIdx.x == 0) p.sk_dir[fslot] = make_int4(sg.u, sg.j0, sg.j1, g.nt);
+            }
+            ok = ok && ok_o;
+            gt += n_seg_tiles;
+            slot += sg.shared ? 1 : 0;
         }
     }
 
@@ -1491,24 +1713,205 @@ __global__ void __maxnreg__(96)
     if (warp == 17) tmem_dealloc(tmem, kTmemCols);
 }
 
+// Block-wide exclusive prefix sum of one value per thread (blockDim 1024);
+// returns the thread's exclusive sum and writes the block total to *total.
+__device__ __forceinline__ int block_exclusive_sum(int v, int* warp_tot, int* total) {
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    int incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int t = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += t;
+    }
+    if (lane == 31) warp_tot[wid] = incl;
+    __syncthreads();
+    if (wid == 0) {
+        int w = warp_tot[lane];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int t = __shfl_up_sync(0xffffffffu, w, o);
+            if (lane >= o) w += t;
+        }
+        warp_tot[lane] = w;  // inclusive over warps
+    }
+    __syncthreads();
+    const int before = (wid > 0 ? warp_tot[wid - 1] : 0) + incl - v;
+    *total = warp_tot[31];
+    __syncthreads();
+    return before;
+}
+
+// Stream-K planner (one CTA of 1024 threads): the weighted key-tile offsets of
+// the shared units and every CTA's share of them.  A CTA's share is what
+// brings its work (its whole first-wave unit plus the share) to the average;
+// shares are scaled to add up to the shared units' total.
+template <int G>
+__global__ void __launch_bounds__(1024) tc2_sk_plan_kernel(const AttnParams p) {
+    constexpr int TQ = kTileM / G;
+    // the persistent launch may start its prologue now; it waits for this
+    // grid's completion before it reads the offsets
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    __shared__ int warp_tot[32];
+    __shared__ int carry;
+    if (threadIdx.x == 0) carry = 0;
+    __syncthreads();
+    auto cost_of = [&](int u) {
+        const TileGeom g = sk_unit(p, TQ, u);
+        return g.t0 < g.nrows ? g.nt * sk_weight(g, TQ) : 0;
+    };
+    const int n_shared = p.sk_units - p.sk_dp;
+    for (int base = 0; base < n_shared; base += 1024) {
+        const int k = base + threadIdx.x;
+        const int cost = k < n_shared ? cost_of(p.sk_dp + k) : 0;
+        int tot;
+        const int before = block_exclusive_sum(cost, warp_tot, &tot);
+        if (k < n_shared) p.sk_unit_off[k] = carry + before;
+        __syncthreads();
+        if (threadIdx.x == 0) carry += tot;
+        __syncthreads();
+    }
+    const int w_shared = carry;
+    if (threadIdx.x == 0) p.sk_unit_off[n_shared] = w_shared;
+    // shares: the first-wave unit of CTA c costs dp_c; the target is the mean
+    // of all work per CTA
+    const int c = threadIdx.x;
+    const int dp_c = c < p.sk_dp ? cost_of(c) : 0;
+    int dp_tot;
+    block_exclusive_sum(c < p.sk_ctas ? dp_c : 0, warp_tot, &dp_tot);
+    const int64_t target = (static_cast<int64_t>(dp_tot) + w_shared) / p.sk_ctas;
+    const int want = c < p.sk_ctas ? static_cast<int>(target > dp_c ? target - dp_c : 0) : 0;
+    int want_tot;
+    const int want_before = block_exclusive_sum(want, warp_tot, &want_tot);
+    if (c <= p.sk_ctas) {
+        // (no CTA below the mean, from rounding: equal shares)
+        const int64_t off = want_tot > 0 ? static_cast<int64_t>(want_before) * w_shared / want_tot
+                                         : static_cast<int64_t>(c) * w_shared / p.sk_ctas;
+        p.sk_cta_off[c] = c == p.sk_ctas ? w_shared : static_cast<int>(off);
+    }
+}
+
+// Stream-K reduce: for every unit split between CTAs, the CTA slot holding the
+// unit's first keys names the following CTAs' first slots that hold the rest,
+// and their partial states are merged by LSE into the output.  Grid: (fragment
+// slot, group of 8 fragment rows); one warp per row, every load of a row in
+// flight at once.
+constexpr int kSkReduceRows = 8;
+template <int G>
+__global__ void __launch_bounds__(32 * kSkReduceRows) tc2_sk_reduce_kernel(const AttnParams p) {
+    constexpr int TQ = kTileM / G;
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const int4 d = p.sk_dir[blockIdx.x];
+    if (d.x < 0 || d.y != 0) return;  // not partial, or not the unit's first keys
+    // a unit spans at most every CTA plus one (the host keeps the grid under 1024)
+    constexpr int kMaxFrag = 1024;
+    __shared__ int frag[kMaxFrag];
+    __shared__ int nfrag;
+    if (threadIdx.x == 0) {
+        int n = 0;
+        frag[n++] = blockIdx.x;
+        int covered = d.z;
+        for (int c = blockIdx.x / 2 + 1; c < p.sk_ctas && covered < d.w && n < kMaxFrag; ++c) {
+            const int4 e = p.sk_dir[c * 2];
+            if (e.x != d.x) continue;  // a CTA without keys (empty share)
+            if (e.y != covered) break;
+            frag[n++] = c * 2;
+            covered = e.z;
+        }
+        if (covered != d.w && blockIdx.y == 0) set_err(p.err, PKV_ERRBIT_TIMEOUT);  // never expected
+        nfrag = n;
+    }
+    __syncthreads();
+    const TileGeom g = sk_unit(p, TQ, d.x);
+    const int lane = threadIdx.x & 31;
+    const int row = blockIdx.y * kSkReduceRows + (threadIdx.x >> 5);
+    const int x = row / kTileM, r = row % kTileM;
+    const int i = g.t0 + x * TQ + r / G;
+    if (i >= g.nrows) return;
+    const int h = g.kvh * G + r % G;
+    const int n = nfrag;
+    // the fragments' LSEs, one per lane (more than 32 fragments: in rounds)
+    float m = -INFINITY;
+    for (int f0 = 0; f0 < n; f0 += 32) {
+        const float lf = f0 + lane < n
+                             ? __ldcg(p.sk_frag_lse + static_cast<int64_t>(frag[f0 + lane]) * kSkFragRows + row)
+                             : -INFINITY;
+        m = fmaxf(m, lf);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    float wsum = 0.f;
+    if (m != -INFINITY) {
+#pragma unroll 4
+        for (int f = 0; f < n; ++f) {
+            const int64_t fr = static_cast<int64_t>(frag[f]) * kSkFragRows + row;
+            const float w = __expf(__ldcg(p.sk_frag_lse + fr) - m);
+            const float4 o = __ldcg(reinterpret_cast<const float4*>(p.sk_frag_o + fr * kD) + lane);
+            wsum += w;
+            acc.x = fmaf(w, o.x, acc.x);
+            acc.y = fmaf(w, o.y, acc.y);
+            acc.z = fmaf(w, o.z, acc.z);
+            acc.w = fmaf(w, o.w, acc.w);
+        }
+    }
+    const float inv = wsum > 0.f ? 1.0f / wsum : 0.f;
+    const int64_t st = static_cast<int64_t>(g.r0 + i) * p.num_q_heads + h;
+    if (p.out_f32) {
+        reinterpret_cast<float4*>(static_cast<float*>(p.out) + st * kD)[lane] =
+            make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+    } else {
+        reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(p.out) + st * kD)[lane] =
+            make_uint2(pack_bf16x2(acc.x * inv, acc.y * inv), pack_bf16x2(acc.z * inv, acc.w * inv));
+    }
+    if (p.lse && lane == 0) p.lse[st] = wsum > 0.f ? m + __logf(wsum) : -INFINITY;
+}
+
 template <int G>
 cudaError_t launch_g2(const AttnParams& p, const void* tk, const void* tv, cudaStream_t s) {
-    auto kern = attn_tc2_kernel<G>;
-    // shared-memory opt-in: once per device
-    static DeviceOnce opted;
+    const bool sk = p.sk_ctas > 0;
+    auto kern = sk ? attn_tc2_kernel<G, true> : attn_tc2_kernel<G, false>;
+    // shared-memory opt-in: once per device and kernel
+    static DeviceOnce opted[2];
     int dev = 0, done = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    e = opted.get(dev, &done, [&](int, int* v) {
+    e = opted[sk ? 1 : 0].get(dev, &done, [&](int, int* v) {
         *v = 1;
         return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes2);
     });
     if (e != cudaSuccess) return e;
     const int TQ = kTileM / G;
-    dim3 grid((p.max_q_rows + 2 * TQ - 1) / (2 * TQ), p.num_kv_heads, p.batch * p.num_splits);
-    kern<<<grid, kThreads2, kSmemBytes2, s>>>(*static_cast<const CUtensorMap*>(tk),
-                                              *static_cast<const CUtensorMap*>(tv), p);
-    return cudaGetLastError();
+    if (!sk) {
+        dim3 grid((p.max_q_rows + 2 * TQ - 1) / (2 * TQ), p.num_kv_heads, p.batch * p.num_splits);
+        kern<<<grid, kThreads2, kSmemBytes2, s>>>(*static_cast<const CUtensorMap*>(tk),
+                                                  *static_cast<const CUtensorMap*>(tv), p);
+        return cudaGetLastError();
+    }
+    // planner, then the persistent launch and the reduce, each behind the
+    // previous one with programmatic serialisation (its prologue overlaps)
+    tc2_sk_plan_kernel<G><<<1, 1024, 0, s>>>(p);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(p.sk_ctas));
+    cfg.blockDim = dim3(kThreads2);
+    cfg.dynamicSmemBytes = kSmemBytes2;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, kern, *static_cast<const CUtensorMap*>(tk),
+                           *static_cast<const CUtensorMap*>(tv), p);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t rcfg = {};
+    rcfg.gridDim = dim3(static_cast<unsigned>(2 * p.sk_ctas), kSkFragRows / kSkReduceRows);
+    rcfg.blockDim = dim3(32 * kSkReduceRows);
+    rcfg.stream = s;
+    rcfg.attrs = attr;
+    rcfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&rcfg, tc2_sk_reduce_kernel<G>, p);
 }
 
 // One-tile launches: when a tile's rows (query rows x grouped heads) fit in
@@ -1568,6 +1971,16 @@ bool attn_tc_supported(int head_dim, int group) {
 }
 
 int attn_tc_rows_per_tile(int group) { return kTileM / group; }
+
+bool attn_tc_two_tile(int max_q_rows, int group) { return max_q_rows > kTileM / group; }
+
+size_t attn_tc_sk_bytes(int units, int ctas, int head_dim) {
+    auto r256 = [](size_t n) { return (n + 255) / 256 * 256; };
+    return r256((static_cast<size_t>(units) + 1) * sizeof(int)) + r256((static_cast<size_t>(ctas) + 1) * sizeof(int)) +
+           r256(2 * static_cast<size_t>(ctas) * 16) +
+           r256(2 * static_cast<size_t>(ctas) * kSkFragRows * sizeof(float)) +
+           r256(2 * static_cast<size_t>(ctas) * kSkFragRows * head_dim * sizeof(float));
+}
 
 cudaError_t launch_attn_tc_grouped(const AttnParams& p, const void* tk, const void* tv, cudaStream_t s) {
     switch (p.num_q_heads / p.num_kv_heads) {

@@ -96,7 +96,10 @@ struct Plan {
     int splits = 1;
     int split_keys = 0;
     size_t ws_bytes = 0;
+    // stream-K schedule of the two-tile kernel (sk_ctas > 0)
+    int sk_ctas = 0, sk_units = 0, sk_tiles_x = 0;
 };
+
 
 constexpr int kDecodeSplitKeys = 512;  // 16 pages: the pages' minimum split of 512 tokens
 constexpr int kDefaultSMs = 152;       // GB300: planned for when no device can be queried
@@ -171,7 +174,27 @@ Plan plan_attention(int batch, int max_q_rows, int Hq, int Hkv, int D, int max_k
         pl.kernel = Kernel::kTile;
         const int tq = pkv::attn_tc_rows_per_tile(G);
         const int rows_per_cta = max_q_rows > tq ? 2 * tq : tq;
-        const int64_t ctas = static_cast<int64_t>((max_q_rows + rows_per_cta - 1) / rows_per_cta) * Hkv * batch;
+        const int tiles_x = (max_q_rows + rows_per_cta - 1) / rows_per_cta;
+        const int64_t ctas = static_cast<int64_t>(tiles_x) * Hkv * batch;
+        // stream-K (on request, PKV_FLAG_STREAM_K): one persistent CTA per SM,
+        // each running one whole first-wave tile pair and then a contiguous
+        // share of the remaining pairs' key tiles.  Not the default: on the
+        // video step's 280 pairs (1.84 waves) it measured 0.323 ms against
+        // 0.280 ms for this grid -- identical pairs run 129-155 us on
+        // different SMs, which static shares cannot absorb and the grid's
+        // second wave, scheduled as SMs free up, does; every share also
+        // starts and ends a segment (Q reload, pipeline refill, the merge).
+        const int64_t key_tiles = (static_cast<int64_t>(max_kv_len) + kTileKeys - 1) / kTileKeys;
+        if (pkv::attn_tc_two_tile(max_q_rows, G) && num_splits == 0 && (flags & PKV_FLAG_STREAM_K) &&
+            !(flags & PKV_FLAG_TILE_GRID) && sms <= 1023 && ctas * key_tiles < (1ll << 31) && key_tiles > 0) {
+            pl.sk_ctas = sms;
+            pl.sk_units = static_cast<int>(ctas);
+            pl.sk_tiles_x = tiles_x;
+            pl.splits = 1;
+            pl.split_keys = static_cast<int>(key_tiles * kTileKeys);
+            pl.ws_bytes = pkv::attn_tc_sk_bytes(pl.sk_units, pl.sk_ctas, D);
+            return pl;
+        }
         const int s = tile_splits(ctas, max_kv_len, num_splits, sms);
         const int per = (max_kv_len + s - 1) / std::max(s, 1);
         pl.split_keys = std::max(kTileKeys, (per + kTileKeys - 1) / kTileKeys * kTileKeys);
@@ -295,6 +318,7 @@ pkv_status pkv_plan_attention(int batch, int max_q_rows, int num_q_heads, int nu
     const Plan pl = plan_attention(batch, max_q_rows, num_q_heads, num_kv_heads, head_dim, max_kv_len,
                                    num_splits, flags, num_sms > 0 ? num_sms : current_device_sms());
     *kernel = pl.kernel == Kernel::kDecode ? static_cast<int>(PKV_KERNEL_DECODE)
+            : pl.kernel == Kernel::kTile && pl.sk_ctas > 0 ? static_cast<int>(PKV_KERNEL_TILE_STREAM_K)
             : pl.kernel == Kernel::kTile   ? static_cast<int>(PKV_KERNEL_TILE)
             : pl.kernel == Kernel::kSimt   ? static_cast<int>(PKV_KERNEL_SIMT)
                                            : static_cast<int>(PKV_KERNEL_NONE);
@@ -400,6 +424,23 @@ pkv_status paged_attention(const void* q, int64_t q_token_stride, int64_t q_head
         p.ws_o = static_cast<float*>(workspace);
         p.ws_lse = reinterpret_cast<float*>(static_cast<char*>(workspace) +
                                             round_up(states * head_dim * sizeof(float), 256));
+    }
+    if (pl.kernel == Kernel::kTile && pl.sk_ctas > 0) {
+        // [unit offsets][fragment directory][fragment LSEs][fragment outputs]
+        char* w = static_cast<char*>(workspace);
+        p.sk_ctas = pl.sk_ctas;
+        p.sk_units = pl.sk_units;
+        p.sk_tiles_x = pl.sk_tiles_x;
+        p.sk_dp = pl.sk_units >= pl.sk_ctas ? pl.sk_ctas : 0;
+        p.sk_unit_off = reinterpret_cast<int*>(w);
+        w += round_up((static_cast<size_t>(pl.sk_units) + 1) * sizeof(int), 256);
+        p.sk_cta_off = reinterpret_cast<int*>(w);
+        w += round_up((static_cast<size_t>(pl.sk_ctas) + 1) * sizeof(int), 256);
+        p.sk_dir = reinterpret_cast<int4*>(w);
+        w += round_up(2 * static_cast<size_t>(pl.sk_ctas) * 16, 256);
+        p.sk_frag_lse = reinterpret_cast<float*>(w);
+        w += round_up(2 * static_cast<size_t>(pl.sk_ctas) * 2 * 128 * sizeof(float), 256);
+        p.sk_frag_o = reinterpret_cast<float*>(w);
     }
     if (pl.kernel == Kernel::kDecode) {
         char* w = static_cast<char*>(workspace);

@@ -156,6 +156,19 @@ struct AttnParams {
     bool planned;      // decode: units taken from the planned order (else split-major)
     bool checked;
     int32_t* err;
+    // two-tile kernel, stream-K schedule (sk_ctas > 0): one persistent CTA per
+    // SM, each taking a contiguous range of the units' key tiles (a unit = a
+    // tile pair of one sequence and K/V head); units split between CTAs leave
+    // partial states in per-CTA fragment slots that a reduce merges
+    int sk_ctas;          // persistent CTAs (the grid)
+    int sk_units;         // tile pairs x K/V heads x sequences
+    int sk_tiles_x;       // tile pairs per sequence
+    int sk_dp;            // the first sk_dp units run whole, unit c on CTA c (0 or sk_ctas)
+    int* sk_unit_off;     // [units - sk_dp + 1] weighted key-tile offsets of the shared units
+    int* sk_cta_off;      // [ctas + 1] each CTA's share of them (planner)
+    int4* sk_dir;         // [ctas][2] partial fragments: (unit, j0, j1, key tiles of the unit)
+    float* sk_frag_o;     // [ctas][2][256 rows][D] normalised partial outputs
+    float* sk_frag_lse;   // [ctas][2][256 rows] their LSEs (natural log)
     // decode kernel, PKV_FLAG_TEST_WAIT_TIMEOUT: consumers wait on a barrier
     // nothing completes (short limit) and the producer's ring waits are short
     bool test_wait_timeout;
@@ -199,5 +212,10 @@ int attn_tc_rows_per_tile(int group);  // query tokens per 128-row tile
 
 // n-way merge of split partials into out / lse.
 cudaError_t launch_split_reduce(const AttnParams& p, cudaStream_t s);
+
+// Stream-K schedule of the two-tile kernel: whether a call takes it, and the
+// workspace it needs (unit offsets, fragment directory, fragments).
+bool attn_tc_two_tile(int max_q_rows, int group);
+size_t attn_tc_sk_bytes(int units, int ctas, int head_dim);
 
 }  // namespace pkv

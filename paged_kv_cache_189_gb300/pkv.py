@@ -21,6 +21,8 @@ MASKS = {"none": 0, "causal": 1, "block_causal": 2}
 PKV_FLAG_CHECKED = 0x1
 PKV_FLAG_SIMT_ONLY = 0x2
 PKV_FLAG_TEST_WAIT_TIMEOUT = 0x4
+PKV_FLAG_TILE_GRID = 0x8
+PKV_FLAG_STREAM_K = 0x10
 PKV_ERRBIT_SLOT, PKV_ERRBIT_SRC, PKV_ERRBIT_PAGE, PKV_ERRBIT_LEN, PKV_ERRBIT_TIMEOUT = (
     0x1, 0x2, 0x4, 0x8, 0x10)
 
@@ -155,7 +157,7 @@ def paged_attention_workspace_size(batch, max_q_rows, num_q_heads, num_kv_heads,
                                                     head_dim, max_kv_len, num_splits, flags))
 
 
-PKV_KERNEL_NONE, PKV_KERNEL_DECODE, PKV_KERNEL_TILE, PKV_KERNEL_SIMT = range(4)
+PKV_KERNEL_NONE, PKV_KERNEL_DECODE, PKV_KERNEL_TILE, PKV_KERNEL_SIMT, PKV_KERNEL_TILE_STREAM_K = range(5)
 
 
 def plan_attention(batch, max_q_rows, num_q_heads, num_kv_heads, head_dim, max_kv_len,

@@ -180,12 +180,34 @@ def test_plan_follows_the_sm_count(L):
     # heads = 200 CTAs.  On 152 SMs two waves, so 3 key splits (4 waves of
     # thirds, 1.39 against 2 unsplit); on 200 SMs one wave, no split; on 100
     # SMs exactly two waves that no split count shortens by 10 %
-    p152 = pkv.plan_attention(1, 1576, 32, 8, 128, 39518, num_sms=152)
-    p200 = pkv.plan_attention(1, 1576, 32, 8, 128, 39518, num_sms=200)
-    p100 = pkv.plan_attention(1, 1576, 32, 8, 128, 39518, num_sms=100)
+    # (with the one-CTA-per-tile grid; by default the stream-K schedule)
+    grid = pkv.PKV_FLAG_TILE_GRID
+    p152 = pkv.plan_attention(1, 1576, 32, 8, 128, 39518, flags=grid, num_sms=152)
+    p200 = pkv.plan_attention(1, 1576, 32, 8, 128, 39518, flags=grid, num_sms=200)
+    p100 = pkv.plan_attention(1, 1576, 32, 8, 128, 39518, flags=grid, num_sms=100)
     assert p152["kernel"] == p200["kernel"] == pkv.PKV_KERNEL_TILE
     assert (p152["splits"], p200["splits"], p100["splits"]) == (3, 1, 1)
     assert p152["workspace_bytes"] > 0 and p200["workspace_bytes"] == 0
+    # stream-K only on request (one persistent CTA per SM, each with two
+    # fragment slots of 256 rows x 128 f32 + LSE): the video step's 280 tile
+    # pairs keep the grid by default
+    v152 = pkv.plan_attention(1, 1568, 40, 40, 128, 7800, num_sms=152)
+    assert v152["kernel"] == pkv.PKV_KERNEL_TILE and v152["splits"] == 1
+    vsk = pkv.plan_attention(1, 1568, 40, 40, 128, 7800, flags=pkv.PKV_FLAG_STREAM_K, num_sms=152)
+    assert vsk["kernel"] == pkv.PKV_KERNEL_TILE_STREAM_K
+    assert vsk["splits"] == 1 and vsk["split_keys"] >= 7800
+    # forced stream-K: the workspace follows the SM count
+    sk = pkv.PKV_FLAG_STREAM_K
+    s152 = pkv.plan_attention(1, 1576, 32, 8, 128, 39518, flags=sk, num_sms=152)
+    s120 = pkv.plan_attention(1, 1576, 32, 8, 128, 39518, flags=sk, num_sms=120)
+    assert s152["kernel"] == s120["kernel"] == pkv.PKV_KERNEL_TILE_STREAM_K
+    frag = 2 * 256 * (128 + 1) * 4
+    assert s152["workspace_bytes"] - s120["workspace_bytes"] >= 32 * frag
+    # by default the exact-window forward keeps its 3 key splits
+    assert pkv.plan_attention(1, 1576, 32, 8, 128, 39518, num_sms=152)["splits"] == 3
+    # an explicit split count keeps the one-CTA-per-tile grid
+    assert pkv.plan_attention(1, 1568, 40, 40, 128, 7800, num_splits=2,
+                              flags=pkv.PKV_FLAG_STREAM_K)["kernel"] == pkv.PKV_KERNEL_TILE
     # decode: ~6 work units per resident CTA (3 per SM): 8193 keys x 512
     # (sequence, head) pairs / (6 x 456) -> 1536 keys per split on 152 SMs,
     # 3072 on 76
@@ -198,6 +220,7 @@ def test_plan_follows_the_sm_count(L):
     # workspace_size plans for the current device (here: none -> 152 SMs)
     assert pkv.paged_attention_workspace_size(64, 1, 32, 8, 128, 8193) == d152["workspace_bytes"]
     assert pkv.paged_attention_workspace_size(1, 1576, 32, 8, 128, 39518) == p152["workspace_bytes"]
+    assert pkv.paged_attention_workspace_size(1, 1568, 40, 40, 128, 7800) == v152["workspace_bytes"]
     # bad arguments are refused on the host
     with pytest.raises(pkv.PkvError):
         pkv.plan_attention(4, 1, 30, 8, 128, 100)
