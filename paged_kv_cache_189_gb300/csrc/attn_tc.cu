@@ -39,27 +39,41 @@
 namespace pkv {
 namespace {
 
-constexpr int kD = 128;                 // head dim handled here
 constexpr int kTileM = 128;             // query rows per tile (tensor-memory lanes)
 constexpr int kTileN = 128;             // keys per tile
 constexpr int kKStages = 2;
 constexpr int kVStages = 3;
 constexpr int kThreads = 192;
 constexpr int kHalfBytes = kTileM * 128;           // 128 rows x 64 bf16 = 16 KiB
-constexpr int kTileBytes = 2 * kHalfBytes;         // 128 x 128 bf16 = 32 KiB
-constexpr int kQOff = 0;
-constexpr int kKOff = kQOff + kTileBytes;
-constexpr int kVOff = kKOff + kKStages * kTileBytes;
-constexpr int kPOff = kVOff + kVStages * kTileBytes;
-constexpr int kBarOff = kPOff + kTileBytes;
+constexpr int kPBytes = 2 * kHalfBytes;            // P: 128 rows x 128 keys bf16 = 32 KiB
+constexpr int kMaxGroup = 64;           // head groups the tiles take (2 tokens per pair at least)
+
+// Head-dim dependent sizes: a Q, K or V tile is 128 rows of D bf16, stored as
+// D / 64 column halves of 128-byte swizzled rows (one TMA box each).
+template <int D>
+struct TileDim {
+    static_assert(D == 64 || D == 128, "head dim 64 or 128");
+    static constexpr int kHalves = D / 64;
+    static constexpr int kChunks = D / 8;        // 16-byte chunks of a row
+    static constexpr int kTile = kHalves * kHalfBytes;
+    // one-tile kernel: Q, K ring, V ring, P, barriers, tensor-memory slot, flags, exchange
+    static constexpr int kQOff = 0;
+    static constexpr int kKOff = kQOff + kTile;
+    static constexpr int kVOff = kKOff + kKStages * kTile;
+    static constexpr int kPOff = kVOff + kVStages * kTile;
+    static constexpr int kBarOff = kPOff + kPBytes;
+};
 // barriers: q_ready, k_full[2], k_empty[2], v_full[3], v_empty[3], s_full[2], p_full, p_free
 constexpr int kNumBars = 1 + 2 * kKStages + 2 * kVStages + 2 + 2;
-constexpr int kTmemSlotOff = kBarOff + kNumBars * 8;
-constexpr int kFlagOff = kTmemSlotOff + 8;
-constexpr int kXchOff = kFlagOff + 16;            // replicated rows: [2][4][32] maxima, [2][4][32] sums
-constexpr int kSmemBytes = kXchOff + 2 * 2 * 4 * 32 * 4;
-static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
-constexpr uint32_t kTmemCols = 512;     // S0 [0,128), S1 [128,256), O [256,384)
+template <int D>
+struct OneTileSmem {
+    static constexpr int kTmemSlotOff = TileDim<D>::kBarOff + kNumBars * 8;
+    static constexpr int kFlagOff = kTmemSlotOff + 8;
+    static constexpr int kXchOff = kFlagOff + 16;   // replicated rows: [2][4][32] maxima, [2][4][32] sums
+    static constexpr int kBytes = kXchOff + 2 * 2 * 4 * 32 * 4;
+    static_assert(kBytes <= 227 * 1024, "shared memory per CTA");
+};
+constexpr uint32_t kTmemCols = 512;     // S0 [0,128), S1 [128,256), O [256,256 + D)
 constexpr float kLazyRescale = 8.0f;    // move the running max only past 2^8 growth
 constexpr int kOrderMaxBatch = 128;     // longest-first dispatch up to this batch (B^2 ranking)
 
@@ -248,6 +262,7 @@ __device__ __forceinline__ TileGeom tile_geometry(const AttnParams& p, int TQ, i
 }
 
 // Columns [32c, 32c + 32) of one row's normalised output (or split partial).
+template <int D>
 __device__ __forceinline__ void store_row_chunk(const AttnParams& p, const TileGeom& g, int row_in_seq,
                                                 int h, int c, const uint32_t (&v)[32], float inv_l) {
     const int64_t st = static_cast<int64_t>(g.r0 + row_in_seq) * p.num_q_heads + h;
@@ -255,7 +270,7 @@ __device__ __forceinline__ void store_row_chunk(const AttnParams& p, const TileG
 #pragma unroll
     for (int e = 0; e < 32; ++e) o[e] = __uint_as_float(v[e]) * inv_l;
     if (p.num_splits == 1 && !p.out_f32) {
-        uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + st * kD + c * 32);
+        uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + st * D + c * 32);
 #pragma unroll
         for (int q = 0; q < 4; ++q)
             dst[q] = make_uint4(pack_bf16x2(o[8 * q], o[8 * q + 1]), pack_bf16x2(o[8 * q + 2], o[8 * q + 3]),
@@ -264,10 +279,10 @@ __device__ __forceinline__ void store_row_chunk(const AttnParams& p, const TileG
     }
     float* base;
     if (p.num_splits == 1) {
-        base = static_cast<float*>(p.out) + st * kD;
+        base = static_cast<float*>(p.out) + st * D;
     } else {
         if (g.r0 + row_in_seq >= static_cast<int64_t>(p.batch) * p.max_q_rows) return;
-        base = p.ws_o + (st * p.num_splits + g.split) * kD;
+        base = p.ws_o + (st * p.num_splits + g.split) * D;
     }
     float4* dst = reinterpret_cast<float4*>(base + c * 32);
 #pragma unroll
@@ -338,12 +353,15 @@ __device__ __forceinline__ TileGeom group_geometry(const AttnParams& p, int TQ, 
     return g;
 }
 
-template <int G, bool GRP, int REP>
+template <int D, bool GRP, int REP>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                    const AttnParams p) {
+    using TD = TileDim<D>;
+    using SM = OneTileSmem<D>;
     constexpr int ND = kTileM / REP;  // distinct rows of the tile (each held REP times)
-    constexpr int TQ = ND / G;
+    const int G = p.num_q_heads / p.num_kv_heads;
+    const int TQ = ND / G;            // tokens of the tile; rows from TQ * G on hold none
     extern __shared__ __align__(1024) uint8_t smem[];
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -352,7 +370,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int grp_first = 0, grp_count = 0;
     if constexpr (!GRP) {
         int b = blockIdx.z / p.num_splits;
-        if (p.order_by_keys) b = longest_first(p, b, reinterpret_cast<int*>(smem + kKOff));
+        if (p.order_by_keys) b = longest_first(p, b, reinterpret_cast<int*>(smem + TD::kKOff));
         g = tile_geometry(p, TQ, b);
         if (g.t0 >= g.nrows) return;  // tile past this sequence's rows (uniform)
     } else {
@@ -360,10 +378,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (g.t0 >= g.nrows) return;  // empty group slot, or tile past the group's tokens
         // the keys the tile's rows see end at the largest of their visible ends
         // (reduced in the flag area of shared memory, initialised further down)
-        int* s_keyhi = reinterpret_cast<int*>(smem + kFlagOff + 8);
+        int* s_keyhi = reinterpret_cast<int*>(smem + SM::kFlagOff + 8);
         if (threadIdx.x == 0) *s_keyhi = 0;
         __syncthreads();
-        if (threadIdx.x < ND) {
+        if (threadIdx.x < TQ * G) {
             const GroupRow gr = group_row(p, g.b, grp_first, grp_count, g.t0 + threadIdx.x / G);
             if (gr.tok >= 0) atomicMax(s_keyhi, max(gr.a, gr.c));
         }
@@ -375,7 +393,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (g.nt == 0) {
         // no visible key in this split for any row of the tile: empty states
-        if (threadIdx.x < ND) {
+        if (threadIdx.x < TQ * G) {
             const int r = threadIdx.x;
             int i = g.t0 + r / G;
             bool exists = i < g.nrows;
@@ -389,7 +407,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int e = 0; e < 32; ++e) zero[e] = 0u;
 #pragma unroll
-                for (int c = 0; c < 4; ++c) store_row_chunk(p, g, i, g.kvh * G + r % G, c, zero, 0.f);
+                for (int c = 0; c < D / 32; ++c) store_row_chunk<D>(p, g, i, g.kvh * G + r % G, c, zero, 0.f);
                 store_row_lse(p, g, i, g.kvh * G + r % G, -INFINITY);
             }
         }
@@ -400,7 +418,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         return;
     }
 
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kBarOff);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + TD::kBarOff);
     uint64_t* q_ready = bars;
     uint64_t* k_full = bars + 1;
     uint64_t* k_empty = k_full + kKStages;
@@ -409,8 +427,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* s_full = v_empty + kVStages;
     uint64_t* p_full = s_full + 2;
     uint64_t* p_free = p_full + 1;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kTmemSlotOff);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kFlagOff);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + SM::kTmemSlotOff);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + SM::kFlagOff);
 
     if (threadIdx.x == 0) {
         mbar_init(q_ready, kTileM);
@@ -457,7 +475,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int last_page = (g.kv_len + 31) / 32;  // pages at or past it are never read
             int k_issued = 0, v_issued = 0;
             auto load_tile = [&](const CUtensorMap* tm, uint8_t* dst, uint64_t* bar, int j) {
-                mbar_arrive_expect_tx(bar, kTileBytes);
+                mbar_arrive_expect_tx(bar, TD::kTile);
 #pragma unroll
                 for (int pg = 0; pg < 4; ++pg) {
                     const int lp = (g.kb + j * kTileN) / 32 + pg;
@@ -467,7 +485,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         phys = static_cast<int>(p.num_pages);
                     }
 #pragma unroll
-                    for (int h = 0; h < 2; ++h)
+                    for (int h = 0; h < TD::kHalves; ++h)
                         tma_load_4d(dst + h * kHalfBytes + pg * 4096, tm, bar, h * 64, g.kvh, 0, phys);
                 }
             };
@@ -477,14 +495,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (k_issued < g.nt && k_issued < v_issued + kKStages) {
                     const int s = k_issued % kKStages;
                     if (k_issued >= kKStages && !wait(&k_empty[s], ((k_issued / kKStages) - 1) & 1)) break;
-                    load_tile(&tm_k, smem + kKOff + s * kTileBytes, &k_full[s], k_issued);
+                    load_tile(&tm_k, smem + TD::kKOff + s * TD::kTile, &k_full[s], k_issued);
                     ++k_issued;
                     progressed = true;
                 }
                 if (v_issued < g.nt && v_issued < k_issued) {
                     const int s = v_issued % kVStages;
                     if (v_issued >= kVStages && !wait(&v_empty[s], ((v_issued / kVStages) - 1) & 1)) break;
-                    load_tile(&tm_v, smem + kVOff + s * kTileBytes, &v_full[s], v_issued);
+                    load_tile(&tm_v, smem + TD::kVOff + s * TD::kTile, &v_full[s], v_issued);
                     ++v_issued;
                     progressed = true;
                 }
@@ -501,15 +519,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ============================== MMA ================================
         if (lane == 0) {
             constexpr uint32_t kIdescS = idesc_bf16(kTileM, kTileN, false);  // K rows are K-major
-            constexpr uint32_t kIdescO = idesc_bf16(kTileM, kD, true);       // V rows are MN-major
+            constexpr uint32_t kIdescO = idesc_bf16(kTileM, D, true);        // V rows are MN-major
             const uint32_t tmem_o = tmem + 256;
             auto issue_s = [&](int j) -> bool {
                 const int s = j % kKStages;
                 if (!wait(&k_full[s], (j / kKStages) & 1)) return false;
                 tc_fence_after();
-                const uint32_t qa = sbase + kQOff, kbse = sbase + kKOff + s * kTileBytes;
+                const uint32_t qa = sbase + TD::kQOff, kbse = sbase + TD::kKOff + s * TD::kTile;
 #pragma unroll
-                for (int kk = 0; kk < kD / 16; ++kk) {
+                for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
                     umma_bf16(tmem + (j & 1) * 128, sdesc_sw128(qa + off, 16, 1024),
                               sdesc_sw128(kbse + off, 16, 1024), kIdescS, kk > 0);
@@ -524,8 +542,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int j = 0; ok && j < g.nt; ++j) {
                 if (!wait(p_full, j & 1) || !wait(&v_full[j % kVStages], (j / kVStages) & 1)) break;
                 tc_fence_after();
-                const uint32_t pa = sbase + kPOff;
-                const uint32_t vb = sbase + kVOff + (j % kVStages) * kTileBytes;
+                const uint32_t pa = sbase + TD::kPOff;
+                const uint32_t vb = sbase + TD::kVOff + (j % kVStages) * TD::kTile;
 #pragma unroll
                 for (int kk = 0; kk < kTileN / 16; ++kk) {
                     // A = P (K-major over keys), B = V (rows = keys, columns = dims: MN-major);
@@ -546,13 +564,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int t = r / G, hg = r % G;
             const int h = g.kvh * G + hg;
             int i = g.t0 + t;                      // query row within the sequence (grouped: token)
-            bool row_exists = i < g.nrows;
+            bool row_exists = t < TQ && i < g.nrows;
             int limit = 0;
             int vis_a = 0, vis_b = 0, vis_c = 0;   // grouped: visible keys [0, a) u [b, c)
             if constexpr (GRP) {
                 const GroupRow gr = group_row(p, g.b, grp_first, grp_count, i);
                 i = gr.tok;
-                row_exists = gr.tok >= 0;
+                row_exists = t < TQ && gr.tok >= 0;
                 vis_a = gr.a;
                 vis_b = gr.b;
                 vis_c = gr.c;
@@ -565,9 +583,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     static_cast<const __nv_bfloat16*>(p.q) + static_cast<int64_t>(g.r0 + i) * p.q_token_stride +
                     static_cast<int64_t>(h) * p.q_head_stride);
     #pragma unroll
-                for (int c = 0; c < 16; ++c) {
+                for (int c = 0; c < TD::kChunks; ++c) {
                     const uint4 v = row_exists ? src[c] : make_uint4(0u, 0u, 0u, 0u);
-                    *reinterpret_cast<uint4*>(smem + kQOff + (c >> 3) * kHalfBytes +
+                    *reinterpret_cast<uint4*>(smem + TD::kQOff + (c >> 3) * kHalfBytes +
                                               sw128_offset(r, c & 7)) = v;
                 }
                 fence_proxy_async_smem();
@@ -576,7 +594,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t lane_addr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
             float m_used = -INFINITY;   // base-2 running maximum used for the exponentials
             float l = 0.f, l_b = 0.f;
-            uint8_t* prow = smem + kPOff;
+            uint8_t* prow = smem + TD::kPOff;
             // warp-collective tensor-memory accesses follow every wait, so a wait
             // counts as passed only if it passed in every lane of the warp
             auto wait_warp = [&](uint64_t* bar, uint32_t parity) -> bool {
@@ -657,7 +675,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (live && j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
                     // O *= alpha for this row (warp-collective tensor-memory access)
     #pragma unroll
-                    for (int c = 0; c < 4; ++c) {
+                    for (int c = 0; c < D / 32; ++c) {
                         uint32_t v[32];
                         tmem_load32(lane_addr + 256 + c * 32, v);
     #pragma unroll
@@ -683,9 +701,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (!wait_warp(&v_full[vs], (j / kVStages) & 1)) break;
                     const int first = g.kv_len - key0;
                     const int last = min(kTileN, (first + 31) / 32 * 32);
-                    uint8_t* vt = smem + kVOff + vs * kTileBytes;
-                    for (int idx = r; idx < (last - first) * 16; idx += kTileM) {
-                        const int row = first + idx / 16, c = idx % 16;
+                    uint8_t* vt = smem + TD::kVOff + vs * TD::kTile;
+                    for (int idx = r; idx < (last - first) * TD::kChunks; idx += kTileM) {
+                        const int row = first + idx / TD::kChunks, c = idx % TD::kChunks;
                         *reinterpret_cast<uint4*>(vt + (c >> 3) * kHalfBytes + sw128_offset(row, c & 7)) =
                             make_uint4(0u, 0u, 0u, 0u);
                     }
@@ -703,13 +721,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (any_gap) {
                         const int vs = j % kVStages;
                         if (!wait_warp(&v_full[vs], (j / kVStages) & 1)) break;
-                        uint8_t* vt = smem + kVOff + vs * kTileBytes;
+                        uint8_t* vt = smem + TD::kVOff + vs * TD::kTile;
                         for (int k = 0; k < grp_count; ++k) {
                             const int m = p.grp_perm[grp_first + k];
                             const int g0 = 32 * p.grp_tail_start[m] + p.grp_tail_lens[m];
                             const int lo = max(g0, key0) - key0, hi = min((g0 + 31) / 32 * 32, key0 + kTileN) - key0;
-                            for (int idx = r; idx < (hi - lo) * 16; idx += kTileM) {
-                                const int row = lo + idx / 16, c = idx % 16;
+                            for (int idx = r; idx < (hi - lo) * TD::kChunks; idx += kTileM) {
+                                const int row = lo + idx / TD::kChunks, c = idx % TD::kChunks;
                                 *reinterpret_cast<uint4*>(vt + (c >> 3) * kHalfBytes + sw128_offset(row, c & 7)) =
                                     make_uint4(0u, 0u, 0u, 0u);
                             }
@@ -726,10 +744,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool any = l > 0.f && l_b > 0.f;
             const float inv_l = any ? 1.0f / l_b : 0.f;
     #pragma unroll
-            for (int c = 0; c < 4; ++c) {
+            for (int c = 0; c < D / 32; ++c) {
                 uint32_t v[32];
                 tmem_load32(lane_addr + 256 + c * 32, v);
-                if (ok && row_exists) store_row_chunk(p, g, i, h, c, v, inv_l);
+                if (ok && row_exists) store_row_chunk<D>(p, g, i, h, c, v, inv_l);
             }
             if (ok && row_exists) store_row_lse(p, g, i, h, any ? (m_used + __log2f(l)) * kLn2 : -INFINITY);
         } else {
@@ -745,13 +763,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int t = dr / G, hg = dr % G;
             const int h = g.kvh * G + hg;
             int i = g.t0 + t;                      // query row within the sequence (grouped: token)
-            bool row_exists = i < g.nrows;
+            bool row_exists = t < TQ && i < g.nrows;
             int limit = 0;
             int vis_a = 0, vis_b = 0, vis_c = 0;   // grouped: visible keys [0, a) u [b, c)
             if constexpr (GRP) {
                 const GroupRow gr = group_row(p, g.b, grp_first, grp_count, i);
                 i = gr.tok;
-                row_exists = gr.tok >= 0;
+                row_exists = t < TQ && gr.tok >= 0;
                 vis_a = gr.a;
                 vis_b = gr.b;
                 vis_c = gr.c;
@@ -764,9 +782,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     static_cast<const __nv_bfloat16*>(p.q) + static_cast<int64_t>(g.r0 + i) * p.q_token_stride +
                     static_cast<int64_t>(h) * p.q_head_stride);
     #pragma unroll
-                for (int c = 0; c < 16; ++c) {
+                for (int c = 0; c < TD::kChunks; ++c) {
                     const uint4 v = row_exists ? src[c] : make_uint4(0u, 0u, 0u, 0u);
-                    *reinterpret_cast<uint4*>(smem + kQOff + (c >> 3) * kHalfBytes +
+                    *reinterpret_cast<uint4*>(smem + TD::kQOff + (c >> 3) * kHalfBytes +
                                               sw128_offset(r, c & 7)) = v;
                 }
                 fence_proxy_async_smem();
@@ -775,8 +793,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t lane_addr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
             float m_used = -INFINITY;   // base-2 running maximum used for the exponentials
             float l = 0.f, l_b = 0.f;
-            uint8_t* prow = smem + kPOff;
-            float* xmax = reinterpret_cast<float*>(smem + kXchOff);  // [key tile parity][part][dr]
+            uint8_t* prow = smem + TD::kPOff;
+            float* xmax = reinterpret_cast<float*>(smem + SM::kXchOff);  // [key tile parity][part][dr]
             float* xsum = xmax + 2 * 4 * 32;                          // [l, l_b][part][dr]
             // warp-collective tensor-memory accesses follow every wait, so a wait
             // counts as passed only if it passed in every lane of the warp
@@ -884,7 +902,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (live && j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
                         // O *= alpha for this row (warp-collective tensor-memory access)
     #pragma unroll
-                        for (int c = 0; c < 4; ++c) {
+                        for (int c = 0; c < D / 32; ++c) {
                             uint32_t v[32];
                             tmem_load32(lane_addr + 256 + c * 32, v);
     #pragma unroll
@@ -922,9 +940,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (ok_run) {
                             const int first = g.kv_len - key0;
                             const int last = min(kTileN, (first + 31) / 32 * 32);
-                            uint8_t* vt = smem + kVOff + vs * kTileBytes;
-                            for (int idx = r; idx < (last - first) * 16; idx += kTileM) {
-                                const int row = first + idx / 16, c = idx % 16;
+                            uint8_t* vt = smem + TD::kVOff + vs * TD::kTile;
+                            for (int idx = r; idx < (last - first) * TD::kChunks; idx += kTileM) {
+                                const int row = first + idx / TD::kChunks, c = idx % TD::kChunks;
                                 *reinterpret_cast<uint4*>(vt + (c >> 3) * kHalfBytes + sw128_offset(row, c & 7)) =
                                     make_uint4(0u, 0u, 0u, 0u);
                             }
@@ -944,13 +962,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                             const int vs = j % kVStages;
                             ok_run = ok_run && wait_warp(&v_full[vs], (j / kVStages) & 1);
                             if (REP == 1 && !ok_run) break;
-                            uint8_t* vt = smem + kVOff + vs * kTileBytes;
+                            uint8_t* vt = smem + TD::kVOff + vs * TD::kTile;
                             for (int k = 0; ok_run && k < grp_count; ++k) {
                                 const int m = p.grp_perm[grp_first + k];
                                 const int g0 = 32 * p.grp_tail_start[m] + p.grp_tail_lens[m];
                                 const int lo = max(g0, key0) - key0, hi = min((g0 + 31) / 32 * 32, key0 + kTileN) - key0;
-                                for (int idx = r; idx < (hi - lo) * 16; idx += kTileM) {
-                                    const int row = lo + idx / 16, c = idx % 16;
+                                for (int idx = r; idx < (hi - lo) * TD::kChunks; idx += kTileM) {
+                                    const int row = lo + idx / TD::kChunks, c = idx % TD::kChunks;
                                     *reinterpret_cast<uint4*>(vt + (c >> 3) * kHalfBytes + sw128_offset(row, c & 7)) =
                                         make_uint4(0u, 0u, 0u, 0u);
                                 }
@@ -969,10 +987,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const bool any = l > 0.f && l_b > 0.f;
                 const float inv_l = any ? 1.0f / l_b : 0.f;
     #pragma unroll
-                for (int c = 0; c < 4; ++c) {
+                for (int c = 0; c < D / 32; ++c) {
                     uint32_t v[32];
                     tmem_load32(lane_addr + 256 + c * 32, v);
-                    if (ok && row_exists) store_row_chunk(p, g, i, h, c, v, inv_l);
+                    if (ok && row_exists) store_row_chunk<D>(p, g, i, h, c, v, inv_l);
                 }
                 if (ok && row_exists) store_row_lse(p, g, i, h, any ? (m_used + __log2f(l)) * kLn2 : -INFINITY);
             } else {
@@ -980,17 +998,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // through the K ring (drained: every K tile was consumed by an S that
                 // finished before the last P.V); float4 q of a row sits at slot
                 // (q + dr) mod 32 so that a warp's stores spread over the banks
-                float4* obuf = reinterpret_cast<float4*>(smem + kKOff);
+                float4* obuf = reinterpret_cast<float4*>(smem + TD::kKOff);
+                constexpr int kRowF4 = D / 4;  // float4 of an O row
                 xsum[(0 * REP + part) * ND + dr] = l;
                 xsum[(1 * REP + part) * ND + dr] = l_b;
     #pragma unroll
-                for (int c = 0; c < 4; ++c) {
+                for (int c = 0; c < D / 32; ++c) {
                     uint32_t v[32];
                     tmem_load32(lane_addr + 256 + c * 32, v);
     #pragma unroll
                     for (int k = 0; k < 8; ++k) {
                         const int q = c * 8 + k;
-                        obuf[(part * ND + dr) * 32 + ((q + dr) & 31)] =
+                        obuf[(part * ND + dr) * kRowF4 + ((q + dr) & (kRowF4 - 1))] =
                             make_float4(__uint_as_float(v[4 * k]), __uint_as_float(v[4 * k + 1]),
                                         __uint_as_float(v[4 * k + 2]), __uint_as_float(v[4 * k + 3]));
                     }
@@ -1004,17 +1023,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 const bool any = lt > 0.f && lbt > 0.f;
                 const float inv_l = any ? 1.0f / lbt : 0.f;
-                // this lane adds up the copies' columns [part * CW, part * CW + CW) of its row
-    #pragma unroll
-                for (int cc = 0; cc < CW / 32; ++cc) {
+                // this lane adds up the copies' 32-column output chunks part,
+                // part + REP, ... of its row
+                for (int cc = part; cc < D / 32; cc += REP) {
                     uint32_t v[32];
     #pragma unroll
                     for (int k = 0; k < 8; ++k) {
-                        const int q = (part * CW / 32 + cc) * 8 + k;
+                        const int q = cc * 8 + k;
                         float4 a4 = make_float4(0.f, 0.f, 0.f, 0.f);
     #pragma unroll
                         for (int c2 = 0; c2 < REP; ++c2) {
-                            const float4 b4 = obuf[(c2 * ND + dr) * 32 + ((q + dr) & 31)];
+                            const float4 b4 = obuf[(c2 * ND + dr) * kRowF4 + ((q + dr) & (kRowF4 - 1))];
                             a4.x += b4.x;
                             a4.y += b4.y;
                             a4.z += b4.z;
@@ -1025,7 +1044,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         v[4 * k + 2] = __float_as_uint(a4.z);
                         v[4 * k + 3] = __float_as_uint(a4.w);
                     }
-                    if (ok && row_exists) store_row_chunk(p, g, i, h, part * (CW / 32) + cc, v, inv_l);
+                    if (ok && row_exists) store_row_chunk<D>(p, g, i, h, cc, v, inv_l);
                 }
                 if (ok && row_exists && part == 0)
                     store_row_lse(p, g, i, h, any ? (m_used + __log2f(lt)) * kLn2 : -INFINITY);
@@ -1039,10 +1058,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 5) tmem_dealloc(tmem, kTmemCols);
 }
 
-constexpr int kQ2Off = 0;                                   // Q_A, Q_B
-constexpr int kK2Off = kQ2Off + 2 * kTileBytes;
-constexpr int kV2Off = kK2Off + kKStages * kTileBytes;
-constexpr int kBar2Off = kV2Off + kVStages * kTileBytes;
 // barriers: q_ready, k_full[2], k_empty[2], v_full[3], v_empty[3], s_full[2], p_full[2], o_full[2]
 constexpr int kNumBars2 = 1 + 2 * kKStages + 2 * kVStages + 6;
 
@@ -1092,11 +1107,19 @@ __device__ __forceinline__ void umma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, u
 // so the two leave the key loop together.
 // ===========================================================================
 constexpr int kThreads2 = 576;
-constexpr int kXch2Off = kBar2Off + kNumBars2 * 8;            // float [2 tiles][2 halves][128 rows]
-constexpr int kTmemSlot2Off = kXch2Off + 2 * 2 * kTileM * 4;
-constexpr int kFlag2Off = kTmemSlot2Off + 8;
-constexpr int kSmemBytes2 = kFlag2Off + 16;
-static_assert(kSmemBytes2 <= 227 * 1024, "shared memory per CTA");
+template <int D>
+struct TwoTileSmem {
+    static constexpr int kTile = TileDim<D>::kTile;
+    static constexpr int kQOff = 0;                          // Q_A, Q_B
+    static constexpr int kKOff = kQOff + 2 * kTile;
+    static constexpr int kVOff = kKOff + kKStages * kTile;
+    static constexpr int kBarOff = kVOff + kVStages * kTile;
+    static constexpr int kXchOff = kBarOff + kNumBars2 * 8;  // float [2 tiles][2 halves][128 rows]
+    static constexpr int kTmemSlotOff = kXchOff + 2 * 2 * kTileM * 4;
+    static constexpr int kFlagOff = kTmemSlotOff + 8;
+    static constexpr int kBytes = kFlagOff + 16;
+    static_assert(kBytes <= 227 * 1024, "shared memory per CTA");
+};
 
 
 // ---------------------------------------------------------------------------
@@ -1230,26 +1253,28 @@ struct SegIter {
 
 // Zero output and LSE = -inf for the existing rows of a pair whose rows see no
 // key.  Threads 0 .. 2 * kTileM - 1 each take one row.
-template <int G>
-__device__ __forceinline__ void zero_pair_rows(const AttnParams& p, const TileGeom& g) {
-    constexpr int TQ = kTileM / G;
+template <int D>
+__device__ __forceinline__ void zero_pair_rows(const AttnParams& p, const TileGeom& g, int G, int TQ) {
     if (threadIdx.x >= 2 * kTileM) return;
     const int x = threadIdx.x / kTileM, r = threadIdx.x % kTileM;
     const int i = g.t0 + x * TQ + r / G;
-    if (i >= g.nrows) return;
+    if (r / G >= TQ || i >= g.nrows) return;
     uint32_t zero[32];
 #pragma unroll
     for (int e = 0; e < 32; ++e) zero[e] = 0u;
 #pragma unroll
-    for (int c = 0; c < 4; ++c) store_row_chunk(p, g, i, g.kvh * G + r % G, c, zero, 0.f);
+    for (int c = 0; c < D / 32; ++c) store_row_chunk<D>(p, g, i, g.kvh * G + r % G, c, zero, 0.f);
     store_row_lse(p, g, i, g.kvh * G + r % G, -INFINITY);
 }
 
-template <int G, bool SK>
+template <int D, bool SK>
 __global__ void __maxnreg__(96)
     attn_tc2_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                     const AttnParams p) {
-    constexpr int TQ = kTileM / G;
+    using TD = TileDim<D>;
+    using SM = TwoTileSmem<D>;
+    const int G = p.num_q_heads / p.num_kv_heads;
+    const int TQ = kTileM / G;  // tokens per tile; rows from TQ * G on hold none
     extern __shared__ __align__(1024) uint8_t smem[];
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -1264,7 +1289,7 @@ __global__ void __maxnreg__(96)
         // pairs with rows but no visible key: zero rows (units u = CTA mod grid)
         for (int u = blockIdx.x; u < p.sk_units; u += p.sk_ctas) {
             const TileGeom g = sk_unit(p, TQ, u);
-            if (g.t0 < g.nrows && g.nt == 0) zero_pair_rows<G>(p, g);
+            if (g.t0 < g.nrows && g.nt == 0) zero_pair_rows<D>(p, g, G, TQ);
         }
         it0.init(p);
     } else {
@@ -1272,7 +1297,7 @@ __global__ void __maxnreg__(96)
                                          blockIdx.z % p.num_splits);
         if (g.t0 >= g.nrows) return;  // uniform
         if (g.nt == 0) {
-            zero_pair_rows<G>(p, g);
+            zero_pair_rows<D>(p, g, G, TQ);
             return;
         }
     }
@@ -1287,7 +1312,7 @@ __global__ void __maxnreg__(96)
         return;
     }
 
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kBar2Off);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + SM::kBarOff);
     uint64_t* q_ready = bars;
     uint64_t* k_full = bars + 1;
     uint64_t* k_empty = k_full + kKStages;
@@ -1296,9 +1321,9 @@ __global__ void __maxnreg__(96)
     uint64_t* s_full = v_empty + kVStages;  // [tile]
     uint64_t* p_full = s_full + 2;          // [tile]
     uint64_t* o_full = p_full + 2;          // [tile]
-    float* xch = reinterpret_cast<float*>(smem + kXch2Off);
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kTmemSlot2Off);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kFlag2Off);
+    float* xch = reinterpret_cast<float*>(smem + SM::kXchOff);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + SM::kTmemSlotOff);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + SM::kFlagOff);
 
     if (threadIdx.x == 0) {
         mbar_init(q_ready, 4 * kTileM);
@@ -1352,7 +1377,7 @@ __global__ void __maxnreg__(96)
                 const int32_t* bt = p.block_table + static_cast<int64_t>(g.b) * p.block_table_stride;
                 const int last_page = (g.kv_len + 31) / 32;
                 auto load_tile = [&](const CUtensorMap* tm, uint8_t* dst, uint64_t* bar, int j) {
-                    mbar_arrive_expect_tx(bar, kTileBytes);
+                    mbar_arrive_expect_tx(bar, TD::kTile);
 #pragma unroll
                     for (int pg = 0; pg < 4; ++pg) {
                         const int lp = (g.kb + j * kTileN) / 32 + pg;
@@ -1362,7 +1387,7 @@ __global__ void __maxnreg__(96)
                             phys = static_cast<int>(p.num_pages);
                         }
 #pragma unroll
-                        for (int h = 0; h < 2; ++h)
+                        for (int h = 0; h < TD::kHalves; ++h)
                             tma_load_4d(dst + h * kHalfBytes + pg * 4096, tm, bar, h * 64, g.kvh, 0, phys);
                     }
                 };
@@ -1372,14 +1397,14 @@ __global__ void __maxnreg__(96)
                         alive = false;
                         break;
                     }
-                    load_tile(&tm_k, smem + kK2Off + sk * kTileBytes, &k_full[sk], j);
+                    load_tile(&tm_k, smem + SM::kKOff + sk * TD::kTile, &k_full[sk], j);
                     ++kn;
                     const int sv = vn % kVStages;
                     if (vn >= kVStages && !wait(&v_empty[sv], ((vn / kVStages) - 1) & 1)) {
                         alive = false;
                         break;
                     }
-                    load_tile(&tm_v, smem + kV2Off + sv * kTileBytes, &v_full[sv], j);
+                    load_tile(&tm_v, smem + SM::kVOff + sv * TD::kTile, &v_full[sv], j);
                     ++vn;
                 }
             }
@@ -1393,12 +1418,12 @@ __global__ void __maxnreg__(96)
         // ============================== MMA ================================
         if (lane == 0) {
             constexpr uint32_t kIdescS = idesc_bf16(kTileM, kTileN, false);
-            constexpr uint32_t kIdescO = idesc_bf16(kTileM, kD, true);
+            constexpr uint32_t kIdescO = idesc_bf16(kTileM, D, true);
             auto issue_s = [&](int x, int gt) {
-                const uint32_t qa = sbase + kQ2Off + x * kTileBytes;
-                const uint32_t kbse = sbase + kK2Off + (gt % kKStages) * kTileBytes;
+                const uint32_t qa = sbase + SM::kQOff + x * TD::kTile;
+                const uint32_t kbse = sbase + SM::kKOff + (gt % kKStages) * TD::kTile;
 #pragma unroll
-                for (int kk = 0; kk < kD / 16; ++kk) {
+                for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
                     umma_bf16(tmem + x * 256, sdesc_sw128(qa + off, 16, 1024),
                               sdesc_sw128(kbse + off, 16, 1024), kIdescS, kk > 0);
@@ -1406,7 +1431,7 @@ __global__ void __maxnreg__(96)
                 umma_commit(&s_full[x]);
             };
             auto issue_pv = [&](int x, int gt, bool acc) {
-                const uint32_t vb = sbase + kV2Off + (gt % kVStages) * kTileBytes;
+                const uint32_t vb = sbase + SM::kVOff + (gt % kVStages) * TD::kTile;
 #pragma unroll
                 for (int kk = 0; kk < kTileN / 16; ++kk) {
                     // A = P in tensor memory: keys [0,64) packed in columns [0,32),
@@ -1481,7 +1506,8 @@ __global__ void __maxnreg__(96)
         const int bar_id = 1 + x * 4 + (warp & 3);  // the two warps of this lane quadrant
         const uint32_t lane_addr = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16) + x * 256;
         const uint32_t s_addr = lane_addr + hf * 64;        // this half's S columns
-        const uint32_t o_addr = lane_addr + 128 + hf * 64;  // this half's O columns
+        constexpr int OH = D / 2;                            // O columns of each half
+        const uint32_t o_addr = lane_addr + 128 + hf * OH;  // this half's O columns
         float* xmine = xch + (x * 2 + hf) * kTileM + r;
         const float* xother = xch + (x * 2 + (hf ^ 1)) * kTileM + r;
         float* xl = xch + x * 2 * kTileM + r;  // [tile][0: l, 1: l_b][row]
@@ -1498,7 +1524,7 @@ __global__ void __maxnreg__(96)
             const TileGeom& g = sg.g;
             const int i = g.t0 + x * TQ + t;
             const int h = g.kvh * G + hg;
-            const bool row_exists = i < g.nrows;
+            const bool row_exists = t < TQ && i < g.nrows;
             const int limit = row_exists ? visible_keys(i, g.qreal, g.kv_len, p.mask, max(p.causal_block, 1))
                                          : 0;
             {
@@ -1506,14 +1532,16 @@ __global__ void __maxnreg__(96)
                 // segment's S MMAs have finished reading this Q tile (their S was
                 // consumed), and its O was read before this arrive, ahead of the
                 // segment's first P.V
+                constexpr int QC = TD::kChunks / 2;  // 16-byte chunks of the row per half-warp
                 const uint4* src = reinterpret_cast<const uint4*>(
                     static_cast<const __nv_bfloat16*>(p.q) + static_cast<int64_t>(g.r0 + i) * p.q_token_stride +
-                    static_cast<int64_t>(h) * p.q_head_stride) + hf * 8;
-                uint8_t* qt = smem + kQ2Off + x * kTileBytes + hf * kHalfBytes;
+                    static_cast<int64_t>(h) * p.q_head_stride) + hf * QC;
+                uint8_t* qt = smem + SM::kQOff + x * TD::kTile;
 #pragma unroll
-                for (int c = 0; c < 8; ++c) {
+                for (int c = 0; c < QC; ++c) {
+                    const int gc = hf * QC + c;
                     const uint4 v = row_exists ? src[c] : make_uint4(0u, 0u, 0u, 0u);
-                    *reinterpret_cast<uint4*>(qt + sw128_offset(r, c)) = v;
+                    *reinterpret_cast<uint4*>(qt + (gc >> 3) * kHalfBytes + sw128_offset(r, gc & 7)) = v;
                 }
                 fence_proxy_async_smem();
                 tc_fence_before();
@@ -1574,10 +1602,10 @@ __global__ void __maxnreg__(96)
                         alpha = fast_exp2(m_used - mx);
                         m_used = mx;
                     }
-                    // O *= alpha on this half's 64 columns
+                    // O *= alpha on this half's columns
                     if (j > sg.j0 && __any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll
-                        for (int c = 0; c < 2; ++c) {
+                        for (int c = 0; c < OH / 32; ++c) {
                             uint32_t v[32];
                             tmem_load32(o_addr + c * 32, v);
 #pragma unroll
@@ -1637,9 +1665,9 @@ __global__ void __maxnreg__(96)
                     if (ok_t) {
                         const int first = g.kv_len - key0;
                         const int lastr = min(kTileN, (first + 31) / 32 * 32);
-                        uint8_t* vt = smem + kV2Off + vs * kTileBytes;
-                        for (int idx = hf * kTileM + r; idx < (lastr - first) * 16; idx += 2 * kTileM) {
-                            const int row = first + idx / 16, c16 = idx % 16;
+                        uint8_t* vt = smem + SM::kVOff + vs * TD::kTile;
+                        for (int idx = hf * kTileM + r; idx < (lastr - first) * TD::kChunks; idx += 2 * kTileM) {
+                            const int row = first + idx / TD::kChunks, c16 = idx % TD::kChunks;
                             *reinterpret_cast<uint4*>(vt + (c16 >> 3) * kHalfBytes + sw128_offset(row, c16 & 7)) =
                                 make_uint4(0u, 0u, 0u, 0u);
                         }
@@ -1680,16 +1708,16 @@ __global__ void __maxnreg__(96)
             bar_sync_n(bar_id, 2 * 32);
             if (hf == 1) inv_l = xl[0];
 #pragma unroll
-            for (int c = 0; c < 2; ++c) {
+            for (int c = 0; c < OH / 32; ++c) {
                 uint32_t v[32];
                 tmem_load32(o_addr + c * 32, v);
                 if (ok_o && row_exists) {
                     if (whole) {
-                        store_row_chunk(p, g, i, h, hf * 2 + c, v, inv_l);
+                        store_row_chunk<D>(p, g, i, h, hf * (OH / 32) + c, v, inv_l);
                     } else {
                         float4* dst = reinterpret_cast<float4*>(
-                            p.sk_frag_o + (static_cast<int64_t>(fslot) * kSkFragRows + x * kTileM + r) * kD +
-                            (hf * 2 + c) * 32);
+                            p.sk_frag_o + (static_cast<int64_t>(fslot) * kSkFragRows + x * kTileM + r) * D +
+                            (hf * (OH / 32) + c) * 32);
 #pragma unroll
                         for (int q = 0; q < 8; ++q)
                             dst[q] = make_float4(__uint_as_float(v[4 * q]) * inv_l, __uint_as_float(v[4 * q + 1]) * inv_l,
@@ -1745,9 +1773,8 @@ __device__ __forceinline__ int block_exclusive_sum(int v, int* warp_tot, int* to
 // the shared units and every CTA's share of them.  A CTA's share is what
 // brings its work (its whole first-wave unit plus the share) to the average;
 // shares are scaled to add up to the shared units' total.
-template <int G>
 __global__ void __launch_bounds__(1024) tc2_sk_plan_kernel(const AttnParams p) {
-    constexpr int TQ = kTileM / G;
+    const int TQ = kTileM / (p.num_q_heads / p.num_kv_heads);
     // the persistent launch may start its prologue now; it waits for this
     // grid's completion before it reads the offsets
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -1796,9 +1823,10 @@ __global__ void __launch_bounds__(1024) tc2_sk_plan_kernel(const AttnParams p) {
 // slot, group of 8 fragment rows); one warp per row, every load of a row in
 // flight at once.
 constexpr int kSkReduceRows = 8;
-template <int G>
+template <int D>
 __global__ void __launch_bounds__(32 * kSkReduceRows) tc2_sk_reduce_kernel(const AttnParams p) {
-    constexpr int TQ = kTileM / G;
+    const int G = p.num_q_heads / p.num_kv_heads;
+    const int TQ = kTileM / G;
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const int4 d = p.sk_dir[blockIdx.x];
     if (d.x < 0 || d.y != 0) return;  // not partial, or not the unit's first keys
@@ -1826,7 +1854,7 @@ __global__ void __launch_bounds__(32 * kSkReduceRows) tc2_sk_reduce_kernel(const
     const int row = blockIdx.y * kSkReduceRows + (threadIdx.x >> 5);
     const int x = row / kTileM, r = row % kTileM;
     const int i = g.t0 + x * TQ + r / G;
-    if (i >= g.nrows) return;
+    if (r / G >= TQ || i >= g.nrows) return;
     const int h = g.kvh * G + r % G;
     const int n = nfrag;
     // the fragments' LSEs, one per lane (more than 32 fragments: in rounds)
@@ -1846,7 +1874,8 @@ __global__ void __launch_bounds__(32 * kSkReduceRows) tc2_sk_reduce_kernel(const
         for (int f = 0; f < n; ++f) {
             const int64_t fr = static_cast<int64_t>(frag[f]) * kSkFragRows + row;
             const float w = __expf(__ldcg(p.sk_frag_lse + fr) - m);
-            const float4 o = __ldcg(reinterpret_cast<const float4*>(p.sk_frag_o + fr * kD) + lane);
+            const float4 o = lane < D / 4 ? __ldcg(reinterpret_cast<const float4*>(p.sk_frag_o + fr * D) + lane)
+                                          : make_float4(0.f, 0.f, 0.f, 0.f);
             wsum += w;
             acc.x = fmaf(w, o.x, acc.x);
             acc.y = fmaf(w, o.y, acc.y);
@@ -1856,20 +1885,23 @@ __global__ void __launch_bounds__(32 * kSkReduceRows) tc2_sk_reduce_kernel(const
     }
     const float inv = wsum > 0.f ? 1.0f / wsum : 0.f;
     const int64_t st = static_cast<int64_t>(g.r0 + i) * p.num_q_heads + h;
-    if (p.out_f32) {
-        reinterpret_cast<float4*>(static_cast<float*>(p.out) + st * kD)[lane] =
-            make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
-    } else {
-        reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(p.out) + st * kD)[lane] =
-            make_uint2(pack_bf16x2(acc.x * inv, acc.y * inv), pack_bf16x2(acc.z * inv, acc.w * inv));
+    if (lane < D / 4) {
+        if (p.out_f32) {
+            reinterpret_cast<float4*>(static_cast<float*>(p.out) + st * D)[lane] =
+                make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+        } else {
+            reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(p.out) + st * D)[lane] =
+                make_uint2(pack_bf16x2(acc.x * inv, acc.y * inv), pack_bf16x2(acc.z * inv, acc.w * inv));
+        }
     }
     if (p.lse && lane == 0) p.lse[st] = wsum > 0.f ? m + __logf(wsum) : -INFINITY;
 }
 
-template <int G>
+template <int D>
 cudaError_t launch_g2(const AttnParams& p, const void* tk, const void* tv, cudaStream_t s) {
     const bool sk = p.sk_ctas > 0;
-    auto kern = sk ? attn_tc2_kernel<G, true> : attn_tc2_kernel<G, false>;
+    auto kern = sk ? attn_tc2_kernel<D, true> : attn_tc2_kernel<D, false>;
+    constexpr int kSmem = TwoTileSmem<D>::kBytes;
     // shared-memory opt-in: once per device and kernel
     static DeviceOnce opted[2];
     int dev = 0, done = 0;
@@ -1877,19 +1909,19 @@ cudaError_t launch_g2(const AttnParams& p, const void* tk, const void* tv, cudaS
     if (e != cudaSuccess) return e;
     e = opted[sk ? 1 : 0].get(dev, &done, [&](int, int* v) {
         *v = 1;
-        return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes2);
+        return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
     });
     if (e != cudaSuccess) return e;
-    const int TQ = kTileM / G;
+    const int TQ = kTileM / (p.num_q_heads / p.num_kv_heads);
     if (!sk) {
         dim3 grid((p.max_q_rows + 2 * TQ - 1) / (2 * TQ), p.num_kv_heads, p.batch * p.num_splits);
-        kern<<<grid, kThreads2, kSmemBytes2, s>>>(*static_cast<const CUtensorMap*>(tk),
-                                                  *static_cast<const CUtensorMap*>(tv), p);
+        kern<<<grid, kThreads2, kSmem, s>>>(*static_cast<const CUtensorMap*>(tk),
+                                            *static_cast<const CUtensorMap*>(tv), p);
         return cudaGetLastError();
     }
     // planner, then the persistent launch and the reduce, each behind the
     // previous one with programmatic serialisation (its prologue overlaps)
-    tc2_sk_plan_kernel<G><<<1, 1024, 0, s>>>(p);
+    tc2_sk_plan_kernel<<<1, 1024, 0, s>>>(p);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     cudaLaunchAttribute attr[1];
@@ -1898,7 +1930,7 @@ cudaError_t launch_g2(const AttnParams& p, const void* tk, const void* tv, cudaS
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(p.sk_ctas));
     cfg.blockDim = dim3(kThreads2);
-    cfg.dynamicSmemBytes = kSmemBytes2;
+    cfg.dynamicSmemBytes = kSmem;
     cfg.stream = s;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
@@ -1911,15 +1943,16 @@ cudaError_t launch_g2(const AttnParams& p, const void* tk, const void* tv, cudaS
     rcfg.stream = s;
     rcfg.attrs = attr;
     rcfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&rcfg, tc2_sk_reduce_kernel<G>, p);
+    return cudaLaunchKernelEx(&rcfg, tc2_sk_reduce_kernel<D>, p);
 }
 
 // One-tile launches: when a tile's rows (query rows x grouped heads) fit in
 // one 32-lane quadrant, they are held four times and each warp takes a
 // quarter of every key tile's columns.
-template <int G, bool GRP, int REP>
+template <int D, bool GRP, int REP>
 cudaError_t launch_one(const AttnParams& p, int rows, const void* tk, const void* tv, cudaStream_t s) {
-    auto kern = attn_tc_kernel<G, GRP, REP>;
+    auto kern = attn_tc_kernel<D, GRP, REP>;
+    constexpr int kSmem = OneTileSmem<D>::kBytes;
     // shared-memory opt-in: once per device
     static DeviceOnce opted;
     int dev = 0, done = 0;
@@ -1927,10 +1960,10 @@ cudaError_t launch_one(const AttnParams& p, int rows, const void* tk, const void
     if (e != cudaSuccess) return e;
     e = opted.get(dev, &done, [&](int, int* v) {
         *v = 1;
-        return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+        return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
     });
     if (e != cudaSuccess) return e;
-    const int TQ = kTileM / (G * REP);
+    const int TQ = kTileM / (p.num_q_heads / p.num_kv_heads * REP);
     dim3 grid((rows + TQ - 1) / TQ, p.num_kv_heads, p.batch * p.num_splits);
     // more than one wave of CTAs (one per SM) over a small batch: dispatch the
     // longest sequences first, so the last wave holds the shortest ones
@@ -1943,31 +1976,22 @@ cudaError_t launch_one(const AttnParams& p, int rows, const void* tk, const void
     AttnParams q = p;
     q.order_by_keys = !GRP && p.batch >= 2 && p.batch <= kOrderMaxBatch &&
                       static_cast<int64_t>(grid.x) * grid.y * grid.z > sms;
-    kern<<<grid, kThreads, kSmemBytes, s>>>(*static_cast<const CUtensorMap*>(tk),
-                                            *static_cast<const CUtensorMap*>(tv), q);
+    kern<<<grid, kThreads, kSmem, s>>>(*static_cast<const CUtensorMap*>(tk),
+                                       *static_cast<const CUtensorMap*>(tv), q);
     return cudaGetLastError();
 }
 
-template <int G, bool GRP>
+template <int D, bool GRP>
 cudaError_t launch_one_rep(const AttnParams& p, int rows, const void* tk, const void* tv, cudaStream_t s) {
-    if (rows * G <= kTileM / 4) return launch_one<G, GRP, 4>(p, rows, tk, tv, s);
-    return launch_one<G, GRP, 1>(p, rows, tk, tv, s);
-}
-
-template <int G>
-cudaError_t launch_grp(const AttnParams& p, const void* tk, const void* tv, cudaStream_t s) {
-    return launch_one_rep<G, true>(p, p.grp_max_tokens, tk, tv, s);
-}
-
-template <int G>
-cudaError_t launch_g(const AttnParams& p, const void* tk, const void* tv, cudaStream_t s) {
-    return launch_one_rep<G, false>(p, p.max_q_rows, tk, tv, s);
+    const int G = p.num_q_heads / p.num_kv_heads;
+    if (rows * G <= kTileM / 4) return launch_one<D, GRP, 4>(p, rows, tk, tv, s);
+    return launch_one<D, GRP, 1>(p, rows, tk, tv, s);
 }
 
 }  // namespace
 
 bool attn_tc_supported(int head_dim, int group) {
-    return head_dim == kD && (group == 1 || group == 2 || group == 4 || group == 8 || group == 16);
+    return (head_dim == 64 || head_dim == 128) && group >= 1 && group <= kMaxGroup;
 }
 
 int attn_tc_rows_per_tile(int group) { return kTileM / group; }
@@ -1983,36 +2007,19 @@ size_t attn_tc_sk_bytes(int units, int ctas, int head_dim) {
 }
 
 cudaError_t launch_attn_tc_grouped(const AttnParams& p, const void* tk, const void* tv, cudaStream_t s) {
-    switch (p.num_q_heads / p.num_kv_heads) {
-        case 1: return launch_grp<1>(p, tk, tv, s);
-        case 2: return launch_grp<2>(p, tk, tv, s);
-        case 4: return launch_grp<4>(p, tk, tv, s);
-        case 8: return launch_grp<8>(p, tk, tv, s);
-        case 16: return launch_grp<16>(p, tk, tv, s);
-    }
+    if (p.head_dim == 128) return launch_one_rep<128, true>(p, p.grp_max_tokens, tk, tv, s);
+    if (p.head_dim == 64) return launch_one_rep<64, true>(p, p.grp_max_tokens, tk, tv, s);
     return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_attn_tc(const AttnParams& p, const void*, const void* tk, const void* tv,
                            cudaStream_t s) {
     const int G = p.num_q_heads / p.num_kv_heads;
-    if (p.max_q_rows > kTileM / G) {
-        switch (G) {
-            case 1: return launch_g2<1>(p, tk, tv, s);
-            case 2: return launch_g2<2>(p, tk, tv, s);
-            case 4: return launch_g2<4>(p, tk, tv, s);
-            case 8: return launch_g2<8>(p, tk, tv, s);
-            case 16: return launch_g2<16>(p, tk, tv, s);
-        }
-        return cudaErrorInvalidValue;
-    }
-    switch (G) {
-        case 1: return launch_g<1>(p, tk, tv, s);
-        case 2: return launch_g<2>(p, tk, tv, s);
-        case 4: return launch_g<4>(p, tk, tv, s);
-        case 8: return launch_g<8>(p, tk, tv, s);
-        case 16: return launch_g<16>(p, tk, tv, s);
-    }
+    const bool two = p.max_q_rows > kTileM / G;
+    if (p.head_dim == 128)
+        return two ? launch_g2<128>(p, tk, tv, s) : launch_one_rep<128, false>(p, p.max_q_rows, tk, tv, s);
+    if (p.head_dim == 64)
+        return two ? launch_g2<64>(p, tk, tv, s) : launch_one_rep<64, false>(p, p.max_q_rows, tk, tv, s);
     return cudaErrorInvalidValue;
 }
 

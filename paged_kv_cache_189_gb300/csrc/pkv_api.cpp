@@ -527,7 +527,7 @@ pkv_status shared_prefix_attention(const void* q, int64_t q_token_stride, int64_
     if (page_size != 32)
         return fail(PKV_ERR_UNSUPPORTED, "shared prefix: page_size %d (only 32-token pages)", page_size);
     if (!pkv::attn_tc_supported(head_dim, num_q_heads / num_kv_heads))
-        return fail(PKV_ERR_UNSUPPORTED, "shared prefix: head_dim 128 and 1-16 grouped heads only");
+        return fail(PKV_ERR_UNSUPPORTED, "shared prefix: head_dim 64 or 128 and 1-64 grouped heads only");
     if (out_dtype != PKV_BF16 && out_dtype != PKV_F32)
         return fail(PKV_ERR_UNSUPPORTED, "shared prefix: output dtype must be bf16 or f32");
     if (batch > 65535 || num_kv_heads > 65535)

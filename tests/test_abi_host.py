@@ -164,8 +164,8 @@ def test_plan_and_shared_prefix_host_validation(L):
         return L.shared_prefix_attention(FAKE, 4096, 128, FAKE, FAKE, 100, page, 32 * Hkv * 128, FAKE, row_stride,
                                          FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 16, 1, 8, max_keys, Hq, Hkv, D,
                                          0.0, out, pkv.PKV_BF16, None, ws, ws_bytes, 0, 0, None, None)
-    assert spa(D=64) == pkv.PKV_ERR_UNSUPPORTED              # tensor-core tiles: head_dim 128
-    assert spa(Hq=24) == pkv.PKV_ERR_UNSUPPORTED             # group of 3
+    assert spa(D=96) == pkv.PKV_ERR_UNSUPPORTED              # tensor-core tiles: head_dim 64 or 128
+    assert spa(Hq=8 * 65) == pkv.PKV_ERR_UNSUPPORTED         # a group of 65 query heads
     assert spa(page=16) == pkv.PKV_ERR_UNSUPPORTED
     assert spa(out=None) == pkv.PKV_ERR_INVALID_ARG
     assert spa(row_stride=63) == pkv.PKV_ERR_INVALID_ARG     # row narrower than max_group_keys
@@ -205,6 +205,14 @@ def test_plan_follows_the_sm_count(L):
     assert s152["workspace_bytes"] - s120["workspace_bytes"] >= 32 * frag
     # by default the exact-window forward keeps its 3 key splits
     assert pkv.plan_attention(1, 1576, 32, 8, 128, 39518, num_sms=152)["splits"] == 3
+    # tensor-core tiles for head_dim 64 and for any head group up to 64; the
+    # generic kernel past that
+    assert pkv.plan_attention(4, 300, 32, 8, 64, 4000)["kernel"] == pkv.PKV_KERNEL_TILE
+    for hq, hkv in ((24, 8), (40, 8), (48, 8), (56, 8), (96, 8), (64, 1)):
+        assert pkv.plan_attention(4, 300, hq, hkv, 128, 4000)["kernel"] == pkv.PKV_KERNEL_TILE, (hq, hkv)
+        assert pkv.plan_attention(4, 1, hq, hkv, 128, 4000)["kernel"] == pkv.PKV_KERNEL_TILE, (hq, hkv)
+    assert pkv.plan_attention(4, 300, 65, 1, 128, 4000)["kernel"] == pkv.PKV_KERNEL_SIMT
+    assert pkv.plan_attention(4, 1, 32, 8, 64, 4000)["kernel"] == pkv.PKV_KERNEL_DECODE
     # an explicit split count keeps the one-CTA-per-tile grid
     assert pkv.plan_attention(1, 1568, 40, 40, 128, 7800, num_splits=2,
                               flags=pkv.PKV_FLAG_STREAM_K)["kernel"] == pkv.PKV_KERNEL_TILE
