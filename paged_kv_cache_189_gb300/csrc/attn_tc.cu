@@ -353,14 +353,16 @@ __device__ __forceinline__ TileGeom group_geometry(const AttnParams& p, int TQ, 
     return g;
 }
 
-template <int D, bool GRP, int REP>
+// GC: the head group when fixed at compile time (the common 1, 2, 4, 8, 16),
+// 0 to read it from the call
+template <int D, int GC, bool GRP, int REP>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                    const AttnParams p) {
     using TD = TileDim<D>;
     using SM = OneTileSmem<D>;
     constexpr int ND = kTileM / REP;  // distinct rows of the tile (each held REP times)
-    const int G = p.num_q_heads / p.num_kv_heads;
+    const int G = GC > 0 ? GC : p.num_q_heads / p.num_kv_heads;
     const int TQ = ND / G;            // tokens of the tile; rows from TQ * G on hold none
     extern __shared__ __align__(1024) uint8_t smem[];
     const int warp = threadIdx.x >> 5;
@@ -1267,13 +1269,13 @@ __device__ __forceinline__ void zero_pair_rows(const AttnParams& p, const TileGe
     store_row_lse(p, g, i, g.kvh * G + r % G, -INFINITY);
 }
 
-template <int D, bool SK>
+template <int D, int GC, bool SK>
 __global__ void __maxnreg__(96)
     attn_tc2_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                     const AttnParams p) {
     using TD = TileDim<D>;
     using SM = TwoTileSmem<D>;
-    const int G = p.num_q_heads / p.num_kv_heads;
+    const int G = GC > 0 ? GC : p.num_q_heads / p.num_kv_heads;
     const int TQ = kTileM / G;  // tokens per tile; rows from TQ * G on hold none
     extern __shared__ __align__(1024) uint8_t smem[];
     const int warp = threadIdx.x >> 5;
@@ -1897,10 +1899,11 @@ __global__ void __launch_bounds__(32 * kSkReduceRows) tc2_sk_reduce_kernel(const
     if (p.lse && lane == 0) p.lse[st] = wsum > 0.f ? m + __logf(wsum) : -INFINITY;
 }
 
-template <int D>
+template <int D, int GC>
 cudaError_t launch_g2(const AttnParams& p, const void* tk, const void* tv, cudaStream_t s) {
     const bool sk = p.sk_ctas > 0;
-    auto kern = sk ? attn_tc2_kernel<D, true> : attn_tc2_kernel<D, false>;
+    // the stream-K schedule (on request) reads the group from the call
+    auto kern = sk ? attn_tc2_kernel<D, 0, true> : attn_tc2_kernel<D, GC, false>;
     constexpr int kSmem = TwoTileSmem<D>::kBytes;
     // shared-memory opt-in: once per device and kernel
     static DeviceOnce opted[2];
@@ -1949,9 +1952,9 @@ cudaError_t launch_g2(const AttnParams& p, const void* tk, const void* tv, cudaS
 // One-tile launches: when a tile's rows (query rows x grouped heads) fit in
 // one 32-lane quadrant, they are held four times and each warp takes a
 // quarter of every key tile's columns.
-template <int D, bool GRP, int REP>
+template <int D, int GC, bool GRP, int REP>
 cudaError_t launch_one(const AttnParams& p, int rows, const void* tk, const void* tv, cudaStream_t s) {
-    auto kern = attn_tc_kernel<D, GRP, REP>;
+    auto kern = attn_tc_kernel<D, GC, GRP, REP>;
     constexpr int kSmem = OneTileSmem<D>::kBytes;
     // shared-memory opt-in: once per device
     static DeviceOnce opted;
@@ -1981,11 +1984,41 @@ cudaError_t launch_one(const AttnParams& p, int rows, const void* tk, const void
     return cudaGetLastError();
 }
 
-template <int D, bool GRP>
+template <int D, int GC, bool GRP>
 cudaError_t launch_one_rep(const AttnParams& p, int rows, const void* tk, const void* tv, cudaStream_t s) {
     const int G = p.num_q_heads / p.num_kv_heads;
-    if (rows * G <= kTileM / 4) return launch_one<D, GRP, 4>(p, rows, tk, tv, s);
-    return launch_one<D, GRP, 1>(p, rows, tk, tv, s);
+    if (rows * G <= kTileM / 4) return launch_one<D, GC, GRP, 4>(p, rows, tk, tv, s);
+    return launch_one<D, GC, GRP, 1>(p, rows, tk, tv, s);
+}
+
+// head_dim 128: the common head groups fixed at compile time, any other read
+// from the call; head_dim 64: read from the call
+template <int D, bool GRP>
+cudaError_t launch_one_g(const AttnParams& p, int rows, const void* tk, const void* tv, cudaStream_t s) {
+    if constexpr (D == 128) {
+        switch (p.num_q_heads / p.num_kv_heads) {
+            case 1: return launch_one_rep<D, 1, GRP>(p, rows, tk, tv, s);
+            case 2: return launch_one_rep<D, 2, GRP>(p, rows, tk, tv, s);
+            case 4: return launch_one_rep<D, 4, GRP>(p, rows, tk, tv, s);
+            case 8: return launch_one_rep<D, 8, GRP>(p, rows, tk, tv, s);
+            case 16: return launch_one_rep<D, 16, GRP>(p, rows, tk, tv, s);
+        }
+    }
+    return launch_one_rep<D, 0, GRP>(p, rows, tk, tv, s);
+}
+
+template <int D>
+cudaError_t launch_two_g(const AttnParams& p, const void* tk, const void* tv, cudaStream_t s) {
+    if constexpr (D == 128) {
+        switch (p.num_q_heads / p.num_kv_heads) {
+            case 1: return launch_g2<D, 1>(p, tk, tv, s);
+            case 2: return launch_g2<D, 2>(p, tk, tv, s);
+            case 4: return launch_g2<D, 4>(p, tk, tv, s);
+            case 8: return launch_g2<D, 8>(p, tk, tv, s);
+            case 16: return launch_g2<D, 16>(p, tk, tv, s);
+        }
+    }
+    return launch_g2<D, 0>(p, tk, tv, s);
 }
 
 }  // namespace
@@ -2007,8 +2040,8 @@ size_t attn_tc_sk_bytes(int units, int ctas, int head_dim) {
 }
 
 cudaError_t launch_attn_tc_grouped(const AttnParams& p, const void* tk, const void* tv, cudaStream_t s) {
-    if (p.head_dim == 128) return launch_one_rep<128, true>(p, p.grp_max_tokens, tk, tv, s);
-    if (p.head_dim == 64) return launch_one_rep<64, true>(p, p.grp_max_tokens, tk, tv, s);
+    if (p.head_dim == 128) return launch_one_g<128, true>(p, p.grp_max_tokens, tk, tv, s);
+    if (p.head_dim == 64) return launch_one_g<64, true>(p, p.grp_max_tokens, tk, tv, s);
     return cudaErrorInvalidValue;
 }
 
@@ -2017,9 +2050,9 @@ cudaError_t launch_attn_tc(const AttnParams& p, const void*, const void* tk, con
     const int G = p.num_q_heads / p.num_kv_heads;
     const bool two = p.max_q_rows > kTileM / G;
     if (p.head_dim == 128)
-        return two ? launch_g2<128>(p, tk, tv, s) : launch_one_rep<128, false>(p, p.max_q_rows, tk, tv, s);
+        return two ? launch_two_g<128>(p, tk, tv, s) : launch_one_g<128, false>(p, p.max_q_rows, tk, tv, s);
     if (p.head_dim == 64)
-        return two ? launch_g2<64>(p, tk, tv, s) : launch_one_rep<64, false>(p, p.max_q_rows, tk, tv, s);
+        return two ? launch_two_g<64>(p, tk, tv, s) : launch_one_g<64, false>(p, p.max_q_rows, tk, tv, s);
     return cudaErrorInvalidValue;
 }
 
