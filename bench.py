@@ -71,7 +71,7 @@ def parse():
 # the workloads measured besides the headline one, in the order they run
 EXTRA_WORKLOADS = ("tiny_decode", "chunked_prefill", "shared_prefix", "shared_prefix_fused",
                    "shared_prefix_plain_decode", "block_causal_video", "multi_token_decode",
-                   "exact_window_denoise")
+                   "exact_window_denoise", "exact_window_video")
 
 
 # ----------------------------------------------------------------------------
@@ -566,6 +566,9 @@ WORKLOAD_META = {
     "exact_window_denoise": dict(metric="prefill TFLOP/s", unit="TFLOP/s", scale=1e12,
                                  config=dict(q_heads=32, kv_heads=8, head_dim=128, page=32,
                                              staged_tokens=1576, causal_block=1576)),
+    "exact_window_video": dict(metric="prefill TFLOP/s", unit="TFLOP/s", scale=1e12,
+                               config=dict(q_heads=32, kv_heads=8, head_dim=128, page=32,
+                                           staged_tokens=1576, causal_block=394)),
 }
 WORKLOAD_SEED = {"gqa_decode": 1, "chunked_prefill": 2, "shared_prefix": 3, "block_causal_video": 4,
                  "shared_prefix_fused": 3, "shared_prefix_verify": 3, "shared_prefix_plain_decode": 3,
