@@ -458,6 +458,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     const uint32_t sbase = smem_u32(smem);
+    // grouped mode: the keys [g0, g1) of member k's last tail page past its tail
+    // (seen by no row); members' tails follow each other in the group row, so
+    // these gaps come in increasing key order
+    auto member_gap = [&](int k, int& g0, int& g1) {
+        const int m = p.grp_perm[grp_first + k];
+        g0 = 32 * p.grp_tail_start[m] + p.grp_tail_lens[m];
+        g1 = (g0 + 31) / 32 * 32;
+    };
 
     // a wait that gives up marks the CTA aborted; later waits return at once
     auto wait = [&](uint64_t* bar, uint32_t parity) -> bool {
@@ -605,6 +613,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // a warp none of whose rows sees a key (rows past the sequence, padding
             // rows) writes zero probabilities and skips the softmax arithmetic
             const bool warp_live = GRP || __any_sync(0xffffffffu, limit > 0);
+            int gap_k = 0;  // grouped: the first member whose tail gap may still meet a key tile
             for (int j = 0; j < g.nt; ++j) {
                 if (!wait_warp(&s_full[j & 1], (j >> 1) & 1)) break;
                 tc_fence_after();
@@ -713,21 +722,29 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if constexpr (GRP) {
                     // the rest of each member's last tail page is seen by no row: zero
                     // those V rows too (same reason)
+                    int g0, g1;
+                    while (gap_k < grp_count) {  // gaps that end before this key tile
+                        member_gap(gap_k, g0, g1);
+                        if (g1 > key0) break;
+                        ++gap_k;
+                    }
                     bool any_gap = false;
-                    for (int k = 0; k < grp_count; ++k) {
-                        const int m = p.grp_perm[grp_first + k];
-                        const int g0 = 32 * p.grp_tail_start[m] + p.grp_tail_lens[m];
-                        const int g1 = (g0 + 31) / 32 * 32;
-                        any_gap |= g0 < g1 && g0 < key0 + kTileN && g1 > key0;
+                    for (int k = gap_k; k < grp_count; ++k) {
+                        member_gap(k, g0, g1);
+                        if (g0 >= key0 + kTileN) break;
+                        if (g0 < g1) {
+                            any_gap = true;
+                            break;
+                        }
                     }
                     if (any_gap) {
                         const int vs = j % kVStages;
                         if (!wait_warp(&v_full[vs], (j / kVStages) & 1)) break;
                         uint8_t* vt = smem + TD::kVOff + vs * TD::kTile;
-                        for (int k = 0; k < grp_count; ++k) {
-                            const int m = p.grp_perm[grp_first + k];
-                            const int g0 = 32 * p.grp_tail_start[m] + p.grp_tail_lens[m];
-                            const int lo = max(g0, key0) - key0, hi = min((g0 + 31) / 32 * 32, key0 + kTileN) - key0;
+                        for (int k = gap_k; k < grp_count; ++k) {
+                            member_gap(k, g0, g1);
+                            if (g0 >= key0 + kTileN) break;
+                            const int lo = max(g0, key0) - key0, hi = min(g1, key0 + kTileN) - key0;
                             for (int idx = r; idx < (hi - lo) * TD::kChunks; idx += kTileM) {
                                 const int row = lo + idx / TD::kChunks, c = idx % TD::kChunks;
                                 *reinterpret_cast<uint4*>(vt + (c >> 3) * kHalfBytes + sw128_offset(row, c & 7)) =
@@ -806,9 +823,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             // a warp none of whose rows sees a key (rows past the sequence, padding
             // rows) writes zero probabilities and skips the softmax arithmetic
             const bool warp_live = GRP || __any_sync(0xffffffffu, limit > 0);
+            // this lane owns its P row; the chunks of the other copies' key columns
+            // stay zero for the whole launch, so they are written once here
+            if constexpr (REP > 1) {
+    #pragma unroll
+                for (int c = 0; c < 16; ++c)
+                    if (c / (CW / 8) != part)
+                        *reinterpret_cast<uint4*>(prow + (c >> 3) * kHalfBytes + sw128_offset(r, c & 7)) =
+                            make_uint4(0u, 0u, 0u, 0u);
+            }
             // with copies, the four warps exchange maxima every key tile; a failed
             // wait is carried to the next exchange, where all of them leave together
             bool ok_run = true;
+            int gap_k = 0;  // grouped: the first member whose tail gap may still meet a key tile
             for (int j = 0; j < g.nt; ++j) {
                 ok_run = ok_run && wait_warp(&s_full[j & 1], (j >> 1) & 1);
                 if (REP == 1 && !ok_run) break;
@@ -918,20 +945,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                     }
                     // P row -> shared memory, K-major 128-byte swizzle, two 64-key halves;
-                    // 16-byte chunk c holds keys [8c, 8c + 8): this lane's chunks from pk,
-                    // the others zero
+                    // 16-byte chunk c holds keys [8c, 8c + 8): this lane's chunks from pk
+                    // (the others were zeroed before the key loop)
     #pragma unroll
                     for (int cc = 0; cc < CW / 8; ++cc) {
                         const int c = part * (CW / 8) + cc;
                         *reinterpret_cast<uint4*>(prow + (c >> 3) * kHalfBytes + sw128_offset(r, c & 7)) =
                             make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
-                    }
-                    if constexpr (REP > 1) {
-    #pragma unroll
-                        for (int c = 0; c < 16; ++c)
-                            if (c / (CW / 8) != part)
-                                *reinterpret_cast<uint4*>(prow + (c >> 3) * kHalfBytes + sw128_offset(r, c & 7)) =
-                                    make_uint4(0u, 0u, 0u, 0u);
                     }
                     // V rows of keys past the sequence's length inside its last page hold
                     // whatever the pool holds there; zero them so 0 * garbage cannot make NaN
@@ -953,22 +973,30 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if constexpr (GRP) {
                         // the rest of each member's last tail page is seen by no row: zero
                         // those V rows too (same reason)
+                        int g0, g1;
+                        while (gap_k < grp_count) {  // gaps that end before this key tile
+                            member_gap(gap_k, g0, g1);
+                            if (g1 > key0) break;
+                            ++gap_k;
+                        }
                         bool any_gap = false;
-                        for (int k = 0; k < grp_count; ++k) {
-                            const int m = p.grp_perm[grp_first + k];
-                            const int g0 = 32 * p.grp_tail_start[m] + p.grp_tail_lens[m];
-                            const int g1 = (g0 + 31) / 32 * 32;
-                            any_gap |= g0 < g1 && g0 < key0 + kTileN && g1 > key0;
+                        for (int k = gap_k; k < grp_count; ++k) {
+                            member_gap(k, g0, g1);
+                            if (g0 >= key0 + kTileN) break;
+                            if (g0 < g1) {
+                                any_gap = true;
+                                break;
+                            }
                         }
                         if (any_gap) {
                             const int vs = j % kVStages;
                             ok_run = ok_run && wait_warp(&v_full[vs], (j / kVStages) & 1);
                             if (REP == 1 && !ok_run) break;
                             uint8_t* vt = smem + TD::kVOff + vs * TD::kTile;
-                            for (int k = 0; ok_run && k < grp_count; ++k) {
-                                const int m = p.grp_perm[grp_first + k];
-                                const int g0 = 32 * p.grp_tail_start[m] + p.grp_tail_lens[m];
-                                const int lo = max(g0, key0) - key0, hi = min((g0 + 31) / 32 * 32, key0 + kTileN) - key0;
+                            for (int k = gap_k; ok_run && k < grp_count; ++k) {
+                                member_gap(k, g0, g1);
+                                if (g0 >= key0 + kTileN) break;
+                                const int lo = max(g0, key0) - key0, hi = min(g1, key0 + kTileN) - key0;
                                 for (int idx = r; idx < (hi - lo) * TD::kChunks; idx += kTileM) {
                                     const int row = lo + idx / TD::kChunks, c = idx % TD::kChunks;
                                     *reinterpret_cast<uint4*>(vt + (c >> 3) * kHalfBytes + sw128_offset(row, c & 7)) =
