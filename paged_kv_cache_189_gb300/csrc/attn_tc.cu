@@ -157,6 +157,18 @@ __device__ __forceinline__ void tmem_store32(uint32_t taddr, const uint32_t (&v)
         "tcgen05.wait::st.sync.aligned;"
         ::"r"(taddr), PKV_W8(0), PKV_W8(8), PKV_W8(16), PKV_W8(24) : "memory");
 }
+// entries 0..63 of v to 64 consecutive columns (two 32-column stores); the caller waits
+__device__ __forceinline__ void tmem_store64_nowait(uint32_t taddr, const uint32_t (&v)[128]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
+        "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};\n\t"
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%33], "
+        "{%34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, %48, %49, "
+        "%50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63, %64, %65};"
+        ::"r"(taddr), PKV_W8(0), PKV_W8(8), PKV_W8(16), PKV_W8(24), "r"(taddr + 32), PKV_W8(32), PKV_W8(40),
+          PKV_W8(48), PKV_W8(56) : "memory");
+}
 #undef PKV_W8
 
 // max of three values in one instruction
@@ -1122,21 +1134,26 @@ __device__ __forceinline__ void umma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, u
 // tensor memory, which leaves shared memory for the two Q tiles and the K/V
 // rings.  Tensor memory: S_A [0,128) O_A [128,256) S_B [256,384) O_B [384,512).
 //
-// Eight softmax warps per tile: the two warps that share a tensor-memory lane
-// quadrant (the same 32 rows) take one 64-key half of each 128-key tile each
-// and exchange their partial row maxima through shared memory, which halves
-// each warp's serial work per key tile (the chain softmax -> P.V -> next S
-// that the other tile's MMAs have to cover).  Packed P of the first key half
-// goes to columns [0,32) of the tile's S region, that of the second half to
-// columns [96,128) (written from its last 32 keys backwards), so neither half
-// overwrites S values the other has not read yet.
-// Roles (576 threads): warps 0-7 softmax A, warps 8-15 softmax B (quadrant
-// warp & 3, key half (warp >> 2) & 1), warp 16 TMA producer, warp 17 MMA.
-// Every wait gives up after ~2 s; the exchange barrier of a lane quadrant's two
-// warps (a named barrier per quadrant and tile) also ANDs the waits' results,
-// so the two leave the key loop together.
+// Four softmax warps per tile, one thread per row: a thread reads its row's
+// 128 scores of a key tile from tensor memory in one pass, keeps them in
+// registers for the maximum and the exponentials, and writes the packed P
+// (128 keys in columns [0,64) of the tile's S region) over them; no thread
+// exchanges anything with another.  The 168 registers this takes (the row's
+// scores among them) fit because the CTA has ten warps, at most three per SM
+// sub-partition.  (Eight softmax warps per tile, each taking half a row with
+// the maxima exchanged between the two, capped every thread at 96 registers
+// and read the scores twice per key tile: 0.281 ms against 0.266 ms on the
+// video step.)
+// Roles (320 threads): warps 0-3 softmax A, warps 4-7 softmax B (quadrant
+// warp & 3), warp 8 TMA producer, warp 9 MMA.  Every wait gives up after ~2 s.
 // ===========================================================================
-constexpr int kThreads2 = 576;
+// 10 warps: 0-7 softmax (four per tile), 8 the TMA producer, 9 the MMA
+// issuer.  Three warps per SM sub-partition at most, so each thread may hold
+// 168 registers (the row's 128 scores among them)
+constexpr int kThreads2 = 320;
+constexpr int kProducerWarp2 = 8;
+constexpr int kMmaWarp2 = 9;
+constexpr int kRegs2 = 168;
 template <int D>
 struct TwoTileSmem {
     static constexpr int kTile = TileDim<D>::kTile;
@@ -1298,7 +1315,7 @@ __device__ __forceinline__ void zero_pair_rows(const AttnParams& p, const TileGe
 }
 
 template <int D, int GC, bool SK>
-__global__ void __maxnreg__(96)
+__global__ void __maxnreg__(kRegs2)
     attn_tc2_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                     const AttnParams p) {
     using TD = TileDim<D>;
@@ -1356,7 +1373,7 @@ __global__ void __maxnreg__(96)
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + SM::kFlagOff);
 
     if (threadIdx.x == 0) {
-        mbar_init(q_ready, 4 * kTileM);
+        mbar_init(q_ready, 2 * kTileM);
         for (int s = 0; s < kKStages; ++s) {
             mbar_init(&k_full[s], 1);
             mbar_init(&k_empty[s], 1);
@@ -1367,13 +1384,13 @@ __global__ void __maxnreg__(96)
         }
         for (int x = 0; x < 2; ++x) {
             mbar_init(&s_full[x], 1);
-            mbar_init(&p_full[x], 8);  // one elected arrive per softmax warp
+            mbar_init(&p_full[x], 4);  // one elected arrive per softmax warp of the tile
             mbar_init(&o_full[x], 1);
         }
         *abort_flag = 0;
         fence_mbar_init();
     }
-    if (warp == 17) {
+    if (warp == kMmaWarp2) {
         tmem_alloc(tmem_slot, kTmemCols);
         tmem_relinquish();
     }
@@ -1391,7 +1408,7 @@ __global__ void __maxnreg__(96)
         return false;
     };
 
-    if (warp == 16) {
+    if (warp == kProducerWarp2) {
         // ============================ producer ==============================
         // K and V tiles of every segment in order, through rings that run
         // across segment boundaries (gt counts the tiles of all segments)
@@ -1444,7 +1461,7 @@ __global__ void __maxnreg__(96)
             for (int j = max(0, vn - kVStages); j < vn; ++j)
                 mbar_wait(&v_full[j % kVStages], (j / kVStages) & 1);
         }
-    } else if (warp == 17) {
+    } else if (warp == kMmaWarp2) {
         // ============================== MMA ================================
         if (lane == 0) {
             constexpr uint32_t kIdescS = idesc_bf16(kTileM, kTileN, false);
@@ -1464,9 +1481,9 @@ __global__ void __maxnreg__(96)
                 const uint32_t vb = sbase + SM::kVOff + (gt % kVStages) * TD::kTile;
 #pragma unroll
                 for (int kk = 0; kk < kTileN / 16; ++kk) {
-                    // A = P in tensor memory: keys [0,64) packed in columns [0,32),
-                    // keys [64,128) in columns [96,128); 16 keys = 8 columns per step
-                    const uint32_t pcol = kk < 4 ? kk * 8 : 64 + kk * 8;
+                    // A = P in tensor memory: the 128 keys packed in columns
+                    // [0, 64); 16 keys = 8 columns per step
+                    const uint32_t pcol = kk * 8;
                     const uint64_t bdesc = sdesc_sw128(vb + kk * 16 * 128, kHalfBytes, 1024);
                     umma_bf16_ts(tmem + x * 256 + 128, tmem + x * 256 + pcol, bdesc, kIdescO,
                                  (acc || kk > 0) ? 1u : 0u);
@@ -1527,20 +1544,17 @@ __global__ void __maxnreg__(96)
                 }
             }
         }
-    } else {
+    } else if (warp < 8) {
         // ============================ softmax ===============================
-        const int x = warp >> 3;               // tile
-        const int hf = (warp >> 2) & 1;        // key half of each tile (and O column half)
+        // warps 0-3: tile A, warps 4-7: tile B.  Each thread owns one row (its
+        // lane of its warp's tensor-memory quadrant) and all 128 keys of every
+        // key tile: the scores, their maximum and the probabilities stay in its
+        // registers, with no exchange between threads.
+        const int x = warp >> 2;               // tile
         const int r = (warp & 3) * 32 + lane;  // row in the tile = tensor-memory lane
         const int t = r / G, hg = r % G;
-        const int bar_id = 1 + x * 4 + (warp & 3);  // the two warps of this lane quadrant
         const uint32_t lane_addr = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16) + x * 256;
-        const uint32_t s_addr = lane_addr + hf * 64;        // this half's S columns
-        constexpr int OH = D / 2;                            // O columns of each half
-        const uint32_t o_addr = lane_addr + 128 + hf * OH;  // this half's O columns
-        float* xmine = xch + (x * 2 + hf) * kTileM + r;
-        const float* xother = xch + (x * 2 + (hf ^ 1)) * kTileM + r;
-        float* xl = xch + x * 2 * kTileM + r;  // [tile][0: l, 1: l_b][row]
+        const uint32_t o_addr = lane_addr + 128;  // this row's O columns
         const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
         SegIter<SK> it = it0;
         Seg sg;
@@ -1558,20 +1572,18 @@ __global__ void __maxnreg__(96)
             const int limit = row_exists ? visible_keys(i, g.qreal, g.kv_len, p.mask, max(p.causal_block, 1))
                                          : 0;
             {
-                // this thread's half of the row's 16-byte chunks.  The previous
-                // segment's S MMAs have finished reading this Q tile (their S was
-                // consumed), and its O was read before this arrive, ahead of the
-                // segment's first P.V
-                constexpr int QC = TD::kChunks / 2;  // 16-byte chunks of the row per half-warp
+                // the row's query into the swizzled Q tile.  The previous segment's
+                // S MMAs have finished reading this Q tile (their S was consumed),
+                // and its O was read before this arrive, ahead of the segment's
+                // first P.V
                 const uint4* src = reinterpret_cast<const uint4*>(
                     static_cast<const __nv_bfloat16*>(p.q) + static_cast<int64_t>(g.r0 + i) * p.q_token_stride +
-                    static_cast<int64_t>(h) * p.q_head_stride) + hf * QC;
+                    static_cast<int64_t>(h) * p.q_head_stride);
                 uint8_t* qt = smem + SM::kQOff + x * TD::kTile;
 #pragma unroll
-                for (int c = 0; c < QC; ++c) {
-                    const int gc = hf * QC + c;
+                for (int c = 0; c < TD::kChunks; ++c) {
                     const uint4 v = row_exists ? src[c] : make_uint4(0u, 0u, 0u, 0u);
-                    *reinterpret_cast<uint4*>(qt + (gc >> 3) * kHalfBytes + sw128_offset(r, gc & 7)) = v;
+                    *reinterpret_cast<uint4*>(qt + (c >> 3) * kHalfBytes + sw128_offset(r, c & 7)) = v;
                 }
                 fence_proxy_async_smem();
                 tc_fence_before();
@@ -1593,49 +1605,56 @@ __global__ void __maxnreg__(96)
             float l = 0.f, l_b = 0.f;
             const bool warp_live = __any_sync(0xffffffffu, limit > 0);
             for (int j = sg.j0; j < sg.j1; ++j, ++nit) {
-                bool ok_t = __all_sync(0xffffffffu, wait(&s_full[x], nit & 1));
-                tc_fence_after();
-                const int nvis = limit - (g.kb + j * kTileN) - hf * 64;  // visible columns of this half
-                float mpart = -INFINITY;
-                if (ok_t && warp_live) {
-                    uint32_t sv[32];
-#pragma unroll
-                    for (int c = 0; c < 2; ++c) {
-                        tmem_load32(s_addr + c * 32, sv);
-                        if (nvis < (c + 1) * 32) {
-#pragma unroll
-                            for (int e = 0; e < 32; ++e)
-                                sv[e] = c * 32 + e < nvis ? sv[e] : __float_as_uint(-INFINITY);
-                        }
-                        float a[4];
-#pragma unroll
-                        for (int q = 0; q < 4; ++q) a[q] = __uint_as_float(sv[q]);
-#pragma unroll
-                        for (int e = 4; e < 32; e += 8) {
-#pragma unroll
-                            for (int q = 0; q < 4; ++q)
-                                a[q] = fmax3(a[q], __uint_as_float(sv[e + q]), __uint_as_float(sv[e + 4 + q]));
-                        }
-                        mpart = fmax3(mpart, fmax3(a[0], a[1], a[2]), a[3]);
-                    }
-                }
-                // exchange the two halves' maxima; also agree on whether every wait succeeded
-                *xmine = mpart;
-                if (!bar_and(bar_id, 2 * 32, ok_t)) {
+                if (!__all_sync(0xffffffffu, wait(&s_full[x], nit & 1))) {
                     ok = false;
                     break;
                 }
+                tc_fence_after();
+                const int key0 = g.kb + j * kTileN;
                 if (warp_live) {
-                    const float mx = fmaxf(mpart, *xother) * p.scale_log2;
+                    uint32_t sv[kTileN];  // this row's scores (f32 bits), then its packed P
+                    tmem_load128(lane_addr, sv);
+                    const int nvis = limit - key0;  // keys past it are masked (diagonal tiles only)
+                    if (nvis < kTileN) {
+#pragma unroll
+                        for (int e = 0; e < kTileN; ++e) sv[e] = e < nvis ? sv[e] : __float_as_uint(-INFINITY);
+                    }
+                    float a[8];
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) a[q] = __uint_as_float(sv[q]);
+#pragma unroll
+                    for (int e = 8; e < kTileN; e += 16) {
+#pragma unroll
+                        for (int q = 0; q < 8; ++q)
+                            a[q] = fmax3(a[q], __uint_as_float(sv[e + q]), __uint_as_float(sv[e + 8 + q]));
+                    }
+                    const float mx = fmax3(fmax3(a[0], a[1], a[2]), fmax3(a[3], a[4], a[5]), fmaxf(a[6], a[7])) *
+                                     p.scale_log2;
                     float alpha = 1.f;
-                    if (mx > m_used + kLazyRescale) {
-                        alpha = fast_exp2(m_used - mx);
+                    if (mx > m_used + kLazyRescale) {   // also true the first time a key is visible
+                        alpha = fast_exp2(m_used - mx);  // 0 when m_used was -inf
                         m_used = mx;
                     }
-                    // O *= alpha on this half's columns
+                    const float nm = m_used == -INFINITY ? 0.f : -m_used;
+                    const float2 nm2 = make_float2(nm, nm);
+                    float2 rs2 = make_float2(0.f, 0.f), rsb2 = make_float2(0.f, 0.f);
+                    // probabilities packed in place: keys (2k, 2k + 1) land in sv[k]
+                    // (k <= 2k: read before written); P over S columns [0, 64)
+#pragma unroll
+                    for (int k2 = 0; k2 < kTileN / 2; ++k2) {
+                        const float2 xx = __ffma2_rn(
+                            make_float2(__uint_as_float(sv[2 * k2]), __uint_as_float(sv[2 * k2 + 1])), sc2, nm2);
+                        const float2 pp = make_float2(fast_exp2(xx.x), fast_exp2(xx.y));
+                        sv[k2] = pack_bf16x2(pp.x, pp.y);
+                        rs2 = __fadd2_rn(rs2, pp);
+                        add_bf16x2(rsb2, sv[k2]);
+                    }
+                    tmem_store64_nowait(lane_addr, sv);
+                    // O *= alpha for this row (before the next P.V, which follows
+                    // this warp's arrive below)
                     if (j > sg.j0 && __any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll
-                        for (int c = 0; c < OH / 32; ++c) {
+                        for (int c = 0; c < D / 32; ++c) {
                             uint32_t v[32];
                             tmem_load32(o_addr + c * 32, v);
 #pragma unroll
@@ -1648,55 +1667,25 @@ __global__ void __maxnreg__(96)
                             tmem_store32(o_addr + c * 32, v);
                         }
                     }
-                    const float nm = m_used == -INFINITY ? 0.f : -m_used;
-                    const float2 nm2 = make_float2(nm, nm);
-                    float2 rs2 = make_float2(0.f, 0.f), rsb2 = make_float2(0.f, 0.f);
-                    // half 0: S columns [0,32),[32,64) -> P columns [0,16),[16,32);
-                    // half 1: S columns [96,128),[64,96) -> P columns [112,128),[96,112)
-#pragma unroll
-                    for (int cc = 0; cc < 2; ++cc) {
-                        const int c = hf ? 1 - cc : cc;
-                        uint32_t v[32];
-                        tmem_load32(s_addr + c * 32, v);
-                        if (nvis < (c + 1) * 32) {
-#pragma unroll
-                            for (int e = 0; e < 32; ++e)
-                                v[e] = c * 32 + e < nvis ? v[e] : __float_as_uint(-INFINITY);
-                        }
-                        uint32_t pk[16];
-#pragma unroll
-                        for (int e = 0; e < 32; e += 2) {
-                            const float2 xx = __ffma2_rn(make_float2(__uint_as_float(v[e]), __uint_as_float(v[e + 1])),
-                                                         sc2, nm2);
-                            const float2 pp = make_float2(fast_exp2(xx.x), fast_exp2(xx.y));
-                            pk[e / 2] = pack_bf16x2(pp.x, pp.y);
-                            rs2 = __fadd2_rn(rs2, pp);
-                            add_bf16x2(rsb2, pk[e / 2]);
-                        }
-                        tmem_store16(lane_addr + hf * 96 + c * 16, pk);
-                    }
                     tmem_store_wait();
                     l = l * alpha + (rs2.x + rs2.y);
                     l_b = l_b * alpha + (rsb2.x + rsb2.y);
                 } else {
-                    uint32_t zero[16];
+                    uint32_t zero[kTileN];
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) zero[e] = 0u;
-#pragma unroll
-                    for (int c = 0; c < 2; ++c) tmem_store16(lane_addr + hf * 96 + c * 16, zero);
+                    for (int e = 0; e < kTileN / 2; ++e) zero[e] = 0u;
+                    tmem_store64_nowait(lane_addr, zero);
                     tmem_store_wait();
                 }
                 // keys past the sequence's length inside its last page: zero their V rows
-                const int key0 = g.kb + j * kTileN;
                 if (x == 0 && key0 + kTileN > g.kv_len && g.kv_len > key0) {
                     const int gj = gt + (j - sg.j0);
                     const int vs = gj % kVStages;
-                    ok_t = __all_sync(0xffffffffu, wait(&v_full[vs], (gj / kVStages) & 1));
-                    if (ok_t) {
+                    if (__all_sync(0xffffffffu, wait(&v_full[vs], (gj / kVStages) & 1))) {
                         const int first = g.kv_len - key0;
                         const int lastr = min(kTileN, (first + 31) / 32 * 32);
                         uint8_t* vt = smem + SM::kVOff + vs * TD::kTile;
-                        for (int idx = hf * kTileM + r; idx < (lastr - first) * TD::kChunks; idx += 2 * kTileM) {
+                        for (int idx = r; idx < (lastr - first) * TD::kChunks; idx += kTileM) {
                             const int row = first + idx / TD::kChunks, c16 = idx % TD::kChunks;
                             *reinterpret_cast<uint4*>(vt + (c16 >> 3) * kHalfBytes + sw128_offset(row, c16 & 7)) =
                                 make_uint4(0u, 0u, 0u, 0u);
@@ -1708,46 +1697,31 @@ __global__ void __maxnreg__(96)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&p_full[x]);
             }
-            // ---- epilogue: the two halves' sums, then O / l on this half's columns
+            // ---- epilogue: O / l
             const bool ok_o = __all_sync(0xffffffffu, ok && wait(&o_full[x], nseg & 1));
             ++nseg;
             tc_fence_after();
-            // every key-loop exchange has been read: o_full follows both halves' last P
-            bar_sync_n(bar_id, 2 * 32);
-            if (hf == 1) {
-                xl[0] = l;
-                xl[kTileM] = l_b;
-            }
-            bar_sync_n(bar_id, 2 * 32);
             // a segment that is not its unit's whole key range leaves a partial
             // state in this CTA's fragment slot (the first or the last segment)
             const bool whole = sg.j0 == 0 && sg.j1 == g.nt;
             const int fslot = blockIdx.x * 2 + (slot == 0 ? 0 : 1);
-            float inv_l = 0.f;
-            if (hf == 0) {
-                const float lt = l + xl[0], lbt = l_b + xl[kTileM];
-                const bool any = lt > 0.f && lbt > 0.f;
-                inv_l = any ? 1.0f / lbt : 0.f;
-                const float lse = any ? (m_used + __log2f(lt)) * kLn2 : -INFINITY;
-                if (ok_o && row_exists) {
-                    if (whole) store_row_lse(p, g, i, h, lse);
-                    else p.sk_frag_lse[static_cast<int64_t>(fslot) * kSkFragRows + x * kTileM + r] = lse;
-                }
-                xl[0] = inv_l;
+            const bool any = l > 0.f && l_b > 0.f;
+            const float inv_l = any ? 1.0f / l_b : 0.f;
+            if (ok_o && row_exists) {
+                const float lse = any ? (m_used + __log2f(l)) * kLn2 : -INFINITY;
+                if (whole) store_row_lse(p, g, i, h, lse);
+                else p.sk_frag_lse[static_cast<int64_t>(fslot) * kSkFragRows + x * kTileM + r] = lse;
             }
-            bar_sync_n(bar_id, 2 * 32);
-            if (hf == 1) inv_l = xl[0];
 #pragma unroll
-            for (int c = 0; c < OH / 32; ++c) {
+            for (int c = 0; c < D / 32; ++c) {
                 uint32_t v[32];
                 tmem_load32(o_addr + c * 32, v);
                 if (ok_o && row_exists) {
                     if (whole) {
-                        store_row_chunk<D>(p, g, i, h, hf * (OH / 32) + c, v, inv_l);
+                        store_row_chunk<D>(p, g, i, h, c, v, inv_l);
                     } else {
                         float4* dst = reinterpret_cast<float4*>(
-                            p.sk_frag_o + (static_cast<int64_t>(fslot) * kSkFragRows + x * kTileM + r) * D +
-                            (hf * (OH / 32) + c) * 32);
+                            p.sk_frag_o + (static_cast<int64_t>(fslot) * kSkFragRows + x * kTileM + r) * D + c * 32);
 #pragma unroll
                         for (int q = 0; q < 8; ++q)
                             dst[q] = make_float4(__uint_as_float(v[4 * q]) * inv_l, __uint_as_float(v[4 * q + 1]) * inv_l,
@@ -1768,7 +1742,7 @@ __global__ void __maxnreg__(96)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == 17) tmem_dealloc(tmem, kTmemCols);
+    if (warp == kMmaWarp2) tmem_dealloc(tmem, kTmemCols);
 }
 
 // Block-wide exclusive prefix sum of one value per thread (blockDim 1024);
