@@ -1123,18 +1123,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 5) tmem_dealloc(tmem, kTmemCols);
 }
 
-// barriers: q_ready, k_full[2], k_empty[2], v_full[3], v_empty[3], s_full[2], p_full[2], o_full[2]
-constexpr int kNumBars2 = 1 + 2 * kKStages + 2 * kVStages + 6;
+// barriers: q_ready, k_full[2], k_empty[2], v_full[3], v_empty[3], s_full[2], p_full[2], o_full[2],
+// mma_done
+constexpr int kNumBars2 = 1 + 2 * kKStages + 2 * kVStages + 7;
 
-#define PKV_W4(i) "r"(v[i + 0]), "r"(v[i + 1]), "r"(v[i + 2]), "r"(v[i + 3])
-// 16 consecutive 32-bit columns of this thread's lane
-__device__ __forceinline__ void tmem_store16(uint32_t taddr, const uint32_t (&v)[16]) {
-    asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
-        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};"
-        ::"r"(taddr), PKV_W4(0), PKV_W4(4), PKV_W4(8), PKV_W4(12) : "memory");
-}
-#undef PKV_W4
 __device__ __forceinline__ void tmem_store_wait() {
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
@@ -1391,6 +1383,7 @@ __global__ void __maxnreg__(kRegs2)
     uint64_t* s_full = v_empty + kVStages;  // [tile]
     uint64_t* p_full = s_full + 2;          // [tile]
     uint64_t* o_full = p_full + 2;          // [tile]
+    uint64_t* mma_done = o_full + 2;
     float* xch = reinterpret_cast<float*>(smem + SM::kXchOff);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + SM::kTmemSlotOff);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + SM::kFlagOff);
@@ -1410,6 +1403,7 @@ __global__ void __maxnreg__(kRegs2)
             mbar_init(&p_full[x], 4);  // one elected arrive per softmax warp of the tile
             mbar_init(&o_full[x], 1);
         }
+        mbar_init(mma_done, 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -1423,7 +1417,10 @@ __global__ void __maxnreg__(kRegs2)
     const uint32_t tmem = *tmem_slot;
     const uint32_t sbase = smem_u32(smem);
 
+    // a completed phase passes at once; a pending one gives up early once
+    // another thread of the CTA has timed out
     auto wait = [&](uint64_t* bar, uint32_t parity) -> bool {
+        if (mbar_try_wait(bar, parity)) return true;
         if (*abort_flag) return false;
         if (mbar_wait(bar, parity)) return true;
         *abort_flag = 1;
@@ -1486,30 +1483,36 @@ __global__ void __maxnreg__(kRegs2)
         }
     } else if (warp == kMmaWarp2) {
         // ============================== MMA ================================
+        // An MMA issue returns about when the previous MMA is done, so the
+        // pipe holds about one instruction: every wait and commit between two
+        // batches leaves it idle.  The waits for K and V tiles (normally long
+        // loaded) therefore sit inside a batch, after its fourth MMA, and each
+        // batch builds its two descriptors once (the start address field takes
+        // the offsets of its k-steps as plain additions).
         if (lane == 0) {
             constexpr uint32_t kIdescS = idesc_bf16(kTileM, kTileN, false);
             constexpr uint32_t kIdescO = idesc_bf16(kTileM, D, true);
-            auto issue_s = [&](int x, int gt) {
-                const uint32_t qa = sbase + SM::kQOff + x * TD::kTile;
-                const uint32_t kbse = sbase + SM::kKOff + (gt % kKStages) * TD::kTile;
+            auto nop = [] {};
+            auto issue_s = [&](int x, int gt, auto&& mid) {
+                const uint64_t da = sdesc_sw128(sbase + SM::kQOff + x * TD::kTile, 16, 1024);
+                const uint64_t db = sdesc_sw128(sbase + SM::kKOff + (gt % kKStages) * TD::kTile, 16, 1024);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
-                    umma_bf16(tmem + x * 256, sdesc_sw128(qa + off, 16, 1024),
-                              sdesc_sw128(kbse + off, 16, 1024), kIdescS, kk > 0);
+                    const uint32_t off = ((kk >> 2) * kHalfBytes + (kk & 3) * 32) >> 4;
+                    umma_bf16(tmem + x * 256, da + off, db + off, kIdescS, kk > 0);
+                    if (kk == 3) mid();
                 }
                 umma_commit(&s_full[x]);
             };
-            auto issue_pv = [&](int x, int gt, bool acc) {
-                const uint32_t vb = sbase + SM::kVOff + (gt % kVStages) * TD::kTile;
+            auto issue_pv = [&](int x, int gt, bool acc, auto&& mid) {
+                const uint64_t bd = sdesc_sw128(sbase + SM::kVOff + (gt % kVStages) * TD::kTile, kHalfBytes, 1024);
 #pragma unroll
                 for (int kk = 0; kk < kTileN / 16; ++kk) {
                     // A = P in tensor memory: the 128 keys packed in columns
                     // [0, 64); 16 keys = 8 columns per step
-                    const uint32_t pcol = kk * 8;
-                    const uint64_t bdesc = sdesc_sw128(vb + kk * 16 * 128, kHalfBytes, 1024);
-                    umma_bf16_ts(tmem + x * 256 + 128, tmem + x * 256 + pcol, bdesc, kIdescO,
-                                 (acc || kk > 0) ? 1u : 0u);
+                    umma_bf16_ts(tmem + x * 256 + 128, tmem + x * 256 + kk * 8, bd + ((kk * 16 * 128) >> 4),
+                                 kIdescO, (acc || kk > 0) ? 1u : 0u);
+                    if (kk == 3) mid();
                 }
             };
             SegIter<SK> it = it0;
@@ -1526,25 +1529,33 @@ __global__ void __maxnreg__(kRegs2)
                 ++qn;
                 if (!ok) break;
                 tc_fence_after();
-                issue_s(0, gt);
-                if (two) issue_s(1, gt);
+                bool dok = true;  // the K / V waits made inside batches
+                issue_s(0, gt, [&] {
+                    dok = wait(&v_full[gt % kVStages], (gt / kVStages) & 1);
+                    tc_fence_after();
+                });
+                if (two) issue_s(1, gt, nop);
                 umma_commit(&k_empty[gt % kKStages]);
-                for (int j = sg.j0; j < sg.j1; ++j, ++gt) {
+                for (int j = sg.j0; dok && j < sg.j1; ++j, ++gt) {
+                    // V(gt) was waited for inside the previous batch of tile A
                     const bool more = j + 1 < sg.j1;
-                    if (!wait(&p_full[0], na & 1) || !wait(&v_full[gt % kVStages], (gt / kVStages) & 1)) {
+                    if (!wait(&p_full[0], na & 1)) {
                         ok = false;
                         break;
                     }
                     ++na;
                     tc_fence_after();
-                    issue_pv(0, gt, j > sg.j0);
-                    if (more) {
-                        if (!wait(&k_full[(gt + 1) % kKStages], ((gt + 1) / kKStages) & 1)) {
-                            ok = false;
-                            break;
+                    issue_pv(0, gt, j > sg.j0, [&] {
+                        if (more) {
+                            dok = wait(&k_full[(gt + 1) % kKStages], ((gt + 1) / kKStages) & 1);
+                            tc_fence_after();
                         }
-                        tc_fence_after();
-                        issue_s(0, gt + 1);
+                    });
+                    if (more) {
+                        issue_s(0, gt + 1, [&] {
+                            dok = dok && wait(&v_full[(gt + 1) % kVStages], ((gt + 1) / kVStages) & 1);
+                            tc_fence_after();
+                        });
                     } else {
                         umma_commit(&o_full[0]);
                     }
@@ -1555,17 +1566,22 @@ __global__ void __maxnreg__(kRegs2)
                         }
                         ++nb;
                         tc_fence_after();
-                        issue_pv(1, gt, j > sg.j0);
+                        issue_pv(1, gt, j > sg.j0, nop);
                     }
                     umma_commit(&v_empty[gt % kVStages]);
                     if (more) {
-                        if (two) issue_s(1, gt + 1);
+                        if (two) issue_s(1, gt + 1, nop);
                         umma_commit(&k_empty[(gt + 1) % kKStages]);
                     } else if (two) {
                         umma_commit(&o_full[1]);
                     }
                 }
+                ok = ok && dok;
             }
+            // nothing of this thread's still runs in the tensor pipe when the
+            // CTA winds down (after a failed wait the last batch may be running)
+            umma_commit(mma_done);
+            if (!mbar_wait(mma_done, 0)) set_err(p.err, PKV_ERRBIT_TIMEOUT);
         }
     } else if (warp < 8) {
         // ============================ softmax ===============================
