@@ -63,8 +63,9 @@ struct TileDim {
     static constexpr int kPOff = kVOff + kVStages * kTile;
     static constexpr int kBarOff = kPOff + kPBytes;
 };
-// barriers: q_ready, k_full[2], k_empty[2], v_full[3], v_empty[3], s_full[2], p_full, p_free
-constexpr int kNumBars = 1 + 2 * kKStages + 2 * kVStages + 2 + 2;
+// barriers: q_ready, k_full[2], k_empty[2], v_full[3], v_empty[3], s_full[2], p_full, p_free,
+// mma_done
+constexpr int kNumBars = 1 + 2 * kKStages + 2 * kVStages + 2 + 2 + 1;
 template <int D>
 struct OneTileSmem {
     static constexpr int kTmemSlotOff = TileDim<D>::kBarOff + kNumBars * 8;
@@ -464,6 +465,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* s_full = v_empty + kVStages;
     uint64_t* p_full = s_full + 2;
     uint64_t* p_free = p_full + 1;
+    uint64_t* mma_done = p_free + 1;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + SM::kTmemSlotOff);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + SM::kFlagOff);
 
@@ -481,6 +483,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(&s_full[1], 1);
         mbar_init(p_full, kTileM);
         mbar_init(p_free, 1);
+        mbar_init(mma_done, 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -502,8 +505,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         g1 = (g0 + 31) / 32 * 32;
     };
 
-    // a wait that gives up marks the CTA aborted; later waits return at once
+    // a completed phase passes at once; a wait that gives up marks the CTA
+    // aborted, and later pending waits return at once
     auto wait = [&](uint64_t* bar, uint32_t parity) -> bool {
+        if (mbar_try_wait(bar, parity)) return true;
         if (*abort_flag) return false;
         if (mbar_wait(bar, parity)) return true;
         *abort_flag = 1;
@@ -562,45 +567,87 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp == 5) {
         // ============================== MMA ================================
+        // As in the two-tile kernel: an MMA issue returns about when the
+        // previous one is done, so the waits for K and V tiles sit inside a
+        // batch (after its fourth MMA) and each batch builds its descriptors once.
         if (lane == 0) {
             constexpr uint32_t kIdescS = idesc_bf16(kTileM, kTileN, false);  // K rows are K-major
             constexpr uint32_t kIdescO = idesc_bf16(kTileM, D, true);        // V rows are MN-major
             const uint32_t tmem_o = tmem + 256;
-            auto issue_s = [&](int j) -> bool {
+            const uint64_t dq = sdesc_sw128(sbase + TD::kQOff, 16, 1024);
+            // A = P (K-major over keys): the same layout and offsets as Q
+            const uint64_t dp = sdesc_sw128(sbase + TD::kPOff, 16, 1024);
+            auto issue_s = [&](int j, auto&& mid) {
                 const int s = j % kKStages;
-                if (!wait(&k_full[s], (j / kKStages) & 1)) return false;
-                tc_fence_after();
-                const uint32_t qa = sbase + TD::kQOff, kbse = sbase + TD::kKOff + s * TD::kTile;
+                const uint64_t db = sdesc_sw128(sbase + TD::kKOff + s * TD::kTile, 16, 1024);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
-                    umma_bf16(tmem + (j & 1) * 128, sdesc_sw128(qa + off, 16, 1024),
-                              sdesc_sw128(kbse + off, 16, 1024), kIdescS, kk > 0);
+                    const uint32_t off = ((kk >> 2) * kHalfBytes + (kk & 3) * 32) >> 4;
+                    umma_bf16(tmem + (j & 1) * 128, dq + off, db + off, kIdescS, kk > 0);
+                    if (kk == 3) mid();
                 }
                 umma_commit(&s_full[j & 1]);
                 umma_commit(&k_empty[s]);
+            };
+            const int nt = g.nt;
+            // a tile's barrier is probed inside the batch before it; if its
+            // copy has not landed, the batch goes on and the wait comes after
+            bool ready = false;
+            auto probe = [&](uint64_t* bar, uint32_t parity) {
+                ready = mbar_test(bar, parity);
+                if (ready) tc_fence_after();
+            };
+            auto settle = [&](uint64_t* bar, uint32_t parity) -> bool {
+                if (ready) return true;
+                if (!wait(bar, parity)) return false;
+                tc_fence_after();
                 return true;
             };
-            bool ok = wait(q_ready, 0);
-            if (ok) ok = issue_s(0);
-            if (ok && g.nt > 1) ok = issue_s(1);
-            for (int j = 0; ok && j < g.nt; ++j) {
-                if (!wait(p_full, j & 1) || !wait(&v_full[j % kVStages], (j / kVStages) & 1)) break;
+            bool ok = wait(q_ready, 0) && wait(&k_full[0], 0);
+            if (ok) {
                 tc_fence_after();
-                const uint32_t pa = sbase + TD::kPOff;
-                const uint32_t vb = sbase + TD::kVOff + (j % kVStages) * TD::kTile;
+                issue_s(0, [&] {
+                    if (nt > 1) probe(&k_full[1 % kKStages], (1 / kKStages) & 1);
+                });
+                if (nt > 1) {
+                    ok = settle(&k_full[1 % kKStages], (1 / kKStages) & 1);
+                    if (ok) issue_s(1, [&] { probe(&v_full[0], 0); });
+                } else {
+                    ready = false;
+                }
+                ok = ok && settle(&v_full[0], 0);
+            }
+            for (int j = 0; ok && j < nt; ++j) {
+                // V_j was waited for inside an earlier batch
+                if (!wait(p_full, j & 1)) break;
+                tc_fence_after();
+                const bool s_next = j + 2 < nt;
+                const uint64_t bd = sdesc_sw128(sbase + TD::kVOff + (j % kVStages) * TD::kTile, kHalfBytes, 1024);
 #pragma unroll
                 for (int kk = 0; kk < kTileN / 16; ++kk) {
                     // A = P (K-major over keys), B = V (rows = keys, columns = dims: MN-major);
                     // the two 64-column halves of V are LBO apart, 8-key groups SBO apart
-                    const uint64_t a = sdesc_sw128(pa + (kk >> 2) * kHalfBytes + (kk & 3) * 32, 16, 1024);
-                    const uint64_t bdesc = sdesc_sw128(vb + kk * 16 * 128, kHalfBytes, 1024);
-                    umma_bf16(tmem_o, a, bdesc, kIdescO, (j > 0 || kk > 0) ? 1u : 0u);
+                    const uint32_t offp = ((kk >> 2) * kHalfBytes + (kk & 3) * 32) >> 4;
+                    umma_bf16(tmem_o, dp + offp, bd + ((kk * 16 * 128) >> 4), kIdescO, (j > 0 || kk > 0) ? 1u : 0u);
+                    if (kk == 3 && s_next) probe(&k_full[(j + 2) % kKStages], ((j + 2) / kKStages) & 1);
                 }
                 umma_commit(&v_empty[j % kVStages]);
                 umma_commit(p_free);
-                if (j + 2 < g.nt && !issue_s(j + 2)) break;
+                const bool v_next = j + 1 < nt;
+                if (s_next) {
+                    if (!settle(&k_full[(j + 2) % kKStages], ((j + 2) / kKStages) & 1)) break;
+                    issue_s(j + 2, [&] {
+                        if (v_next) probe(&v_full[(j + 1) % kVStages], ((j + 1) / kVStages) & 1);
+                    });
+                } else {
+                    ready = false;
+                }
+                if (v_next && !settle(&v_full[(j + 1) % kVStages], ((j + 1) / kVStages) & 1)) break;
             }
+            // nothing of this thread's still runs in the tensor pipe when the
+            // CTA winds down (after a failed wait the last batch may be running)
+            umma_commit(mma_done);
+            if (!mbar_wait(mma_done, 0)) set_err(p.err, PKV_ERRBIT_TIMEOUT);
         }
     } else {
         // ============================ softmax ===============================
@@ -1515,6 +1562,19 @@ __global__ void __maxnreg__(kRegs2)
                     if (kk == 3) mid();
                 }
             };
+            // a tile's barrier is probed inside the batch before it; if its copy
+            // has not landed, the batch goes on and the wait comes after
+            bool ready = false;
+            auto probe = [&](uint64_t* bar, uint32_t parity) {
+                ready = mbar_test(bar, parity);
+                if (ready) tc_fence_after();
+            };
+            auto settle = [&](uint64_t* bar, uint32_t parity) -> bool {
+                if (ready) return true;
+                if (!wait(bar, parity)) return false;
+                tc_fence_after();
+                return true;
+            };
             SegIter<SK> it = it0;
             Seg sg;
             int gt = 0;          // K/V tiles consumed (ring position)
@@ -1529,15 +1589,12 @@ __global__ void __maxnreg__(kRegs2)
                 ++qn;
                 if (!ok) break;
                 tc_fence_after();
-                bool dok = true;  // the K / V waits made inside batches
-                issue_s(0, gt, [&] {
-                    dok = wait(&v_full[gt % kVStages], (gt / kVStages) & 1);
-                    tc_fence_after();
-                });
+                issue_s(0, gt, [&] { probe(&v_full[gt % kVStages], (gt / kVStages) & 1); });
                 if (two) issue_s(1, gt, nop);
                 umma_commit(&k_empty[gt % kKStages]);
-                for (int j = sg.j0; dok && j < sg.j1; ++j, ++gt) {
-                    // V(gt) was waited for inside the previous batch of tile A
+                ok = settle(&v_full[gt % kVStages], (gt / kVStages) & 1);
+                for (int j = sg.j0; ok && j < sg.j1; ++j, ++gt) {
+                    // V(gt) has landed (settled at the end of the previous step)
                     const bool more = j + 1 < sg.j1;
                     if (!wait(&p_full[0], na & 1)) {
                         ok = false;
@@ -1546,15 +1603,15 @@ __global__ void __maxnreg__(kRegs2)
                     ++na;
                     tc_fence_after();
                     issue_pv(0, gt, j > sg.j0, [&] {
-                        if (more) {
-                            dok = wait(&k_full[(gt + 1) % kKStages], ((gt + 1) / kKStages) & 1);
-                            tc_fence_after();
-                        }
+                        if (more) probe(&k_full[(gt + 1) % kKStages], ((gt + 1) / kKStages) & 1);
                     });
                     if (more) {
+                        if (!settle(&k_full[(gt + 1) % kKStages], ((gt + 1) / kKStages) & 1)) {
+                            ok = false;
+                            break;
+                        }
                         issue_s(0, gt + 1, [&] {
-                            dok = dok && wait(&v_full[(gt + 1) % kVStages], ((gt + 1) / kVStages) & 1);
-                            tc_fence_after();
+                            probe(&v_full[(gt + 1) % kVStages], ((gt + 1) / kVStages) & 1);
                         });
                     } else {
                         umma_commit(&o_full[0]);
@@ -1572,11 +1629,14 @@ __global__ void __maxnreg__(kRegs2)
                     if (more) {
                         if (two) issue_s(1, gt + 1, nop);
                         umma_commit(&k_empty[(gt + 1) % kKStages]);
+                        if (!settle(&v_full[(gt + 1) % kVStages], ((gt + 1) / kVStages) & 1)) {
+                            ok = false;
+                            break;
+                        }
                     } else if (two) {
                         umma_commit(&o_full[1]);
                     }
                 }
-                ok = ok && dok;
             }
             // nothing of this thread's still runs in the tensor pipe when the
             // CTA winds down (after a failed wait the last batch may be running)
