@@ -147,29 +147,6 @@ __device__ __forceinline__ void tmem_load128(uint32_t taddr, uint32_t (&v)[128])
           PKV_R8(112), PKV_R8(120)
         : "r"(taddr), "r"(taddr + 32), "r"(taddr + 64), "r"(taddr + 96) : "memory");
 }
-// 128 consecutive 32-bit columns like tmem_load128, with the maximum of each
-// 32-column load reduced on the way (tcgen05.ld.red, f32 max) into m[0..3]
-__device__ __forceinline__ void tmem_load128_max(uint32_t taddr, uint32_t (&v)[128], float (&m)[4]) {
-    asm volatile(
-        "tcgen05.ld.red.sync.aligned.32x32b.x32.max.f32 "
-        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
-        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, %128, [%132];\n\t"
-        "tcgen05.ld.red.sync.aligned.32x32b.x32.max.f32 "
-        "{%32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, "
-        "%48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63}, %129, [%133];\n\t"
-        "tcgen05.ld.red.sync.aligned.32x32b.x32.max.f32 "
-        "{%64, %65, %66, %67, %68, %69, %70, %71, %72, %73, %74, %75, %76, %77, %78, %79, "
-        "%80, %81, %82, %83, %84, %85, %86, %87, %88, %89, %90, %91, %92, %93, %94, %95}, %130, [%134];\n\t"
-        "tcgen05.ld.red.sync.aligned.32x32b.x32.max.f32 "
-        "{%96, %97, %98, %99, %100, %101, %102, %103, %104, %105, %106, %107, %108, %109, %110, "
-        "%111, %112, %113, %114, %115, %116, %117, %118, %119, %120, %121, %122, %123, %124, %125, "
-        "%126, %127}, %131, [%135];\n\t"
-        "tcgen05.wait::ld.sync.aligned;"
-        : PKV_R8(0), PKV_R8(8), PKV_R8(16), PKV_R8(24), PKV_R8(32), PKV_R8(40), PKV_R8(48),
-          PKV_R8(56), PKV_R8(64), PKV_R8(72), PKV_R8(80), PKV_R8(88), PKV_R8(96), PKV_R8(104),
-          PKV_R8(112), PKV_R8(120), "=f"(m[0]), "=f"(m[1]), "=f"(m[2]), "=f"(m[3])
-        : "r"(taddr), "r"(taddr + 32), "r"(taddr + 64), "r"(taddr + 96) : "memory");
-}
 #undef PKV_R8
 #define PKV_W8(i) "r"(v[i + 0]), "r"(v[i + 1]), "r"(v[i + 2]), "r"(v[i + 3]), \
                   "r"(v[i + 4]), "r"(v[i + 5]), "r"(v[i + 6]), "r"(v[i + 7])
@@ -1712,25 +1689,22 @@ __global__ void __maxnreg__(kRegs2)
                 const int key0 = g.kb + j * kTileN;
                 if (warp_live) {
                     uint32_t sv[kTileN];  // this row's scores (f32 bits), then its packed P
-                    float part[4];        // maxima of the four 32-column loads
-                    tmem_load128_max(lane_addr, sv, part);
-                    float mraw = fmaxf(fmax3(part[0], part[1], part[2]), part[3]);
+                    tmem_load128(lane_addr, sv);
                     const int nvis = limit - key0;  // keys past it are masked (diagonal tiles only)
                     if (__any_sync(0xffffffffu, nvis < kTileN)) {
-                        // the loads' maxima include keys the row does not see
 #pragma unroll
                         for (int e = 0; e < kTileN; ++e) sv[e] = e < nvis ? sv[e] : __float_as_uint(-INFINITY);
-                        float a[8];
-#pragma unroll
-                        for (int q = 0; q < 8; ++q) a[q] = __uint_as_float(sv[q]);
-#pragma unroll
-                        for (int e = 8; e < kTileN; e += 16) {
-#pragma unroll
-                            for (int q = 0; q < 8; ++q)
-                                a[q] = fmax3(a[q], __uint_as_float(sv[e + q]), __uint_as_float(sv[e + 8 + q]));
-                        }
-                        mraw = fmax3(fmax3(a[0], a[1], a[2]), fmax3(a[3], a[4], a[5]), fmaxf(a[6], a[7]));
                     }
+                    float a[8];
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) a[q] = __uint_as_float(sv[q]);
+#pragma unroll
+                    for (int e = 8; e < kTileN; e += 16) {
+#pragma unroll
+                        for (int q = 0; q < 8; ++q)
+                            a[q] = fmax3(a[q], __uint_as_float(sv[e + q]), __uint_as_float(sv[e + 8 + q]));
+                    }
+                    const float mraw = fmax3(fmax3(a[0], a[1], a[2]), fmax3(a[3], a[4], a[5]), fmaxf(a[6], a[7]));
                     const float mx = mraw * p.scale_log2;
                     float alpha = 1.f;
                     if (mx > m_used + kLazyRescale) {   // also true the first time a key is visible
