@@ -1200,8 +1200,7 @@ struct TwoTileSmem {
     static constexpr int kKOff = kQOff + 2 * kTile;
     static constexpr int kVOff = kKOff + kKStages * kTile;
     static constexpr int kBarOff = kVOff + kVStages * kTile;
-    static constexpr int kXchOff = kBarOff + kNumBars2 * 8;  // float [2 tiles][2 halves][128 rows]
-    static constexpr int kTmemSlotOff = kXchOff + 2 * 2 * kTileM * 4;
+    static constexpr int kTmemSlotOff = kBarOff + kNumBars2 * 8;
     static constexpr int kFlagOff = kTmemSlotOff + 8;
     static constexpr int kBytes = kFlagOff + 16;
     static_assert(kBytes <= 227 * 1024, "shared memory per CTA");
@@ -1408,7 +1407,6 @@ __global__ void __maxnreg__(kRegs2)
     uint64_t* p_full = s_full + 2;          // [tile]
     uint64_t* o_full = p_full + 2;          // [tile]
     uint64_t* mma_done = o_full + 2;
-    float* xch = reinterpret_cast<float*>(smem + SM::kXchOff);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + SM::kTmemSlotOff);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + SM::kFlagOff);
 
