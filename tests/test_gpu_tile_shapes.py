@@ -113,3 +113,25 @@ def test_head_dim_64_page_permutation_bit_identical():
     out2, lse2, *_ = gpu_step(c2)
     assert torch.equal(out1.cpu(), out2.cpu())
     assert torch.equal(lse1.cpu(), lse2.cpu())
+
+
+def test_head_dim_64_two_tile_after_grouped_launches():
+    """Kernels run before a tile call leave their data in shared and tensor
+    memory.  A reducing tensor-memory load once let rows of a warp that also held
+    padding rows come out as zero with LSE -inf after the shared-prefix planner and
+    grouped launches had run (the suite's file order exposed it).  The same
+    sequence in one test: those launches, then every head-dim-64 two-tile case."""
+    import itertools
+    import test_gpu_plan as tp
+    for seed in range(6):
+        tp.test_plan_matches_oracle_random(seed)
+    tp.test_plan_matches_oracle_edge_cases()
+    for q_len, heads in itertools.product([1, 4, 16], [(32, 8), (8, 8), (16, 1)]):
+        tp.test_fused_shared_prefix_small(q_len, heads)
+    tp.test_fused_nan_in_unused_slots_and_random_batches()
+    for q_len in (1, 4):
+        tp.test_fused_shared_prefix_full_size(q_len)
+    tp.test_fused_shared_prefix_graph_replay()
+    for (mask, cb), (hq, hkv) in itertools.product([("causal", 0), ("block_causal", 77), ("none", 0)],
+                                                   [(16, 4), (8, 8), (32, 2)]):
+        test_head_dim_64_two_tile(mask, cb, hq, hkv)
