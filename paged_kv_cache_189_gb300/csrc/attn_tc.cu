@@ -9,7 +9,14 @@
 // output + LSE for the merge).  Prefill, block-causal and shared-prefix tiles
 // are dense contractions: enough query rows share each K/V page.
 //
-// One CTA = one tile of 128 query rows packed as (token, grouped head): token
+// Two kernels: the one-tile kernel described next (sequences whose rows fit
+// one tile, grouped shared-prefix tiles, rows held four times for few rows),
+// and the two-tile kernel further down (two 128-row tiles per CTA sharing
+// every K/V tile, for sequences with more rows).  Both issue their MMAs from
+// one lane in batches of eight with the next K/V tile's barrier probed inside
+// a batch.
+//
+// One-tile kernel: one CTA = one tile of 128 query rows packed as (token, grouped head): token
 // t0 + r / G, query head kvh * G + r % G for tensor-memory lane r, so the G
 // query heads that share a K/V head share every K/V load.  Keys are walked in
 // tiles of 128 (four 32-token pages) within the CTA's key split.
