@@ -157,6 +157,9 @@ def visible_keys(i: int, q_real: int, kv_len: int, mask: str, causal_block: int)
       before this step's tokens plus every new token up to the end of its
       block.  READING: a last, shorter block when q_real is not a multiple.
     * padding rows (``i >= q_real``) see nothing ([VG] seq_len bullet).
+    * READING: with more new tokens than keys (``q_real > kv_len``) the first
+      positions fall below key 0; a row whose last visible position is below 0
+      sees no key (count 0).
     """
     if i >= q_real:
         return 0
@@ -164,11 +167,11 @@ def visible_keys(i: int, q_real: int, kv_len: int, mask: str, causal_block: int)
     if mask == MASK_NONE:
         return kv_len
     if mask == MASK_CAUSAL:
-        return first_new + i + 1
+        return max(0, first_new + i + 1)
     if mask == MASK_BLOCK_CAUSAL:
         assert causal_block > 0
         block_end = (i // causal_block + 1) * causal_block
-        return first_new + min(q_real, block_end)
+        return max(0, first_new + min(q_real, block_end))
     raise ValueError(mask)
 
 
