@@ -79,8 +79,12 @@ def assert_attention_close(out, lse, O, L, case, rows=None):
         assert diff.mean() <= O_MEAN_ABS, f"mean abs {diff.mean():.3e}"
         if lse is not None:
             gl = lse.cpu().numpy().astype(np.float64)
-            dl = np.abs(gl[r_sel] - L[r_sel])
-            assert dl.max() <= LSE_MAX_ABS, f"lse max abs {dl.max():.3e}"
+            # real rows with an empty visible set: exactly -inf (and zero output)
+            none = np.isneginf(L[r_sel])
+            assert np.isneginf(gl[r_sel][none]).all(), "empty visible set must give LSE -inf"
+            assert (got[r_sel][none] == 0).all(), "empty visible set must give zero output"
+            dl = np.abs(gl[r_sel][~none] - L[r_sel][~none])
+            assert dl.size == 0 or dl.max() <= LSE_MAX_ABS, f"lse max abs {dl.max():.3e}"
     if len(p_sel):
         assert (got[p_sel] == 0).all(), "padding rows must be zero"
         if lse is not None:
