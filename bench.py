@@ -990,14 +990,17 @@ def measure(plan, name, args, rank, world, local, dev, stream, dist):
         del graph
 
     # ---- end to end through the public API: pinned host inputs -> device,
-    #      the whole step, result read back to the host, every step.
-    #      The host runs one step ahead, as a serving loop does: it enqueues
-    #      step i (inputs copied in, the step, the result copied into one of
-    #      two pinned buffers) and then waits for step i - 1's result.
-    #      A step's inputs travel as one copy: one pinned host buffer holds them
-    #      all (each at a 256-byte aligned offset) and the step's device input
-    #      tensors are rebound to views of one device buffer of the same
-    #      layout; the results (output and LSE) likewise come back as one copy.
+    #      the whole step, result read back to the host, every step, as a
+    #      pipelined serving loop.  A step's inputs travel as one copy (one
+    #      pinned host buffer holds them all, each at a 256-byte aligned offset)
+    #      into one of two device staging buffers on an input copy stream while
+    #      the previous step runs; the step copies them on the device into the
+    #      buffer its input tensors are views of, runs, and copies its results
+    #      (output and LSE, likewise packed) into one of two device staging
+    #      buffers, which an output copy stream brings to one of two pinned
+    #      host buffers while the next step runs.  The host stays one step
+    #      ahead: it waits for step i - 1's result on the host after enqueueing
+    #      step i.  Every copy of every step lies inside the timed region.
     e2e_value = None
     srcs, dsts = plan.h2d
     d_in, in_offs = packed_device(dsts, dev)
@@ -1007,27 +1010,58 @@ def measure(plan, name, args, rank, world, local, dev, stream, dist):
         h_in[o:o + n].copy_(x.contiguous().view(-1).view(torch.uint8))
     d_out, _ = packed_device(plan.d2h, dev)
     h_out = [torch.empty(d_out.numel(), dtype=torch.uint8).pin_memory() for _ in range(2)]
+    in_stage = [torch.empty_like(d_in) for _ in range(2)]
+    out_stage = [torch.empty_like(d_out) for _ in range(2)]
     h2d = h_in.numel()
     d2h = d_out.numel()
-    done = [torch.cuda.Event(), torch.cuda.Event()]
+    in_stream = torch.cuda.Stream(device=dev)
+    out_stream = torch.cuda.Stream(device=dev)
+    staged = [torch.cuda.Event() for _ in range(2)]     # inputs of a step are on the device
+    consumed = [torch.cuda.Event() for _ in range(2)]   # a step took its inputs and left its results
+    on_host = [torch.cuda.Event() for _ in range(2)]    # a step's results are on the host
 
-    def e2e_steps(n):
+    def e2e_steps(n, start=None):
+        # copy stream order: inputs of steps 0 and 1, then results of step i
+        # before inputs of step i + 2 (whose staging buffer step i frees)
+        def bring_in(i):
+            with torch.cuda.stream(in_stream):
+                if i >= 2:
+                    in_stream.wait_event(consumed[i % 2])
+                in_stage[i % 2].copy_(h_in, non_blocking=True)
+                staged[i % 2].record(in_stream)
+        if start is not None:
+            in_stream.wait_event(start)
+            out_stream.wait_event(start)
+        bring_in(0)
+        if n > 1:
+            bring_in(1)
         for i in range(n):
             with torch.cuda.stream(stream):
-                d_in.copy_(h_in, non_blocking=True)
+                stream.wait_event(staged[i % 2])
+                d_in.copy_(in_stage[i % 2], non_blocking=True)
                 step()
-                h_out[i % 2].copy_(d_out, non_blocking=True)
-                done[i % 2].record(stream)
+                if i >= 2:
+                    stream.wait_event(on_host[i % 2])  # step i - 2's results have left
+                out_stage[i % 2].copy_(d_out, non_blocking=True)
+                consumed[i % 2].record(stream)
+            with torch.cuda.stream(out_stream):
+                out_stream.wait_event(consumed[i % 2])
+                h_out[i % 2].copy_(out_stage[i % 2], non_blocking=True)
+                on_host[i % 2].record(out_stream)
+            if i + 2 < n:
+                bring_in(i + 2)
             if i >= 1:
-                done[(i - 1) % 2].synchronize()  # step i - 1's result is on the host
-        done[(n - 1) % 2].synchronize()
+                on_host[(i - 1) % 2].synchronize()  # step i - 1's result is on the host
+        on_host[(n - 1) % 2].synchronize()
+        stream.wait_event(on_host[(n - 1) % 2])
 
     if args.e2e_steps > 0:
         e2e_steps(3)
         barrier(dist)
+        torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        e2e_steps(args.e2e_steps)
+        e2e_steps(args.e2e_steps, start=e0)
         e1.record(stream)
         torch.cuda.synchronize()
         e2e_ms = max_over_ranks(dist, e0.elapsed_time(e1), dev)
@@ -1051,7 +1085,11 @@ def measure(plan, name, args, rank, world, local, dev, stream, dist):
                      "peak_source": plan.peak_src},
         "clocks": clk,
         "e2e": {"value": e2e_value, "unit": plan.unit, "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "steps": args.e2e_steps},
+                "d2h_bytes_per_step": d2h, "steps": args.e2e_steps,
+                "loop": "pipelined: each step's inputs copied in (one pinned buffer, one copy) "
+                        "while the previous step runs and its results copied out while the "
+                        "next one runs, on two copy streams through double-buffered device "
+                        "staging; the host waits for each step's result one step behind"},
         "gpu_launches": plan.launches * args.steps,
         "aux": aux_out,
     }
