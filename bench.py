@@ -360,6 +360,12 @@ def measured_tensor_peak():
     return 1900.0, "fallback"
 
 
+# End to end: steps that move at least this many bytes between host and device
+# overlap their copies with the neighbouring steps (copy streams); smaller ones
+# keep them on the compute stream.
+PIPELINE_MIN_BYTES = 256 * 1024
+
+
 def committed_traffic(workload, kernel_sources):
     """DRAM bytes per launch from a committed ncu summary, valid only while the
     kernel's sources are unchanged (hash recorded beside the figure)."""
@@ -1001,6 +1007,10 @@ def measure(plan, name, args, rank, world, local, dev, stream, dist):
     #      host buffers while the next step runs.  The host stays one step
     #      ahead: it waits for step i - 1's result on the host after enqueueing
     #      step i.  Every copy of every step lies inside the timed region.
+    #      A step that moves under PIPELINE_MIN_BYTES keeps the copies on the
+    #      compute stream instead: there the pipelined loop's extra host calls
+    #      cost more than the copies it hides (the tiny decode step is
+    #      host-bound).
     e2e_value = None
     srcs, dsts = plan.h2d
     d_in, in_offs = packed_device(dsts, dev)
@@ -1020,7 +1030,22 @@ def measure(plan, name, args, rank, world, local, dev, stream, dist):
     consumed = [torch.cuda.Event() for _ in range(2)]   # a step took its inputs and left its results
     on_host = [torch.cuda.Event() for _ in range(2)]    # a step's results are on the host
 
+    pipelined = h2d + d2h >= PIPELINE_MIN_BYTES
+
+    def e2e_serial(n, start=None):
+        for i in range(n):
+            with torch.cuda.stream(stream):
+                d_in.copy_(h_in, non_blocking=True)
+                step()
+                h_out[i % 2].copy_(d_out, non_blocking=True)
+                on_host[i % 2].record(stream)
+            if i >= 1:
+                on_host[(i - 1) % 2].synchronize()
+        on_host[(n - 1) % 2].synchronize()
+
     def e2e_steps(n, start=None):
+        if not pipelined:
+            return e2e_serial(n, start)
         # copy stream order: inputs of steps 0 and 1, then results of step i
         # before inputs of step i + 2 (whose staging buffer step i frees)
         def bring_in(i):
@@ -1086,10 +1111,14 @@ def measure(plan, name, args, rank, world, local, dev, stream, dist):
         "clocks": clk,
         "e2e": {"value": e2e_value, "unit": plan.unit, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": args.e2e_steps,
-                "loop": "pipelined: each step's inputs copied in (one pinned buffer, one copy) "
-                        "while the previous step runs and its results copied out while the "
-                        "next one runs, on two copy streams through double-buffered device "
-                        "staging; the host waits for each step's result one step behind"},
+                "loop": ("pipelined: each step's inputs copied in (one pinned buffer, one copy) "
+                         "while the previous step runs and its results copied out while the "
+                         "next one runs, on two copy streams through double-buffered device "
+                         "staging; the host waits for each step's result one step behind"
+                         if pipelined else
+                         "serial: each step's inputs copied in (one copy), the step, its results "
+                         "copied out (one copy), all on the compute stream; the host waits for "
+                         "each step's result one step behind")},
         "gpu_launches": plan.launches * args.steps,
         "aux": aux_out,
     }
