@@ -264,6 +264,79 @@ __global__ void __launch_bounds__(kPlanThreads) decode_plan_kernel(const AttnPar
     if (tid == 0) *sc.total = full_units + (partials + n_empty) * Hkv;
 }
 
+// The same order for a small batch (B <= kSmallPlanSeqs sequences, fewer than
+// kSmallPlanSplits full splits each), one thread per sequence and exact ranks
+// instead of counting passes: four warps and three barriers instead of 32 warps
+// and a dozen.  Sequence b with f full splits and a partial split of r keys:
+//  * its full split s < f is unit Hkv * (P(s) + rank_f(b)) + h, where P(s) =
+//    sum over all sequences of min(f, s) (the units of the splits before s) and
+//    rank_f(b) = #{sequences with more full splits, or as many and a lower
+//    index} -- exactly the sequences ahead of b among those with a split s;
+//  * its partial split follows every full one, at rank_r(b) = #{sequences with
+//    a longer partial split, or as long and a lower index};
+//  * a row without keys (split 0, zeros) follows every partial split.
+constexpr int kSmallPlanSeqs = 128;
+constexpr int kSmallPlanSplits = 64;
+
+__global__ void __launch_bounds__(kSmallPlanSeqs) decode_plan_small_kernel(const AttnParams p) {
+    __shared__ int2 s_fr[kSmallPlanSeqs];        // (full splits, partial keys); f = -1: no rows
+    __shared__ int s_cnt[kSmallPlanSplits];      // sequences per full-split count
+    __shared__ int s_p[kSmallPlanSplits];        // P(s)
+    __shared__ int s_tot[3];                     // full seq-splits, partial splits, empty rows
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    const int B = p.batch, Hkv = p.num_kv_heads, SK = p.split_keys;
+    const int t = threadIdx.x;
+    const Sched sc(p.ws_counters, B, Hkv);
+    for (int i = t; i <= B * Hkv; i += kSmallPlanSeqs) sc.counters[i] = 0;
+    if (t < kSmallPlanSplits) s_cnt[t] = 0;
+    if (t < 3) s_tot[t] = 0;
+    const int kv = t < B ? row_keys(p, t) : -1;
+    const int f = kv > 0 ? kv / SK : 0;
+    const int r = kv > 0 ? kv - f * SK : 0;
+    s_fr[t] = make_int2(kv >= 0 ? f : -1, r);
+    __syncthreads();
+    if (kv >= 0) {
+        atomicAdd(&s_cnt[f], 1);
+        if (f > 0) atomicAdd(&s_tot[0], f);
+        if (r > 0) atomicAdd(&s_tot[1], 1);
+        if (kv == 0) atomicAdd(&s_tot[2], 1);
+    }
+    __syncthreads();
+    if (t < kSmallPlanSplits) {
+        int acc = 0;
+        for (int v = 1; v < kSmallPlanSplits; ++v) acc += s_cnt[v] * min(v, t);
+        s_p[t] = acc;
+    }
+    // ranks among the batch (ties by index)
+    int rank_f = 0, rank_r = 0, rank_e = 0;
+    for (int o = 0; o < B; ++o) {
+        const int2 x = s_fr[o];
+        rank_f += (x.x > f || (x.x == f && o < t)) ? 1 : 0;
+        rank_r += (x.y > r || (x.y == r && o < t)) ? 1 : 0;
+        rank_e += (x.x == 0 && x.y == 0 && o < t) ? 1 : 0;
+    }
+    __syncthreads();
+    const int full_units = s_tot[0] * Hkv, partials = s_tot[1], empty = s_tot[2];
+    if (kv >= 0) {
+        // rank_e counted the earlier entries (0, 0): rows without keys
+        // (sequences without rows carry f = -1)
+        for (int s = 0; s < f; ++s) {
+            const int u = Hkv * (s_p[s] + rank_f);
+            for (int h = 0; h < Hkv; ++h) sc.list[u + h] = make_int2(s, t * Hkv + h);
+        }
+        int at = -1, split = 0;
+        if (r > 0) {
+            at = full_units + rank_r * Hkv;
+            split = f;
+        } else if (kv == 0) {
+            at = full_units + (partials + rank_e) * Hkv;
+        }
+        if (at >= 0)
+            for (int h = 0; h < Hkv; ++h) sc.list[at + h] = make_int2(split, t * Hkv + h);
+    }
+    if (t == 0) *sc.total = full_units + (partials + empty) * Hkv;
+}
+
 __device__ __forceinline__ void consumer_sync() {
     asm volatile("bar.sync 1, %0;" ::"r"(kWarps * 32) : "memory");
 }
@@ -800,7 +873,10 @@ cudaError_t launch_dg(const AttnParams& p_in, const void* tk, const void* tv, in
     AttnParams p = p_in;
     p.planned = units > grid && plan_fits(p);
     if (p.planned) {
-        decode_plan_kernel<<<1, kPlanThreads, 0, s>>>(p);
+        if (p.batch <= kSmallPlanSeqs && p.max_kv_len / p.split_keys < kSmallPlanSplits)
+            decode_plan_small_kernel<<<1, kSmallPlanSeqs, 0, s>>>(p);
+        else
+            decode_plan_kernel<<<1, kPlanThreads, 0, s>>>(p);
         e = cudaGetLastError();
     } else {
         e = cudaMemsetAsync(p.ws_counters, 0, Sched::counters_bytes(p.batch, p.num_kv_heads), s);

@@ -203,3 +203,80 @@ def test_gqa_decode_full_size():
     O, L, *_ = oracle_step(c)
     assert err == 0
     assert_attention_close(out, lse, O, L, c)
+
+
+def _planned_units(ws, B, Hkv):
+    """The decode scheduling region at the start of the workspace: the unit
+    count after the ticket and split counters, then the unit list of (split,
+    sequence * Hkv + head) pairs after the sequence order."""
+    a256 = lambda n: -(-n // 256) * 256
+    raw = ws.cpu().numpy()
+    off_total = a256((B * Hkv + 1) * 4)
+    total = int(raw[off_total:off_total + 4].view(np.int32)[0])
+    off_list = off_total + 256 + a256(B * 4)
+    lst = raw[off_list:off_list + total * 8].view(np.int32).reshape(total, 2)
+    return total, lst
+
+
+@pytest.mark.parametrize("B", [96, 128, 200])
+def test_decode_planned_unit_order(B):
+    """The planned order itself, read back from the workspace: every unit once;
+    the full splits first, split-major, sequences with more full splits first;
+    then the partial last splits, longest first (exactly up to 128 sequences,
+    by 1/1024-split buckets above); then the rows without keys.  Outputs
+    against the oracle as well."""
+    rng = np.random.default_rng(53 + B)
+    Hq, Hkv, D = 32, 8, 128
+    kv = rng.integers(1, 7000, size=B, endpoint=True)
+    kv[5] = 7000                              # the longest row fixes the split size
+    sk = pkv.plan_attention(B, 1, Hq, Hkv, D, 7000)["split_keys"]
+    assert sk < 7000
+    kv[0:5] = [sk, 7000 // sk * sk, 1, sk + 1, sk - 1]   # split boundaries, one key
+    kv[40:43] = 1234                          # equal lengths
+    q_rows = np.ones(B, dtype=np.int64)
+    q_real = np.ones(B, dtype=np.int64)
+    q_rows[[10, 11]] = 0
+    q_real[[10, 11]] = 0                      # sequences without rows
+    q_real[[20, 21, 22]] = 0                  # rows without keys
+    c = wl.build_pool_case("unit_order", 53 + B, kv, q_rows, q_real, Hq, Hkv, D, mask="causal")
+    plan = pkv.plan_attention(B, 1, Hq, Hkv, D, c.max_kv_len)
+    assert plan["kernel"] == pkv.PKV_KERNEL_DECODE and plan["split_keys"] == sk
+    k_pool, v_pool = c.k_pool.to(DEV), c.v_pool.to(DEV)
+    pkv.kv_scatter_slots(c.new_k.to(DEV), c.new_v.to(DEV), c.slots.to(DEV), k_pool, v_pool)
+    out = torch.full((B, Hq, D), float("nan"), dtype=torch.bfloat16, device=DEV)
+    lse = torch.full((B, Hq), float("nan"), device=DEV)
+    ws = torch.zeros(plan["workspace_bytes"], dtype=torch.uint8, device=DEV)
+    pkv.paged_attention(c.q.to(DEV), k_pool, v_pool, c.block_table.to(DEV), c.kv_lens.to(DEV),
+                        c.q_indptr.to(DEV), out, q_real=c.q_real.to(DEV), lse=lse, max_q_rows=1,
+                        max_kv_len=c.max_kv_len, workspace=ws)
+    torch.cuda.synchronize()
+    O, L, *_ = oracle_step(c)
+    assert_attention_close(out, lse, O, L, c)
+
+    # the units of the call: keys per row (0 for a row without keys; none for a
+    # sequence without rows), cut into splits of sk keys
+    keys = {b: (int(kv[b]) if q_real[b] > 0 else 0) for b in range(B) if q_rows[b] > 0}
+    expect = set()
+    for b, n in keys.items():
+        for h in range(Hkv):
+            for s in range(max(1, -(-n // sk))):
+                expect.add((s, b * Hkv + h))
+    total, lst = _planned_units(ws, B, Hkv)
+    got = [tuple(int(v) for v in e) for e in lst]
+    assert total == len(expect) and len(set(got)) == total and set(got) == expect
+
+    f = {b: n // sk for b, n in keys.items()}
+    r = {b: n % sk for b, n in keys.items()}
+    kind = []
+    for s, bh in got:
+        b = bh // Hkv
+        kind.append(0 if s < f[b] else (1 if r[b] > 0 else 2))
+    assert kind == sorted(kind)                       # full, then partial, then no keys
+    full = [(s, bh // Hkv) for (s, bh), k in zip(got, kind) if k == 0]
+    assert [s for s, _ in full] == sorted(s for s, _ in full)   # split-major
+    for s in set(x for x, _ in full):
+        fs = [f[b] for x, b in full if x == s]
+        assert fs == sorted(fs, reverse=True)                   # more full splits first
+    part = [r[bh // Hkv] for (s, bh), k in zip(got, kind) if k == 1]
+    key = part if B <= 128 else [x * 1024 // sk for x in part]
+    assert key == sorted(key, reverse=True)                     # longest partial first
