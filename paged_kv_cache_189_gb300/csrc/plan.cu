@@ -22,7 +22,7 @@
 //    row's tail = its keys past the run.
 // One CTA (B <= 1024) computes the grouping: the batch-wide ranks and offsets
 // are block scans in shared memory, the leader search O(B^2 / threads) in
-// shared memory, the common-prefix scan one thread per (member, page) pair.
+// shared memory, the common-prefix scan one warp per member row.
 // A second kernel writes the group rows, one CTA per group slot.
 #include "pkv_common.cuh"
 #include "pkv_internal.h"
@@ -110,48 +110,36 @@ __global__ void __launch_bounds__(kMaxRows) plan_kernel(PlanArgs a) {
     }
     __syncthreads();
     const int leader = row ? s_leader[r] : r;
-    // shared run: every member lowers its leader's run to the first page where
-    // they differ; one thread per (member, page) pair over the batch (offsets of
-    // each row's pairs by a block scan), every load independent
-    {
-        int npairs = 0;
-        if (row && leader != r) {
-            npairs = min(cp, s_cp[leader]);
-            atomicMin(&s_run[leader], cp);  // never past a member's new tokens
-        }
-        const int off = block_exclusive_scan(npairs, s_scan);
-        s_tp[r] = row ? off : 0;            // scratch: first pair of row r
-        __shared__ int s_total_pairs;
-        if (r == blockDim.x - 1) s_total_pairs = off + npairs;
-        __syncthreads();
-        const int total = s_total_pairs;
-        // 8 pairs per thread per round: all 16 loads issued before any compare
-        for (int f0 = r; f0 < total; f0 += 8 * blockDim.x) {
+    // shared run: every member lowers its leader's run to its own committed
+    // pages and to the first page where its table differs from the leader's.
+    // One warp per member row compares 32 pages per ballot, the loads of eight
+    // steps in flight before any compare, and stops at the first difference (a
+    // member's table usually differs from its leader's a few pages past the
+    // shared prefix).  (Two rows per warp step, twice the loads in flight,
+    // measured the same.)
+    if (row && leader != r) atomicMin(&s_run[leader], cp);  // never past a member's new tokens
+    for (int rr = warp; rr < B; rr += nwarps) {
+        const int ld = s_leader[rr];
+        if (ld == rr) continue;  // uniform in the warp
+        const int n = min(s_cp[rr], s_cp[ld]);
+        const int32_t* ta = a.block_table + static_cast<int64_t>(rr) * a.block_table_stride;
+        const int32_t* tb = a.block_table + static_cast<int64_t>(ld) * a.block_table_stride;
+        int first = n;
+        for (int base = 0; base < n && first == n; base += 8 * 32) {
             int32_t va[8], vb[8];
-            int pg[8], ld[8];
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
-                const int f = f0 + k * blockDim.x;
-                va[k] = vb[k] = 0;
-                pg[k] = -1;
-                ld[k] = 0;
-                if (f < total) {
-                    // the row whose pairs hold f: last row with start <= f (binary search)
-                    int lo = 0, hi = B - 1;
-                    while (lo < hi) {
-                        const int mid = (lo + hi + 1) >> 1;
-                        if (s_tp[mid] <= f) lo = mid; else hi = mid - 1;
-                    }
-                    pg[k] = f - s_tp[lo];
-                    ld[k] = s_leader[lo];
-                    va[k] = a.block_table[static_cast<int64_t>(lo) * a.block_table_stride + pg[k]];
-                    vb[k] = a.block_table[static_cast<int64_t>(ld[k]) * a.block_table_stride + pg[k]];
-                }
+                const int pg = base + k * 32 + lane;
+                va[k] = pg < n ? ta[pg] : 0;
+                vb[k] = pg < n ? tb[pg] : 0;
             }
 #pragma unroll
-            for (int k = 0; k < 8; ++k)
-                if (pg[k] >= 0 && va[k] != vb[k]) atomicMin(&s_run[ld[k]], pg[k]);
+            for (int k = 0; k < 8; ++k) {
+                const unsigned diff = __ballot_sync(0xffffffffu, va[k] != vb[k]);
+                if (diff != 0u && first == n) first = base + k * 32 + __ffs(static_cast<int>(diff)) - 1;
+            }
         }
+        if (lane == 0 && first < n) atomicMin(&s_run[ld], first);
     }
     __syncthreads();
     if (row && leader == r && s_size[r] < 2) s_run[r] = 0;
@@ -197,8 +185,10 @@ __global__ void __launch_bounds__(kMaxRows) plan_kernel(PlanArgs a) {
     }
     // group index and offsets (scans over leader flags / sizes in row order)
     const bool is_leader = row && leader == r;
-    const int gidx_mine = block_exclusive_scan(is_leader ? 1 : 0, s_scan);
-    const int goff_mine = block_exclusive_scan(is_leader ? s_size[r] : 0, s_scan);
+    // one scan of (leader flag << 16 | members): both sums stay below 2^11
+    const int packed = block_exclusive_scan(is_leader ? (1 << 16) | s_size[r] : 0, s_scan);
+    const int gidx_mine = packed >> 16;
+    const int goff_mine = packed & 0xffff;
     // publish the leaders' values through shared memory
     __shared__ int s_gidx[kMaxRows];
     __shared__ int s_goff[kMaxRows];
