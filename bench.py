@@ -1031,12 +1031,30 @@ def measure(plan, name, args, rank, world, local, dev, stream, dist):
     on_host = [torch.cuda.Event() for _ in range(2)]    # a step's results are on the host
 
     pipelined = h2d + d2h >= PIPELINE_MIN_BYTES
+    # the step's launches (every call of the step through the public API, on
+    # the compute stream and any side stream it forks) captured once as a CUDA
+    # graph, as a serving loop replays a decode step: one host call per step
+    # instead of one per launch.  A step that cannot be captured runs eagerly.
+    graph = torch.cuda.CUDAGraph()
+    try:
+        with torch.cuda.stream(stream):
+            step()
+            torch.cuda.synchronize()
+            with torch.cuda.graph(graph, stream=stream):
+                step()
+        torch.cuda.synchronize()
+        run_step = graph.replay
+    except Exception as exc:  # capture refused: keep the eager step
+        print(f"bench: {name}: step not captured ({type(exc).__name__}: {exc}); eager end to end",
+              file=sys.stderr)
+        torch.cuda.synchronize()
+        run_step = step
 
     def e2e_serial(n, start=None):
         for i in range(n):
             with torch.cuda.stream(stream):
                 d_in.copy_(h_in, non_blocking=True)
-                step()
+                run_step()
                 h_out[i % 2].copy_(d_out, non_blocking=True)
                 on_host[i % 2].record(stream)
             if i >= 1:
@@ -1064,7 +1082,7 @@ def measure(plan, name, args, rank, world, local, dev, stream, dist):
             with torch.cuda.stream(stream):
                 stream.wait_event(staged[i % 2])
                 d_in.copy_(in_stage[i % 2], non_blocking=True)
-                step()
+                run_step()
                 if i >= 2:
                     stream.wait_event(on_host[i % 2])  # step i - 2's results have left
                 out_stage[i % 2].copy_(d_out, non_blocking=True)
@@ -1118,7 +1136,9 @@ def measure(plan, name, args, rank, world, local, dev, stream, dist):
                          if pipelined else
                          "serial: each step's inputs copied in (one copy), the step, its results "
                          "copied out (one copy), all on the compute stream; the host waits for "
-                         "each step's result one step behind")},
+                         "each step's result one step behind")
+                        + ("; the step's launches replayed as one captured CUDA graph"
+                           if run_step is not step else "; the step's calls made eagerly")},
         "gpu_launches": plan.launches * args.steps,
         "aux": aux_out,
     }
