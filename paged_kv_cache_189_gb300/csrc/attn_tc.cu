@@ -508,12 +508,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int32_t* bt = p.block_table + static_cast<int64_t>(g.b) * p.block_table_stride;
             const int last_page = (g.kv_len + 31) / 32;  // pages at or past it are never read
             int k_issued = 0, v_issued = 0;
-            auto load_tile = [&](const CUtensorMap* tm, uint8_t* dst, uint64_t* bar, int j) {
+            // the physical pages of key tile j (past the last page: the
+            // out-of-range sentinel, which the copy fills with zeros)
+            auto fetch_pages = [&](int j, int (&ph)[4]) {
+#pragma unroll
+                for (int pg = 0; pg < 4; ++pg) {
+                    const int lp = (g.kb + j * kTileN) / 32 + pg;
+                    ph[pg] = lp < last_page ? bt[lp] : static_cast<int>(p.num_pages);
+                }
+            };
+            auto load_tile = [&](const CUtensorMap* tm, uint8_t* dst, uint64_t* bar, int j, const int (&ph)[4]) {
                 mbar_arrive_expect_tx(bar, TD::kTile);
 #pragma unroll
                 for (int pg = 0; pg < 4; ++pg) {
                     const int lp = (g.kb + j * kTileN) / 32 + pg;
-                    int phys = lp < last_page ? bt[lp] : static_cast<int>(p.num_pages);
+                    int phys = ph[pg];
                     if (p.checked && lp < last_page && (phys < 0 || phys >= p.num_pages)) {
                         set_err(p.err, PKV_ERRBIT_PAGE);
                         phys = static_cast<int>(p.num_pages);
@@ -523,20 +532,30 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tma_load_4d(dst + h * kHalfBytes + pg * 4096, tm, bar, h * 64, g.kvh, 0, phys);
                 }
             };
+            // The block-table reads of the next K tile are issued one tile ahead
+            // (before the wait for a free stage), so a freed stage is refilled
+            // without a dependent global read in between; V tile j reads the
+            // pages K tile j read (cache hits).
+            int k_next[4] = {0, 0, 0, 0};
+            if (g.nt > 0) fetch_pages(0, k_next);
             // K runs ahead of V by the depth of its ring
             for (int j = 0; j < g.nt || v_issued < g.nt;) {
                 bool progressed = false;
                 if (k_issued < g.nt && k_issued < v_issued + kKStages) {
                     const int s = k_issued % kKStages;
+                    const int k_cur[4] = {k_next[0], k_next[1], k_next[2], k_next[3]};
+                    if (k_issued + 1 < g.nt) fetch_pages(k_issued + 1, k_next);
                     if (k_issued >= kKStages && !wait(&k_empty[s], ((k_issued / kKStages) - 1) & 1)) break;
-                    load_tile(&tm_k, smem + TD::kKOff + s * TD::kTile, &k_full[s], k_issued);
+                    load_tile(&tm_k, smem + TD::kKOff + s * TD::kTile, &k_full[s], k_issued, k_cur);
                     ++k_issued;
                     progressed = true;
                 }
                 if (v_issued < g.nt && v_issued < k_issued) {
                     const int s = v_issued % kVStages;
+                    int v_pages[4];
+                    fetch_pages(v_issued, v_pages);
                     if (v_issued >= kVStages && !wait(&v_empty[s], ((v_issued / kVStages) - 1) & 1)) break;
-                    load_tile(&tm_v, smem + TD::kVOff + s * TD::kTile, &v_full[s], v_issued);
+                    load_tile(&tm_v, smem + TD::kVOff + s * TD::kTile, &v_full[s], v_issued, v_pages);
                     ++v_issued;
                     progressed = true;
                 }
