@@ -21,18 +21,19 @@
 // query heads that share a K/V head share every K/V load.  Keys are walked in
 // tiles of 128 (four 32-token pages) within the CTA's key split.
 //
-// Roles (192 threads, one CTA per SM):
+// Roles (224 threads, one CTA per SM):
 //  * warps 0-3 (softmax): load the Q tile into swizzled shared memory; for
 //    each key tile read S = Q K^T from tensor memory (one row per thread),
 //    mask, online softmax in base 2 with a lazily moved maximum, write P as
 //    bf16 into shared memory in the MMA's K-major swizzled layout, rescale O
 //    in tensor memory when the maximum moved; finally normalise O and store it.
-//  * warp 4 lane 0 (producer): TMA loads of K pages (2-stage ring) and V
-//    pages (3-stage ring: V of tile j + 3 can only start once P.V of tile j
-//    finished, so the deeper ring goes to V), 4 pages x 2 column halves per
-//    128-key tile, through
-//    the block table; pages past the sequence are read out of bounds, which
-//    TMA fills with zeros.
+//  * warp 4 lane 0 and warp 6 lane 0 (producers): TMA loads of K pages
+//    (2-stage ring) and of V pages (3-stage ring: V of tile j + 3 can only
+//    start once P.V of tile j finished, so the deeper ring goes to V), one
+//    issuing thread per ring, 4 pages x 2 column halves per 128-key tile,
+//    through the block table, whose entries for the next tile are read one
+//    tile ahead; pages past the sequence are read out of bounds, which TMA
+//    fills with zeros.
 //  * warp 5 (MMA): allocates 512 tensor-memory columns (two S buffers and O),
 //    issues S_{j+2} = Q K_{j+2}^T and O += P_j V_j with tcgen05.mma
 //    (kind::f16, bf16 in, f32 accumulate, M = N = 128), and signals through
@@ -50,7 +51,7 @@ constexpr int kTileM = 128;             // query rows per tile (tensor-memory la
 constexpr int kTileN = 128;             // keys per tile
 constexpr int kKStages = 2;
 constexpr int kVStages = 3;
-constexpr int kThreads = 192;
+constexpr int kThreads = 224;
 constexpr int kHalfBytes = kTileM * 128;           // 128 rows x 64 bf16 = 16 KiB
 constexpr int kPBytes = 2 * kHalfBytes;            // P: 128 rows x 128 keys bf16 = 32 KiB
 constexpr int kMaxGroup = 64;           // head groups the tiles take (2 tokens per pair at least)
@@ -500,14 +501,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         return false;
     };
 
-    if (warp == 4) {
-        // ============================ producer ==============================
+    if (warp == 4 || warp == 6) {
+        // ============================ producers =============================
+        // Lane 0 of warp 4 streams the K tiles, lane 0 of warp 6 the V tiles,
+        // each through its own ring, so one ring's copies are issued while the
+        // other thread waits for a free stage.  Each reads the next tile's
+        // block-table entries one tile ahead (before that wait), so a freed
+        // stage is refilled without a dependent global read in between.
         if (lane == 0) {
-            prefetch_tmap(&tm_k);
-            prefetch_tmap(&tm_v);
+            const bool is_k = warp == 4;
+            const CUtensorMap* tm = is_k ? &tm_k : &tm_v;
+            prefetch_tmap(tm);
+            const int stages = is_k ? kKStages : kVStages;
+            uint8_t* ring = smem + (is_k ? TD::kKOff : TD::kVOff);
+            uint64_t* full = is_k ? k_full : v_full;
+            uint64_t* empty = is_k ? k_empty : v_empty;
             const int32_t* bt = p.block_table + static_cast<int64_t>(g.b) * p.block_table_stride;
             const int last_page = (g.kv_len + 31) / 32;  // pages at or past it are never read
-            int k_issued = 0, v_issued = 0;
             // the physical pages of key tile j (past the last page: the
             // out-of-range sentinel, which the copy fills with zeros)
             auto fetch_pages = [&](int j, int (&ph)[4]) {
@@ -517,56 +527,31 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ph[pg] = lp < last_page ? bt[lp] : static_cast<int>(p.num_pages);
                 }
             };
-            auto load_tile = [&](const CUtensorMap* tm, uint8_t* dst, uint64_t* bar, int j, const int (&ph)[4]) {
-                mbar_arrive_expect_tx(bar, TD::kTile);
+            int next[4] = {0, 0, 0, 0};
+            if (g.nt > 0) fetch_pages(0, next);
+            int issued = 0;
+            for (; issued < g.nt; ++issued) {
+                const int s = issued % stages;
+                const int cur[4] = {next[0], next[1], next[2], next[3]};
+                if (issued + 1 < g.nt) fetch_pages(issued + 1, next);
+                if (issued >= stages && !wait(&empty[s], ((issued / stages) - 1) & 1)) break;
+                mbar_arrive_expect_tx(&full[s], TD::kTile);
 #pragma unroll
                 for (int pg = 0; pg < 4; ++pg) {
-                    const int lp = (g.kb + j * kTileN) / 32 + pg;
-                    int phys = ph[pg];
+                    const int lp = (g.kb + issued * kTileN) / 32 + pg;
+                    int phys = cur[pg];
                     if (p.checked && lp < last_page && (phys < 0 || phys >= p.num_pages)) {
                         set_err(p.err, PKV_ERRBIT_PAGE);
                         phys = static_cast<int>(p.num_pages);
                     }
 #pragma unroll
                     for (int h = 0; h < TD::kHalves; ++h)
-                        tma_load_4d(dst + h * kHalfBytes + pg * 4096, tm, bar, h * 64, g.kvh, 0, phys);
+                        tma_load_4d(ring + s * TD::kTile + h * kHalfBytes + pg * 4096, tm, &full[s], h * 64, g.kvh,
+                                    0, phys);
                 }
-            };
-            // The block-table reads of the next K tile are issued one tile ahead
-            // (before the wait for a free stage), so a freed stage is refilled
-            // without a dependent global read in between; V tile j reads the
-            // pages K tile j read (cache hits).
-            int k_next[4] = {0, 0, 0, 0};
-            if (g.nt > 0) fetch_pages(0, k_next);
-            // K runs ahead of V by the depth of its ring
-            for (int j = 0; j < g.nt || v_issued < g.nt;) {
-                bool progressed = false;
-                if (k_issued < g.nt && k_issued < v_issued + kKStages) {
-                    const int s = k_issued % kKStages;
-                    const int k_cur[4] = {k_next[0], k_next[1], k_next[2], k_next[3]};
-                    if (k_issued + 1 < g.nt) fetch_pages(k_issued + 1, k_next);
-                    if (k_issued >= kKStages && !wait(&k_empty[s], ((k_issued / kKStages) - 1) & 1)) break;
-                    load_tile(&tm_k, smem + TD::kKOff + s * TD::kTile, &k_full[s], k_issued, k_cur);
-                    ++k_issued;
-                    progressed = true;
-                }
-                if (v_issued < g.nt && v_issued < k_issued) {
-                    const int s = v_issued % kVStages;
-                    int v_pages[4];
-                    fetch_pages(v_issued, v_pages);
-                    if (v_issued >= kVStages && !wait(&v_empty[s], ((v_issued / kVStages) - 1) & 1)) break;
-                    load_tile(&tm_v, smem + TD::kVOff + s * TD::kTile, &v_full[s], v_issued, v_pages);
-                    ++v_issued;
-                    progressed = true;
-                }
-                j = k_issued;
-                if (!progressed) break;
             }
             // do not leave with copies into this CTA's shared memory in flight
-            for (int j = max(0, k_issued - kKStages); j < k_issued; ++j)
-                mbar_wait(&k_full[j % kKStages], (j / kKStages) & 1);
-            for (int j = max(0, v_issued - kVStages); j < v_issued; ++j)
-                mbar_wait(&v_full[j % kVStages], (j / kVStages) & 1);
+            for (int j = max(0, issued - stages); j < issued; ++j) mbar_wait(&full[j % stages], (j / stages) & 1);
         }
     } else if (warp == 5) {
         // ============================== MMA ================================
@@ -652,7 +637,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             umma_commit(mma_done);
             if (!mbar_wait(mma_done, 0)) set_err(p.err, PKV_ERRBIT_TIMEOUT);
         }
-    } else {
+    } else if (warp < 4) {
         // ============================ softmax ===============================
         if constexpr (REP == 1) {
             const int r = threadIdx.x;             // tile row = tensor-memory lane
