@@ -1194,15 +1194,17 @@ __device__ __forceinline__ void umma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, u
 // the maxima exchanged between the two, capped every thread at 96 registers
 // and read the scores twice per key tile: 0.281 ms against 0.266 ms on the
 // video step.)
-// Roles (320 threads): warps 0-3 softmax A, warps 4-7 softmax B (quadrant
-// warp & 3), warp 8 TMA producer, warp 9 MMA.  Every wait gives up after ~2 s.
+// Roles (352 threads): warps 0-3 softmax A, warps 4-7 softmax B (quadrant
+// warp & 3), warp 8 the K producer, warp 9 MMA, warp 10 the V producer.
+// Every wait gives up after ~2 s.
 // ===========================================================================
-// 10 warps: 0-7 softmax (four per tile), 8 the TMA producer, 9 the MMA
-// issuer.  Three warps per SM sub-partition at most, so each thread may hold
-// 168 registers (the row's 128 scores among them)
-constexpr int kThreads2 = 320;
+// 11 warps: 0-7 softmax (four per tile), 8 and 10 the TMA producers (K and
+// V rings), 9 the MMA issuer.  Three warps per SM sub-partition at most, so
+// each thread may hold 168 registers (the row's 128 scores among them)
+constexpr int kThreads2 = 352;
 constexpr int kProducerWarp2 = 8;
 constexpr int kMmaWarp2 = 9;
+constexpr int kVProducerWarp2 = 10;
 constexpr int kRegs2 = 168;
 template <int D>
 struct TwoTileSmem {
@@ -1461,58 +1463,65 @@ __global__ void __maxnreg__(kRegs2)
         return false;
     };
 
-    if (warp == kProducerWarp2) {
-        // ============================ producer ==============================
-        // K and V tiles of every segment in order, through rings that run
-        // across segment boundaries (gt counts the tiles of all segments)
+    if (warp == kProducerWarp2 || warp == kVProducerWarp2) {
+        // ============================ producers =============================
+        // Lane 0 of warp 8 streams the K tiles of every segment in order, lane
+        // 0 of warp 10 the V tiles, each through its own ring running across
+        // segment boundaries (n counts the tiles of all segments), so one
+        // ring's copies are issued while the other thread waits for a free
+        // stage.  Each reads the next tile's block-table entries one tile ahead.
         if (lane == 0) {
-            prefetch_tmap(&tm_k);
-            prefetch_tmap(&tm_v);
+            const bool is_k = warp == kProducerWarp2;
+            const CUtensorMap* tm = is_k ? &tm_k : &tm_v;
+            prefetch_tmap(tm);
+            const int stages = is_k ? kKStages : kVStages;
+            uint8_t* ring = smem + (is_k ? SM::kKOff : SM::kVOff);
+            uint64_t* full = is_k ? k_full : v_full;
+            uint64_t* empty = is_k ? k_empty : v_empty;
             SegIter<SK> it = it0;
             Seg sg;
-            int kn = 0, vn = 0;  // K and V tiles issued
+            int n = 0;  // tiles issued
             bool alive = true;
             while (alive && it.next(p, TQ, sg)) {
                 const TileGeom& g = sg.g;
                 const int32_t* bt = p.block_table + static_cast<int64_t>(g.b) * p.block_table_stride;
                 const int last_page = (g.kv_len + 31) / 32;
-                auto load_tile = [&](const CUtensorMap* tm, uint8_t* dst, uint64_t* bar, int j) {
-                    mbar_arrive_expect_tx(bar, TD::kTile);
+                auto fetch_pages = [&](int j, int (&ph)[4]) {
 #pragma unroll
                     for (int pg = 0; pg < 4; ++pg) {
                         const int lp = (g.kb + j * kTileN) / 32 + pg;
-                        int phys = lp < last_page ? bt[lp] : static_cast<int>(p.num_pages);
+                        ph[pg] = lp < last_page ? bt[lp] : static_cast<int>(p.num_pages);
+                    }
+                };
+                int next[4] = {0, 0, 0, 0};
+                if (sg.j0 < sg.j1) fetch_pages(sg.j0, next);
+                for (int j = sg.j0; j < sg.j1; ++j) {
+                    const int s = n % stages;
+                    const int cur[4] = {next[0], next[1], next[2], next[3]};
+                    if (j + 1 < sg.j1) fetch_pages(j + 1, next);
+                    if (n >= stages && !wait(&empty[s], ((n / stages) - 1) & 1)) {
+                        alive = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&full[s], TD::kTile);
+#pragma unroll
+                    for (int pg = 0; pg < 4; ++pg) {
+                        const int lp = (g.kb + j * kTileN) / 32 + pg;
+                        int phys = cur[pg];
                         if (p.checked && lp < last_page && (phys < 0 || phys >= p.num_pages)) {
                             set_err(p.err, PKV_ERRBIT_PAGE);
                             phys = static_cast<int>(p.num_pages);
                         }
 #pragma unroll
                         for (int h = 0; h < TD::kHalves; ++h)
-                            tma_load_4d(dst + h * kHalfBytes + pg * 4096, tm, bar, h * 64, g.kvh, 0, phys);
+                            tma_load_4d(ring + s * TD::kTile + h * kHalfBytes + pg * 4096, tm, &full[s], h * 64,
+                                        g.kvh, 0, phys);
                     }
-                };
-                for (int j = sg.j0; j < sg.j1; ++j) {
-                    const int sk = kn % kKStages;
-                    if (kn >= kKStages && !wait(&k_empty[sk], ((kn / kKStages) - 1) & 1)) {
-                        alive = false;
-                        break;
-                    }
-                    load_tile(&tm_k, smem + SM::kKOff + sk * TD::kTile, &k_full[sk], j);
-                    ++kn;
-                    const int sv = vn % kVStages;
-                    if (vn >= kVStages && !wait(&v_empty[sv], ((vn / kVStages) - 1) & 1)) {
-                        alive = false;
-                        break;
-                    }
-                    load_tile(&tm_v, smem + SM::kVOff + sv * TD::kTile, &v_full[sv], j);
-                    ++vn;
+                    ++n;
                 }
             }
             // do not leave with copies into this CTA's shared memory in flight
-            for (int j = max(0, kn - kKStages); j < kn; ++j)
-                mbar_wait(&k_full[j % kKStages], (j / kKStages) & 1);
-            for (int j = max(0, vn - kVStages); j < vn; ++j)
-                mbar_wait(&v_full[j % kVStages], (j / kVStages) & 1);
+            for (int j = max(0, n - stages); j < n; ++j) mbar_wait(&full[j % stages], (j / stages) & 1);
         }
     } else if (warp == kMmaWarp2) {
         // ============================== MMA ================================
