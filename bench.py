@@ -1037,6 +1037,8 @@ def measure(plan, name, args, rank, world, local, dev, stream, dist):
     # instead of one per launch.  A step that cannot be captured runs eagerly.
     graph = torch.cuda.CUDAGraph()
     try:
+        if args.e2e_steps <= 0:
+            raise RuntimeError("no end-to-end steps requested")
         with torch.cuda.stream(stream):
             step()
             torch.cuda.synchronize()
@@ -1044,9 +1046,10 @@ def measure(plan, name, args, rank, world, local, dev, stream, dist):
                 step()
         torch.cuda.synchronize()
         run_step = graph.replay
-    except Exception as exc:  # capture refused: keep the eager step
-        print(f"bench: {name}: step not captured ({type(exc).__name__}: {exc}); eager end to end",
-              file=sys.stderr)
+    except Exception as exc:  # capture refused (or not needed): keep the eager step
+        if args.e2e_steps > 0:
+            print(f"bench: {name}: step not captured ({type(exc).__name__}: {exc}); eager end to end",
+                  file=sys.stderr)
         torch.cuda.synchronize()
         run_step = step
 
