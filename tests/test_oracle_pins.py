@@ -119,6 +119,46 @@ def test_attention_matches_sdpa(mask, cb, Hq, Hkv, D):
         assert np.isneginf(L[r0:r1][q_real[b]:]).all()
 
 
+@pytest.mark.parametrize("mask,cb", [("causal", 0), ("block_causal", 2), ("block_causal", 4), ("none", 0)])
+def test_more_new_tokens_than_keys_matches_sdpa(mask, cb):
+    """Rows positioned before key 0 (q_real > kv_len): the oracle against SDPA
+    with the block-membership mask, where new token j - first_new with
+    first_new < 0 is key j.  Rows the mask leaves empty come back zero with
+    LSE -inf (SDPA has no value for them)."""
+    gen = torch.Generator().manual_seed(21)
+    Hq, Hkv, D = 4, 2, 16
+    cases = [(3, 7), (1, 5), (6, 9)]                 # (kv_len, q_real)
+    Ks = [wl.randn_bf16((L, Hkv, D), gen) for L, _ in cases]
+    Vs = [wl.randn_bf16((L, Hkv, D), gen) for L, _ in cases]
+    q_real = [qr for _, qr in cases]
+    q = wl.randn_bf16((sum(q_real), Hq, D), gen, scale=2.0)
+    k_pool, table = build_pool(Ks, 7)
+    v_pool, _ = build_pool(Vs, 7)
+    indptr = np.concatenate([[0], np.cumsum(q_real)]).astype(np.int32)
+    kv_lens = [L for L, _ in cases]
+    O, L = orc.paged_attention(q, k_pool, v_pool, table, kv_lens, indptr, q_real, mask=mask, causal_block=cb)
+    scale = 1.0 / math.sqrt(D)
+    empty_seen = 0
+    for b, (kv, qr) in enumerate(cases):
+        r0, r1 = indptr[b], indptr[b + 1]
+        vis = mask_by_block_membership(qr, qr, kv, mask, cb)
+        some = vis.any(axis=1)
+        Qt = torch.from_numpy(f64(q[r0:r1])).permute(1, 0, 2)
+        Kt = torch.from_numpy(f64(Ks[b])).permute(1, 0, 2)
+        Vt = torch.from_numpy(f64(Vs[b])).permute(1, 0, 2)
+        if some.any():
+            ref = torch.nn.functional.scaled_dot_product_attention(
+                Qt[:, some], Kt, Vt, attn_mask=torch.from_numpy(vis[some]), scale=scale,
+                enable_gqa=True).permute(1, 0, 2).numpy()
+            np.testing.assert_allclose(O[r0:r1][some], ref, rtol=1e-11, atol=1e-12)
+        assert (O[r0:r1][~some] == 0).all() and np.isneginf(L[r0:r1][~some]).all()
+        empty_seen += int((~some).sum())
+        for i in range(qr):
+            assert orc.visible_keys(i, qr, kv, mask, max(cb, 1)) == int(vis[i].sum())
+    if mask != "none":
+        assert empty_seen > 0
+
+
 # ----------------------------------------------------------------------------
 # visible-key sets against the hand-derived golden fixture
 # ----------------------------------------------------------------------------
